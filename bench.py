@@ -1,0 +1,397 @@
+"""Throughput of the TTT inner-loop forward on one B300 (or N, one replica per
+GPU under torchrun), plus roofline fraction, clocks, an end-to-end number
+through host buffers and the CPU oracle as a reported baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one call of the library entry point over one batch of the workload
+(the whole hot path: every mini-batch of every (batch, head) scan).  Inputs are
+synthetic (seeded, see test_sequence_layers_08_b300/inputs.py) and resident in
+HBM; consecutive steps rotate through enough input/output copies that their
+union exceeds the 126 MB L2, so no step starts with its inputs in L2.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from test_sequence_layers_08_b300.inputs import CONFIGS, make_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "linear_bf16_B8_H12_L2048"
+L2_BYTES = 126 * 2 ** 20
+METRIC = "TTT-layer fwd tokens/s at 1 B300 and % of roofline (TC peak vs HBM GB/s)"
+
+
+def flops_per_head_token(cfg) -> float:
+    """Algorithmic FLOPs of one head-token (dense contractions only).
+    Linear: key product, query product and update (3 d^2 MACs) plus Q K^T and
+    the masked (Q K^T + 1) G product (2 b d MACs).  MLP: 7 d dh MACs (two key
+    layers, G2 W2^T, two updates, two query layers) plus 2 b (d + dh)."""
+    d, b = cfg.d, cfg.mini_batch
+    if cfg.kind == "linear":
+        return 2.0 * (3 * d * d + 2 * b * d)
+    return 2.0 * (7 * d * cfg.dh + 2 * b * (d + cfg.dh))
+
+
+def algorithmic_bytes(cfg) -> float:
+    """Bytes one launch must move at minimum: Q, K, V read and Z written in the
+    I/O type, eta read (fp32), initial state read once per head, final state
+    written once per (batch, head) in fp32."""
+    es = 2 if cfg.io == "bf16" else 4
+    seq = cfg.B * cfg.H * cfg.L
+    io = seq * (4 * cfg.d * es + 4)
+    if cfg.kind == "linear":
+        state = (cfg.d * cfg.d + cfg.d) * 4
+    else:
+        state = (2 * cfg.d * cfg.dh + cfg.dh + cfg.d) * 4
+    ln = 2 * cfg.H * cfg.d * 4 if cfg.ln else 0
+    return float(io + state * cfg.H + state * cfg.B * cfg.H + ln)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        m = json.load(open(p))
+        return {"hbm_gbs": m["hbm_gbs"], "bf16_tflops": m["bf16_tflops"],
+                "bf16_tflops_sustained": m.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, name):
+        self.marks.append((name, time.time()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            if t0 <= ts <= t1:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reported baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_rate(cfg, x, budget_s: float, threads: int):
+    """Time the oracle as it stands on whole (batch, head) scans of the
+    workload, as many as fit the time budget.  Returns (tokens/s, pairs, s)."""
+    import oracle
+    pairs = [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
+    kw = dict(mini_batch=cfg.mini_batch, ln=cfg.ln, eps=cfg.eps)
+    # calibrate with one pair
+    t0 = time.perf_counter()
+    oracle.run_pairs(cfg.kind, x, pairs[:1], threads=1, **kw)
+    one = time.perf_counter() - t0
+    n = max(1, min(len(pairs), int(budget_s * threads / max(one, 1e-6))))
+    n = max(n - n % threads, min(threads, len(pairs)))
+    t0 = time.perf_counter()
+    oracle.run_pairs(cfg.kind, x, pairs[:n], threads=threads, **kw)
+    dt = time.perf_counter() - t0
+    head_tokens = n * cfg.L
+    return head_tokens / cfg.H / dt, n, dt
+
+
+def run_reference(args, cfg, world, rank):
+    if rank != 0:
+        return
+    x = make_inputs(cfg, 0)
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_rate(cfg, x, budget / 4, threads)
+    rates, n_pairs = [], 0
+    for _ in range(args.steps):
+        r, n_pairs, _ = oracle_rate(cfg, x, budget, threads)
+        rates.append(r)
+    value = statistics.median(rates)
+    sample = (f"{n_pairs} of {cfg.B * cfg.H} (batch, head) scans, full L={cfg.L}, per step; "
+              f"tokens/s = head-tokens/s / H")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": cfg.tokens / value * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "L": cfg.L, "d": cfg.d,
+                       "mini_batch": cfg.mini_batch, "io": cfg.io, "residual_ln": cfg.ln,
+                       "kind": cfg.kind},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, cfg, world, rank, local):
+    import torch
+    import test_sequence_layers_08_b300 as ttt
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    x = make_inputs(cfg, 0)
+    io = torch.bfloat16 if cfg.io == "bf16" else torch.float32
+    state_keys = ["W0", "b0"] if cfg.kind == "linear" else ["W1", "b1", "W2", "b2"]
+
+    def dev_inputs():
+        d = {}
+        for k in ("Q", "K", "V"):
+            d[k] = torch.from_numpy(x[k]).to(dev).to(io)
+        for k in ["eta", "gamma", "beta"] + state_keys:
+            d[k] = None if x[k] is None else torch.from_numpy(x[k]).to(dev)
+        return d
+
+    per_set = algorithmic_bytes(cfg)
+    n_sets = max(1, min(8, math.ceil(3 * L2_BYTES / per_set)))
+    sets = [dev_inputs() for _ in range(n_sets)]
+    outs = [None] * n_sets
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        s = sets[i % n_sets]
+        kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps,
+                  out=outs[i % n_sets], stream=stream)
+        if cfg.kind == "linear":
+            o = ttt.ttt_linear_fwd(s["Q"], s["K"], s["V"], s["eta"], s["W0"], s["b0"],
+                                   s["gamma"], s["beta"], **kw)
+        else:
+            o = ttt.ttt_mlp_fwd(s["Q"], s["K"], s["V"], s["eta"], s["W1"], s["b1"], s["W2"],
+                                s["b2"], s["gamma"], s["beta"], **kw)
+        outs[i % n_sets] = o
+
+    desc = ttt.make_desc(sets[0]["Q"], cfg.mini_batch, cfg.ln, cfg.eps,
+                         d_hidden=cfg.dh if cfg.kind == "mlp" else 0)
+    kname = ttt.kernel_name(desc, cfg.kind == "mlp")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(args.warmup):
+        step(i)
+    ttt.ttt_sync_status(stream)
+    # soak: keep the same load running for ~1.5 s so the clock samples taken
+    # around the timed region describe this workload
+    t_soak = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    step(0)
+    e1.record(stream)
+    e1.synchronize()
+    one_ms = max(e0.elapsed_time(e1), 1e-3)
+    soak_n = int(min(20000, max(0, 1500.0 / one_ms)))
+    for i in range(soak_n):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(world)
+    ttt.ttt_sync_status(stream)
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(world, ms_total)
+    ms_step = ms_total / args.steps
+    value = world * cfg.tokens / (ms_step * 1e-3)
+    if time.time() - t_wall1 < 0.4:
+        time.sleep(0.4)   # let the sampler log past the end of the timed region
+    clk = clocks.summary(t_soak, time.time())
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    host = {}
+    for k in ("Q", "K", "V"):
+        host[k] = torch.from_numpy(x[k]).to(io).pin_memory()
+    for k in ["eta"] + state_keys:
+        host[k] = torch.from_numpy(x[k]).pin_memory()
+    dset = sets[0]
+    hout = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs[0]]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in host)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step():
+        for k in host:
+            dset[k].copy_(host[k], non_blocking=True)
+        step(0)
+        for hb, db in zip(hout, outs[0]):
+            hb.copy_(db, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    n_e2e = max(3, min(args.steps, 50))
+    barrier(world)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(world, s0.elapsed_time(s1)) / n_e2e
+    e2e_value = world * cfg.tokens / (e2e_ms * 1e-3)
+
+    clocks.stop()
+    peaks = load_peaks()
+    alg_bytes = algorithmic_bytes(cfg)
+    alg_flops = flops_per_head_token(cfg) * cfg.head_tokens
+    achieved_gbs = alg_bytes / (ms_step * 1e-3) / 1e9
+    achieved_tf = alg_flops / (ms_step * 1e-3) / 1e12
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg_flops / (peaks["bf16_tflops"] * 1e12)
+    if t_tc > t_hbm:
+        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"]}
+    else:
+        roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"]}
+    roof.update({"traffic": None, "peak_source": peaks["source"], "kernel": kname,
+                 "algorithmic_bytes": alg_bytes, "algorithmic_flops": alg_flops,
+                 "roofline_ms": max(t_hbm, t_tc) * 1e3})
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 1
+        rate, n_pairs, secs = oracle_rate(cfg, x, args.cpu_seconds, threads)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n_pairs} of {cfg.B * cfg.H} (batch, head) scans at full L={cfg.L} "
+                         f"in {secs:.1f} s; tokens/s = head-tokens/s / H"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if cfg.io == "bf16" else "f32", "data": "synthetic",
+                "config": {"workload": cfg.name, "kind": cfg.kind, "B": cfg.B, "H": cfg.H,
+                           "L": cfg.L, "d": cfg.d, "mini_batch": cfg.mini_batch,
+                           "io": cfg.io, "state": "f32", "residual_ln": cfg.ln,
+                           "l2": f"inputs rotate over {n_sets} copies "
+                                 f"({n_sets * alg_bytes / 1e6:.0f} MB > L2)",
+                           "parallelism": f"replica x{world}, one CTA per (batch, head)"},
+                "head_tokens_per_s": value * cfg.H, "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h},
+                "gpu_launches": args.steps, "clocks": clk,
+                "wall_s_timed": t_wall1 - t_wall0}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(CONFIGS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    cfg = CONFIGS[args.workload]
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, cfg, world, rank)
+        else:
+            run_ours(args, cfg, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

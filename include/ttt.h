@@ -1,0 +1,136 @@
+/*
+ * ttt.h -- C ABI of the TTT inner-loop forward library (libttt.so).
+ *
+ * The method (TTT layer, mini-batch form, forward only).  Per (batch, head) a
+ * fast-weight state is trained while the sequence is read:
+ *   - update/apply recurrence: W_t = W_{t-1} - eta_t grad_W l(W_{t-1}; x_t),
+ *     o_t = f(q_t; W_t)  -- damodev.csdn.net TTT article, section 3.1, equation;
+ *     the output uses the weights after the token's own update;
+ *   - mini-batch TTT: inside each mini-batch of b tokens every gradient is taken
+ *     at the mini-batch's starting weights, and the state reached at the end of
+ *     the mini-batch is carried to the next one -- same article, sections 4.1-4.2;
+ *   - loss l = 1/2 || f(k_t) - v_t ||^2 (summed over features, no 1/d);
+ *   - TTT-Linear f(k) = k W + c with W [d, d] row-major and c [d] -- same article,
+ *     sections 4.2 (XK @ W1 + b1) and 4.3 (W1 [heads, d, d], b1 [heads, 1, d]);
+ *   - TTT-MLP f(k) = GELU_tanh(k W1 + b1) W2 + b2, W1 [d, dh], W2 [dh, d] --
+ *     lryc.cn TTT article, section 2.1 (d -> 4d GELU -> d);
+ *   - optional residual LayerNorm f(k) = k + LN(f_res(k)) with per-head gamma,
+ *     beta [H, d], biased variance and eps = ln_eps -- lryc.cn article, section 2.1;
+ *     the loss target of f_res is then v - k (damodev article, section 4.2).
+ * The per-token learning rate eta (the gate eta_base * sigmoid(theta_lr x) of
+ * the lryc.cn article, section 2.2) is computed by the caller and passed in.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc or equivalent) owned
+ *     by the caller.  The library allocates no memory and keeps no per-call
+ *     state; it only launches kernels on `stream` and returns.  Results are
+ *     valid once the stream has been synchronised (ttt_sync_status does that
+ *     and also reports device-side failures).
+ *   - Layouts are dense row-major, no padding, 16-byte aligned base pointers:
+ *       Q, K, V, Z   [B, H, L, d]   element type desc->io_dtype
+ *       eta          [B, H, L]      float
+ *       gamma, beta  [H, d]         float  (may be NULL iff residual_ln == 0)
+ *       initial state: leading [H] (init_per_batch == 0) or [B, H]
+ *       final state:   always leading [B, H]; always float.
+ *   - Z must not alias any input.  A final-state buffer may alias the matching
+ *     initial-state buffer only when init_per_batch == 1 (same shape).
+ *   - Errors: TTT_ERR_INVALID_ARG for NULL pointers, non-positive sizes,
+ *     L % mini_batch != 0, misaligned pointers or forbidden aliasing;
+ *     TTT_ERR_UNSUPPORTED for shapes no kernel handles; TTT_ERR_CUDA when a
+ *     CUDA call or launch fails.  Nothing is launched when an error is
+ *     returned.  No C++ exception crosses this interface.  ttt_last_error()
+ *     gives a one-line description of the calling thread's last failure.
+ */
+#ifndef TTT_H
+#define TTT_H
+
+#if defined(__GNUC__)
+#define TTT_API __attribute__((visibility("default")))
+#else
+#define TTT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *ttt_stream_t;
+
+typedef enum {
+    TTT_OK = 0,
+    TTT_ERR_INVALID_ARG = 1,
+    TTT_ERR_UNSUPPORTED = 2,
+    TTT_ERR_CUDA = 3,
+    TTT_ERR_TIMEOUT = 4 /* a device-side bounded wait gave up (see ttt_sync_status) */
+} ttt_status;
+
+typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
+
+typedef struct {
+    int B;              /* batch                                               */
+    int H;              /* heads                                               */
+    int L;              /* sequence length, a multiple of mini_batch           */
+    int d;              /* head dimension (features of q, k, v, z)             */
+    int d_hidden;       /* TTT-MLP hidden width dh; 0 means 4 d (linear: unused) */
+    int mini_batch;     /* b, tokens per mini-batch                            */
+    ttt_dtype io_dtype; /* element type of Q, K, V and Z; state is always float */
+    int residual_ln;    /* 0: f = f_res;  1: f(k) = k + LN(f_res(k))           */
+    float ln_eps;       /* LayerNorm eps (used iff residual_ln)                */
+    int init_per_batch; /* 0: initial state [H, ...];  1: [B, H, ...]          */
+} ttt_desc;
+
+/*
+ * TTT-Linear forward.
+ *   in : Q, K, V [B,H,L,d] (io_dtype); eta [B,H,L]; W0 [H or B,H, d, d];
+ *        b0 [H or B,H, d]; gamma, beta [H, d] (NULL allowed without LN).
+ *   out: Z [B,H,L,d] (io_dtype): z_t = f(q_t; W_t, c_t) with the weights after
+ *        token t's update; W_final [B,H,d,d], b_final [B,H,d]: state after
+ *        the last mini-batch.
+ * Supported: any d <= 128 and b <= 64 (generic kernels, fp32 arithmetic);
+ * bf16 I/O with d = 64, b = 16 runs the tensor-core kernel.
+ */
+TTT_API ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
+                          const float *eta, const float *W0, const float *b0,
+                          const float *gamma, const float *beta, void *Z, float *W_final,
+                          float *b_final, ttt_stream_t stream);
+
+/*
+ * TTT-MLP forward (two-layer fast weights, GELU tanh).
+ *   in : Q, K, V, eta as above; W1_0 [H or B,H, d, dh]; b1_0 [H or B,H, dh];
+ *        W2_0 [H or B,H, dh, d]; b2_0 [H or B,H, d]; gamma, beta [H, d].
+ *   out: Z [B,H,L,d]; W1_f [B,H,d,dh]; b1_f [B,H,dh]; W2_f [B,H,dh,d]; b2_f [B,H,d].
+ * Supported: d <= 128, dh <= 512, b <= 64 while the state fits on chip.
+ */
+TTT_API ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
+                       const float *eta, const float *W1_0, const float *b1_0,
+                       const float *W2_0, const float *b2_0, const float *gamma,
+                       const float *beta, void *Z, float *W1_f, float *b1_f, float *W2_f,
+                       float *b2_f, ttt_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reports TTT_ERR_CUDA if a CUDA error is pending
+ * and TTT_ERR_TIMEOUT if any kernel launched by this library on the current
+ * device since the previous ttt_sync_status call gave up on a bounded wait
+ * (its outputs are then unspecified).  Clears the device-side flag it read.
+ */
+TTT_API ttt_status ttt_sync_status(ttt_stream_t stream);
+
+/* Static, NUL-terminated name of a status code. */
+TTT_API const char *ttt_status_string(ttt_status status);
+
+/* One-line description of the calling thread's most recent failure ("" if none). */
+TTT_API const char *ttt_last_error(void);
+
+/* Name of the kernel ttt_linear_fwd / ttt_mlp_fwd would launch for `desc`
+ * (is_mlp = 0 or 1), or NULL when the descriptor is rejected. */
+TTT_API const char *ttt_kernel_name(const ttt_desc *desc, int is_mlp);
+
+/* Library ABI version (major * 100 + minor). */
+TTT_API int ttt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTT_H */

@@ -1,0 +1,183 @@
+"""Python binding of libttt.so: the TTT inner-loop forward on B300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/ttt.h``.  Torch tensors are
+used for device memory and streams.  There is no CPU fallback: if the
+library has not been built, or the GPU is missing, calls raise.
+
+Functions mirror the C entry points:
+    ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma, beta, ...) -> (Z, W_final, b_final)
+    ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma, beta, ...) -> (Z, W1_f, b1_f, W2_f, b2_f)
+    ttt_sync_status(stream=None)
+    kernel_name(...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["TTTError", "Desc", "load", "library_path", "ttt_linear_fwd", "ttt_mlp_fwd",
+           "ttt_sync_status", "kernel_name", "version", "STATUS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libttt.so")
+_lock = threading.Lock()
+_lib = None
+
+TTT_F32, TTT_BF16 = 0, 1
+STATUS = {0: "TTT_OK", 1: "TTT_ERR_INVALID_ARG", 2: "TTT_ERR_UNSUPPORTED", 3: "TTT_ERR_CUDA",
+          4: "TTT_ERR_TIMEOUT"}
+
+
+class TTTError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("L", ctypes.c_int),
+                ("d", ctypes.c_int), ("d_hidden", ctypes.c_int), ("mini_batch", ctypes.c_int),
+                ("io_dtype", ctypes.c_int), ("residual_ln", ctypes.c_int),
+                ("ln_eps", ctypes.c_float), ("init_per_batch", ctypes.c_int)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libttt.so (built in place by ``build.py``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError(f"libttt.so not built ({_LIB_PATH}); run "
+                                  "`python -m test_sequence_layers_08_b300.build`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, dp = ctypes.c_void_p, ctypes.POINTER(Desc)
+            lib.ttt_linear_fwd.restype = ctypes.c_int
+            lib.ttt_linear_fwd.argtypes = [dp] + [vp] * 12
+            lib.ttt_mlp_fwd.restype = ctypes.c_int
+            lib.ttt_mlp_fwd.argtypes = [dp] + [vp] * 16
+            lib.ttt_sync_status.restype = ctypes.c_int
+            lib.ttt_sync_status.argtypes = [vp]
+            lib.ttt_status_string.restype = ctypes.c_char_p
+            lib.ttt_status_string.argtypes = [ctypes.c_int]
+            lib.ttt_last_error.restype = ctypes.c_char_p
+            lib.ttt_last_error.argtypes = []
+            lib.ttt_kernel_name.restype = ctypes.c_char_p
+            lib.ttt_kernel_name.argtypes = [dp, ctypes.c_int]
+            lib.ttt_version.restype = ctypes.c_int
+            lib.ttt_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def version() -> int:
+    return load().ttt_version()
+
+
+def _check(status: int):
+    if status != 0:
+        raise TTTError(status, load().ttt_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_desc(Q, mini_batch: int, residual_ln: bool, ln_eps: float = 1e-6,
+              init_per_batch: bool = False, d_hidden: int = 0) -> Desc:
+    import torch
+    B, H, L, d = Q.shape
+    io = {torch.float32: TTT_F32, torch.bfloat16: TTT_BF16}.get(Q.dtype)
+    if io is None:
+        raise TypeError(f"unsupported I/O dtype {Q.dtype}")
+    return Desc(B, H, L, d, d_hidden, mini_batch, io, int(residual_ln), float(ln_eps),
+                int(init_per_batch))
+
+
+def kernel_name(desc: Desc, mlp: bool = False):
+    n = load().ttt_kernel_name(ctypes.byref(desc), int(mlp))
+    return None if n is None else n.decode()
+
+
+def _check_tensor(name, t, dtype, device):
+    if t.dtype != dtype or t.device != device or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous {dtype} tensor on {device}")
+
+
+def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: int = 16,
+                   residual_ln: bool = False, ln_eps: float = 1e-6, init_per_batch: bool = False,
+                   out=None, stream=None):
+    """TTT-Linear forward on the GPU.  Q,K,V: [B,H,L,d] (float32 or bfloat16);
+    eta [B,H,L] float32; W0 [H,d,d] (or [B,H,d,d]); b0 [H,d] (or [B,H,d]);
+    gamma, beta [H,d] float32 (residual LayerNorm only).  Returns (Z, W_final,
+    b_final); pass ``out=(Z, W_final, b_final)`` to reuse buffers.  The call is
+    asynchronous on ``stream`` (default: torch's current stream)."""
+    import torch
+    lib = load()
+    desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch)
+    dev = Q.device
+    for n, t in (("K", K), ("V", V)):
+        _check_tensor(n, t, Q.dtype, dev)
+    for n, t in (("eta", eta), ("W0", W0), ("b0", b0)):
+        _check_tensor(n, t, torch.float32, dev)
+    if residual_ln:
+        _check_tensor("gamma", gamma, torch.float32, dev)
+        _check_tensor("beta", beta, torch.float32, dev)
+    B, H, L, d = Q.shape
+    if out is None:
+        out = (torch.empty_like(Q), torch.empty((B, H, d, d), device=dev, dtype=torch.float32),
+               torch.empty((B, H, d), device=dev, dtype=torch.float32))
+    Z, Wf, bf = out
+    _check(lib.ttt_linear_fwd(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta),
+                              _ptr(W0), _ptr(b0), _ptr(gamma if residual_ln else None),
+                              _ptr(beta if residual_ln else None), _ptr(Z), _ptr(Wf), _ptr(bf),
+                              _stream_handle(stream)))
+    return Z, Wf, bf
+
+
+def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_batch: int = 16,
+                residual_ln: bool = False, ln_eps: float = 1e-6, init_per_batch: bool = False,
+                out=None, stream=None):
+    """TTT-MLP forward on the GPU.  W1 [H,d,dh], b1 [H,dh], W2 [H,dh,d], b2 [H,d]
+    (leading B when init_per_batch).  Returns (Z, W1_f, b1_f, W2_f, b2_f)."""
+    import torch
+    lib = load()
+    dh = b1.shape[-1]
+    desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, d_hidden=dh)
+    dev = Q.device
+    for n, t in (("K", K), ("V", V)):
+        _check_tensor(n, t, Q.dtype, dev)
+    for n, t in (("eta", eta), ("W1", W1), ("b1", b1), ("W2", W2), ("b2", b2)):
+        _check_tensor(n, t, torch.float32, dev)
+    if residual_ln:
+        _check_tensor("gamma", gamma, torch.float32, dev)
+        _check_tensor("beta", beta, torch.float32, dev)
+    B, H, L, d = Q.shape
+    if out is None:
+        f32 = dict(device=dev, dtype=torch.float32)
+        out = (torch.empty_like(Q), torch.empty((B, H, d, dh), **f32), torch.empty((B, H, dh), **f32),
+               torch.empty((B, H, dh, d), **f32), torch.empty((B, H, d), **f32))
+    Z, W1f, b1f, W2f, b2f = out
+    _check(lib.ttt_mlp_fwd(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta), _ptr(W1),
+                           _ptr(b1), _ptr(W2), _ptr(b2), _ptr(gamma if residual_ln else None),
+                           _ptr(beta if residual_ln else None), _ptr(Z), _ptr(W1f), _ptr(b1f),
+                           _ptr(W2f), _ptr(b2f), _stream_handle(stream)))
+    return Z, W1f, b1f, W2f, b2f
+
+
+def ttt_sync_status(stream=None):
+    """Synchronise the stream; raise TTTError on a pending CUDA error or a
+    device-side bounded-wait timeout."""
+    _check(load().ttt_sync_status(_stream_handle(stream)))

@@ -1,0 +1,266 @@
+// ttt_api.cu -- host side of the C ABI declared in include/ttt.h: argument
+// checks, kernel choice, launch on the caller's stream, status reporting.
+// No allocation happens here; the only device memory the library owns is the
+// 4-byte failure flag below, which the module loader places in the image.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+
+#include "ttt_internal.h"
+
+namespace {
+
+// Set (atomicOr) by a kernel whose bounded wait gave up; read and cleared by
+// ttt_sync_status.  One per device; shared by every call on that device.
+__device__ unsigned int g_ttt_failure_flag;
+
+thread_local char g_last_error[256];
+
+ttt_status fail(ttt_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+ttt_status ok()
+{
+    g_last_error[0] = '\0';
+    return TTT_OK;
+}
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const void *p, size_t bytes)
+{
+    uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Range{a, a + bytes};
+}
+
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+ttt_status check_desc(const ttt_desc *s, bool mlp)
+{
+    if (!s) return fail(TTT_ERR_INVALID_ARG, "desc is NULL");
+    if (s->B <= 0 || s->H <= 0 || s->L <= 0 || s->d <= 0 || s->mini_batch <= 0)
+        return fail(TTT_ERR_INVALID_ARG, "B, H, L, d and mini_batch must be positive");
+    if (s->L % s->mini_batch != 0)
+        return fail(TTT_ERR_INVALID_ARG, "L (%d) is not a multiple of mini_batch (%d)", s->L,
+                    s->mini_batch);
+    if (s->io_dtype != TTT_F32 && s->io_dtype != TTT_BF16)
+        return fail(TTT_ERR_INVALID_ARG, "io_dtype must be TTT_F32 or TTT_BF16");
+    if (s->residual_ln != 0 && s->residual_ln != 1)
+        return fail(TTT_ERR_INVALID_ARG, "residual_ln must be 0 or 1");
+    if (s->init_per_batch != 0 && s->init_per_batch != 1)
+        return fail(TTT_ERR_INVALID_ARG, "init_per_batch must be 0 or 1");
+    if (s->residual_ln && !(std::isfinite(s->ln_eps) && s->ln_eps >= 0.f))
+        return fail(TTT_ERR_INVALID_ARG, "ln_eps must be finite and >= 0");
+    if (mlp && s->d_hidden < 0) return fail(TTT_ERR_INVALID_ARG, "d_hidden must be >= 0");
+    if ((long long)s->B * s->H > 0x7fffffffLL)
+        return fail(TTT_ERR_INVALID_ARG, "B * H exceeds the grid limit");
+    return TTT_OK;
+}
+
+ttt_status check_ptr(const void *p, const char *name)
+{
+    if (!p) return fail(TTT_ERR_INVALID_ARG, "%s is NULL", name);
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+        return fail(TTT_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+    return TTT_OK;
+}
+
+// Pointer to this device's failure flag (looked up once per device).
+unsigned int *failure_flag(ttt_status *st)
+{
+    static unsigned int *cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *st = fail(TTT_ERR_CUDA, "cudaGetDevice failed");
+        return nullptr;
+    }
+    if (!cache[dev]) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_ttt_failure_flag);
+        if (e != cudaSuccess) {
+            *st = fail(TTT_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        cache[dev] = static_cast<unsigned int *>(ptr);
+    }
+    *st = TTT_OK;
+    return cache[dev];
+}
+
+const char *linear_kernel(const ttt_desc &s)
+{
+    if (ttt::linear_tc_supported(s)) return "ttt_linear_tc";
+    if (ttt::linear_generic_smem_bytes(s)) return "ttt_linear_generic";
+    return nullptr;
+}
+
+const char *mlp_kernel(const ttt_desc &s)
+{
+    if (ttt::mlp_generic_smem_bytes(s)) return "ttt_mlp_generic";
+    return nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ttt_version(void) { return 100; }
+
+const char *ttt_status_string(ttt_status s)
+{
+    switch (s) {
+    case TTT_OK: return "TTT_OK";
+    case TTT_ERR_INVALID_ARG: return "TTT_ERR_INVALID_ARG";
+    case TTT_ERR_UNSUPPORTED: return "TTT_ERR_UNSUPPORTED";
+    case TTT_ERR_CUDA: return "TTT_ERR_CUDA";
+    case TTT_ERR_TIMEOUT: return "TTT_ERR_TIMEOUT";
+    }
+    return "TTT_ERR_UNKNOWN";
+}
+
+const char *ttt_last_error(void) { return g_last_error; }
+
+const char *ttt_kernel_name(const ttt_desc *desc, int is_mlp)
+{
+    if (check_desc(desc, is_mlp != 0) != TTT_OK) return nullptr;
+    if (is_mlp) {
+        ttt_desc s = *desc;
+        if (s.d_hidden == 0) s.d_hidden = 4 * s.d;
+        return mlp_kernel(s);
+    }
+    return linear_kernel(*desc);
+}
+
+ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
+                          const float *eta, const float *W0, const float *b0,
+                          const float *gamma, const float *beta, void *Z, float *W_final,
+                          float *b_final, ttt_stream_t stream)
+{
+    ttt_status st = check_desc(desc, false);
+    if (st != TTT_OK) return st;
+    const ttt_desc &s = *desc;
+    const void *ptrs[] = {Q, K, V, eta, W0, b0, Z, W_final, b_final};
+    const char *names[] = {"Q", "K", "V", "eta", "W0", "b0", "Z", "W_final", "b_final"};
+    for (int i = 0; i < 9; ++i)
+        if ((st = check_ptr(ptrs[i], names[i])) != TTT_OK) return st;
+    if (s.residual_ln) {
+        if ((st = check_ptr(gamma, "gamma")) != TTT_OK) return st;
+        if ((st = check_ptr(beta, "beta")) != TTT_OK) return st;
+    }
+    const size_t es = s.io_dtype == TTT_BF16 ? 2 : 4;
+    const size_t BH = (size_t)s.B * s.H, ninit = s.init_per_batch ? BH : (size_t)s.H;
+    const size_t dd = (size_t)s.d * s.d;
+    const Range rq = range_of(Q, BH * s.L * s.d * es), rk = range_of(K, BH * s.L * s.d * es),
+                rv = range_of(V, BH * s.L * s.d * es), re = range_of(eta, BH * s.L * 4),
+                rw0 = range_of(W0, ninit * dd * 4), rb0 = range_of(b0, ninit * s.d * 4),
+                rz = range_of(Z, BH * s.L * s.d * es), rwf = range_of(W_final, BH * dd * 4),
+                rbf = range_of(b_final, BH * s.d * 4);
+    Range ins[] = {rq, rk, rv, re, rw0, rb0, range_of(gamma, s.residual_ln ? s.H * s.d * 4 : 0),
+                   range_of(beta, s.residual_ln ? s.H * s.d * 4 : 0)};
+    for (const Range &r : ins)
+        if (overlap(rz, r)) return fail(TTT_ERR_INVALID_ARG, "Z overlaps an input");
+    if (overlap(rwf, rbf) || overlap(rz, rwf) || overlap(rz, rbf))
+        return fail(TTT_ERR_INVALID_ARG, "output buffers overlap");
+    for (int i = 0; i < 8; ++i) {
+        const Range &r = ins[i];
+        bool wf_ok = s.init_per_batch && i == 4 && r.lo == rwf.lo;  // in-place state carry
+        bool bf_ok = s.init_per_batch && i == 5 && r.lo == rbf.lo;
+        if (overlap(rwf, r) && !wf_ok) return fail(TTT_ERR_INVALID_ARG, "W_final overlaps an input");
+        if (overlap(rbf, r) && !bf_ok) return fail(TTT_ERR_INVALID_ARG, "b_final overlaps an input");
+    }
+    const char *kname = linear_kernel(s);
+    if (!kname)
+        return fail(TTT_ERR_UNSUPPORTED, "no kernel for d=%d mini_batch=%d", s.d, s.mini_batch);
+
+    ttt::LinearArgs a{s, Q, K, V, eta, W0, b0, gamma, beta, Z, W_final, b_final,
+                      reinterpret_cast<cudaStream_t>(stream), nullptr};
+    a.status = failure_flag(&st);
+    if (st != TTT_OK) return st;
+    cudaError_t e = ttt::linear_tc_supported(s) ? ttt::launch_linear_tc(a)
+                                                : ttt::launch_linear_generic(a);
+    if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "%s launch: %s", kname, cudaGetErrorString(e));
+    return ok();
+}
+
+ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
+                       const float *eta, const float *W1_0, const float *b1_0,
+                       const float *W2_0, const float *b2_0, const float *gamma,
+                       const float *beta, void *Z, float *W1_f, float *b1_f, float *W2_f,
+                       float *b2_f, ttt_stream_t stream)
+{
+    ttt_status st = check_desc(desc, true);
+    if (st != TTT_OK) return st;
+    ttt_desc s = *desc;
+    if (s.d_hidden == 0) s.d_hidden = 4 * s.d;
+    const void *ptrs[] = {Q, K, V, eta, W1_0, b1_0, W2_0, b2_0, Z, W1_f, b1_f, W2_f, b2_f};
+    const char *names[] = {"Q", "K", "V", "eta", "W1_0", "b1_0", "W2_0", "b2_0",
+                           "Z", "W1_f", "b1_f", "W2_f", "b2_f"};
+    for (int i = 0; i < 13; ++i)
+        if ((st = check_ptr(ptrs[i], names[i])) != TTT_OK) return st;
+    if (s.residual_ln) {
+        if ((st = check_ptr(gamma, "gamma")) != TTT_OK) return st;
+        if ((st = check_ptr(beta, "beta")) != TTT_OK) return st;
+    }
+    const size_t es = s.io_dtype == TTT_BF16 ? 2 : 4;
+    const size_t BH = (size_t)s.B * s.H, ninit = s.init_per_batch ? BH : (size_t)s.H;
+    const size_t n1 = (size_t)s.d * s.d_hidden;
+    const size_t seq = BH * s.L * s.d;
+    Range ins[] = {range_of(Q, seq * es), range_of(K, seq * es), range_of(V, seq * es),
+                   range_of(eta, BH * s.L * 4), range_of(W1_0, ninit * n1 * 4),
+                   range_of(b1_0, ninit * s.d_hidden * 4), range_of(W2_0, ninit * n1 * 4),
+                   range_of(b2_0, ninit * s.d * 4),
+                   range_of(gamma, s.residual_ln ? s.H * s.d * 4 : 0),
+                   range_of(beta, s.residual_ln ? s.H * s.d * 4 : 0)};
+    Range outs[] = {range_of(Z, seq * es), range_of(W1_f, BH * n1 * 4),
+                    range_of(b1_f, BH * s.d_hidden * 4), range_of(W2_f, BH * n1 * 4),
+                    range_of(b2_f, BH * s.d * 4)};
+    for (int o = 0; o < 5; ++o) {
+        for (int o2 = o + 1; o2 < 5; ++o2)
+            if (overlap(outs[o], outs[o2])) return fail(TTT_ERR_INVALID_ARG, "output buffers overlap");
+        for (int i = 0; i < 10; ++i) {
+            // final state o (1..4) may sit exactly on initial state i = o + 3 when per batch
+            bool same = s.init_per_batch && o >= 1 && i == o + 3 && outs[o].lo == ins[i].lo;
+            if (overlap(outs[o], ins[i]) && !same)
+                return fail(TTT_ERR_INVALID_ARG, "%s overlaps an input", names[8 + o]);
+        }
+    }
+    const char *kname = mlp_kernel(s);
+    if (!kname)
+        return fail(TTT_ERR_UNSUPPORTED, "no kernel for d=%d d_hidden=%d mini_batch=%d", s.d,
+                    s.d_hidden, s.mini_batch);
+    ttt::MlpArgs a{s, Q, K, V, eta, W1_0, b1_0, W2_0, b2_0, gamma, beta, Z,
+                   W1_f, b1_f, W2_f, b2_f, reinterpret_cast<cudaStream_t>(stream), nullptr};
+    a.status = failure_flag(&st);
+    if (st != TTT_OK) return st;
+    cudaError_t e = ttt::launch_mlp_generic(a);
+    if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "%s launch: %s", kname, cudaGetErrorString(e));
+    return ok();
+}
+
+ttt_status ttt_sync_status(ttt_stream_t stream)
+{
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    unsigned int flag = 0;
+    e = cudaMemcpyFromSymbol(&flag, g_ttt_failure_flag, sizeof(flag));
+    if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "reading the failure flag: %s", cudaGetErrorString(e));
+    if (flag != ttt::kStatusOk) {
+        const unsigned int zero = 0;
+        cudaMemcpyToSymbol(g_ttt_failure_flag, &zero, sizeof(zero));
+        return fail(TTT_ERR_TIMEOUT, "a kernel gave up on a bounded wait (flag 0x%x)", flag);
+    }
+    return ok();
+}
+
+}  // extern "C"

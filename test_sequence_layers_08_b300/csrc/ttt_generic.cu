@@ -1,0 +1,471 @@
+// ttt_generic.cu -- generic TTT inner-loop forward kernels (any small shape).
+//
+// One CTA per (batch, head) scans the L / b mini-batches in order.  The fast
+// weights live in shared memory in fp32 for the whole scan; every contraction
+// is plain fp32 FFMA.  These kernels serve the fp32-I/O workload (where a
+// relative error of 1e-5 rules out tf32/bf16 tensor-core operands) and every
+// shape the tensor-core kernels do not take.
+//
+// Per mini-batch (damodev.csdn.net TTT article, sections 4.1-4.2; lryc.cn TTT
+// article, section 2.1 for the MLP and the residual LayerNorm):
+//   Zk = K W + 1c,  G = dl/dZk  (Zk - V, or the LayerNorm-fused L2 backward
+//                                against V - K),
+//   A  = tril(Q K^T + 1) diag(eta)           (diagonal included),
+//   Zb = Q W + 1c - A G,  out = Zb or Q + LN(Zb),
+//   W -= K^T diag(eta) G,  c -= eta^T G.
+// The MLP does the same per layer, with X2 = GELU(Z1) as the second layer's
+// input and the back-propagated G1 = (G2 W2^T) * GELU'(Z1).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ttt_internal.h"
+
+namespace ttt {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ float load_io(const float *p, size_t i) { return p[i]; }
+__device__ __forceinline__ float load_io(const __nv_bfloat16 *p, size_t i)
+{
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store_io(float *p, size_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void store_io(__nv_bfloat16 *p, size_t i, float v)
+{
+    p[i] = __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Mean and 1/sqrt(biased var + eps) of one row, two passes; whole warp.
+__device__ __forceinline__ void row_stats(const float *z, int d, float eps, float &mu,
+                                          float &r)
+{
+    const int lane = threadIdx.x & 31;
+    float s = 0.f;
+    for (int j = lane; j < d; j += 32) s += z[j];
+    mu = warp_sum(s) / d;
+    float v = 0.f;
+    for (int j = lane; j < d; j += 32) {
+        float t = z[j] - mu;
+        v += t * t;
+    }
+    r = rsqrtf(warp_sum(v) / d + eps);
+}
+
+// In place: z <- d/dz 1/2 || gamma * norm(z) + beta - y ||^2, y = v - k.
+__device__ void ln_l2_bwd_row(float *z, const float *v, const float *k, const float *gam,
+                              const float *bet, int d, float eps)
+{
+    const int lane = threadIdx.x & 31;
+    float mu, r;
+    row_stats(z, d, eps, mu, r);
+    float m1 = 0.f, m2 = 0.f;
+    for (int j = lane; j < d; j += 32) {
+        float xh = (z[j] - mu) * r;
+        float gx = gam[j] * (gam[j] * xh + bet[j] - (v[j] - k[j]));
+        m1 += gx;
+        m2 += gx * xh;
+    }
+    m1 = warp_sum(m1) / d;
+    m2 = warp_sum(m2) / d;
+    __syncwarp();
+    for (int j = lane; j < d; j += 32) {
+        float xh = (z[j] - mu) * r;
+        float gx = gam[j] * (gam[j] * xh + bet[j] - (v[j] - k[j]));
+        z[j] = r * (gx - m1 - xh * m2);
+    }
+    __syncwarp();
+}
+
+// out_row = q + gamma * norm(z) + beta, written to global in the I/O type.
+template <typename IO>
+__device__ void ln_out_row(const float *z, const float *q, const float *gam,
+                           const float *bet, int d, float eps, IO *out)
+{
+    const int lane = threadIdx.x & 31;
+    float mu, r;
+    row_stats(z, d, eps, mu, r);
+    for (int j = lane; j < d; j += 32) store_io(out, j, q[j] + gam[j] * (z[j] - mu) * r + bet[j]);
+}
+
+__device__ __forceinline__ float gelu_tanh(float x)
+{
+    const float s = 0.7978845608028654f;  // sqrt(2/pi)
+    return 0.5f * x * (1.f + tanhf(s * (x + 0.044715f * x * x * x)));
+}
+
+__device__ __forceinline__ float gelu_tanh_prime(float x)
+{
+    const float s = 0.7978845608028654f;
+    float th = tanhf(s * (x + 0.044715f * x * x * x));
+    return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * s * (1.f + 3.f * 0.044715f * x * x);
+}
+
+struct LinearParams {
+    int H, L, d, mb, ln, init_per_batch;
+    float eps;
+    const void *Q, *K, *V;
+    const float *eta, *W0, *b0, *gamma, *beta;
+    void *Z;
+    float *Wf, *bf;
+};
+
+// ---------------------------------------------------------------------------
+// TTT-Linear
+// ---------------------------------------------------------------------------
+template <typename IO, bool LN>
+__global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p)
+{
+    extern __shared__ float sm[];
+    const int d = p.d, mb = p.mb, L = p.L;
+    const int bh = blockIdx.x, h = bh % p.H;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    float *W = sm;                 // d*d
+    float *c = W + d * d;          // d
+    float *Kt = c + d;             // mb*d
+    float *Qt = Kt + mb * d;
+    float *Vt = Qt + mb * d;
+    float *G = Vt + mb * d;        // Zk, then G
+    float *Zb = G + mb * d;
+    float *A = Zb + mb * d;        // mb*mb
+    float *et = A + mb * mb;       // mb
+    float *gam = et + mb;          // d
+    float *bet = gam + d;          // d
+
+    const size_t init = p.init_per_batch ? (size_t)bh : (size_t)h;
+    for (int i = tid; i < d * d; i += kThreads) W[i] = p.W0[init * d * d + i];
+    for (int j = tid; j < d; j += kThreads) {
+        c[j] = p.b0[init * d + j];
+        if (LN) {
+            gam[j] = p.gamma[(size_t)h * d + j];
+            bet[j] = p.beta[(size_t)h * d + j];
+        }
+    }
+    const IO *Qg = static_cast<const IO *>(p.Q) + (size_t)bh * L * d;
+    const IO *Kg = static_cast<const IO *>(p.K) + (size_t)bh * L * d;
+    const IO *Vg = static_cast<const IO *>(p.V) + (size_t)bh * L * d;
+    IO *Zg = static_cast<IO *>(p.Z) + (size_t)bh * L * d;
+    const float *eg = p.eta + (size_t)bh * L;
+    const int nt = mb * d;
+
+    for (int n0 = 0; n0 < L; n0 += mb) {
+        __syncthreads();
+        for (int i = tid; i < nt; i += kThreads) {
+            size_t gi = (size_t)n0 * d + i;
+            Kt[i] = load_io(Kg, gi);
+            Qt[i] = load_io(Qg, gi);
+            Vt[i] = load_io(Vg, gi);
+        }
+        for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
+        __syncthreads();
+        // key- and query-side products at the mini-batch's starting weights
+        for (int i = tid; i < nt; i += kThreads) {
+            const int s = i / d, j = i - s * d;
+            float ak = c[j], aq = c[j];
+            const float *kr = Kt + s * d, *qr = Qt + s * d;
+            for (int u = 0; u < d; ++u) {
+                const float w = W[u * d + j];
+                ak = fmaf(kr[u], w, ak);
+                aq = fmaf(qr[u], w, aq);
+            }
+            G[i] = ak;
+            Zb[i] = aq;
+        }
+        for (int i = tid; i < mb * mb; i += kThreads) {
+            const int t = i / mb, s = i - t * mb;
+            float a = 0.f;
+            if (s <= t) {
+                const float *qr = Qt + t * d, *kr = Kt + s * d;
+                for (int u = 0; u < d; ++u) a = fmaf(qr[u], kr[u], a);
+                a = (a + 1.f) * et[s];
+            }
+            A[i] = a;
+        }
+        __syncthreads();
+        if (LN) {
+            for (int s = warp; s < mb; s += kWarps)
+                ln_l2_bwd_row(G + s * d, Vt + s * d, Kt + s * d, gam, bet, d, p.eps);
+        } else {
+            for (int i = tid; i < nt; i += kThreads) G[i] -= Vt[i];
+        }
+        __syncthreads();
+        // dual-form outputs
+        for (int i = tid; i < nt; i += kThreads) {
+            const int t = i / d, j = i - t * d;
+            float z = Zb[i];
+            for (int s = 0; s <= t; ++s) z = fmaf(-A[t * mb + s], G[s * d + j], z);
+            if (LN)
+                Zb[i] = z;
+            else
+                store_io(Zg, (size_t)(n0 + t) * d + j, z);
+        }
+        // carry: W -= K^T diag(eta) G, c -= eta^T G
+        for (int i = tid; i < d * d; i += kThreads) {
+            const int u = i / d, j = i - u * d;
+            float acc = 0.f;
+            for (int s = 0; s < mb; ++s) acc = fmaf(et[s] * Kt[s * d + u], G[s * d + j], acc);
+            W[i] -= acc;
+        }
+        for (int j = tid; j < d; j += kThreads) {
+            float acc = 0.f;
+            for (int s = 0; s < mb; ++s) acc = fmaf(et[s], G[s * d + j], acc);
+            c[j] -= acc;
+        }
+        if (LN) {
+            __syncthreads();
+            for (int t = warp; t < mb; t += kWarps)
+                ln_out_row(Zb + t * d, Qt + t * d, gam, bet, d, p.eps, Zg + (size_t)(n0 + t) * d);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < d * d; i += kThreads) p.Wf[(size_t)bh * d * d + i] = W[i];
+    for (int j = tid; j < d; j += kThreads) p.bf[(size_t)bh * d + j] = c[j];
+}
+
+// ---------------------------------------------------------------------------
+// TTT-MLP
+// ---------------------------------------------------------------------------
+struct MlpParams {
+    int H, L, d, dh, mb, ln, init_per_batch;
+    float eps;
+    const void *Q, *K, *V;
+    const float *eta, *W1, *b1, *W2, *b2, *gamma, *beta;
+    void *Z;
+    float *W1f, *b1f, *W2f, *b2f;
+};
+
+template <typename IO, bool LN>
+__global__ void __launch_bounds__(kThreads) mlp_generic_kernel(MlpParams p)
+{
+    extern __shared__ float sm[];
+    const int d = p.d, dh = p.dh, mb = p.mb, L = p.L;
+    const int bh = blockIdx.x, h = bh % p.H;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    float *W1 = sm;               // d*dh
+    float *W2 = W1 + d * dh;      // dh*d
+    float *b1 = W2 + dh * d;      // dh
+    float *b2 = b1 + dh;          // d
+    float *Kt = b2 + d;           // mb*d
+    float *Qt = Kt + mb * d;
+    float *Vt = Qt + mb * d;
+    float *Z1 = Vt + mb * d;      // mb*dh : Z1, then G1
+    float *X2 = Z1 + mb * dh;     // mb*dh
+    float *Zb1 = X2 + mb * dh;    // mb*dh : Zb1, then Xb2
+    float *Z2 = Zb1 + mb * dh;    // mb*d  : Z2, then G2
+    float *Zb2 = Z2 + mb * d;     // mb*d
+    float *A = Zb2 + mb * d;      // mb*mb
+    float *et = A + mb * mb;      // mb
+    float *gam = et + mb;         // d
+    float *bet = gam + d;         // d
+
+    const size_t init = p.init_per_batch ? (size_t)bh : (size_t)h;
+    for (int i = tid; i < d * dh; i += kThreads) {
+        W1[i] = p.W1[init * d * dh + i];
+        W2[i] = p.W2[init * d * dh + i];
+    }
+    for (int m = tid; m < dh; m += kThreads) b1[m] = p.b1[init * dh + m];
+    for (int j = tid; j < d; j += kThreads) {
+        b2[j] = p.b2[init * d + j];
+        if (LN) {
+            gam[j] = p.gamma[(size_t)h * d + j];
+            bet[j] = p.beta[(size_t)h * d + j];
+        }
+    }
+    const IO *Qg = static_cast<const IO *>(p.Q) + (size_t)bh * L * d;
+    const IO *Kg = static_cast<const IO *>(p.K) + (size_t)bh * L * d;
+    const IO *Vg = static_cast<const IO *>(p.V) + (size_t)bh * L * d;
+    IO *Zg = static_cast<IO *>(p.Z) + (size_t)bh * L * d;
+    const float *eg = p.eta + (size_t)bh * L;
+    const int nt = mb * d, nh = mb * dh;
+
+    for (int n0 = 0; n0 < L; n0 += mb) {
+        __syncthreads();
+        for (int i = tid; i < nt; i += kThreads) {
+            size_t gi = (size_t)n0 * d + i;
+            Kt[i] = load_io(Kg, gi);
+            Qt[i] = load_io(Qg, gi);
+            Vt[i] = load_io(Vg, gi);
+        }
+        for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
+        __syncthreads();
+        // first layer at the starting weights, key and query side
+        for (int i = tid; i < nh; i += kThreads) {
+            const int s = i / dh, m = i - s * dh;
+            float ak = b1[m], aq = b1[m];
+            for (int u = 0; u < d; ++u) {
+                const float w = W1[u * dh + m];
+                ak = fmaf(Kt[s * d + u], w, ak);
+                aq = fmaf(Qt[s * d + u], w, aq);
+            }
+            Z1[i] = ak;
+            X2[i] = gelu_tanh(ak);
+            Zb1[i] = aq;
+        }
+        for (int i = tid; i < mb * mb; i += kThreads) {
+            const int t = i / mb, s = i - t * mb;
+            float a = 0.f;
+            if (s <= t) {
+                for (int u = 0; u < d; ++u) a = fmaf(Qt[t * d + u], Kt[s * d + u], a);
+                a = (a + 1.f) * et[s];
+            }
+            A[i] = a;
+        }
+        __syncthreads();
+        // second layer, key side
+        for (int i = tid; i < nt; i += kThreads) {
+            const int s = i / d, j = i - s * d;
+            float a = b2[j];
+            for (int m = 0; m < dh; ++m) a = fmaf(X2[s * dh + m], W2[m * d + j], a);
+            Z2[i] = a;
+        }
+        __syncthreads();
+        if (LN) {
+            for (int s = warp; s < mb; s += kWarps)
+                ln_l2_bwd_row(Z2 + s * d, Vt + s * d, Kt + s * d, gam, bet, d, p.eps);
+        } else {
+            for (int i = tid; i < nt; i += kThreads) Z2[i] -= Vt[i];
+        }
+        __syncthreads();
+        // G1 = (G2 W2^T) * GELU'(Z1), in place over Z1; query side of layer 1
+        for (int i = tid; i < nh; i += kThreads) {
+            const int s = i / dh, m = i - s * dh;
+            float a = 0.f;
+            for (int j = 0; j < d; ++j) a = fmaf(Z2[s * d + j], W2[m * d + j], a);
+            Z1[i] = a * gelu_tanh_prime(Z1[i]);
+        }
+        __syncthreads();
+        for (int i = tid; i < nh; i += kThreads) {
+            const int t = i / dh, m = i - t * dh;
+            float z = Zb1[i];
+            for (int s = 0; s <= t; ++s) z = fmaf(-A[t * mb + s], Z1[s * dh + m], z);
+            Zb1[i] = gelu_tanh(z);  // Xb2
+        }
+        __syncthreads();
+        for (int i = tid; i < mb * mb; i += kThreads) {
+            const int t = i / mb, s = i - t * mb;
+            float a = 0.f;
+            if (s <= t) {
+                for (int m = 0; m < dh; ++m) a = fmaf(Zb1[t * dh + m], X2[s * dh + m], a);
+                a = (a + 1.f) * et[s];
+            }
+            A[i] = a;
+        }
+        __syncthreads();
+        for (int i = tid; i < nt; i += kThreads) {
+            const int t = i / d, j = i - t * d;
+            float z = b2[j];
+            for (int m = 0; m < dh; ++m) z = fmaf(Zb1[t * dh + m], W2[m * d + j], z);
+            for (int s = 0; s <= t; ++s) z = fmaf(-A[t * mb + s], Z2[s * d + j], z);
+            if (LN)
+                Zb2[i] = z;
+            else
+                store_io(Zg, (size_t)(n0 + t) * d + j, z);
+        }
+        __syncthreads();
+        // carry
+        for (int i = tid; i < d * dh; i += kThreads) {
+            const int u = i / dh, m = i - u * dh;
+            float acc = 0.f;
+            for (int s = 0; s < mb; ++s) acc = fmaf(et[s] * Kt[s * d + u], Z1[s * dh + m], acc);
+            W1[i] -= acc;
+        }
+        for (int i = tid; i < dh * d; i += kThreads) {
+            const int m = i / d, j = i - m * d;
+            float acc = 0.f;
+            for (int s = 0; s < mb; ++s) acc = fmaf(et[s] * X2[s * dh + m], Z2[s * d + j], acc);
+            W2[i] -= acc;
+        }
+        for (int m = tid; m < dh; m += kThreads) {
+            float acc = 0.f;
+            for (int s = 0; s < mb; ++s) acc = fmaf(et[s], Z1[s * dh + m], acc);
+            b1[m] -= acc;
+        }
+        for (int j = tid; j < d; j += kThreads) {
+            float acc = 0.f;
+            for (int s = 0; s < mb; ++s) acc = fmaf(et[s], Z2[s * d + j], acc);
+            b2[j] -= acc;
+        }
+        if (LN) {
+            for (int t = warp; t < mb; t += kWarps)
+                ln_out_row(Zb2 + t * d, Qt + t * d, gam, bet, d, p.eps, Zg + (size_t)(n0 + t) * d);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < d * dh; i += kThreads) {
+        p.W1f[(size_t)bh * d * dh + i] = W1[i];
+        p.W2f[(size_t)bh * d * dh + i] = W2[i];
+    }
+    for (int m = tid; m < dh; m += kThreads) p.b1f[(size_t)bh * dh + m] = b1[m];
+    for (int j = tid; j < d; j += kThreads) p.b2f[(size_t)bh * d + j] = b2[j];
+}
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+template <typename K>
+cudaError_t launch(K kernel, int grid, size_t smem, cudaStream_t stream, const void *params)
+{
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    void *args[] = {const_cast<void *>(params)};
+    return cudaLaunchKernel((const void *)kernel, dim3(grid), dim3(kThreads), args, smem, stream);
+}
+
+}  // namespace
+
+size_t linear_generic_smem_bytes(const ttt_desc &s)
+{
+    if (s.d > 128 || s.mini_batch > 64) return 0;
+    size_t d = s.d, mb = s.mini_batch;
+    size_t n = d * d + d + 5 * mb * d + mb * mb + mb + 2 * d;
+    size_t bytes = n * sizeof(float);
+    return bytes <= kMaxSmem ? bytes : 0;
+}
+
+cudaError_t launch_linear_generic(const LinearArgs &a)
+{
+    const ttt_desc &s = a.desc;
+    LinearParams p{s.H, s.L, s.d, s.mini_batch, s.residual_ln, s.init_per_batch, s.ln_eps,
+                   a.Q, a.K, a.V, a.eta, a.W0, a.b0, a.gamma, a.beta, a.Z, a.W_final, a.b_final};
+    const size_t smem = linear_generic_smem_bytes(s);
+    const int grid = s.B * s.H;
+    if (s.io_dtype == TTT_F32)
+        return s.residual_ln ? launch(linear_generic_kernel<float, true>, grid, smem, a.stream, &p)
+                             : launch(linear_generic_kernel<float, false>, grid, smem, a.stream, &p);
+    return s.residual_ln ? launch(linear_generic_kernel<__nv_bfloat16, true>, grid, smem, a.stream, &p)
+                         : launch(linear_generic_kernel<__nv_bfloat16, false>, grid, smem, a.stream, &p);
+}
+
+size_t mlp_generic_smem_bytes(const ttt_desc &s)
+{
+    if (s.d > 128 || s.d_hidden > 512 || s.mini_batch > 64) return 0;
+    size_t d = s.d, dh = s.d_hidden, mb = s.mini_batch;
+    size_t n = 2 * d * dh + dh + d + 3 * mb * d + 3 * mb * dh + 2 * mb * d + mb * mb + mb + 2 * d;
+    size_t bytes = n * sizeof(float);
+    return bytes <= kMaxSmem ? bytes : 0;
+}
+
+cudaError_t launch_mlp_generic(const MlpArgs &a)
+{
+    const ttt_desc &s = a.desc;
+    MlpParams p{s.H, s.L, s.d, s.d_hidden, s.mini_batch, s.residual_ln, s.init_per_batch, s.ln_eps,
+                a.Q, a.K, a.V, a.eta, a.W1_0, a.b1_0, a.W2_0, a.b2_0, a.gamma, a.beta, a.Z,
+                a.W1_f, a.b1_f, a.W2_f, a.b2_f};
+    const size_t smem = mlp_generic_smem_bytes(s);
+    const int grid = s.B * s.H;
+    if (s.io_dtype == TTT_F32)
+        return s.residual_ln ? launch(mlp_generic_kernel<float, true>, grid, smem, a.stream, &p)
+                             : launch(mlp_generic_kernel<float, false>, grid, smem, a.stream, &p);
+    return s.residual_ln ? launch(mlp_generic_kernel<__nv_bfloat16, true>, grid, smem, a.stream, &p)
+                         : launch(mlp_generic_kernel<__nv_bfloat16, false>, grid, smem, a.stream, &p);
+}
+
+}  // namespace ttt

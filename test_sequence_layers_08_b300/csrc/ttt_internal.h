@@ -1,0 +1,47 @@
+// ttt_internal.h -- declarations shared by the host side of libttt.so
+// (argument checks in ttt_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "../../include/ttt.h"
+
+namespace ttt {
+
+// Everything a launcher needs for one TTT-Linear call (pointers already checked).
+struct LinearArgs {
+    ttt_desc desc;
+    const void *Q, *K, *V;
+    const float *eta, *W0, *b0, *gamma, *beta;
+    void *Z;
+    float *W_final, *b_final;
+    cudaStream_t stream;
+    unsigned int *status;  // device-side failure flag (bounded waits)
+};
+
+struct MlpArgs {
+    ttt_desc desc;  // desc.d_hidden already resolved (> 0)
+    const void *Q, *K, *V;
+    const float *eta, *W1_0, *b1_0, *W2_0, *b2_0, *gamma, *beta;
+    void *Z;
+    float *W1_f, *b1_f, *W2_f, *b2_f;
+    cudaStream_t stream;
+    unsigned int *status;
+};
+
+// Generic kernels: one CTA per (batch, head), fp32 FFMA arithmetic, state in
+// shared memory.  *_smem_bytes returns 0 when the shape does not fit.
+size_t linear_generic_smem_bytes(const ttt_desc &d);
+cudaError_t launch_linear_generic(const LinearArgs &a);
+size_t mlp_generic_smem_bytes(const ttt_desc &d);
+cudaError_t launch_mlp_generic(const MlpArgs &a);
+
+// Tensor-core TTT-Linear kernel (bf16 I/O, d = 64, b = 16).
+bool linear_tc_supported(const ttt_desc &d);
+cudaError_t launch_linear_tc(const LinearArgs &a);
+
+// Device-side status word values.
+enum : unsigned int { kStatusOk = 0u, kStatusTimeout = 1u };
+
+}  // namespace ttt

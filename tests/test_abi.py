@@ -1,0 +1,106 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, names its status codes, and rejects bad arguments before any
+CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import test_sequence_layers_08_b300 as ttt
+from test_sequence_layers_08_b300 import build as ttt_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ttt_build.build()
+    return ttt.load()
+
+
+def header_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"^TTT_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for n in ("ttt_linear_fwd", "ttt_mlp_fwd", "ttt_sync_status", "ttt_status_string",
+              "ttt_last_error", "ttt_kernel_name", "ttt_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in header_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in ttt.STATUS.items():
+        assert lib.ttt_status_string(code).decode() == name
+    assert lib.ttt_version() >= 100
+
+
+def desc(**kw):
+    base = dict(B=2, H=3, L=64, d=64, d_hidden=0, mini_batch=16, io_dtype=1, residual_ln=0,
+                ln_eps=1e-6, init_per_batch=0)
+    base.update(kw)
+    return ttt.Desc(**base)
+
+
+FAKE = 1 << 20   # an aligned address; validation never dereferences pointers
+
+
+def call_linear(lib, dsc, ptrs=None):
+    p = [FAKE + i * (1 << 30) for i in range(11)] if ptrs is None else ptrs
+    return lib.ttt_linear_fwd(ctypes.byref(dsc), *[ctypes.c_void_p(x) if x else None for x in p],
+                              None)
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=-1), dict(L=0), dict(d=0), dict(mini_batch=0),
+                                dict(L=40), dict(io_dtype=7), dict(residual_ln=2),
+                                dict(init_per_batch=3), dict(residual_ln=1, ln_eps=-1.0)])
+def test_bad_descriptor_is_invalid_arg(lib, kw):
+    assert call_linear(lib, desc(**kw)) == 1
+    assert lib.ttt_last_error().decode() != ""
+    assert lib.ttt_kernel_name(ctypes.byref(desc(**kw)), 0) is None
+
+
+def test_null_and_misaligned_pointers(lib):
+    base = [FAKE + i * (1 << 30) for i in range(11)]
+    for i in (0, 1, 2, 3, 4, 5, 8, 9, 10):
+        p = list(base)
+        p[i] = 0
+        assert call_linear(lib, desc(), p) == 1
+        p[i] = base[i] + 4
+        assert call_linear(lib, desc(), p) == 1
+    # gamma / beta only required with the residual LayerNorm
+    p = list(base)
+    p[6] = 0
+    assert call_linear(lib, desc(residual_ln=1), p) == 1
+
+
+def test_aliasing_rules(lib):
+    base = [FAKE + i * (1 << 30) for i in range(11)]
+    p = list(base)
+    p[8] = p[0]          # Z on top of Q
+    assert call_linear(lib, desc(), p) == 1
+    p = list(base)
+    p[9] = p[4]          # W_final on W0 with a head-shared W0: shapes differ
+    assert call_linear(lib, desc(), p) == 1
+    assert "W_final" in lib.ttt_last_error().decode()
+
+
+def test_kernel_choice(lib):
+    k = lambda **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), 0))
+    assert k(io_dtype=0) == "ttt_linear_generic"
+    assert k(d=32) == "ttt_linear_generic"
+    assert k(d=256) is None
+    m = lambda **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), 1))
+    assert m(residual_ln=1) is not None
+    assert m(d_hidden=4096) is None
