@@ -116,6 +116,23 @@ TTT_API ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *
  */
 TTT_API ttt_status ttt_sync_status(ttt_stream_t stream);
 
+/*
+ * Bound of every wait a kernel makes on an mbarrier (a copy landing, a buffer
+ * being released), in nanoseconds of GPU wall time; <= 0 restores the default
+ * of one second.  A wait that runs out makes the kernel stop waiting, finish
+ * without faulting, and flag TTT_ERR_TIMEOUT for ttt_sync_status.  Process-wide
+ * setting read at launch time.
+ */
+TTT_API void ttt_set_wait_timeout_ns(long long ns);
+
+/*
+ * Test hook for the timeout path: while `on` is non-zero, the copy-issuing warp
+ * of the fused kernels issues no copies, so every wait for data runs out after
+ * the timeout above and the call reports TTT_ERR_TIMEOUT (outputs unspecified).
+ * Nothing faults or hangs.  Process-wide; leave it off outside tests.
+ */
+TTT_API void ttt_debug_withhold_loads(int on);
+
 /* Static, NUL-terminated name of a status code. */
 TTT_API const char *ttt_status_string(ttt_status status);
 

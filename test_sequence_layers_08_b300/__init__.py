@@ -18,7 +18,8 @@ import os
 import threading
 
 __all__ = ["TTTError", "Desc", "load", "library_path", "ttt_linear_fwd", "ttt_mlp_fwd",
-           "ttt_sync_status", "kernel_name", "version", "STATUS"]
+           "ttt_sync_status", "kernel_name", "version", "STATUS", "set_wait_timeout_ns",
+           "debug_withhold_loads"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libttt.so")
@@ -71,6 +72,10 @@ def load():
             lib.ttt_kernel_name.argtypes = [dp, ctypes.c_int]
             lib.ttt_version.restype = ctypes.c_int
             lib.ttt_version.argtypes = []
+            lib.ttt_set_wait_timeout_ns.restype = None
+            lib.ttt_set_wait_timeout_ns.argtypes = [ctypes.c_longlong]
+            lib.ttt_debug_withhold_loads.restype = None
+            lib.ttt_debug_withhold_loads.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -175,6 +180,17 @@ def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_bat
                            _ptr(beta if residual_ln else None), _ptr(Z), _ptr(W1f), _ptr(b1f),
                            _ptr(W2f), _ptr(b2f), _stream_handle(stream)))
     return Z, W1f, b1f, W2f, b2f
+
+
+def set_wait_timeout_ns(ns: int):
+    """Bound (ns) of every mbarrier wait in the fused kernels; <= 0 restores 1 s."""
+    load().ttt_set_wait_timeout_ns(int(ns))
+
+
+def debug_withhold_loads(on: bool):
+    """Test hook: the fused kernels' copy warp issues no copies, so their waits
+    run out and the next ttt_sync_status reports TTT_ERR_TIMEOUT."""
+    load().ttt_debug_withhold_loads(int(bool(on)))
 
 
 def ttt_sync_status(stream=None):

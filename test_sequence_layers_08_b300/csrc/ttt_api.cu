@@ -100,7 +100,7 @@ unsigned int *failure_flag(ttt_status *st)
 
 const char *linear_kernel(const ttt_desc &s)
 {
-    if (ttt::linear_tc_supported(s)) return "ttt_linear_tc";
+    if (ttt::linear_tc_supported(s)) return "ttt_linear_fused";
     if (ttt::linear_generic_smem_bytes(s)) return "ttt_linear_generic";
     return nullptr;
 }
@@ -247,6 +247,10 @@ ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const
     if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "%s launch: %s", kname, cudaGetErrorString(e));
     return ok();
 }
+
+void ttt_set_wait_timeout_ns(long long ns) { ttt::set_wait_timeout_ns(ns); }
+
+void ttt_debug_withhold_loads(int on) { ttt::set_withhold_loads(on); }
 
 ttt_status ttt_sync_status(ttt_stream_t stream)
 {

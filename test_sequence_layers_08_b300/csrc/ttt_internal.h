@@ -40,6 +40,9 @@ cudaError_t launch_mlp_generic(const MlpArgs &a);
 // Tensor-core TTT-Linear kernel (bf16 I/O, d = 64, b = 16).
 bool linear_tc_supported(const ttt_desc &d);
 cudaError_t launch_linear_tc(const LinearArgs &a);
+// Test hooks of the bounded waits (process-wide; see ttt.h).
+void set_wait_timeout_ns(long long ns);
+void set_withhold_loads(int on);
 
 // Device-side status word values.
 enum : unsigned int { kStatusOk = 0u, kStatusTimeout = 1u };

@@ -98,6 +98,8 @@ def test_aliasing_rules(lib):
 
 def test_kernel_choice(lib):
     k = lambda **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), 0))
+    assert k() == "ttt_linear_fused"
+    assert k(residual_ln=1) == "ttt_linear_fused"
     assert k(io_dtype=0) == "ttt_linear_generic"
     assert k(d=32) == "ttt_linear_generic"
     assert k(d=256) is None
