@@ -18,7 +18,7 @@ def sources():
 
 
 def deps():
-    return sources() + sorted(glob.glob(os.path.join(HERE, "csrc", "*.h"))) + [
+    return sources() + sorted(glob.glob(os.path.join(HERE, "csrc", "*.h"))) + sorted(glob.glob(os.path.join(HERE, "csrc", "*.cuh"))) + [
         os.path.join(os.path.dirname(HERE), "include", "ttt.h")]
 
 

@@ -3,40 +3,40 @@
 // The method (damodev.csdn.net TTT article, sections 3.1 and 4.1-4.2; residual
 // LayerNorm of the lryc.cn TTT article, section 2.1): per (batch, head) the
 // fast weights (W, c) are updated once per mini-batch of 16 tokens, every
-// token's gradient taken at the mini-batch's starting weights, and each output
-// read with the weights after its own token's update:
+// token's gradient taken at the mini-batch's starting weights, and each
+// output read with the weights after its own token's update.  With
 //   P_n = K_n W_n + 1 c_n                        (key-side forward, 16 x 64)
 //   G_n = P_n - V_n  or  LNbwd(P_n; V_n - K_n)   (per-token gradient)
 //   W_{n+1} = W_n - K_n^T diag(eta_n) G_n,  c_{n+1} = c_n - eta_n^T G_n
-//   Z_n = f_out(Q_n W_n + 1 c_n - tril(Q_n K_n^T + 1) diag(eta_n) G_n).
+//   Z_n = f_out(Q_n W_n + 1 c_n - (tril(Q_n K_n^T + 1) diag(eta_n)) G_n)
+// the only sequential dependency is P_n -> G_n -> W_{n+1} -> P_{n+1}.  The
+// key-side product of the next mini-batch is re-associated exactly,
+//   P_{n+1} = (K_{n+1} W_n + 1 c_n) - ((K_{n+1} K_n^T + 1) diag(eta_n)) G_n,
+// so the sequential chain per mini-batch is G_n -> one 16 x 16 x 16 product ->
+// G_{n+1}; the d x d update and both d x d products are off that chain.
 //
-// The only sequential dependency is G_n -> P_{n+1}.  It is shortened with an
-// exact four-step lookahead: with C_{t,l} = K_t K_l^T + 1,
-//   P_t = (K_t W_{t-4} + 1 c_{t-4}) - sum_{l=t-4}^{t-1} C_{t,l} diag(eta_l) G_l.
-// The product with W_{t-4} and the corrections from G_{t-4}, G_{t-3} run on the
-// tcgen05 tensor cores well ahead of time; only the two newest corrections
-// (16 x 16 x 64 each) and the LayerNorm backward sit on the chain, on warp MMAs.
-//
-// B300 design.  One CTA (14 warps) per (batch, head):
-//   * warp 12 streams 64-token stages of K, Q, V (TMA, 128-byte swizzle) and
-//     eta (bulk copy) into a 5-deep ring;
-//   * warp 13 issues every tcgen05 MMA: per stage the Gram block
-//     [K_s; Q_s] [K_{s-1}; K_s]^T; per step the state update
-//     W~^T -= (eta G)^T [K | 1] into one of two TMEM accumulators (W~ = [W; c],
-//     alternating so that reading one never stalls the next update), the
-//     products K_{n+4} W~_n and Q_n W~_n (bias folded in through a column of
-//     ones), the output correction and the lookahead corrections;
-//   * warps 0-3 ("chain") each own 16 output features: they finish P_n, compute
-//     G_n with the LayerNorm statistics reduced in fp32 (warp shuffles and one
-//     shared-memory exchange, and publish (eta G_n)^T for the tensor cores;
-//   * warps 4-7 convert the fp32 TMEM state into the bf16 operand tile the
-//     products read, and cut the Gram blocks into masked bf16 operands;
-//   * warps 8-11 (one per mini-batch of a stage) finish the outputs: residual
-//     LayerNorm, bf16 conversion, TMA store.
-// TMEM (512 columns): two W~^T accumulators (2 x 80), six lookahead
-// accumulators (6 x 16), two output accumulators (2 x 64), one Gram (128).
+// B300 design.  The scan is latency-bound: 16 tokens of one (batch, head) per
+// step, each step waiting on the last.  One CTA per (batch, head), five warps:
+//   * warp 4 streams 64-token stages of Q, K, V (TMA, 128-byte swizzle) and
+//     eta (bulk copy) into a 6-deep shared-memory ring, mbarrier-synchronised;
+//   * warps 0-3 each own 16 output features.  W^T lives in registers as fp32
+//     warp-MMA accumulators for the whole scan; every contraction is a
+//     bf16 m16n8k16 MMA on register fragments, so the recurrence never leaves
+//     the register file.  (A tcgen05 MMA pays ~80 issue cycles and a ~250-cycle
+//     round trip through TMEM and an mbarrier; a dependent warp MMA takes ~21
+//     cycles.  On a chain of 16-token steps the warp MMA wins.)
+//   * each step is one straight-line block on either side of a single named
+//     barrier, so the compiler can fill the latency of the LayerNorm chain
+//     (shuffle rounds, the barrier, rsqrt) with the off-chain work: the
+//     deferred state update, the two d x d products, the 16 x 16 input blocks
+//     of the next mini-batch and the previous step's output;
+//   * LayerNorm statistics are reduced with a warp reduce-scatter plus one
+//     shared-memory exchange; the backward statistics use one pass (sums of z,
+//     z^2, g^2 z, g^2 z^2, g b' z, g b' with b' = beta - v + k), all in fp32;
+//   * Z tiles are transposed back with stmatrix into a swizzled staging ring
+//     and written by TMA stores.
 // Every mbarrier wait is bounded; a wait that runs out sets the library's
-// failure flag, and from then on no role waits again, so the kernel finishes.
+// failure flag and the kernel finishes without waiting again.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -50,719 +50,55 @@
 namespace ttt {
 namespace {
 
-constexpr int D = 64;          // head dim
-constexpr int MB = 16;         // mini-batch
-constexpr int ST = 64;         // tokens per pipeline stage
-constexpr int TPS = ST / MB;   // mini-batches per stage
-constexpr int NSS = 5;         // stage ring depth
-constexpr int XR = 6;          // lookahead accumulators
-constexpr int GR = 4;          // (eta G)^T tiles
-constexpr int PS = 3;          // prepared-operand slots (one per stage)
-constexpr int YR = 2;          // output accumulators
-constexpr int kWarps = 14;
-constexpr int kThreads = kWarps * 32;
-constexpr int kAux0 = 4, kEpi0 = 8, kProd = 12, kIssue = 13;
-
-constexpr uint32_t TM_W = 0;     // 2 x 80 columns: W^T (64) and the bias tile (column 64)
-constexpr uint32_t TM_X = 160;   // XR x 16
-constexpr uint32_t TM_Y = 256;   // YR x 64
-constexpr uint32_t TM_G = 384;   // 128
-constexpr uint32_t TM_COLS = 512;
-
-constexpr uint32_t kTileBytes = ST * D * 2;   // 8 KB
+constexpr int D = 64;           // head dim
+constexpr int MB = 16;          // mini-batch
+constexpr int ST = 64;          // tokens per pipeline stage
+constexpr int TPS = ST / MB;    // mini-batches per stage
+constexpr int NSS = 6;          // stages in the ring
+constexpr int NZ = 4;           // Z staging tiles
+constexpr int kMathThreads = 128;
+constexpr int kThreads = 160;
+constexpr uint32_t kStageTileBytes = ST * D * 2;   // 8 KB
 
 struct __align__(1024) Smem {
-    __nv_bfloat16 stage[NSS][3][ST * D];     // [slot][0 K, 1 Q, 2 V], 128-byte swizzled rows
-    __nv_bfloat16 wt[2][D * D];              // bf16 W^T [j][i], 128-byte swizzle
-    __nv_bfloat16 zst[4][MB * D];            // Z staging, one per epilogue warp
-    __nv_bfloat16 cb[PS][TPS][2][MB * MB];   // lookahead B tiles [t][s]: [0] C_{t,t-4}, [1] C_{t,t-3}
-    __nv_bfloat16 bout[PS][ST * MB];         // output-correction A tiles [t'][s]
-    __nv_bfloat16 gt[GR][D * MB];            // (eta G)^T [j][s]
-    __nv_bfloat16 ct[2][D * MB];             // bias tile [j][16], column 0 = c_j
-    __nv_bfloat16 onesA[ST * MB];            // [t'][16], column 0 = 1
-    __nv_bfloat16 onesB[MB * MB];            // [t][16], column 0 = 1
-    __nv_bfloat16 onesR[MB * MB];            // [n][16], row 0 = 1
-    uint32_t cfrag[PS][TPS][2][32][4];       // chain A fragments: [0] -C_{t,t-2}, [1] -C_{t,t-1}
-    float xtr[4][MB * 20];                   // chain transposes
-    float stats[3][MB][8];                   // per-token LayerNorm sums
+    __nv_bfloat16 q[NSS][ST * D];
+    __nv_bfloat16 k[NSS][ST * D];
+    __nv_bfloat16 v[NSS][ST * D];
+    __nv_bfloat16 z[NZ][MB * D];
     float eta[NSS][ST];
-    unsigned long long full[NSS], empty[NSS];
-    unsigned long long gram_full, prep_full[PS], prep_free[PS];
-    unsigned long long wbuf_full[2], wbuf_free[2], wupd_full[2];
-    unsigned long long x_full[XR];
-    unsigned long long g_full[GR], g_free[GR];
-    unsigned long long z_full[TPS], y_free[YR];   // z_full: one per epilogue warp
-    unsigned long long fin;
-    uint32_t tmem;
+    uint32_t sfrag[3][2][2][32][2];   // [mini-batch % 3][0: chain, 1: output][s half][lane][t n-tile]
+    float red[2][MB][8][4];           // [parity][token][quantity][warp]
+    float zred[2][MB][2][4];          // [parity][token][sum z, sum z^2][warp]
+    unsigned long long full[NSS];
+    unsigned long long empty[NSS];
     int abort_flag;
 };
 
 struct Params {
-    int H, L, N, NST, init_per_batch;
+    int H, L, ln;
     float eps;
-    long long wait_ns;
-    int withhold_loads;
+    long long wait_ns;       // bound of every mbarrier wait
+    int withhold_loads;      // test hook: the producer issues no copies
     const float *eta, *W0, *b0, *gamma, *beta;
     float *Wf, *bf;
     unsigned int *status;
+    int init_per_batch;
 };
 
-static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory budget");
-
+// Bound of the final wait for copies still in flight (they land in microseconds).
 constexpr long long kDrainNs = 1000000000ll;
 constexpr long long kDefaultWaitNs = 1000000000ll;
 
-// Bounded waits sharing one abort flag: once any wait has run out, every
-// later wait returns at once and the roles run to the end without blocking.
-// The first wait to run out records, in the failure flag, which barrier of
-// which role gave up at which step (bit 0: timeout; bits 8-19: step mod 4096;
-// bits 20-27: barrier index in the shared-memory block; bits 28-31: role).
-struct Waiter {
-    int *abort_flag;
-    unsigned int *status;
-    long long ns;
-    const unsigned long long *bar0;
-    unsigned int role;
-    __device__ __forceinline__ bool operator()(unsigned long long *bar, uint32_t parity, int step = 0) const
-    {
-        if (*(volatile int *)abort_flag) return false;
-        const uint32_t a = ptx::smem_addr(bar);
-        if (ptx::mbar_try_wait(a, parity)) return true;
-        const unsigned long long t0 = ptx::globaltimer_ns();
-        for (;;) {
-            for (int i = 0; i < 32; ++i)
-                if (ptx::mbar_try_wait(a, parity)) return true;
-            if (*(volatile int *)abort_flag) return false;
-            if ((long long)(ptx::globaltimer_ns() - t0) > ns) break;
-        }
-        if (atomicExch(abort_flag, 1) == 0) {
-            const unsigned int idx = (unsigned int)(bar - bar0) & 0xffu;
-            atomicCAS(status, 0u, kStatusTimeout | ((unsigned int)(step & 0xfff) << 8) | (idx << 20) |
-                                      (role << 28));
-            atomicOr(status, kStatusTimeout);
-        }
-        return false;
-    }
-};
-
-__device__ __forceinline__ uint32_t bar_addr(unsigned long long *b) { return ptx::smem_addr(b); }
-
-// ---------------------------------------------------------------------------
-// roles
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ void producer(Smem &s, const Params &p, const CUtensorMap *tmK,
-                                         const CUtensorMap *tmQ, const CUtensorMap *tmV, int bh,
-                                         const Waiter &wait)
+// Slow path of a bounded wait, out of line so the step stays small in the
+// instruction cache.  Returns false when the wait ran out (or another one did).
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, long long limit, int *abort_flag,
+                                       unsigned int *status)
 {
-    ptx::prefetch_tmap(tmK);
-    ptx::prefetch_tmap(tmQ);
-    ptx::prefetch_tmap(tmV);
-    const float *eta_bh = p.eta + (size_t)bh * p.L;
-    int issued = 0;
-    for (int st = 0; st < (p.withhold_loads ? 0 : p.NST); ++st) {
-        const int b = st % NSS;
-        if (st >= NSS && !wait(&s.empty[b], ((st / NSS) - 1) & 1, st)) break;
-        const int ntok = min(ST, p.L - st * ST);
-        const uint32_t fb = bar_addr(&s.full[b]);
-        ptx::mbar_arrive_expect_tx(fb, 3 * kTileBytes + ntok * 4);
-        ptx::tma_load_3d(ptx::smem_addr(s.stage[b][0]), tmK, fb, 0, st * ST, bh);
-        ptx::tma_load_3d(ptx::smem_addr(s.stage[b][1]), tmQ, fb, 0, st * ST, bh);
-        ptx::tma_load_3d(ptx::smem_addr(s.stage[b][2]), tmV, fb, 0, st * ST, bh);
-        ptx::bulk_load(ptx::smem_addr(s.eta[b]), eta_bh + st * ST, ntok * 4, fb);
-        issued = st + 1;
-    }
-    // every copy issued must land before the CTA may exit
-    for (int st = max(0, issued - NSS); st < issued; ++st)
-        ptx::mbar_wait_bounded(bar_addr(&s.full[st % NSS]), (st / NSS) & 1, kDrainNs);
-}
-
-__device__ __forceinline__ void issuer(Smem &s, const Params &p, uint32_t tm, const Waiter &wait)
-{
-    const int N = p.N, NST = p.NST;
-    constexpr uint32_t idG = ptx::idesc_bf16(128, 64, false, false, false);
-    constexpr uint32_t idX = ptx::idesc_bf16(64, 16, false, false, false);
-    constexpr uint32_t idY = ptx::idesc_bf16(64, 64, false, false, false);
-    constexpr uint32_t idW = ptx::idesc_bf16(64, 64, false, true, true);
-    constexpr uint32_t idC = ptx::idesc_bf16(64, 16, false, false, true);
-    constexpr uint32_t idO = ptx::idesc_bf16(64, 64, false, false, true);
-    constexpr uint32_t idK = ptx::idesc_bf16(64, 16, false, false, true);
-    const uint32_t onesA = ptx::smem_addr(s.onesA), onesB = ptx::smem_addr(s.onesB);
-    const uint32_t onesR = ptx::smem_addr(s.onesR);
-
-    auto ktile = [&](int st) { return ptx::smem_addr(s.stage[st % NSS][0]); };
-    auto qtile = [&](int st) { return ptx::smem_addr(s.stage[st % NSS][1]); };
-    auto gram = [&](int st) {
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = ptx::sdesc_sw128(ktile(st) + 32 * kk);   // [K_st; Q_st]: 128 rows
-            ptx::tc_mma(tm + TM_G + 64, a, ptx::sdesc_sw128(ktile(st) + 32 * kk), idG, kk > 0);
-            if (st > 0)
-                ptx::tc_mma(tm + TM_G, a, ptx::sdesc_sw128(ktile(st - 1) + 32 * kk), idG, kk > 0);
-        }
-        ptx::tc_commit(bar_addr(&s.gram_full));
-    };
-    // X''_t = W~_wb^T [K_t | 1]^T  (features x tokens)
-    auto product_x = [&](int t, int wb) {
-        const uint32_t d = tm + TM_X + 16 * (t % XR);
-        const uint32_t kb = ktile(t / TPS) + (t % TPS) * MB * 128;
-        const uint32_t w = ptx::smem_addr(s.wt[wb]);
-        for (int kk = 0; kk < 4; ++kk)
-            ptx::tc_mma(d, ptx::sdesc_sw128(w + 32 * kk), ptx::sdesc_sw128(kb + 32 * kk), idX, kk > 0);
-        ptx::tc_mma(d, ptx::sdesc_sw32(ptx::smem_addr(s.ct[wb])), ptx::sdesc_sw32(onesB), idX, 1);
-    };
-
-    // ---- prologue: Gram of stage 0, lookahead products of targets 0..3 from W_0
-    if (wait(&s.full[0], 0)) ptx::tc_fence_after();
-    gram(0);
-    if (wait(&s.wbuf_full[0], 0)) ptx::tc_fence_after();
-    for (int t = 0; t < min(4, N); ++t) product_x(t, 0);
-    for (int t = 0; t < min(3, N); ++t) ptx::tc_commit(bar_addr(&s.x_full[t % XR]));
-    wait(&s.prep_full[0], 0);
-    if (NST > 1) {
-        if (wait(&s.full[1 % NSS], 0)) ptx::tc_fence_after();
-        gram(1);
-    }
-
-    for (int n = 0; n < N; ++n) {
-        const int st = n / TPS, m = n % TPS;
-        // ---- (A1) as soon as G_n is published: the state update (critical for the
-        // products four steps ahead) and the last tensor-core correction of target n + 3
-        if (wait(&s.g_full[n % GR], (n / GR) & 1, n)) ptx::tc_fence_after();
-        const uint32_t g_n = ptx::smem_addr(s.gt[n % GR]);
-        {
-            // W~_{n+1} = W~_{n-1} - (eta G)^T [K | 1] for l = n-1, n (accumulator (n+1) % 2);
-            // the converter finished reading W~_{n-1} before W~_n was released to step n's products
-            const uint32_t d = tm + TM_W + 80 * ((n + 1) & 1);
-            for (int l = max(0, n - 1); l <= n; ++l) {
-                const uint32_t gl = ptx::smem_addr(s.gt[l % GR]);
-                const uint32_t kb = ktile(l / TPS) + (l % TPS) * MB * 128;
-                ptx::tc_mma(d, ptx::sdesc_sw32(gl), ptx::sdesc_sw128_mn(kb), idW, 1);
-                ptx::tc_mma(d + 64, ptx::sdesc_sw32(gl), ptx::sdesc_sw32(onesR), idC, 1);
-            }
-            ptx::tc_commit(bar_addr(&s.wupd_full[(n + 1) & 1]));
-        }
-        if (n + 3 < N) {
-            const int t = n + 3;
-            ptx::tc_mma(tm + TM_X + 16 * (t % XR), ptx::sdesc_sw32(g_n),
-                        ptx::sdesc_sw32(ptx::smem_addr(s.cb[(t / TPS) % PS][t % TPS][1])), idK, 1);
-            ptx::tc_commit(bar_addr(&s.x_full[t % XR]));
-        }
-        // ---- (B) products of W~_n: the output of step n and the lookahead of target n + 4
-        if (m == 0) {
-            if (st + 1 < NST) wait(&s.prep_full[(st + 1) % PS], ((st + 1) / PS) & 1, n);
-            if (st + 2 < NST) {
-                if (wait(&s.full[(st + 2) % NSS], ((st + 2) / NSS) & 1, n)) ptx::tc_fence_after();
-                gram(st + 2);
-            }
-        }
-        const int wb = n & 1;
-        if (n > 0) wait(&s.wbuf_full[wb], (n >> 1) & 1, n);
-        if (n >= YR) wait(&s.y_free[n % YR], ((n - YR) / YR) & 1, n);
-        ptx::tc_fence_after();
-        {
-            // Y_n = [Q_stage | 1] W~_n  (stage tokens x features; rows of mini-batch m are valid)
-            const uint32_t d = tm + TM_Y + 64 * (n % YR);
-            const uint32_t w = ptx::smem_addr(s.wt[wb]);
-            for (int kk = 0; kk < 4; ++kk)
-                ptx::tc_mma(d, ptx::sdesc_sw128(qtile(st) + 32 * kk), ptx::sdesc_sw128(w + 32 * kk), idY,
-                            kk > 0);
-            ptx::tc_mma(d, ptx::sdesc_sw32(onesA), ptx::sdesc_sw32(ptx::smem_addr(s.ct[wb])), idY, 1);
-        }
-        if (n + 4 < N) product_x(n + 4, wb);
-        ptx::tc_commit(bar_addr(&s.wbuf_free[wb]));
-        // ---- (A2) the terms of G_n that need this step's products: output correction
-        // Y_n -= tril(Q K^T + 1) (eta G), and the first correction of target n + 4
-        ptx::tc_mma(tm + TM_Y + 64 * (n % YR), ptx::sdesc_sw32(ptx::smem_addr(s.bout[st % PS])),
-                    ptx::sdesc_sw32(g_n), idO, 1);
-        ptx::tc_commit(bar_addr(&s.z_full[n % TPS]));
-        if (n + 4 < N) {
-            const int t = n + 4;
-            ptx::tc_mma(tm + TM_X + 16 * (t % XR), ptx::sdesc_sw32(g_n),
-                        ptx::sdesc_sw32(ptx::smem_addr(s.cb[(t / TPS) % PS][t % TPS][0])), idK, 1);
-        }
-        if (n >= 1) ptx::tc_commit(bar_addr(&s.g_free[(n - 1) % GR]));
-        if (m == TPS - 1 || n == N - 1) ptx::tc_commit(bar_addr(&s.prep_free[st % PS]));
-        if (n >= 1 && (n - 1) % TPS == TPS - 1) ptx::tc_commit(bar_addr(&s.empty[((n - 1) / TPS) % NSS]));
-        if (n == N - 1) ptx::tc_commit(bar_addr(&s.empty[st % NSS]));
-    }
-    // every MMA must be complete before the tensor memory is released
-    ptx::tc_commit(bar_addr(&s.fin));
-    ptx::mbar_wait_bounded(bar_addr(&s.fin), 0, kDrainNs);
-}
-
-// Converter + operand preparation (warps 4-7; quarter q of the TMEM lanes).
-template <bool LN>
-__device__ __forceinline__ void aux(Smem &s, const Params &p, uint32_t tm, int q, int bh,
-                                    const Waiter &wait)
-{
-    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-    const int N = p.N;
-    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-
-    // W^T fragment registers (rows 16q + g (+8), columns 8k + 2c (+1)) -> bf16 tile
-    auto write_wtile = [&](int buf, const float *w) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            pk[2 * k] = ptx::pack_bf16(w[4 * k], w[4 * k + 1]);
-            pk[2 * k + 1] = ptx::pack_bf16(w[4 * k + 2], w[4 * k + 3]);
-        }
-        const uint32_t base = ptx::smem_addr(s.wt[buf]);
-        const int sel = lane >> 3, r = lane & 7;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int k = 2 * i + (sel >> 1), row = 16 * q + 8 * (sel & 1) + r;
-            ptx::stsm_x4(base + ptx::sw128(row, k), pk + 4 * i);
-        }
-    };
-    auto write_bias = [&](int buf, float c_lo, float c_hi) {
-        if (c == 0) {
-            __nv_bfloat16 *ct = s.ct[buf];
-            const int r0 = 16 * q + g, r1 = r0 + 8;
-            *reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<unsigned char *>(ct) + ptx::sw32(r0, 0)) =
-                __float2bfloat16_rn(c_lo);
-            *reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<unsigned char *>(ct) + ptx::sw32(r1, 0)) =
-                __float2bfloat16_rn(c_hi);
-        }
-    };
-
-    // ---- initial state into both TMEM accumulators and the first bf16 tile
-    {
-        const size_t init = p.init_per_batch ? (size_t)bh : (size_t)(bh % p.H);
-        const float *W0 = p.W0 + init * D * D;
-        const float *b0 = p.b0 + init * D;
-        float w[32];
-        const int j0 = 16 * q + g, j1 = j0 + 8;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int i = 8 * k + 2 * c;
-            w[4 * k] = W0[i * D + j0];
-            w[4 * k + 1] = W0[(i + 1) * D + j0];
-            w[4 * k + 2] = W0[i * D + j1];
-            w[4 * k + 3] = W0[(i + 1) * D + j1];
-        }
-        const float c_lo = b0[j0], c_hi = b0[j1];
-        uint32_t wr[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) wr[i] = __float_as_uint(w[i]);
-        uint32_t cr[4] = {c == 0 ? __float_as_uint(c_lo) : 0u, 0u, c == 0 ? __float_as_uint(c_hi) : 0u, 0u};
-        for (int b = 0; b < 2; ++b) {
-            ptx::tc_st16_x8(tm + TM_W + 80 * b + lane_base, wr);
-            ptx::tc_st16_x1(tm + TM_W + 80 * b + 64 + lane_base, cr);
-        }
-        ptx::tc_wait_st();
-        write_wtile(0, w);
-        write_bias(0, c_lo, c_hi);
-        ptx::fence_proxy_async();
-        __syncwarp();
-        ptx::tc_fence_before();
-        if (lane == 0) ptx::mbar_arrive(bar_addr(&s.wbuf_full[0]));
-    }
-
-    // ---- operand preparation for target t (blocks whose rows live in this quarter)
-    auto prep = [&](int t) {
-        const int st = t / TPS, mt = t % TPS, ps = st % PS;
-        if (mt == 0) {
-            if (st >= PS) wait(&s.prep_free[ps], ((st / PS) - 1) & 1, t);
-            if (wait(&s.gram_full, st & 1, t)) ptx::tc_fence_after();
-        }
-        if (q == (mt >> 1)) {
-            // K_t rows: C_{t,l} = K_t K_l^T + 1 for l = t-1 .. t-4
-            const uint32_t row_base = (uint32_t)(16 * mt) << 16;
-            for (int dl = 1; dl <= 4; ++dl) {
-                const int l = t - dl;
-                if (l < 0) break;
-                const uint32_t col = (l >= st * TPS) ? 64 + 16 * (l % TPS) : 16 * (l % TPS);
-                uint32_t r[8];
-                ptx::tc_ld16_x2(tm + TM_G + col + row_base, r);
-                ptx::tc_wait_ld();
-                float v[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]) + 1.f;
-                if (dl <= 2) {
-                    uint4 a;
-                    a.x = ptx::pack_bf16(-v[0], -v[1]);
-                    a.y = ptx::pack_bf16(-v[2], -v[3]);
-                    a.z = ptx::pack_bf16(-v[4], -v[5]);
-                    a.w = ptx::pack_bf16(-v[6], -v[7]);
-                    *reinterpret_cast<uint4 *>(s.cfrag[ps][mt][dl == 1 ? 1 : 0][lane]) = a;
-                } else {
-                    uint32_t a[4] = {ptx::pack_bf16(v[0], v[1]), ptx::pack_bf16(v[2], v[3]),
-                                     ptx::pack_bf16(v[4], v[5]), ptx::pack_bf16(v[6], v[7])};
-                    const int sel = lane >> 3, rr = lane & 7;
-                    const uint32_t base = ptx::smem_addr(s.cb[ps][mt][dl == 4 ? 0 : 1]);
-                    ptx::stsm_x4(base + ptx::sw32(rr + 8 * (sel & 1), sel >> 1), a);
-                }
-            }
-        } else if (q == 2 + (mt >> 1)) {
-            // Q_t rows: tril(Q_t K_t^T + 1) into rows 16 mt of the stage's output tile
-            const uint32_t row_base = (uint32_t)(64 + 16 * mt) << 16;
-            uint32_t r[8];
-            ptx::tc_ld16_x2(tm + TM_G + 64 + 16 * mt + row_base, r);
-            ptx::tc_wait_ld();
-            float v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int tt = g + 8 * ((i >> 1) & 1), ss = 2 * c + (i & 1) + 8 * (i >> 2);
-                v[i] = ss <= tt ? __uint_as_float(r[i]) + 1.f : 0.f;
-            }
-            uint32_t a[4] = {ptx::pack_bf16(v[0], v[1]), ptx::pack_bf16(v[2], v[3]),
-                             ptx::pack_bf16(v[4], v[5]), ptx::pack_bf16(v[6], v[7])};
-            const int sel = lane >> 3, rr = lane & 7;
-            ptx::stsm_x4(ptx::smem_addr(s.bout[ps]) + ptx::sw32(16 * mt + rr + 8 * (sel & 1), sel >> 1), a);
-        }
-        if (mt == TPS - 1 || t == N - 1) {
-            ptx::fence_proxy_async();
-            __syncwarp();
-            ptx::tc_fence_before();
-            if (lane == 0) ptx::mbar_arrive(bar_addr(&s.prep_full[ps]));
-        }
-    };
-
-    for (int t = 0; t < min(N, 2 * TPS); ++t) prep(t);
-
-    for (int n = 0; n < N; ++n) {
-        // ---- W~_{n+1} (accumulator (n+1) % 2): bf16 operand tile, or the final state
-        const int b = (n + 1) & 1;
-        if (wait(&s.wupd_full[b], (n >> 1) & 1, n)) ptx::tc_fence_after();
-        uint32_t wr[32], cr[4];
-        ptx::tc_ld16_x8(tm + TM_W + 80 * b + lane_base, wr);
-        ptx::tc_ld16_x1(tm + TM_W + 80 * b + 64 + lane_base, cr);
-        ptx::tc_wait_ld();
-        float w[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = __uint_as_float(wr[i]);
-        const float c_lo = __uint_as_float(cr[0]), c_hi = __uint_as_float(cr[2]);
-        if (n + 1 < N) {
-            if (n >= 1) wait(&s.wbuf_free[b], ((n - 1) >> 1) & 1, n);
-            write_wtile(b, w);
-            write_bias(b, c_lo, c_hi);
-            ptx::fence_proxy_async();
-            __syncwarp();
-            ptx::tc_fence_before();
-            if (lane == 0) ptx::mbar_arrive(bar_addr(&s.wbuf_full[b]));
-        } else {
-            float *Wf = p.Wf + (size_t)bh * D * D;
-            const int j0 = 16 * q + g, j1 = j0 + 8;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int i = 8 * k + 2 * c;
-                Wf[i * D + j0] = w[4 * k];
-                Wf[(i + 1) * D + j0] = w[4 * k + 1];
-                Wf[i * D + j1] = w[4 * k + 2];
-                Wf[(i + 1) * D + j1] = w[4 * k + 3];
-            }
-            if (c == 0) {
-                p.bf[(size_t)bh * D + j0] = c_lo;
-                p.bf[(size_t)bh * D + j1] = c_hi;
-            }
-        }
-        if (n + 2 * TPS < N) prep(n + 2 * TPS);
-    }
-}
-
-// Chain warps 0-3: quarter q owns output features 16q .. 16q + 15.
-template <bool LN>
-__device__ __forceinline__ void chain(Smem &s, const Params &p, uint32_t tm, int q, const Waiter &wait)
-{
-    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-    const int tid = threadIdx.x;   // 0..127
-    const int N = p.N, h = blockIdx.x % p.H;
-    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    // this thread's features: n-tile nt, element e: 16q + 8 nt + 2c + e
-    float ga[2][2], be[2][2], g2[2][2];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int j = 16 * q + 8 * nt + 2 * c + e;
-            ga[nt][e] = LN ? p.gamma[(size_t)h * D + j] : 1.f;
-            be[nt][e] = LN ? p.beta[(size_t)h * D + j] : 0.f;
-            g2[nt][e] = ga[nt][e] * ga[nt][e];
-        }
-    float C1 = 0.f;
-    if (LN)
-        for (int j = 0; j < D; ++j) {
-            const float gj = p.gamma[(size_t)h * D + j];
-            C1 = fmaf(gj, gj, C1);
-        }
-    uint32_t gB1[4] = {0, 0, 0, 0}, gB2[4] = {0, 0, 0, 0};   // (eta G) B fragments of steps m-1, m-2
-    float *xt = s.xtr[q];
-
-    for (int m = 0; m < N; ++m) {
-        const int st = m / TPS, mt = m % TPS, slot = st % NSS, ps = st % PS;
-        if (mt == 0) {
-            if (wait(&s.full[slot], (st / NSS) & 1, m)) {
-            }
-            wait(&s.prep_full[ps], (st / PS) & 1, m);
-        }
-        // ---- X''_m (features x tokens in TMEM) -> token-major fragments
-        if (wait(&s.x_full[m % XR], (m / XR) & 1, m)) ptx::tc_fence_after();
-        uint32_t xr[8];
-        ptx::tc_ld16_x2(tm + TM_X + 16 * (m % XR) + lane_base, xr);
-        ptx::tc_wait_ld();
-        __syncwarp();
-        xt[(2 * c) * 20 + g] = __uint_as_float(xr[0]);
-        xt[(2 * c + 1) * 20 + g] = __uint_as_float(xr[1]);
-        xt[(2 * c) * 20 + g + 8] = __uint_as_float(xr[2]);
-        xt[(2 * c + 1) * 20 + g + 8] = __uint_as_float(xr[3]);
-        xt[(8 + 2 * c) * 20 + g] = __uint_as_float(xr[4]);
-        xt[(9 + 2 * c) * 20 + g] = __uint_as_float(xr[5]);
-        xt[(8 + 2 * c) * 20 + g + 8] = __uint_as_float(xr[6]);
-        xt[(9 + 2 * c) * 20 + g + 8] = __uint_as_float(xr[7]);
-        __syncwarp();
-        float pz[2][4];
-        {
-            const float2 a = *reinterpret_cast<const float2 *>(&xt[g * 20 + 2 * c]);
-            const float2 b = *reinterpret_cast<const float2 *>(&xt[(g + 8) * 20 + 2 * c]);
-            const float2 e = *reinterpret_cast<const float2 *>(&xt[g * 20 + 8 + 2 * c]);
-            const float2 f = *reinterpret_cast<const float2 *>(&xt[(g + 8) * 20 + 8 + 2 * c]);
-            pz[0][0] = a.x; pz[0][1] = a.y; pz[0][2] = b.x; pz[0][3] = b.y;
-            pz[1][0] = e.x; pz[1][1] = e.y; pz[1][2] = f.x; pz[1][3] = f.y;
-        }
-        // ---- V (and K) of this mini-batch in the same fragment layout
-        const int mrow = lane & 7, mat = lane >> 3;
-        const int vrow = 16 * mt + mrow + 8 * (mat & 1), vchunk = 2 * q + (mat >> 1);
-        uint32_t vr[4];
-        ptx::ldsm_x4(ptx::smem_addr(s.stage[slot][2]) + ptx::sw128(vrow, vchunk), vr);
-        float bp[2][4];   // LN: b' = gamma (beta - v + k);  plain: v
-        if (LN) {
-            uint32_t kr[4];
-            ptx::ldsm_x4(ptx::smem_addr(s.stage[slot][0]) + ptx::sw128(vrow, vchunk), kr);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint32_t vv = vr[2 * nt + hh], kk = kr[2 * nt + hh];
-                    bp[nt][2 * hh] = ga[nt][0] * (be[nt][0] - ptx::bf16_lo(vv) + ptx::bf16_lo(kk));
-                    bp[nt][2 * hh + 1] = ga[nt][1] * (be[nt][1] - ptx::bf16_hi(vv) + ptx::bf16_hi(kk));
-                }
-        } else {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    bp[nt][2 * hh] = ptx::bf16_lo(vr[2 * nt + hh]);
-                    bp[nt][2 * hh + 1] = ptx::bf16_hi(vr[2 * nt + hh]);
-                }
-        }
-        // ---- the two newest corrections: P -= C_{m,m-2} (eta G_{m-2}) + C_{m,m-1} (eta G_{m-1})
-        if (m >= 2) {
-            const uint4 a = *reinterpret_cast<const uint4 *>(s.cfrag[ps][mt][0][lane]);
-            const uint32_t af[4] = {a.x, a.y, a.z, a.w};
-            ptx::mma_bf16(pz[0], af, gB2[0], gB2[1]);
-            ptx::mma_bf16(pz[1], af, gB2[2], gB2[3]);
-        }
-        if (m >= 1) {
-            const uint4 a = *reinterpret_cast<const uint4 *>(s.cfrag[ps][mt][1][lane]);
-            const uint32_t af[4] = {a.x, a.y, a.z, a.w};
-            ptx::mma_bf16(pz[0], af, gB1[0], gB1[1]);
-            ptx::mma_bf16(pz[1], af, gB1[2], gB1[3]);
-        }
-        // ---- G_m
-        float gm[2][4];
-        if (LN) {
-            // per-token sums over this warp's 16 features, in fp32: partials over the
-            // thread's 4 features, then a butterfly over the 4 lanes of the quad
-            float sv[2][6];   // [token g / g+8][S1 z, S2 z^2, S3 g^2 z, S4 g^2 z^2, S5 b'z, S6 b']
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float a1 = 0.f, a2 = 0.f, a3 = 0.f, a4 = 0.f, a5 = 0.f, a6 = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float z = pz[nt][2 * hh + e], b = bp[nt][2 * hh + e];
-                        const float w = g2[nt][e] * z;
-                        a1 += z;
-                        a2 = fmaf(z, z, a2);
-                        a3 += w;
-                        a4 = fmaf(w, z, a4);
-                        a5 = fmaf(b, z, a5);
-                        a6 += b;
-                    }
-                sv[hh][0] = a1; sv[hh][1] = a2; sv[hh][2] = a3; sv[hh][3] = a4; sv[hh][4] = a5; sv[hh][5] = a6;
-            }
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int i = 0; i < 6; ++i) {
-                    sv[hh][i] += __shfl_xor_sync(0xffffffffu, sv[hh][i], 1);
-                    sv[hh][i] += __shfl_xor_sync(0xffffffffu, sv[hh][i], 2);
-                }
-            const int buf = m % 3;
-            ptx::st_shared_f32(ptx::smem_addr(&s.stats[(m + 1) % 3][0][0]) + 4 * tid, 0.f);
-            if (c == 0) {
-                const uint32_t sb = ptx::smem_addr(&s.stats[buf][0][0]);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int i = 0; i < 6; ++i) ptx::red_add_shared(sb + 4 * ((g + 8 * hh) * 8 + i), sv[hh][i]);
-            }
-            ptx::named_bar(1, 128);
-            float mu[2], al[2], bt[2], rr[2], de[2];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float4 a = *reinterpret_cast<const float4 *>(&s.stats[buf][g + 8 * hh][0]);
-                const float2 b = *reinterpret_cast<const float2 *>(&s.stats[buf][g + 8 * hh][4]);
-                const float S1 = a.x, S2 = a.y, S3 = a.z, S4 = a.w, S5 = b.x, S6 = b.y;
-                const float inv_d = 1.f / D;
-                const float u = S1 * inv_d;
-                const float var = fmaxf(fmaf(S2, inv_d, -u * u), 0.f);
-                const float r = rsqrtf(var + p.eps);
-                const float A3 = fmaf(-u, C1, S3);
-                const float A4 = fmaf(u * u, C1, fmaf(-2.f * u, S3, S4));
-                const float A5 = fmaf(-u, S6, S5);
-                const float m1 = fmaf(r, A3, S6) * inv_d;
-                const float m2 = fmaf(r * r, A4, r * A5) * inv_d;
-                mu[hh] = u;
-                al[hh] = r * r;
-                bt[hh] = r * r * m2;
-                rr[hh] = r;
-                de[hh] = r * m1;
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int hh = i >> 1, e = i & 1;
-                    const float coef = fmaf(al[hh], g2[nt][e], -bt[hh]);
-                    gm[nt][i] = fmaf(pz[nt][i] - mu[hh], coef, fmaf(rr[hh], bp[nt][i], -de[hh]));
-                }
-        } else {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) gm[nt][i] = pz[nt][i] - bp[nt][i];
-        }
-        // ---- eta G: B fragments for the next two steps, (eta G)^T tile for the tensor cores
-        const float eg = s.eta[slot][16 * mt + g], eh = s.eta[slot][16 * mt + g + 8];
-        uint32_t e4[4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            e4[2 * nt] = ptx::pack_bf16(eg * gm[nt][0], eg * gm[nt][1]);
-            e4[2 * nt + 1] = ptx::pack_bf16(eh * gm[nt][2], eh * gm[nt][3]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            gB2[i] = gB1[i];
-            gB1[i] = ptx::movm_t(e4[i]);
-        }
-        if (m >= GR) wait(&s.g_free[m % GR], ((m - GR) / GR) & 1, m);
-        {
-            const int sel = lane >> 3, rr = lane & 7;
-            ptx::stsm_x4_t(ptx::smem_addr(s.gt[m % GR]) + ptx::sw32(16 * q + 8 * (sel >> 1) + rr, sel & 1), e4);
-        }
-        ptx::fence_proxy_async();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_addr(&s.g_full[m % GR]));
-        if (mt == TPS - 1 || m == N - 1) {
-            if (lane == 0) {
-                ptx::mbar_arrive(bar_addr(&s.empty[slot]));
-                ptx::mbar_arrive(bar_addr(&s.prep_free[ps]));
-            }
-        }
-    }
-}
-
-// Epilogue warps 8-11: warp p finishes mini-batches n = p, p + 4, ...
-template <bool LN>
-__device__ __forceinline__ void epilogue(Smem &s, const Params &p, uint32_t tm, int pq,
-                                         const CUtensorMap *tmZ, int bh, const Waiter &wait)
-{
-    const int lane = threadIdx.x & 31, c = lane & 3;
-    const int N = p.N, h = bh % p.H;
-    const uint32_t lane_base = (uint32_t)(32 * pq) << 16;
-    float ga[16], be[16];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int j = 8 * k + 2 * c + e;
-            ga[2 * k + e] = LN ? p.gamma[(size_t)h * D + j] : 1.f;
-            be[2 * k + e] = LN ? p.beta[(size_t)h * D + j] : 0.f;
-        }
-    const uint32_t zb = ptx::smem_addr(s.zst[pq]);
-    const int sel = lane >> 3, r8 = lane & 7;
-    for (int n = pq; n < N; n += TPS) {
-        const int st = n / TPS, slot = st % NSS;
-        if (wait(&s.z_full[pq], (n / TPS) & 1, n)) ptx::tc_fence_after();
-        uint32_t zr[32];
-        ptx::tc_ld16_x8(tm + TM_Y + 64 * (n % YR) + lane_base, zr);
-        ptx::tc_wait_ld();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_addr(&s.y_free[n % YR]));
-        float z[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(zr[i]);
-        float o[32];
-        if (LN) {
-            wait(&s.full[slot], (st / NSS) & 1, n);
-            uint32_t qr[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                ptx::ldsm_x4(ptx::smem_addr(s.stage[slot][1]) +
-                                 ptx::sw128(16 * pq + r8 + 8 * (sel & 1), 2 * i + (sel >> 1)),
-                             qr + 4 * i);
-            float s1[2] = {0.f, 0.f}, s2[2] = {0.f, 0.f};
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const float a = z[4 * k + 2 * hh], b = z[4 * k + 2 * hh + 1];
-                    s1[hh] += a + b;
-                    s2[hh] = fmaf(a, a, fmaf(b, b, s2[hh]));
-                }
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                s1[hh] += __shfl_xor_sync(0xffffffffu, s1[hh], 1);
-                s2[hh] += __shfl_xor_sync(0xffffffffu, s2[hh], 1);
-                s1[hh] += __shfl_xor_sync(0xffffffffu, s1[hh], 2);
-                s2[hh] += __shfl_xor_sync(0xffffffffu, s2[hh], 2);
-            }
-            float mu[2], r[2];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                mu[hh] = s1[hh] * (1.f / D);
-                r[hh] = rsqrtf(fmaxf(fmaf(s2[hh], 1.f / D, -mu[hh] * mu[hh]), 0.f) + p.eps);
-            }
-            // q fragments: qr[4i + sel'] with sel' = (row half) + 2 (chunk parity); chunk k = 2i + (sel' >> 1)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint32_t qq = qr[4 * (k >> 1) + 2 * (k & 1) + hh];
-                    const float q0 = ptx::bf16_lo(qq), q1 = ptx::bf16_hi(qq);
-                    o[4 * k + 2 * hh] = q0 + fmaf(ga[2 * k] * (z[4 * k + 2 * hh] - mu[hh]), r[hh], be[2 * k]);
-                    o[4 * k + 2 * hh + 1] =
-                        q1 + fmaf(ga[2 * k + 1] * (z[4 * k + 2 * hh + 1] - mu[hh]), r[hh], be[2 * k + 1]);
-                }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = z[i];
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            pk[2 * k] = ptx::pack_bf16(o[4 * k], o[4 * k + 1]);
-            pk[2 * k + 1] = ptx::pack_bf16(o[4 * k + 2], o[4 * k + 3]);
-        }
-        if (lane == 0) ptx::bulk_wait_read<0>();
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            ptx::stsm_x4(zb + ptx::sw128(r8 + 8 * (sel & 1), 2 * i + (sel >> 1)), pk + 4 * i);
-        ptx::fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) {
-            ptx::tma_store_3d(tmZ, zb, 0, n * MB, bh);
-            ptx::bulk_commit();
-            ptx::mbar_arrive(bar_addr(&s.empty[slot]));
-        }
-    }
-    if (lane == 0) ptx::bulk_wait<0>();
+    if (*(volatile int *)abort_flag) return false;
+    if (ptx::mbar_wait_bounded(bar, parity, limit)) return true;
+    *(volatile int *)abort_flag = 1;
+    atomicOr(status, kStatusTimeout);
+    return false;
 }
 
 template <bool LN>
@@ -772,89 +108,522 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     Params p)
 {
     extern __shared__ unsigned char smem_raw[];
-    Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // align to 1024 B by offsetting the shared array itself (not through an integer
+    // cast), so that plain accesses to the block compile to shared-memory loads/stores
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    Smem &s = *reinterpret_cast<Smem *>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x, h = bh % p.H;
+    const int N = p.L / MB;                 // mini-batches
+    const int NST = (p.L + ST - 1) / ST;    // stages
 
     if (tid == 0) {
         for (int i = 0; i < NSS; ++i) {
-            ptx::mbar_init(bar_addr(&s.full[i]), 1);
-            ptx::mbar_init(bar_addr(&s.empty[i]), 9);   // issuer + 4 chain + 4 epilogue
+            ptx::mbar_init(ptx::smem_addr(&s.full[i]), 1);
+            ptx::mbar_init(ptx::smem_addr(&s.empty[i]), 1);
         }
-        ptx::mbar_init(bar_addr(&s.gram_full), 1);
-        for (int i = 0; i < PS; ++i) {
-            ptx::mbar_init(bar_addr(&s.prep_full[i]), 4);
-            ptx::mbar_init(bar_addr(&s.prep_free[i]), 5);   // 4 chain + issuer
-        }
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(bar_addr(&s.wbuf_full[i]), 4);
-            ptx::mbar_init(bar_addr(&s.wbuf_free[i]), 1);
-            ptx::mbar_init(bar_addr(&s.wupd_full[i]), 1);
-        }
-        for (int i = 0; i < XR; ++i) ptx::mbar_init(bar_addr(&s.x_full[i]), 1);
-        for (int i = 0; i < GR; ++i) {
-            ptx::mbar_init(bar_addr(&s.g_full[i]), 4);
-            ptx::mbar_init(bar_addr(&s.g_free[i]), 1);
-        }
-        for (int i = 0; i < TPS; ++i) ptx::mbar_init(bar_addr(&s.z_full[i]), 1);
-        for (int i = 0; i < YR; ++i) ptx::mbar_init(bar_addr(&s.y_free[i]), 1);
-        ptx::mbar_init(bar_addr(&s.fin), 1);
         s.abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp >= kAux0 && warp < kAux0 + 4) {
-        // constant operand tiles: zeroed bias tiles, columns of ones
-        const int t = tid - 32 * kAux0;   // 0..127
-        uint32_t *ct = reinterpret_cast<uint32_t *>(s.ct);
-        for (int i = t; i < 2 * D * MB / 2; i += 128) ct[i] = 0u;
-        uint32_t *oa = reinterpret_cast<uint32_t *>(s.onesA);
-        for (int i = t; i < ST * MB / 2; i += 128) oa[i] = 0u;
-        uint32_t *ob = reinterpret_cast<uint32_t *>(s.onesB);
-        for (int i = t; i < MB * MB / 2; i += 128) ob[i] = 0u;
-        uint32_t *orr = reinterpret_cast<uint32_t *>(s.onesR);
-        for (int i = t; i < MB * MB / 2; i += 128) orr[i] = 0u;
-        float *st = &s.stats[0][0][0];
-        for (int i = t; i < 3 * MB * 8; i += 128) st[i] = 0.f;
-    }
-    if (warp == kIssue) {
-        ptx::tmem_alloc(ptx::smem_addr(&s.tmem), TM_COLS);
-        ptx::tmem_relinquish();
-    }
     __syncthreads();
-    if (warp >= kAux0 && warp < kAux0 + 4) {
-        const int t = tid - 32 * kAux0;
-        const __nv_bfloat16 one = __float2bfloat16_rn(1.f);
-        unsigned char *oa = reinterpret_cast<unsigned char *>(s.onesA);
-        if (t < ST) *reinterpret_cast<__nv_bfloat16 *>(oa + ptx::sw32(t, 0)) = one;
-        unsigned char *ob = reinterpret_cast<unsigned char *>(s.onesB);
-        if (t < MB) *reinterpret_cast<__nv_bfloat16 *>(ob + ptx::sw32(t, 0)) = one;
-        unsigned char *orr = reinterpret_cast<unsigned char *>(s.onesR);
-        if (t < MB) *reinterpret_cast<__nv_bfloat16 *>(orr + ptx::sw32(0, t >> 3) + 2 * (t & 7)) = one;
-        ptx::fence_proxy_async();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    const uint32_t tm = s.tmem;
-    const unsigned int role = warp < 4 ? 1u : warp < kEpi0 ? 2u : warp < kProd ? 3u : warp == kProd ? 4u : 5u;
-    const Waiter wait{&s.abort_flag, p.status, p.wait_ns, s.full, role};
 
-    if (warp < 4) {
-        chain<LN>(s, p, tm, warp, wait);
-    } else if (warp < kEpi0) {
-        aux<LN>(s, p, tm, warp - kAux0, bh, wait);
-    } else if (warp < kProd) {
-        epilogue<LN>(s, p, tm, warp - kEpi0, &tmZ, bh, wait);
-    } else if (warp == kProd) {
-        if (lane == 0) producer(s, p, &tmK, &tmQ, &tmV, bh, wait);
-    } else {
-        if (lane == 0) issuer(s, p, tm, wait);
-        __syncwarp();
+    // ------------------------------------------------------------------ producer
+    if (warp == 4) {
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tmQ);
+            ptx::prefetch_tmap(&tmK);
+            ptx::prefetch_tmap(&tmV);
+            const float *eta_bh = p.eta + (size_t)bh * p.L;
+            int issued = 0;
+            for (int st = 0; st < (p.withhold_loads ? 0 : NST); ++st) {
+                const int b = st % NSS;
+                if (st >= NSS) {
+                    if (*(volatile int *)&s.abort_flag) break;
+                    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&s.empty[b]), ((st / NSS) - 1) & 1,
+                                                p.wait_ns)) {
+                        *(volatile int *)&s.abort_flag = 1;
+                        atomicOr(p.status, kStatusTimeout);
+                        break;
+                    }
+                }
+                const int ntok = min(ST, p.L - st * ST);
+                const uint32_t fb = ptx::smem_addr(&s.full[b]);
+                ptx::mbar_arrive_expect_tx(fb, 3 * kStageTileBytes + ntok * 4);
+                ptx::tma_load_3d(ptx::smem_addr(s.q[b]), &tmQ, fb, 0, st * ST, bh);
+                ptx::tma_load_3d(ptx::smem_addr(s.k[b]), &tmK, fb, 0, st * ST, bh);
+                ptx::tma_load_3d(ptx::smem_addr(s.v[b]), &tmV, fb, 0, st * ST, bh);
+                ptx::bulk_load(ptx::smem_addr(s.eta[b]), eta_bh + st * ST, ntok * 4, fb);
+                issued = st + 1;
+            }
+            // every copy issued must land before the CTA may exit
+            for (int st = max(0, issued - NSS); st < issued; ++st)
+                ptx::mbar_wait_bounded(ptx::smem_addr(&s.full[st % NSS]), (st / NSS) & 1, kDrainNs);
+        }
+        return;
     }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    if (warp == kIssue) ptx::tmem_dealloc(tm, TM_COLS);
+
+    // ------------------------------------------------------------------ math warps
+    const int g = lane >> 2, c = lane & 3, mrow = lane & 7, mat = lane >> 3;
+    const int j0 = warp * 16 + g, j1 = j0 + 8;      // this thread's two features
+    bool aborted = false;
+
+    auto wait_stage = [&](int st) {
+        if (aborted) return;
+        const uint32_t bar = ptx::smem_addr(&s.full[st % NSS]);
+        if (ptx::mbar_try_wait(bar, (st / NSS) & 1)) return;
+        aborted = !wait_slow(bar, (st / NSS) & 1, p.wait_ns, &s.abort_flag, p.status);
+    };
+    // shared-memory byte address of row `t` (mini-batch n) / 16-byte chunk of a stage tile
+    auto tile_addr = [&](const __nv_bfloat16 (*arr)[ST * D], int n, int t, int chunk) -> uint32_t {
+        return ptx::smem_addr(arr[(n / TPS) % NSS]) + ptx::sw128((n % TPS) * MB + t, chunk);
+    };
+    auto eta_at = [&](int n, int t) -> float { return s.eta[(n / TPS) % NSS][(n % TPS) * MB + t]; };
+
+    // ---- initial state: W^T rows j0/j1 as fp32 accumulators, c, LN params
+    float wt[8][4];
+    const size_t init = p.init_per_batch ? (size_t)bh : (size_t)h;
+    {
+        const float *W0 = p.W0 + init * D * D;
+#pragma unroll
+        for (int pt = 0; pt < 8; ++pt) {
+            const int i = pt * 8 + 2 * c;
+            wt[pt][0] = W0[i * D + j0];
+            wt[pt][1] = W0[(i + 1) * D + j0];
+            wt[pt][2] = W0[i * D + j1];
+            wt[pt][3] = W0[(i + 1) * D + j1];
+        }
+    }
+    float cb0 = p.b0[init * D + j0];
+    float cb1 = p.b0[init * D + j1];
+    float ga0 = 1.f, ga1 = 1.f, be0 = 0.f, be1 = 0.f, C1 = 0.f;
+    if (LN) {
+        ga0 = p.gamma[(size_t)h * D + j0];
+        ga1 = p.gamma[(size_t)h * D + j1];
+        be0 = p.beta[(size_t)h * D + j0];
+        be1 = p.beta[(size_t)h * D + j1];
+        // sum of gamma^2 over all features: this thread's two, then the warp, then the warps
+        float part = ga0 * ga0 + ga1 * ga1;
+        part += __shfl_xor_sync(0xffffffffu, part, 4);
+        part += __shfl_xor_sync(0xffffffffu, part, 8);
+        part += __shfl_xor_sync(0xffffffffu, part, 16);
+        if (lane == 0) s.red[0][0][0][warp] = part;
+        ptx::named_bar(1, kMathThreads);
+        const float4 w4 = *reinterpret_cast<const float4 *>(s.red[0][0][0]);
+        C1 = (w4.x + w4.y) + (w4.z + w4.w);
+        ptx::named_bar(1, kMathThreads);
+    }
+    const float g20 = ga0 * ga0, g21 = ga1 * ga1;
+
+    uint32_t wa[4][4];   // bf16 A fragments of W^T, k-steps of 16 input features
+    auto pack_w = [&]() {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            wa[q][0] = ptx::pack_bf16(wt[2 * q][0], wt[2 * q][1]);
+            wa[q][1] = ptx::pack_bf16(wt[2 * q][2], wt[2 * q][3]);
+            wa[q][2] = ptx::pack_bf16(wt[2 * q + 1][0], wt[2 * q + 1][1]);
+            wa[q][3] = ptx::pack_bf16(wt[2 * q + 1][2], wt[2 * q + 1][3]);
+        }
+    };
+
+    // acc[u][*] = W^T X_n^T + c for a 16-token tile X of mini-batch n
+    auto product = [&](float (*acc)[4], const __nv_bfloat16 (*arr)[ST * D], int n) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            acc[u][0] = cb0; acc[u][1] = cb0; acc[u][2] = cb1; acc[u][3] = cb1;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // matrices: (t-block 0, i-chunk 2q), (t0, 2q+1), (t1, 2q), (t1, 2q+1)
+            uint32_t r[4];
+            ptx::ldsm_x4(tile_addr(arr, n, (mat >> 1) * 8 + mrow, 2 * q + (mat & 1)), r);
+            ptx::mma_bf16(acc[0], wa[q], r[0], r[1]);
+            ptx::mma_bf16(acc[1], wa[q], r[2], r[3]);
+        }
+    };
+
+    // C-fragment layout (rows = features j0/j1, cols = tokens) of a bf16 tile, transposed
+    auto load_T = [&](float (*out)[4], const __nv_bfloat16 (*arr)[ST * D], int n) {
+        // matrices: (t-block 0, j-block 0), (t0, j1), (t1, j0), (t1, j1)
+        uint32_t r[4];
+        ptx::ldsm_x4_t(tile_addr(arr, n, (mat >> 1) * 8 + mrow, warp * 2 + (mat & 1)), r);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            out[u][0] = ptx::bf16_lo(r[2 * u]);
+            out[u][1] = ptx::bf16_hi(r[2 * u]);
+            out[u][2] = ptx::bf16_lo(r[2 * u + 1]);
+            out[u][3] = ptx::bf16_hi(r[2 * u + 1]);
+        }
+    };
+
+    // Input-only 16x16 blocks of mini-batch m, as B fragments (k = source token s,
+    // n = target token t):
+    //   chain : eta_s (K_{m+1}[t] . K_m[s] + 1)
+    //   output: eta_s (Q_m[t] . K_m[s] + 1) [s <= t]
+    // warp w: matrix (w >> 1) (0 output, 1 chain), source half (w & 1).  Indices past
+    // the sequence are clamped: those blocks are computed but never used.
+    auto compute_sfrag = [&](int m) {
+        const int which = warp >> 1, half = warp & 1;   // which: 0 output, 1 chain
+        const int mm = min(m, N - 1);
+        const int na = which ? min(m + 1, N - 1) : mm;
+        const __nv_bfloat16(*A)[ST * D] = which ? s.k : s.q;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // A = rows t of the target tile, k = features 16q..16q+15
+            // matrices: (t0, chunk 2q), (t1, 2q), (t0, 2q+1), (t1, 2q+1)
+            uint32_t a[4];
+            ptx::ldsm_x4(tile_addr(A, na, (mat & 1) * 8 + mrow, 2 * q + (mat >> 1)), a);
+            // B = K_m rows s in [8 half, 8 half + 8), k = features: (s, chunk 2q), (s, 2q+1)
+            uint32_t b[4];
+            ptx::ldsm_x4(tile_addr(s.k, mm, half * 8 + mrow, 2 * q + (mat & 1)), b);
+            ptx::mma_bf16(acc, a, b[0], b[1]);
+        }
+        // acc: rows t = g (acc0,1), g + 8 (acc2,3); cols s = 8 half + 2c, +1
+        const int s0 = half * 8 + 2 * c;
+        const float e0 = eta_at(mm, s0), e1 = eta_at(mm, s0 + 1);
+        const bool causal = which == 0;   // mask s <= t on the output block
+        const float v0 = (causal && s0 > g) ? 0.f : e0 * (acc[0] + 1.f);
+        const float v1 = (causal && s0 + 1 > g) ? 0.f : e1 * (acc[1] + 1.f);
+        const float v2 = (causal && s0 > g + 8) ? 0.f : e0 * (acc[2] + 1.f);
+        const float v3 = (causal && s0 + 1 > g + 8) ? 0.f : e1 * (acc[3] + 1.f);
+        uint32_t *dst = s.sfrag[m % 3][which ? 0 : 1][half][lane];
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(ptx::pack_bf16(v0, v1), ptx::pack_bf16(v2, v3));
+    };
+    auto read_sfrag = [&](int m, int which, uint32_t (*b)[2]) {   // b[u][half]
+        const uint2 f0 = *reinterpret_cast<const uint2 *>(s.sfrag[m % 3][which][0][lane]);
+        const uint2 f1 = *reinterpret_cast<const uint2 *>(s.sfrag[m % 3][which][1][lane]);
+        b[0][0] = f0.x; b[1][0] = f0.y;
+        b[0][1] = f1.x; b[1][1] = f1.y;
+    };
+
+    // reduce-scatter of 8 per-token values (4 tokens x 2 quantities) over the 8 lanes
+    // sharing c; the lane keeps token t_own (below), quantity g & 1
+    auto rs8 = [&](const float *zs) -> float {
+        float b4[4], b2[2];
+        {
+            const bool hi = (lane >> 4) & 1;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float snd = hi ? zs[i] : zs[4 + i];
+                const float kp = hi ? zs[4 + i] : zs[i];
+                b4[i] = kp + __shfl_xor_sync(0xffffffffu, snd, 16);
+            }
+        }
+        {
+            const bool hi = (lane >> 3) & 1;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float snd = hi ? b4[i] : b4[2 + i];
+                const float kp = hi ? b4[2 + i] : b4[i];
+                b2[i] = kp + __shfl_xor_sync(0xffffffffu, snd, 8);
+            }
+        }
+        const bool hi = (lane >> 2) & 1;
+        const float snd = hi ? b2[0] : b2[1];
+        const float kp = hi ? b2[1] : b2[0];
+        return kp + __shfl_xor_sync(0xffffffffu, snd, 4);
+    };
+    // token of this lane after a reduce-scatter: tk = g / 2 -> t = 8 (tk / 2) + 2c + (tk % 2)
+    const int tk = g >> 1, qh = g & 1;
+    const int t_own = 8 * (tk >> 1) + 2 * c + (tk & 1);
+
+    // per-token output sums of Zbar (for the output LayerNorm), scattered into zred
+    auto zbar_stats = [&](const float (*zb)[4], int par) {
+        float zs[8];
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) {
+            const int u = tq >> 1, e = tq & 1;
+            const float z0 = zb[u][e], z1 = zb[u][2 + e];
+            zs[tq * 2 + 0] = z0 + z1;
+            zs[tq * 2 + 1] = fmaf(z0, z0, z1 * z1);
+        }
+        s.zred[par][t_own][qh][warp] = rs8(zs);
+    };
+
+    // Z_m = Q_m + LN(Zbar_m) (or Zbar_m) -> bf16 staging tile m % NZ
+    auto finish_z = [&](const float (*zb)[4], const float (*qv)[4], int m, int par) {
+        float z[2][4];
+        if (LN) {
+            const float4 w4 = *reinterpret_cast<const float4 *>(s.zred[par][t_own][qh]);
+            const float tot = (w4.x + w4.y) + (w4.z + w4.w);
+            const float oth = __shfl_xor_sync(0xffffffffu, tot, 4);
+            const float s1 = qh ? oth : tot, s2 = qh ? tot : oth;
+            const float mu = s1 * (1.f / D);
+            const float var = fmaxf(s2 * (1.f / D) - mu * mu, 0.f);
+            const float r = rsqrtf(var + p.eps);
+#pragma unroll
+            for (int tq = 0; tq < 4; ++tq) {
+                const float m_t = __shfl_sync(0xffffffffu, mu, c + 8 * tq);
+                const float r_t = __shfl_sync(0xffffffffu, r, c + 8 * tq);
+                const int u = tq >> 1, e = tq & 1;
+                z[u][e] = qv[u][e] + fmaf(ga0 * (zb[u][e] - m_t), r_t, be0);
+                z[u][2 + e] = qv[u][2 + e] + fmaf(ga1 * (zb[u][2 + e] - m_t), r_t, be1);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) z[u][i] = zb[u][i];
+        }
+        uint32_t r[4];
+        r[0] = ptx::pack_bf16(z[0][0], z[0][1]);
+        r[1] = ptx::pack_bf16(z[0][2], z[0][3]);
+        r[2] = ptx::pack_bf16(z[1][0], z[1][1]);
+        r[3] = ptx::pack_bf16(z[1][2], z[1][3]);
+        // matrices (j-block, t-block): (0,0), (1,0), (0,1), (1,1); stored rows = tokens
+        const uint32_t zaddr = ptx::smem_addr(s.z[m % NZ]);
+        ptx::stsm_x4_t(zaddr + ptx::sw128((mat >> 1) * 8 + mrow, warp * 2 + (mat & 1)), r);
+        ptx::fence_proxy_async();
+    };
+
+    // W^T += (-eta G_m)^T K_m, as 8 independent accumulator tiles
+    auto update_w = [&](const uint32_t *nge, int m) {
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+            // matrices (s-block, i-chunk): (0, 2pp), (1, 2pp), (0, 2pp+1), (1, 2pp+1)
+            uint32_t r[4];
+            ptx::ldsm_x4_t(tile_addr(s.k, m, (mat & 1) * 8 + mrow, 2 * pp + (mat >> 1)), r);
+            ptx::mma_bf16(wt[2 * pp], nge, r[0], r[1]);
+            ptx::mma_bf16(wt[2 * pp + 1], nge, r[2], r[3]);
+        }
+    };
+
+    // ---- prologue: P_0 = K_0 W_0 + c_0, input blocks of mini-batch 0
+    wait_stage(0);
+    if (N > TPS) wait_stage(1);
+    pack_w();
+    float pacc[2][4];
+    product(pacc, s.k, 0);
+    compute_sfrag(0);
+    ptx::named_bar(1, kMathThreads);
+
+    // carried between steps: the previous step's -eta G (deferred W update), its output
+    float zprev[2][4] = {}, qprev[2][4] = {};
+    uint32_t ngep[4] = {0u, 0u, 0u, 0u};
+
+    for (int n = 0; n < N; ++n) {
+        const int par = n & 1;
+        // the input blocks of mini-batch n + 1 read K_{n+2}: its stage must have landed
+        if ((n + 2) % TPS == 0 && n + 2 < N) wait_stage((n + 2) / TPS);
+
+        // ======== before the barrier ========
+        // deferred update with G_{n-1} (zero fragments at n = 0): W_n, then its bf16 copy
+        update_w(ngep, max(n - 1, 0));
+        pack_w();
+        // output product Y_n = W_n^T Q_n^T + c_n
+        float yacc[2][4];
+        product(yacc, s.q, n);
+        float vt[2][4], qt[2][4];
+        load_T(vt, s.v, n);
+        load_T(qt, s.q, n);
+        float gb[2][4];
+        if (LN) {
+            float kt[2][4];
+            load_T(kt, s.k, n);
+            // b'_j = beta_j - (v - k); gb = gamma * b'
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                gb[u][0] = ga0 * (be0 - vt[u][0] + kt[u][0]);
+                gb[u][1] = ga0 * (be0 - vt[u][1] + kt[u][1]);
+                gb[u][2] = ga1 * (be1 - vt[u][2] + kt[u][2]);
+                gb[u][3] = ga1 * (be1 - vt[u][3] + kt[u][3]);
+            }
+            // per-token partial sums over this thread's two features
+            float vs[24];
+#pragma unroll
+            for (int t4 = 0; t4 < 4; ++t4) {
+                const int u = t4 >> 1, e = t4 & 1;
+                const float z0 = pacc[u][e], z1 = pacc[u][2 + e];
+                const float a0 = g20 * z0, a1 = g21 * z1;
+                vs[t4 * 6 + 0] = z0 + z1;
+                vs[t4 * 6 + 1] = fmaf(z0, z0, z1 * z1);
+                vs[t4 * 6 + 2] = a0 + a1;
+                vs[t4 * 6 + 3] = fmaf(a0, z0, a1 * z1);
+                vs[t4 * 6 + 4] = fmaf(gb[u][e], z0, gb[u][2 + e] * z1);
+                vs[t4 * 6 + 5] = gb[u][e] + gb[u][2 + e];
+            }
+            // reduce-scatter over the 8 lanes sharing c (lane bits 4, 3, 2)
+            float a12[12], a6[6], a3[3];
+            {
+                const bool hi = (lane >> 4) & 1;
+#pragma unroll
+                for (int i = 0; i < 12; ++i) {
+                    const float snd = hi ? vs[i] : vs[12 + i];
+                    const float kp = hi ? vs[12 + i] : vs[i];
+                    a12[i] = kp + __shfl_xor_sync(0xffffffffu, snd, 16);
+                }
+            }
+            {
+                const bool hi = (lane >> 3) & 1;
+#pragma unroll
+                for (int i = 0; i < 6; ++i) {
+                    const float snd = hi ? a12[i] : a12[6 + i];
+                    const float kp = hi ? a12[6 + i] : a12[i];
+                    a6[i] = kp + __shfl_xor_sync(0xffffffffu, snd, 8);
+                }
+            }
+            {
+                const bool hi = (lane >> 2) & 1;
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    const float snd = hi ? a6[i] : a6[3 + i];
+                    const float kp = hi ? a6[3 + i] : a6[i];
+                    a3[i] = kp + __shfl_xor_sync(0xffffffffu, snd, 4);
+                }
+            }
+            // lane holds token t_own, quantities 3 qh + 0..2
+#pragma unroll
+            for (int i = 0; i < 3; ++i) s.red[par][t_own][3 * qh + i][warp] = a3[i];
+            // output statistics of the previous step ride on the same barrier
+            zbar_stats(zprev, par);
+        }
+        // input blocks of the next mini-batch
+        compute_sfrag(n + 1);
+        if (warp == 0 && lane == 0) ptx::bulk_wait_read<NZ - 2>();
+        ptx::named_bar(1, kMathThreads);
+
+        // ======== after the barrier ========
+        // key product of the next mini-batch from W_n (clamped at the end: unused)
+        float xacc[2][4];
+        product(xacc, s.k, min(n + 1, N - 1));
+        // G_n
+        float gmat[2][4];
+        if (LN) {
+            // totals for (t_own, 3 qh + i), then the partner lane supplies the other three
+            float tot[3];
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                const float4 w4 = *reinterpret_cast<const float4 *>(s.red[par][t_own][3 * qh + i]);
+                tot[i] = (w4.x + w4.y) + (w4.z + w4.w);
+            }
+            float S[6];
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                const float o = __shfl_xor_sync(0xffffffffu, tot[i], 4);
+                S[i] = qh ? o : tot[i];
+                S[3 + i] = qh ? tot[i] : o;
+            }
+            const float mu = S[0] * (1.f / D);
+            const float var = fmaxf(S[1] * (1.f / D) - mu * mu, 0.f);
+            const float r = rsqrtf(var + p.eps);
+            const float sg2zc = S[2] - mu * C1;
+            const float sg2zc2 = S[3] - 2.f * mu * S[2] + mu * mu * C1;
+            const float sgbzc = S[4] - mu * S[5];
+            const float m1 = (r * sg2zc + S[5]) * (1.f / D);
+            const float m2 = (r * r * sg2zc2 + r * sgbzc) * (1.f / D);
+            const float co_a = r * r, co_b = r * r * m2, co_e = r * m1;
+            // G_j = (z - mu) (r^2 gamma_j^2 - r^2 m2) + r gamma_j b'_j - r m1
+#pragma unroll
+            for (int tq = 0; tq < 4; ++tq) {
+                const int src = c + 8 * tq;
+                const float mu_t = __shfl_sync(0xffffffffu, mu, src);
+                const float a_t = __shfl_sync(0xffffffffu, co_a, src);
+                const float b_t = __shfl_sync(0xffffffffu, co_b, src);
+                const float r_t = __shfl_sync(0xffffffffu, r, src);
+                const float e_t = __shfl_sync(0xffffffffu, co_e, src);
+                const int u = tq >> 1, e = tq & 1;
+                const float zc0 = pacc[u][e] - mu_t, zc1 = pacc[u][2 + e] - mu_t;
+                gmat[u][e] = fmaf(zc0, fmaf(a_t, g20, -b_t), fmaf(r_t, gb[u][e], -e_t));
+                gmat[u][2 + e] = fmaf(zc1, fmaf(a_t, g21, -b_t), fmaf(r_t, gb[u][2 + e], -e_t));
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) gmat[u][i] = pacc[u][i] - vt[u][i];
+        }
+
+        // -G and -eta G as A fragments (rows = features, k = tokens)
+        const int s0 = 2 * c;
+        const float e00 = eta_at(n, s0), e01 = eta_at(n, s0 + 1);
+        const float e10 = eta_at(n, s0 + 8), e11 = eta_at(n, s0 + 9);
+        uint32_t ng[4];
+        ng[0] = ptx::pack_bf16(-gmat[0][0], -gmat[0][1]);
+        ng[1] = ptx::pack_bf16(-gmat[0][2], -gmat[0][3]);
+        ng[2] = ptx::pack_bf16(-gmat[1][0], -gmat[1][1]);
+        ng[3] = ptx::pack_bf16(-gmat[1][2], -gmat[1][3]);
+        // chain: P_{n+1} = X_{n+1} - G_n^T M^T
+        uint32_t bf[2][2];
+        read_sfrag(n, 0, bf);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pacc[u][i] = xacc[u][i];
+            ptx::mma_bf16(pacc[u], ng, bf[u][0], bf[u][1]);
+        }
+        // output: Zbar_n = Y_n - G_n^T B^T
+        read_sfrag(n, 1, bf);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) ptx::mma_bf16(yacc[u], ng, bf[u][0], bf[u][1]);
+        // deferred W update operand, and c -= eta^T G now
+        ngep[0] = ptx::pack_bf16(-e00 * gmat[0][0], -e01 * gmat[0][1]);
+        ngep[1] = ptx::pack_bf16(-e00 * gmat[0][2], -e01 * gmat[0][3]);
+        ngep[2] = ptx::pack_bf16(-e10 * gmat[1][0], -e11 * gmat[1][1]);
+        ngep[3] = ptx::pack_bf16(-e10 * gmat[1][2], -e11 * gmat[1][3]);
+        {
+            float d0 = e00 * gmat[0][0] + e01 * gmat[0][1] + e10 * gmat[1][0] + e11 * gmat[1][1];
+            float d1 = e00 * gmat[0][2] + e01 * gmat[0][3] + e10 * gmat[1][2] + e11 * gmat[1][3];
+            d0 += __shfl_xor_sync(0xffffffffu, d0, 1);
+            d1 += __shfl_xor_sync(0xffffffffu, d1, 1);
+            d0 += __shfl_xor_sync(0xffffffffu, d0, 2);
+            d1 += __shfl_xor_sync(0xffffffffu, d1, 2);
+            cb0 -= d0;
+            cb1 -= d1;
+        }
+        // the previous output (its statistics crossed this barrier); at n = 0 this
+        // writes a tile that is overwritten before it is ever stored
+        finish_z(zprev, qprev, n + NZ - 1, par);
+        if (warp == 0 && lane == 0) {
+            // Z_{n-2} was finished before this step's barrier
+            if (n >= 2) {
+                ptx::tma_store_3d(&tmZ, ptx::smem_addr(s.z[(n - 2) % NZ]), 0, (n - 2) * MB, bh);
+                ptx::bulk_commit();
+            }
+            // the stage holding n - 1 is no longer read (its last reader, the update
+            // with G_{n-1}, ran before this barrier)
+            if (n >= 1 && (n % TPS) == 0) ptx::mbar_arrive(ptx::smem_addr(&s.empty[((n / TPS) - 1) % NSS]));
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                zprev[u][i] = yacc[u][i];
+                qprev[u][i] = qt[u][i];
+            }
+    }
+
+    // ---- tail: last update, last output, final stores, final state
+    update_w(ngep, N - 1);
+    {
+        const int par = N & 1;
+        if (LN) zbar_stats(zprev, par);
+        if (warp == 0 && lane == 0) ptx::bulk_wait_read<NZ - 2>();
+        ptx::named_bar(1, kMathThreads);
+        finish_z(zprev, qprev, N - 1, par);
+        ptx::named_bar(1, kMathThreads);
+        if (warp == 0 && lane == 0) {
+            for (int n = max(0, N - 2); n < N; ++n) {
+                ptx::tma_store_3d(&tmZ, ptx::smem_addr(s.z[n % NZ]), 0, n * MB, bh);
+                ptx::bulk_commit();
+            }
+            ptx::bulk_wait<0>();
+        }
+    }
+    {
+        float *Wf = p.Wf + (size_t)bh * D * D;
+#pragma unroll
+        for (int pt = 0; pt < 8; ++pt) {
+            const int i = pt * 8 + 2 * c;
+            Wf[i * D + j0] = wt[pt][0];
+            Wf[(i + 1) * D + j0] = wt[pt][1];
+            Wf[i * D + j1] = wt[pt][2];
+            Wf[(i + 1) * D + j1] = wt[pt][3];
+        }
+        if (c == 0) {
+            p.bf[(size_t)bh * D + j0] = cb0;
+            p.bf[(size_t)bh * D + j1] = cb1;
+        }
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -909,23 +678,8 @@ cudaError_t launch_linear_tc(const LinearArgs &a)
     if (!make_map(&mq, a.Q, d.L, BH, ST) || !make_map(&mk, a.K, d.L, BH, ST) ||
         !make_map(&mv, a.V, d.L, BH, ST) || !make_map(&mz, a.Z, d.L, BH, MB))
         return cudaErrorInvalidValue;
-    Params p;
-    p.H = d.H;
-    p.L = d.L;
-    p.N = d.L / MB;
-    p.NST = (d.L + ST - 1) / ST;
-    p.init_per_batch = d.init_per_batch;
-    p.eps = d.ln_eps;
-    p.wait_ns = g_wait_ns;
-    p.withhold_loads = g_withhold_loads;
-    p.eta = a.eta;
-    p.W0 = a.W0;
-    p.b0 = a.b0;
-    p.gamma = a.gamma;
-    p.beta = a.beta;
-    p.Wf = a.W_final;
-    p.bf = a.b_final;
-    p.status = a.status;
+    Params p{d.H, d.L, d.residual_ln, d.ln_eps, g_wait_ns, g_withhold_loads, a.eta, a.W0, a.b0, a.gamma, a.beta,
+             a.W_final, a.b_final, a.status, d.init_per_batch};
     const size_t smem = sizeof(Smem) + 1024;
     auto kern = d.residual_ln ? linear_fused_kernel<true> : linear_fused_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
