@@ -225,20 +225,30 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
     };
 
-    // acc[u][*] = W^T X_n^T + c for a 16-token tile X of mini-batch n
+    // acc[u][*] = W^T X_n^T + c for a 16-token tile X of mini-batch n (two half-depth
+    // accumulator chains per output tile, summed at the end)
     auto product = [&](float (*acc)[4], const __nv_bfloat16 (*arr)[ST * D], int n) {
+        uint32_t r[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)   // matrices: (t-block 0, i-chunk 2q), (t0, 2q+1), (t1, 2q), (t1, 2q+1)
+            ptx::ldsm_x4(tile_addr(arr, n, (mat >> 1) * 8 + mrow, 2 * q + (mat & 1)), r[q]);
+        float hi[2][4];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             acc[u][0] = cb0; acc[u][1] = cb0; acc[u][2] = cb1; acc[u][3] = cb1;
+            hi[u][0] = 0.f; hi[u][1] = 0.f; hi[u][2] = 0.f; hi[u][3] = 0.f;
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            // matrices: (t-block 0, i-chunk 2q), (t0, 2q+1), (t1, 2q), (t1, 2q+1)
-            uint32_t r[4];
-            ptx::ldsm_x4(tile_addr(arr, n, (mat >> 1) * 8 + mrow, 2 * q + (mat & 1)), r);
-            ptx::mma_bf16(acc[0], wa[q], r[0], r[1]);
-            ptx::mma_bf16(acc[1], wa[q], r[2], r[3]);
+        for (int q = 0; q < 2; ++q) {
+            ptx::mma_bf16(acc[0], wa[q], r[q][0], r[q][1]);
+            ptx::mma_bf16(acc[1], wa[q], r[q][2], r[q][3]);
+            ptx::mma_bf16(hi[0], wa[q + 2], r[q + 2][0], r[q + 2][1]);
+            ptx::mma_bf16(hi[1], wa[q + 2], r[q + 2][2], r[q + 2][3]);
         }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[u][i] += hi[u][i];
     };
 
     // C-fragment layout (rows = features j0/j1, cols = tokens) of a bf16 tile, transposed
@@ -266,18 +276,22 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const int mm = min(m, N - 1);
         const int na = which ? min(m + 1, N - 1) : mm;
         const __nv_bfloat16(*A)[ST * D] = which ? s.k : s.q;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a[4][4], b[4][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             // A = rows t of the target tile, k = features 16q..16q+15
             // matrices: (t0, chunk 2q), (t1, 2q), (t0, 2q+1), (t1, 2q+1)
-            uint32_t a[4];
-            ptx::ldsm_x4(tile_addr(A, na, (mat & 1) * 8 + mrow, 2 * q + (mat >> 1)), a);
+            ptx::ldsm_x4(tile_addr(A, na, (mat & 1) * 8 + mrow, 2 * q + (mat >> 1)), a[q]);
             // B = K_m rows s in [8 half, 8 half + 8), k = features: (s, chunk 2q), (s, 2q+1)
-            uint32_t b[4];
-            ptx::ldsm_x4(tile_addr(s.k, mm, half * 8 + mrow, 2 * q + (mat & 1)), b);
-            ptx::mma_bf16(acc, a, b[0], b[1]);
+            ptx::ldsm_x4(tile_addr(s.k, mm, half * 8 + mrow, 2 * q + (mat & 1)), b[q]);
         }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, ac2[4] = {0.f, 0.f, 0.f, 0.f};
+        ptx::mma_bf16(acc, a[0], b[0][0], b[0][1]);
+        ptx::mma_bf16(ac2, a[2], b[2][0], b[2][1]);
+        ptx::mma_bf16(acc, a[1], b[1][0], b[1][1]);
+        ptx::mma_bf16(ac2, a[3], b[3][0], b[3][1]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] += ac2[i];
         // acc: rows t = g (acc0,1), g + 8 (acc2,3); cols s = 8 half + 2c, +1
         const int s0 = half * 8 + 2 * c;
         const float e0 = eta_at(mm, s0), e1 = eta_at(mm, s0 + 1);
@@ -407,12 +421,16 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if ((n + 2) % TPS == 0 && n + 2 < N) wait_stage((n + 2) / TPS);
 
         // ======== before the barrier ========
+        // input blocks of the next mini-batch (independent of the state)
+        compute_sfrag(n + 1);
         // deferred update with G_{n-1} (zero fragments at n = 0): W_n, then its bf16 copy
         update_w(ngep, max(n - 1, 0));
         pack_w();
-        // output product Y_n = W_n^T Q_n^T + c_n
-        float yacc[2][4];
+        // products from W_n: output Y_n = W_n^T Q_n^T + c_n, and the key product of the
+        // next mini-batch (clamped at the end: unused)
+        float yacc[2][4], xacc[2][4];
         product(yacc, s.q, n);
+        product(xacc, s.k, min(n + 1, N - 1));
         float vt[2][4], qt[2][4];
         load_T(vt, s.v, n);
         load_T(qt, s.q, n);
@@ -477,15 +495,10 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // output statistics of the previous step ride on the same barrier
             zbar_stats(zprev, par);
         }
-        // input blocks of the next mini-batch
-        compute_sfrag(n + 1);
         if (warp == 0 && lane == 0) ptx::bulk_wait_read<NZ - 2>();
         ptx::named_bar(1, kMathThreads);
 
         // ======== after the barrier ========
-        // key product of the next mini-batch from W_n (clamped at the end: unused)
-        float xacc[2][4];
-        product(xacc, s.k, min(n + 1, N - 1));
         // G_n
         float gmat[2][4];
         if (LN) {
