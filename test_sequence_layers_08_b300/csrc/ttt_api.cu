@@ -107,6 +107,7 @@ const char *linear_kernel(const ttt_desc &s)
 
 const char *mlp_kernel(const ttt_desc &s)
 {
+    if (ttt::mlp_tc_supported(s)) return "ttt_mlp_fused";
     if (ttt::mlp_generic_smem_bytes(s)) return "ttt_mlp_generic";
     return nullptr;
 }
@@ -243,7 +244,7 @@ ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const
                    W1_f, b1_f, W2_f, b2_f, reinterpret_cast<cudaStream_t>(stream), nullptr};
     a.status = failure_flag(&st);
     if (st != TTT_OK) return st;
-    cudaError_t e = ttt::launch_mlp_generic(a);
+    cudaError_t e = ttt::mlp_tc_supported(s) ? ttt::launch_mlp_tc(a) : ttt::launch_mlp_generic(a);
     if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "%s launch: %s", kname, cudaGetErrorString(e));
     return ok();
 }

@@ -40,9 +40,14 @@ cudaError_t launch_mlp_generic(const MlpArgs &a);
 // Tensor-core TTT-Linear kernel (bf16 I/O, d = 64, b = 16).
 bool linear_tc_supported(const ttt_desc &d);
 cudaError_t launch_linear_tc(const LinearArgs &a);
-// Test hooks of the bounded waits (process-wide; see ttt.h).
+// Tensor-core TTT-MLP kernel (bf16 I/O, d = 64, d_hidden = 256, b = 16).
+bool mlp_tc_supported(const ttt_desc &d);
+cudaError_t launch_mlp_tc(const MlpArgs &a);
+// Test hooks of the bounded waits (process-wide; see ttt.h), read by both fused kernels.
 void set_wait_timeout_ns(long long ns);
 void set_withhold_loads(int on);
+long long wait_timeout_ns();
+int withhold_loads();
 
 // Device-side status word values.
 enum : unsigned int { kStatusOk = 0u, kStatusTimeout = 1u };

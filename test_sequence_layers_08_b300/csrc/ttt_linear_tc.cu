@@ -677,6 +677,8 @@ int g_withhold_loads = 0;
 
 void set_wait_timeout_ns(long long ns) { g_wait_ns = ns > 0 ? ns : kDefaultWaitNs; }
 void set_withhold_loads(int on) { g_withhold_loads = on != 0; }
+long long wait_timeout_ns() { return g_wait_ns; }
+int withhold_loads() { return g_withhold_loads; }
 
 bool linear_tc_supported(const ttt_desc &d)
 {

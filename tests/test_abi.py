@@ -104,5 +104,8 @@ def test_kernel_choice(lib):
     assert k(d=32) == "ttt_linear_generic"
     assert k(d=256) is None
     m = lambda **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), 1))
-    assert m(residual_ln=1) is not None
+    assert m() == "ttt_mlp_fused"                    # d_hidden 0 -> 4 d = 256
+    assert m(residual_ln=1, d_hidden=256) == "ttt_mlp_fused"
+    assert m(io_dtype=0) == "ttt_mlp_generic"
+    assert m(d_hidden=128) == "ttt_mlp_generic"
     assert m(d_hidden=4096) is None
