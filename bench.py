@@ -61,6 +61,32 @@ def algorithmic_bytes(cfg) -> float:
     return float(io + state * cfg.H + state * cfg.B * cfg.H + ln)
 
 
+KERNEL_SOURCES = {"ttt_linear_fused": "ttt_linear_tc.cu", "ttt_mlp_fused": "ttt_mlp_tc.cu",
+                  "ttt_linear_generic": "ttt_generic.cu", "ttt_mlp_generic": "ttt_generic.cu"}
+
+
+def measured_traffic(kname, workload):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu
+    summary committed under profiles/ for this kernel and workload, if that capture was
+    taken of the kernel source as it is now (its sha256 is recorded in the summary);
+    otherwise None."""
+    import hashlib
+    import re
+    src = KERNEL_SOURCES.get(kname)
+    summary = os.path.join(ROOT, "profiles", f"{kname}_ncu_{workload}.md")
+    if src is None or not os.path.exists(summary):
+        return None
+    text = open(summary).read()
+    m_bytes = re.search(r"^traffic_bytes_per_launch:\s*(\d+)", text, re.M)
+    m_sha = re.search(r"^kernel_source_sha256:\s*([0-9a-f]{64})", text, re.M)
+    if not m_bytes or not m_sha:
+        return None
+    path = os.path.join(ROOT, "test_sequence_layers_08_b300", "csrc", src)
+    if hashlib.sha256(open(path, "rb").read()).hexdigest() != m_sha.group(1):
+        return None
+    return float(m_bytes.group(1))
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -270,7 +296,7 @@ def run_ours(args, cfg, world, rank, local):
     e1.record(stream)
     e1.synchronize()
     one_ms = max(e0.elapsed_time(e1), 1e-3)
-    soak_n = int(min(20000, max(0, 1500.0 / one_ms)))
+    soak_n = int(min(20000, max(0, args.soak_ms / one_ms)))
     for i in range(soak_n):
         step(i)
     torch.cuda.synchronize(dev)
@@ -341,7 +367,7 @@ def run_ours(args, cfg, world, rank, local):
     else:
         roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"]}
-    roof.update({"traffic": None, "peak_source": peaks["source"], "kernel": kname,
+    roof.update({"traffic": measured_traffic(kname, cfg.name), "peak_source": peaks["source"], "kernel": kname,
                  "algorithmic_bytes": alg_bytes, "algorithmic_flops": alg_flops,
                  "roofline_ms": max(t_hbm, t_tc) * 1e3})
 
@@ -380,6 +406,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-ms", type=float, default=1500.0,
+                    help="untimed load before the timed region, so the clock samples describe "
+                         "this workload (0 under a profiler)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

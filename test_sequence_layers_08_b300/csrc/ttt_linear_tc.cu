@@ -173,9 +173,13 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if (ptx::mbar_try_wait(bar, (st / NSS) & 1)) return;
         aborted = !wait_slow(bar, (st / NSS) & 1, p.wait_ns, &s.abort_flag, p.status);
     };
-    // shared-memory byte address of row `t` (mini-batch n) / 16-byte chunk of a stage tile
+    // shared-memory byte address of row `t` (mini-batch n) / 16-byte chunk of a stage tile.
+    // Every caller passes t = 8 k + mrow, so the 128-byte swizzle term (chunk ^ row % 8) is
+    // (chunk ^ mrow): the lane part of each address is the same in every step and stays in a
+    // register; per step only the tile offset of mini-batch n is added.
     auto tile_addr = [&](const __nv_bfloat16 (*arr)[ST * D], int n, int t, int chunk) -> uint32_t {
-        return ptx::smem_addr(arr[(n / TPS) % NSS]) + ptx::sw128((n % TPS) * MB + t, chunk);
+        const uint32_t toff = (uint32_t)(((n / TPS) % NSS) * (ST * D * 2) + (n % TPS) * (MB * 128));
+        return ptx::smem_addr(arr[0]) + toff + (uint32_t)(t * 128 + ((chunk ^ mrow) << 4));
     };
     auto eta_at = [&](int n, int t) -> float { return s.eta[(n / TPS) % NSS][(n % TPS) * MB + t]; };
 
@@ -422,7 +426,7 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
         // ======== before the barrier ========
         // input blocks of the next mini-batch (independent of the state)
-        compute_sfrag(n + 1);
+        if (LN) compute_sfrag(n + 1);
         // deferred update with G_{n-1} (zero fragments at n = 0): W_n, then its bf16 copy
         update_w(ngep, max(n - 1, 0));
         pack_w();
@@ -430,7 +434,9 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // next mini-batch (clamped at the end: unused)
         float yacc[2][4], xacc[2][4];
         product(yacc, s.q, n);
-        product(xacc, s.k, min(n + 1, N - 1));
+        // with LayerNorm the pre-barrier shuffle rounds hide this product; without it the
+        // step is short on both sides and the product balances the post-barrier half
+        if (LN) product(xacc, s.k, min(n + 1, N - 1));
         float vt[2][4], qt[2][4];
         load_T(vt, s.v, n);
         load_T(qt, s.q, n);
@@ -495,10 +501,12 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // output statistics of the previous step ride on the same barrier
             zbar_stats(zprev, par);
         }
+        if (!LN) compute_sfrag(n + 1);
         if (warp == 0 && lane == 0) ptx::bulk_wait_read<NZ - 2>();
         ptx::named_bar(1, kMathThreads);
 
         // ======== after the barrier ========
+        if (!LN) product(xacc, s.k, min(n + 1, N - 1));
         // G_n
         float gmat[2][4];
         if (LN) {
