@@ -67,8 +67,11 @@ struct __align__(1024) Smem {
     __nv_bfloat16 z[NZ][MB * D];
     float eta[NSS][ST];
     uint32_t sfrag[3][2][2][32][2];   // [mini-batch % 3][0: chain, 1: output][s half][lane][t n-tile]
-    float red[2][MB][8][4];           // [parity][token][quantity][warp]
-    float zred[2][MB][2][4];          // [parity][token][sum z, sum z^2][warp]
+    // LayerNorm exchange tables, [parity][token][quantity * 4 + warp].  The token rows are
+    // padded (36 and 12 floats) so the 16-byte reads of the four warps' partials are free
+    // of bank conflicts and the scattered 4-byte writes are at most 4-way.
+    float red[2][MB][36];             // six backward sums (+ 2 spare quantities)
+    float zred[2][MB][12];            // output sums: z, z^2
     unsigned long long full[NSS];
     unsigned long long empty[NSS];
     int abort_flag;
@@ -210,9 +213,9 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         part += __shfl_xor_sync(0xffffffffu, part, 4);
         part += __shfl_xor_sync(0xffffffffu, part, 8);
         part += __shfl_xor_sync(0xffffffffu, part, 16);
-        if (lane == 0) s.red[0][0][0][warp] = part;
+        if (lane == 0) s.red[0][0][warp] = part;
         ptx::named_bar(1, kMathThreads);
-        const float4 w4 = *reinterpret_cast<const float4 *>(s.red[0][0][0]);
+        const float4 w4 = *reinterpret_cast<const float4 *>(s.red[0][0]);
         C1 = (w4.x + w4.y) + (w4.z + w4.w);
         ptx::named_bar(1, kMathThreads);
     }
@@ -355,14 +358,14 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             zs[tq * 2 + 0] = z0 + z1;
             zs[tq * 2 + 1] = fmaf(z0, z0, z1 * z1);
         }
-        s.zred[par][t_own][qh][warp] = rs8(zs);
+        s.zred[par][t_own][4 * qh + warp] = rs8(zs);
     };
 
     // Z_m = Q_m + LN(Zbar_m) (or Zbar_m) -> bf16 staging tile m % NZ
     auto finish_z = [&](const float (*zb)[4], const float (*qv)[4], int m, int par) {
         float z[2][4];
         if (LN) {
-            const float4 w4 = *reinterpret_cast<const float4 *>(s.zred[par][t_own][qh]);
+            const float4 w4 = *reinterpret_cast<const float4 *>(&s.zred[par][t_own][4 * qh]);
             const float tot = (w4.x + w4.y) + (w4.z + w4.w);
             const float oth = __shfl_xor_sync(0xffffffffu, tot, 4);
             const float s1 = qh ? oth : tot, s2 = qh ? tot : oth;
@@ -497,7 +500,7 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
             // lane holds token t_own, quantities 3 qh + 0..2
 #pragma unroll
-            for (int i = 0; i < 3; ++i) s.red[par][t_own][3 * qh + i][warp] = a3[i];
+            for (int i = 0; i < 3; ++i) s.red[par][t_own][4 * (3 * qh + i) + warp] = a3[i];
             // output statistics of the previous step ride on the same barrier
             zbar_stats(zprev, par);
         }
@@ -514,7 +517,7 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             float tot[3];
 #pragma unroll
             for (int i = 0; i < 3; ++i) {
-                const float4 w4 = *reinterpret_cast<const float4 *>(s.red[par][t_own][3 * qh + i]);
+                const float4 w4 = *reinterpret_cast<const float4 *>(&s.red[par][t_own][4 * (3 * qh + i)]);
                 tot[i] = (w4.x + w4.y) + (w4.z + w4.w);
             }
             float S[6];

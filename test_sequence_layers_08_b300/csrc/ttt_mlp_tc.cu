@@ -63,8 +63,10 @@ struct __align__(1024) Smem {
     float eta[NSS][ST];
     uint32_t a1f[2][32][2];             // eta_s (Q_t . K_s + 1) [s <= t] as B fragments [s half][lane][t n-tile]
     uint32_t a2f[2][32][2];             // eta_s (Xb2_t . X2_s + 1) [s <= t], same layout
-    float red[2][MB][8][4];             // LayerNorm-backward partial sums [parity][token][quantity][warp]
-    float zred[2][MB][2][4];            // output LayerNorm partial sums
+    // LayerNorm exchange tables [parity][token][quantity * 4 + warp]; rows padded (36, 12
+    // floats) so the 16-byte reads are free of bank conflicts
+    float red[2][MB][36];               // six backward sums
+    float zred[2][MB][12];              // output sums: z, z^2
     unsigned long long full[NSS];
     int abort_flag;
 };
@@ -203,9 +205,9 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             part += __shfl_xor_sync(0xffffffffu, part, 4);
             part += __shfl_xor_sync(0xffffffffu, part, 8);
             part += __shfl_xor_sync(0xffffffffu, part, 16);
-            if (lane == 0) s.red[0][0][0][warp] = part;
+            if (lane == 0) s.red[0][0][warp] = part;
             ptx::named_bar(kBarLn, 128);
-            const float4 w4 = *reinterpret_cast<const float4 *>(s.red[0][0][0]);
+            const float4 w4 = *reinterpret_cast<const float4 *>(s.red[0][0]);
             C1 = (w4.x + w4.y) + (w4.z + w4.w);
             ptx::named_bar(kBarLn, 128);
         }
@@ -428,12 +430,12 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < 3; ++i) s.red[par][t_own][3 * qh + i][warp] = a3[i];
+                for (int i = 0; i < 3; ++i) s.red[par][t_own][4 * (3 * qh + i) + warp] = a3[i];
                 ptx::named_bar(kBarLn, 128);
                 float tot[3];
 #pragma unroll
                 for (int i = 0; i < 3; ++i) {
-                    const float4 w4 = *reinterpret_cast<const float4 *>(s.red[par][t_own][3 * qh + i]);
+                    const float4 w4 = *reinterpret_cast<const float4 *>(&s.red[par][t_own][4 * (3 * qh + i)]);
                     tot[i] = (w4.x + w4.y) + (w4.z + w4.w);
                 }
                 float S[6];
@@ -633,9 +635,9 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     zs[tq * 2 + 0] = z0 + z1v;
                     zs[tq * 2 + 1] = fmaf(z0, z0, z1v * z1v);
                 }
-                s.zred[par][t_own][qh][warp] = rs8(zs);
+                s.zred[par][t_own][4 * qh + warp] = rs8(zs);
                 ptx::named_bar(kBarLn, 128);
-                const float4 w4 = *reinterpret_cast<const float4 *>(s.zred[par][t_own][qh]);
+                const float4 w4 = *reinterpret_cast<const float4 *>(&s.zred[par][t_own][4 * qh]);
                 const float tot = (w4.x + w4.y) + (w4.z + w4.w);
                 const float oth = __shfl_xor_sync(0xffffffffu, tot, 4);
                 const float s1 = qh ? oth : tot, s2 = qh ? tot : oth;
