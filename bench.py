@@ -216,7 +216,7 @@ def run_reference(args, cfg, world, rank):
         return
     x = make_inputs(cfg, 0)
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    budget = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_rate(cfg, x, budget / 4, threads)
     rates, sample = [], ""
@@ -406,6 +406,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="reference arm: host time spread over warm-up and timed steps")
     ap.add_argument("--soak-ms", type=float, default=1500.0,
                     help="untimed load before the timed region, so the clock samples describe "
                          "this workload (0 under a profiler)")
