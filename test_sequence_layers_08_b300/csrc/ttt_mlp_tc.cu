@@ -25,8 +25,11 @@
 //     memory for its slice;
 //   * warps 0-3 also own 16 of the 64 outputs each and run both LayerNorms (statistics in
 //     fp32: warp reduce-scatter plus one shared-memory exchange);
-//   * warps 4 and 5 compute the 16 x 16 output blocks of each mini-batch.
-// Per mini-batch the warps meet at five named barriers; every mbarrier wait is bounded.
+//   * the two contractions over all hidden units are split by hidden half: warps w and
+//     w + 4 take units 0-127 and 128-255 for the outputs of warp w, and warps 4-7 hand
+//     their fp32 partials over through shared memory; the 16 x 16 Gram Xb2 X2^T is split
+//     the same way over warps 4-7.
+// Per mini-batch the warps meet at six named barriers; every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -62,7 +65,8 @@ struct __align__(1024) Smem {
     __nv_bfloat16 zst[MB * D];          // Z staging [t][o], 128-byte swizzle
     float eta[NSS][ST];
     uint32_t a1f[2][32][2];             // eta_s (Q_t . K_s + 1) [s <= t] as B fragments [s half][lane][t n-tile]
-    uint32_t a2f[2][32][2];             // eta_s (Xb2_t . X2_s + 1) [s <= t], same layout
+    float parta2[2][2][32][4];          // Xb2_t . X2_s partials [s half][hidden half][lane][4] (warps 4-7)
+    float part2[4][32][8];              // X W2 partials over hidden units 128-255 [output warp][lane][8]
     // LayerNorm exchange tables [parity][token][quantity * 4 + warp]; rows padded (36, 12
     // floats) so the 16-byte reads are free of bank conflicts
     float red[2][MB][36];               // six backward sums
@@ -85,9 +89,8 @@ struct Params {
 
 constexpr long long kDrainNs = 1000000000ll;
 
-// Barrier ids: 1 = the eight compute warps, 2 = the four LayerNorm warps,
-// 3 = LayerNorm warps plus the two output-block warps.
-constexpr int kBarAll = 1, kBarLn = 2, kBarOut = 3;
+// Barrier ids: 1 = the eight compute warps, 2 = the four LayerNorm warps.
+constexpr int kBarAll = 1, kBarLn = 2;
 
 __device__ __noinline__ bool mlp_wait_slow(uint32_t bar, uint32_t parity, long long limit, int *abort_flag,
                                            unsigned int *status)
@@ -107,11 +110,13 @@ __device__ __forceinline__ float gelu(float x)
     const float s = 0.7978845608028654f;   // sqrt(2/pi)
     return 0.5f * x * (1.f + tanhf(s * (x + 0.044715f * x * x * x)));
 }
-__device__ __forceinline__ float gelu_prime(float x)
+// GELU(x) and GELU'(x) from one tanh
+__device__ __forceinline__ void gelu_and_prime(float x, float &y, float &dy)
 {
     const float s = 0.7978845608028654f;
     const float th = tanhf(s * (x + 0.044715f * x * x * x));
-    return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * s * (1.f + 3.f * 0.044715f * x * x);
+    y = 0.5f * x * (1.f + th);
+    dy = 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * s * (1.f + 3.f * 0.044715f * x * x);
 }
 
 template <bool LN>
@@ -262,8 +267,9 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             ptx::stsm_x4_t(tile + xh_off((mat >> 1) * 8 + mrow, (hb + 16 * m) / 8 + (mat & 1)), r);
         }
     };
-    // Zbar^T for outputs o0/o1 = b + W2^T X^T over all 256 hidden units (X from a [t][h] tile)
-    auto second_layer = [&](float (*acc)[4], uint32_t xtile, float bo0, float bo1) {
+    // Zbar^T partial for the outputs of warp (warp & 3) = b + W2^T X^T over hidden units
+    // 128 kh .. 128 kh + 127 (X from a [t][h] tile)
+    auto second_layer = [&](float (*acc)[4], uint32_t xtile, float bo0, float bo1, int kh) {
         float hi[2][4];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -272,11 +278,11 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
         const uint32_t wb = ptx::smem_addr(s.w2b);
 #pragma unroll 4
-        for (int q = 0; q < DH / 16; ++q) {
+        for (int q = 8 * kh; q < 8 * kh + 8; ++q) {
             uint32_t a[4], r[4];
             // A = W2^T (m = outputs, k = hidden 16q..): W2 is stored [h][o], so a transposed load of
             // matrices (o-block, h-block): (0,0), (1,0), (0,1), (1,1)
-            ptx::ldsm_x4_t(wb + ptx::sw128(16 * q + 8 * (mat >> 1) + mrow, 2 * warp + (mat & 1)), a);
+            ptx::ldsm_x4_t(wb + ptx::sw128(16 * q + 8 * (mat >> 1) + mrow, 2 * (warp & 3) + (mat & 1)), a);
             // B = X^T (k = hidden, n = tokens): (t0, chunk 2q), (t0, 2q+1), (t1, 2q), (t1, 2q+1)
             ptx::ldsm_x4(xtile + xh_off((mat >> 1) * 8 + mrow, 2 * q + (mat & 1)), r);
             float(*dst)[4] = (q & 1) ? hi : acc;
@@ -323,19 +329,33 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (n % TPS == 0 && n > 0) wait_stage(st);
 
         // ======== phase 1: first layer (key and query side), W2 copy, the Q K^T block
-        float z1[2][2][4], y1[2][2][4];
+        float y1[2][2][4];
+        uint32_t dz[2][2][2];   // GELU'(Z1) as bf16 pairs (it only scales G1, a bf16 operand)
+        uint32_t xa[2][4];      // X2 = GELU(Z1) as bf16 A fragments (rows = hidden, k = tokens)
+        {
+        float z1[2][2][4];
         first_layer(z1, s.k, n);
         first_layer(y1, s.q, n);
-        // X2 = GELU(Z1) as bf16 A fragments (rows = hidden, k = tokens), also stored as [t][h]
-        uint32_t xa[2][4];
+        // X2 also goes to the shared [t][h] tile
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-            xa[m][0] = ptx::pack_bf16(gelu(z1[m][0][0]), gelu(z1[m][0][1]));
-            xa[m][1] = ptx::pack_bf16(gelu(z1[m][0][2]), gelu(z1[m][0][3]));
-            xa[m][2] = ptx::pack_bf16(gelu(z1[m][1][0]), gelu(z1[m][1][1]));
-            xa[m][3] = ptx::pack_bf16(gelu(z1[m][1][2]), gelu(z1[m][1][3]));
+            float y[2][4], dy[2][4];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) gelu_and_prime(z1[m][u][i], y[u][i], dy[u][i]);
+            xa[m][0] = ptx::pack_bf16(y[0][0], y[0][1]);
+            xa[m][1] = ptx::pack_bf16(y[0][2], y[0][3]);
+            xa[m][2] = ptx::pack_bf16(y[1][0], y[1][1]);
+            xa[m][3] = ptx::pack_bf16(y[1][2], y[1][3]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                dz[m][u][0] = ptx::pack_bf16(dy[u][0], dy[u][1]);
+                dz[m][u][1] = ptx::pack_bf16(dy[u][2], dy[u][3]);
+            }
             // matrices (h-block, t-block): (0,0), (1,0), (0,1), (1,1); stored rows = tokens
             ptx::stsm_x4_t(x2t + xh_off((mat >> 1) * 8 + mrow, (hb + 16 * m) / 8 + (mat & 1)), xa[m]);
+        }
         }
         {
             // W2 rows hb.. (bf16) into the [h][o] tile: matrices (h 0-7, o 16k..), (h 8-15, ..), (h 0-7, o 16k+8..), (h 8-15, ..)
@@ -370,13 +390,25 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
         ptx::named_bar(kBarAll, kCompute * 32);
 
-        // ======== phase 2 (warps 0-3): Z2, G2
+        // ======== phase 2: Z2 = X2 W2 + b2 (all warps, one hidden half each), then G2 (warps 0-3)
         float gm[2][4];      // G2^T for o0/o1 (warps 0-3)
         float vt[2][4];
-        float b2_start0 = b2r[0], b2_start1 = b2r[1];
+        const float b2_start0 = b2r[0], b2_start1 = b2r[1];
+        float z2[2][4];
+        second_layer(z2, x2t, b2r[0], b2r[1], warp >> 2);   // b2r is zero on warps 4-7
+        if (!lnw) {
+            float4 *dst = reinterpret_cast<float4 *>(s.part2[warp & 3][lane]);
+            dst[0] = make_float4(z2[0][0], z2[0][1], z2[0][2], z2[0][3]);
+            dst[1] = make_float4(z2[1][0], z2[1][1], z2[1][2], z2[1][3]);
+        }
+        ptx::named_bar(kBarAll, kCompute * 32);
         if (lnw) {
-            float z2[2][4];
-            second_layer(z2, x2t, b2r[0], b2r[1]);
+            {
+                const float4 p0 = reinterpret_cast<const float4 *>(s.part2[warp][lane])[0];
+                const float4 p1 = reinterpret_cast<const float4 *>(s.part2[warp][lane])[1];
+                z2[0][0] += p0.x; z2[0][1] += p0.y; z2[0][2] += p0.z; z2[0][3] += p0.w;
+                z2[1][0] += p1.x; z2[1][1] += p1.y; z2[1][2] += p1.z; z2[1][3] += p1.w;
+            }
             load_T(vt, s.v, n);
             if (LN) {
                 float kt[2][4], gb[2][4];
@@ -526,7 +558,8 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
                 for (int u = 0; u < 2; ++u)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) g1[m][u][i] *= gelu_prime(z1[m][u][i]);
+                    for (int i = 0; i < 4; ++i)
+                        g1[m][u][i] *= (i & 1) ? ptx::bf16_hi(dz[m][u][i >> 1]) : ptx::bf16_lo(dz[m][u][i >> 1]);
         }
         // first output layer: Zb1^T = Y1^T - G1^T (eta (Q K^T + 1) mask)^T, Xb2 = GELU(Zb1)
         {
@@ -593,13 +626,15 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
         ptx::named_bar(kBarAll, kCompute * 32);
 
-        // ======== phase 4: second output layer (warps 0-3), its 16 x 16 block (warps 4, 5)
-        if (warp == 4 || warp == 5) {
-            // eta_s (Xb2_t . X2_s + 1) [s <= t] over all 256 hidden units, source half (warp & 1)
-            const int half = warp & 1;
+        // ======== phase 4: second output layer (all warps, one hidden half each), its 16 x 16
+        // block eta_s (Xb2_t . X2_s + 1) [s <= t] (partials on warps 4-7), then warps 0-3 finish
+        float zb[2][4];
+        second_layer(zb, xb2t, b2_start0, b2_start1, warp >> 2);
+        if (!lnw) {
+            const int half = warp & 1, kq = (warp >> 1) & 1;   // source half, hidden half
             float acc[4] = {0.f, 0.f, 0.f, 0.f}, ac2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-            for (int q = 0; q < DH / 16; ++q) {
+            for (int q = 8 * kq; q < 8 * kq + 8; ++q) {
                 uint32_t a[4], b[4];
                 // A = Xb2 rows t, k = hidden: (t0, 2q), (t1, 2q), (t0, 2q+1), (t1, 2q+1)
                 ptx::ldsm_x4(xb2t + xh_off((mat & 1) * 8 + mrow, 2 * q + (mat >> 1)), a);
@@ -607,24 +642,39 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 ptx::ldsm_x4(x2t + xh_off(half * 8 + mrow, 2 * q + (mat & 1)), b);
                 ptx::mma_bf16((q & 1) ? ac2 : acc, a, b[0], b[1]);
             }
-            const int s0 = half * 8 + 2 * c;
-            const float e0 = eta_at(n, s0), e1 = eta_at(n, s0 + 1);
-            const float v0 = s0 > g ? 0.f : e0 * (acc[0] + ac2[0] + 1.f);
-            const float v1 = s0 + 1 > g ? 0.f : e1 * (acc[1] + ac2[1] + 1.f);
-            const float v2 = s0 > g + 8 ? 0.f : e0 * (acc[2] + ac2[2] + 1.f);
-            const float v3 = s0 + 1 > g + 8 ? 0.f : e1 * (acc[3] + ac2[3] + 1.f);
-            *reinterpret_cast<uint2 *>(s.a2f[half][lane]) = make_uint2(ptx::pack_bf16(v0, v1), ptx::pack_bf16(v2, v3));
-            ptx::named_bar(kBarOut, 192);
-        } else if (lnw) {
-            float zb[2][4];
-            second_layer(zb, xb2t, b2_start0, b2_start1);
-            ptx::named_bar(kBarOut, 192);
-            const uint2 f0 = *reinterpret_cast<const uint2 *>(s.a2f[0][lane]);
-            const uint2 f1 = *reinterpret_cast<const uint2 *>(s.a2f[1][lane]);
+            *reinterpret_cast<float4 *>(s.parta2[half][kq][lane]) =
+                make_float4(acc[0] + ac2[0], acc[1] + ac2[1], acc[2] + ac2[2], acc[3] + ac2[3]);
+            float4 *dst = reinterpret_cast<float4 *>(s.part2[warp & 3][lane]);
+            dst[0] = make_float4(zb[0][0], zb[0][1], zb[0][2], zb[0][3]);
+            dst[1] = make_float4(zb[1][0], zb[1][1], zb[1][2], zb[1][3]);
+        }
+        ptx::named_bar(kBarAll, kCompute * 32);
+        if (lnw) {
+            {
+                const float4 p0 = reinterpret_cast<const float4 *>(s.part2[warp][lane])[0];
+                const float4 p1 = reinterpret_cast<const float4 *>(s.part2[warp][lane])[1];
+                zb[0][0] += p0.x; zb[0][1] += p0.y; zb[0][2] += p0.z; zb[0][3] += p0.w;
+                zb[1][0] += p1.x; zb[1][1] += p1.y; zb[1][2] += p1.z; zb[1][3] += p1.w;
+            }
+            // B fragments (k = source s, n = target t) of the block, per source half
+            uint32_t f[2][2];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const float4 p = *reinterpret_cast<const float4 *>(s.parta2[half][0][lane]);
+                const float4 q2 = *reinterpret_cast<const float4 *>(s.parta2[half][1][lane]);
+                const int s0 = half * 8 + 2 * c;
+                const float e0 = eta_at(n, s0), e1 = eta_at(n, s0 + 1);
+                const float v0 = s0 > g ? 0.f : e0 * (p.x + q2.x + 1.f);
+                const float v1 = s0 + 1 > g ? 0.f : e1 * (p.y + q2.y + 1.f);
+                const float v2 = s0 > g + 8 ? 0.f : e0 * (p.z + q2.z + 1.f);
+                const float v3 = s0 + 1 > g + 8 ? 0.f : e1 * (p.w + q2.w + 1.f);
+                f[half][0] = ptx::pack_bf16(v0, v1);
+                f[half][1] = ptx::pack_bf16(v2, v3);
+            }
             const uint32_t a[4] = {ptx::pack_bf16(-gm[0][0], -gm[0][1]), ptx::pack_bf16(-gm[0][2], -gm[0][3]),
                                    ptx::pack_bf16(-gm[1][0], -gm[1][1]), ptx::pack_bf16(-gm[1][2], -gm[1][3])};
-            ptx::mma_bf16(zb[0], a, f0.x, f1.x);
-            ptx::mma_bf16(zb[1], a, f0.y, f1.y);
+            ptx::mma_bf16(zb[0], a, f[0][0], f[1][0]);
+            ptx::mma_bf16(zb[1], a, f[0][1], f[1][1]);
             float z[2][4];
             if (LN) {
                 float zs[8];
