@@ -16,9 +16,10 @@
 // G_{n+1}; the d x d update and both d x d products are off that chain.
 //
 // B300 design.  The scan is latency-bound: 16 tokens of one (batch, head) per
-// step, each step waiting on the last.  One CTA per (batch, head), five warps:
-//   * warp 4 streams 64-token stages of Q, K, V (TMA, 128-byte swizzle) and
-//     eta (bulk copy) into a 6-deep shared-memory ring, mbarrier-synchronised;
+// step, each step waiting on the last.  One CTA per (batch, head), four warps:
+//   * 64-token stages of Q, K, V (TMA, 128-byte swizzle) and eta (bulk copy)
+//     stream into a 6-deep shared-memory ring; thread 0 refills a slot right after
+//     the step barrier that retires it (no separate copy warp);
 //   * warps 0-3 each own 16 output features.  W^T lives in registers as fp32
 //     warp-MMA accumulators for the whole scan; every contraction is a
 //     bf16 m16n8k16 MMA on register fragments, so the recurrence never leaves
@@ -57,7 +58,7 @@ constexpr int TPS = ST / MB;    // mini-batches per stage
 constexpr int NSS = 6;          // stages in the ring
 constexpr int NZ = 4;           // Z staging tiles
 constexpr int kMathThreads = 128;
-constexpr int kThreads = 160;
+constexpr int kThreads = 128;
 constexpr uint32_t kStageTileBytes = ST * D * 2;   // 8 KB
 
 struct __align__(1024) Smem {
@@ -73,7 +74,6 @@ struct __align__(1024) Smem {
     float red[2][MB][36];             // six backward sums (+ 2 spare quantities)
     float zred[2][MB][12];            // output sums: z, z^2
     unsigned long long full[NSS];
-    unsigned long long empty[NSS];
     int abort_flag;
 };
 
@@ -120,50 +120,33 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int N = p.L / MB;                 // mini-batches
     const int NST = (p.L + ST - 1) / ST;    // stages
 
+    // stage st -> ring slot st % NSS.  There is no copy warp (a waiting copy warp would share
+    // a sub-partition with a math warp): thread 0 issues the first stages, and lane 0 of warp
+    // 3 (warp 0 already issues the Z stores) refills a slot right after the barrier that
+    // retires it.
+    const float *eta_bh = p.eta + (size_t)bh * p.L;
+    auto issue_stage = [&](int st) {
+        const int b = st % NSS, ntok = min(ST, p.L - st * ST);
+        const uint32_t fb = ptx::smem_addr(&s.full[b]);
+        ptx::mbar_arrive_expect_tx(fb, 3 * kStageTileBytes + ntok * 4);
+        ptx::tma_load_3d(ptx::smem_addr(s.q[b]), &tmQ, fb, 0, st * ST, bh);
+        ptx::tma_load_3d(ptx::smem_addr(s.k[b]), &tmK, fb, 0, st * ST, bh);
+        ptx::tma_load_3d(ptx::smem_addr(s.v[b]), &tmV, fb, 0, st * ST, bh);
+        ptx::bulk_load(ptx::smem_addr(s.eta[b]), eta_bh + st * ST, ntok * 4, fb);
+    };
+    const int nissue = p.withhold_loads ? 0 : NST;
+    const int kRefill = 96;
+    int issued = min(NSS, nissue);   // stages handed to the copy engine so far
     if (tid == 0) {
-        for (int i = 0; i < NSS; ++i) {
-            ptx::mbar_init(ptx::smem_addr(&s.full[i]), 1);
-            ptx::mbar_init(ptx::smem_addr(&s.empty[i]), 1);
-        }
+        for (int i = 0; i < NSS; ++i) ptx::mbar_init(ptx::smem_addr(&s.full[i]), 1);
         s.abort_flag = 0;
         ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmQ);
+        ptx::prefetch_tmap(&tmK);
+        ptx::prefetch_tmap(&tmV);
+        for (int st = 0; st < issued; ++st) issue_stage(st);
     }
     __syncthreads();
-
-    // ------------------------------------------------------------------ producer
-    if (warp == 4) {
-        if (lane == 0) {
-            ptx::prefetch_tmap(&tmQ);
-            ptx::prefetch_tmap(&tmK);
-            ptx::prefetch_tmap(&tmV);
-            const float *eta_bh = p.eta + (size_t)bh * p.L;
-            int issued = 0;
-            for (int st = 0; st < (p.withhold_loads ? 0 : NST); ++st) {
-                const int b = st % NSS;
-                if (st >= NSS) {
-                    if (*(volatile int *)&s.abort_flag) break;
-                    if (!ptx::mbar_wait_bounded(ptx::smem_addr(&s.empty[b]), ((st / NSS) - 1) & 1,
-                                                p.wait_ns)) {
-                        *(volatile int *)&s.abort_flag = 1;
-                        atomicOr(p.status, kStatusTimeout);
-                        break;
-                    }
-                }
-                const int ntok = min(ST, p.L - st * ST);
-                const uint32_t fb = ptx::smem_addr(&s.full[b]);
-                ptx::mbar_arrive_expect_tx(fb, 3 * kStageTileBytes + ntok * 4);
-                ptx::tma_load_3d(ptx::smem_addr(s.q[b]), &tmQ, fb, 0, st * ST, bh);
-                ptx::tma_load_3d(ptx::smem_addr(s.k[b]), &tmK, fb, 0, st * ST, bh);
-                ptx::tma_load_3d(ptx::smem_addr(s.v[b]), &tmV, fb, 0, st * ST, bh);
-                ptx::bulk_load(ptx::smem_addr(s.eta[b]), eta_bh + st * ST, ntok * 4, fb);
-                issued = st + 1;
-            }
-            // every copy issued must land before the CTA may exit
-            for (int st = max(0, issued - NSS); st < issued; ++st)
-                ptx::mbar_wait_bounded(ptx::smem_addr(&s.full[st % NSS]), (st / NSS) & 1, kDrainNs);
-        }
-        return;
-    }
 
     // ------------------------------------------------------------------ math warps
     const int g = lane >> 2, c = lane & 3, mrow = lane & 7, mat = lane >> 3;
@@ -603,9 +586,13 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 ptx::tma_store_3d(&tmZ, ptx::smem_addr(s.z[(n - 2) % NZ]), 0, (n - 2) * MB, bh);
                 ptx::bulk_commit();
             }
-            // the stage holding n - 1 is no longer read (its last reader, the update
-            // with G_{n-1}, ran before this barrier)
-            if (n >= 1 && (n % TPS) == 0) ptx::mbar_arrive(ptx::smem_addr(&s.empty[((n / TPS) - 1) % NSS]));
+        }
+        if (tid == kRefill && n >= TPS && n % TPS == 0 && n / TPS - 1 + NSS < nissue && !aborted) {
+            // the stage holding n - 1 is no longer read (its last reader, the update with
+            // G_{n-1}, ran before this step's barrier): refill its slot
+            ptx::fence_proxy_async();
+            issue_stage(n / TPS - 1 + NSS);
+            issued = n / TPS + NSS;
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u)
@@ -633,6 +620,9 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             ptx::bulk_wait<0>();
         }
     }
+    if (tid == kRefill)   // copies still in flight (only after a wait ran out) land before exit
+        for (int st = max(0, issued - NSS); st < issued; ++st)
+            ptx::mbar_wait_bounded(ptx::smem_addr(&s.full[st % NSS]), (st / NSS) & 1, kDrainNs);
     {
         float *Wf = p.Wf + (size_t)bh * D * D;
 #pragma unroll
