@@ -1,6 +1,6 @@
 // ptx.cuh -- thin inline-PTX wrappers used by the sm_103a kernels: mbarrier,
-// TMA (cp.async.bulk.tensor), bulk copies, warp-level MMA, ldmatrix/stmatrix,
-// and tcgen05 (tensor memory allocation, MMA, commit, loads).
+// TMA (cp.async.bulk.tensor), bulk copies, named barriers, warp-level MMA and
+// ldmatrix/stmatrix.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -25,11 +25,6 @@ __device__ __forceinline__ void fence_mbar_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -44,21 +39,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
         "selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// As mbar_try_wait, but lets the thread sleep (up to `hint_ns`) until the phase
-// completes instead of returning at once, so waiting warps leave the issue
-// slots to the working ones.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-        "selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -207,146 +187,21 @@ __device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t *r)
                  : "memory");
 }
 
-// Transpose of one 8x8 b16 matrix held in the mma fragment layout.
-__device__ __forceinline__ uint32_t movm_t(uint32_t a)
+// Two-matrix forms, transposed: lanes 0-7 address the rows of matrix 0, lanes 8-15 those of
+// matrix 1 (the addresses of lanes 16-31 are not used).
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t *r)
 {
-    uint32_t d;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
-    return d;
-}
-
-__device__ __forceinline__ void red_add_shared(uint32_t addr, float v)
-{
-    asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
-{
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-// ---------------------------------------------------------------- tcgen05 (cta_group::1)
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
-{
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(addr)
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_relinquish()
+__device__ __forceinline__ void stsm_x2_t(uint32_t addr, const uint32_t *r)
 {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+    asm volatile("stmatrix.sync.aligned.m8n8.x2.trans.shared.b16 [%0], {%1,%2};" ::"r"(addr), "r"(r[0]),
+                 "r"(r[1])
                  : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// The mbarrier completes one phase arrival when every tcgen05 operation this
-// thread issued before the commit has finished.
-__device__ __forceinline__ void tc_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 operands, fp32 accumulate).
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate)
-{
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Shared-memory matrix descriptor: start address, leading / stride byte
-// offsets, descriptor version 1, layout (0 none, 2 = 128-byte swizzle,
-// 6 = 32-byte swizzle).
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout)
-{
-    return (uint64_t)((addr >> 4) & 0x3fff) | ((uint64_t)((lbo >> 4) & 0x3fff) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3fff) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
-}
-// K-major operand stored as 128-byte swizzled rows (64 bf16 per row), 8-row groups 1 KB apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) { return sdesc(addr, 16, 1024, 2); }
-// MN-major operand whose MN extent is one 128-byte swizzled row; K rows in 8-row groups 1 KB apart.
-__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr) { return sdesc(addr, 8192, 1024, 2); }
-// K-major operand stored as 32-byte swizzled rows (16 bf16 per row), 8-row groups 256 B apart.
-__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t addr) { return sdesc(addr, 16, 256, 6); }
-
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major,
-                                                  bool negate_a)
-{
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((negate_a ? 1u : 0u) << 13) |
-           ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-
-// 16 lanes x 256 bits: the mma.sync C-fragment layout (lane g = lane/4 rows g
-// and g+8, columns 2(lane%4), +1), repeated over .xN groups of 8 columns.
-__device__ __forceinline__ void tc_ld16_x1(uint32_t taddr, uint32_t *r)
-{
-    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(taddr));
-}
-
-__device__ __forceinline__ void tc_ld16_x2(uint32_t taddr, uint32_t *r)
-{
-    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                   "=r"(r[7])
-                 : "r"(taddr));
-}
-
-__device__ __forceinline__ void tc_ld16_x8(uint32_t taddr, uint32_t *r)
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tc_st16_x1(uint32_t taddr, const uint32_t *r)
-{
-    asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]),
-                 "r"(r[1]), "r"(r[2]), "r"(r[3])
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_st16_x8(uint32_t taddr, const uint32_t *r)
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Byte offset of (row, 16-byte chunk) inside a tile of 32-byte rows with the
-// 32-byte swizzle (chunk XOR bit 2 of the row).  Tile base 256-byte aligned.
-__device__ __forceinline__ uint32_t sw32(int row, int chunk)
-{
-    return (uint32_t)(row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4));
 }
 
 }  // namespace ptx

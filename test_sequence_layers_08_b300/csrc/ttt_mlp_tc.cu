@@ -15,7 +15,7 @@
 // B300 design.  One CTA per (batch, head), eight warps (two per SM sub-partition, so
 // each thread may hold 224 registers):
 //   * 64-token stages of Q, K, V (TMA, 128-byte swizzle) and eta stream into a 4-deep
-//     shared-memory ring; thread 0 refills a slot right after the barrier that retires it;
+//     shared-memory ring; thread 0 refills a slot once no warp reads it any more;
 //   * warps 0-7 each own 32 of the 256 hidden units: their rows of W1^T and of W2 stay in
 //     registers as fp32 warp-MMA accumulators for the whole scan.  Every contraction is a
 //     bf16 m16n8k16 warp MMA.  Contractions inside a warp's hidden slice (Z1, Q W1, G1,
@@ -29,7 +29,8 @@
 //     w + 4 take units 0-127 and 128-255 for the outputs of warp w, and warps 4-7 hand
 //     their fp32 partials over through shared memory; the 16 x 16 Gram Xb2 X2^T is split
 //     the same way over warps 4-7.
-// Per mini-batch the warps meet at six named barriers; every mbarrier wait is bounded.
+// Per mini-batch all eight warps meet at five named barriers (warps 4-7 run into the next
+// mini-batch's first layer while warps 0-3 finish the output); every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -105,18 +106,41 @@ __device__ __noinline__ bool mlp_wait_slow(uint32_t bar, uint32_t parity, long l
 // X2 / Xb2 tile: row t (token), 16-byte chunk ch (8 hidden units)
 __device__ __forceinline__ uint32_t xh_off(int t, int ch) { return (uint32_t)(t * 512 + ((ch ^ (t & 7)) << 4)); }
 
-__device__ __forceinline__ float gelu(float x)
+// GELU(tanh) in its logistic form: 1/2 (1 + tanh(u)) = 1 / (1 + exp(-2u)) = p with
+// u = sqrt(2/pi) (x + 0.044715 x^3), so GELU(x) = x p and, since 1/2 (1 - tanh(u)^2) = 2 p (1 - p),
+// GELU'(x) = p + x p (1 - p) 2 du/dx.  exp2 and the reciprocal are the PTX approximate
+// instructions: their relative error is far below the bf16 rounding of every GELU value,
+// which becomes an MMA operand right after.  Large |u| saturate cleanly (exp2 -> 0 or inf,
+// p -> 1 or 0).
+__device__ __forceinline__ float ex2_fast(float x)
 {
-    const float s = 0.7978845608028654f;   // sqrt(2/pi)
-    return 0.5f * x * (1.f + tanhf(s * (x + 0.044715f * x * x * x)));
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
-// GELU(x) and GELU'(x) from one tanh
+__device__ __forceinline__ float rcp_fast(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kGs = 0.7978845608028654f;            // sqrt(2/pi)
+constexpr float kGa = 0.044715f;
+constexpr float kGk = -2.f * kGs * 1.4426950408889634f; // -2 sqrt(2/pi) log2(e)
+__device__ __forceinline__ float gelu_p(float x)      // 1/2 (1 + tanh(u))
+{
+    const float x2 = x * x;
+    return rcp_fast(1.f + ex2_fast(kGk * x * fmaf(kGa, x2, 1.f)));
+}
+__device__ __forceinline__ float gelu(float x) { return x * gelu_p(x); }
 __device__ __forceinline__ void gelu_and_prime(float x, float &y, float &dy)
 {
-    const float s = 0.7978845608028654f;
-    const float th = tanhf(s * (x + 0.044715f * x * x * x));
-    y = 0.5f * x * (1.f + th);
-    dy = 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * s * (1.f + 3.f * 0.044715f * x * x);
+    const float x2 = x * x;
+    const float pr = rcp_fast(1.f + ex2_fast(kGk * x * fmaf(kGa, x2, 1.f)));
+    y = x * pr;
+    // du/dx * 2 = 2 sqrt(2/pi) (1 + 3 a x^2)
+    const float du2 = fmaf(6.f * kGs * kGa, x2, 2.f * kGs);
+    dy = fmaf(x * du2, pr - pr * pr, pr);
 }
 
 template <bool LN>
@@ -725,13 +749,13 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 uint4 *dst = reinterpret_cast<uint4 *>(Zg + ((size_t)bh * p.L + (size_t)n * MB + row) * D) + ch;
                 *dst = val;
             }
-        }
-        ptx::named_bar(kBarAll, kCompute * 32);
-        // every warp is past its last read of stage st: refill its slot
-        if (tid == 0 && n % TPS == TPS - 1 && st + NSS < nissue && !aborted) {
-            ptx::fence_proxy_async();
-            issue_stage(st + NSS);
-            issued = st + NSS + 1;
+            // warps 4-7 have not read stage st since the barrier before this step's output
+            // layer, warps 0-3 since the barrier above: refill its slot
+            if (tid == 0 && n % TPS == TPS - 1 && st + NSS < nissue && !aborted) {
+                ptx::fence_proxy_async();
+                issue_stage(st + NSS);
+                issued = st + NSS + 1;
+            }
         }
     }
     // copies still in flight (only after a wait ran out) must land before the CTA exits
