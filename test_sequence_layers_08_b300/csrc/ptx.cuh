@@ -187,22 +187,5 @@ __device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t *r)
                  : "memory");
 }
 
-// Two-matrix forms, transposed: lanes 0-7 address the rows of matrix 0, lanes 8-15 those of
-// matrix 1 (the addresses of lanes 16-31 are not used).
-__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t *r)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
-                 : "=r"(r[0]), "=r"(r[1])
-                 : "r"(addr)
-                 : "memory");
-}
-
-__device__ __forceinline__ void stsm_x2_t(uint32_t addr, const uint32_t *r)
-{
-    asm volatile("stmatrix.sync.aligned.m8n8.x2.trans.shared.b16 [%0], {%1,%2};" ::"r"(addr), "r"(r[0]),
-                 "r"(r[1])
-                 : "memory");
-}
-
 }  // namespace ptx
 }  // namespace ttt

@@ -12,8 +12,9 @@
 //   Zb2 = Xb2 W2 + b2 - (eta_s (Xb2_t . X2_s + 1) [s <= t]) G2,   Z = Q + LN(Zb2)
 // with the weights of the mini-batch start on the right-hand sides.
 //
-// B300 design.  One CTA per (batch, head), eight warps (two per SM sub-partition, so
-// each thread may hold 224 registers):
+// B300 design.  One CTA per (batch, head), eight warps: two per SM sub-partition, so each
+// thread may hold 255 registers (two warps fill a sub-partition's register file) and the
+// fp32 weight slices plus the step's temporaries fit without spilling:
 //   * 64-token stages of Q, K, V (TMA, 128-byte swizzle) and eta stream into a 4-deep
 //     shared-memory ring; thread 0 refills a slot once no warp reads it any more;
 //   * warps 0-7 each own 32 of the 256 hidden units: their rows of W1^T and of W2 stay in
@@ -144,7 +145,7 @@ __device__ __forceinline__ void gelu_and_prime(float x, float &y, float &dy)
 }
 
 template <bool LN>
-__global__ void __maxnreg__(224)
+__global__ void __maxnreg__(255)
 mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, Params p, __nv_bfloat16 *Zg)
 {
