@@ -100,7 +100,7 @@ def test_head_shards_reassemble_the_single_process_result():
 
 
 def test_reference_arm_under_torchrun_prints_once():
-    """`bench.py --impl reference` launched like the driver does for N = 2: rank 0 alone
+    """`bench.py --impl reference` launched by torchrun with two ranks: rank 0 alone
     runs the oracle and prints one JSON line; rank 1 exits 0 without work."""
     port = free_port()
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
