@@ -126,8 +126,8 @@ TTT_API ttt_status ttt_sync_status(ttt_stream_t stream);
 TTT_API void ttt_set_wait_timeout_ns(long long ns);
 
 /*
- * Test hook for the timeout path: while `on` is non-zero, the copy-issuing warp
- * of the fused kernels issues no copies, so every wait for data runs out after
+ * Test hook for the timeout path: while `on` is non-zero, the fused kernels
+ * issue no copies of the input stages, so every wait for data runs out after
  * the timeout above and the call reports TTT_ERR_TIMEOUT (outputs unspecified).
  * Nothing faults or hangs.  Process-wide; leave it off outside tests.
  */

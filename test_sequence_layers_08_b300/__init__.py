@@ -188,8 +188,8 @@ def set_wait_timeout_ns(ns: int):
 
 
 def debug_withhold_loads(on: bool):
-    """Test hook: the fused kernels' copy warp issues no copies, so their waits
-    run out and the next ttt_sync_status reports TTT_ERR_TIMEOUT."""
+    """Test hook: the fused kernels issue no stage copies, so their waits run out
+    and the next ttt_sync_status reports TTT_ERR_TIMEOUT."""
     load().ttt_debug_withhold_loads(int(bool(on)))
 
 
