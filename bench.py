@@ -460,6 +460,157 @@ def run_ours(args, cfg, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_decode(args, cfg, world, rank, local):
+    """Decode: `ttt_linear_step` on the workload's (B, H, d, I/O type, LayerNorm) with
+    args.decode tokens per call, processed one at a time from a state carried in device memory
+    between calls.  Consecutive calls rotate over enough (inputs, state) sets that their union
+    exceeds L2; each set carries its own state from call to call.  A decode call is a few
+    microseconds of GPU work, less than the Python binding's host cost, so the calls are
+    captured in a CUDA graph (as a serving loop would run them) and the graph is replayed."""
+    import torch
+    import test_sequence_layers_08_b300 as ttt
+    if cfg.kind != "linear":
+        raise SystemExit("--decode runs the TTT-Linear decode step: pick a linear workload")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    T = args.decode
+    dcfg = cfg.with_(L=T, mini_batch=1)
+    x = make_inputs(dcfg, 0)
+    io = torch.bfloat16 if cfg.io == "bf16" else torch.float32
+    es = 2 if cfg.io == "bf16" else 4
+    BH, d = cfg.B * cfg.H, cfg.d
+    state_bytes = BH * (d * d + d) * 4
+    io_bytes = BH * T * (4 * d * es + 4)
+    alg_bytes = 2 * state_bytes + io_bytes            # state read and written once per call
+    alg_flops = 2 * 3 * d * d * BH * T                # k W, the rank-1 update, q W per token
+    n_sets = max(2, min(128, math.ceil(3 * L2_BYTES / (state_bytes + io_bytes))))
+    W0 = np.broadcast_to(x["W0"], (cfg.B, cfg.H, d, d))
+    b0 = np.broadcast_to(x["b0"], (cfg.B, cfg.H, d))
+    gamma = None if x["gamma"] is None else torch.from_numpy(x["gamma"]).to(dev)
+    beta = None if x["beta"] is None else torch.from_numpy(x["beta"]).to(dev)
+    qkv = {k: torch.from_numpy(x[k]).to(dev).to(io) for k in ("Q", "K", "V")}
+    eta = torch.from_numpy(x["eta"]).to(dev)
+    sets = []
+    for _ in range(n_sets):
+        sets.append(dict(Q=qkv["Q"].clone(), K=qkv["K"].clone(), V=qkv["V"].clone(),
+                         eta=eta.clone(), W=torch.from_numpy(np.ascontiguousarray(W0)).to(dev),
+                         b=torch.from_numpy(np.ascontiguousarray(b0)).to(dev),
+                         Z=torch.empty_like(qkv["Q"])))
+    stream = torch.cuda.current_stream(dev)
+
+    def call(s_):   # on the current stream (the capture stream inside a graph capture)
+        ttt.ttt_linear_step(s_["Q"], s_["K"], s_["V"], s_["eta"], s_["W"], s_["b"], gamma, beta,
+                            residual_ln=cfg.ln, ln_eps=cfg.eps, out=s_["Z"])
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(max(args.warmup, n_sets)):
+        call(sets[i % n_sets])
+    ttt.ttt_sync_status(stream)
+    per_graph = n_sets                      # one call on every set per replay
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(per_graph):
+            call(sets[i])
+    replays = max(1, math.ceil(args.steps / per_graph))
+    t_soak = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    e1.synchronize()
+    soak_n = int(min(20000, max(0, args.soak_ms / max(e0.elapsed_time(e1), 1e-3))))
+    for _ in range(soak_n):
+        graph.replay()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ttt.ttt_sync_status(stream)
+    n_calls = replays * per_graph
+    ms_step = max_over_ranks(world, start.elapsed_time(end)) / n_calls
+    value = world * cfg.B * T / (ms_step * 1e-3)
+    time.sleep(0.4)
+    clk = clocks.summary(t_soak, time.time())
+
+    # end to end: every call copies its tokens in and its outputs out; the state stays on
+    # the device (the decode cache)
+    s0_ = sets[0]
+    in_keys = ["Q", "K", "V", "eta"]
+    hin_flat, hin = packed([(tuple(s0_[k].shape), s0_[k].dtype) for k in in_keys], "cpu", pin=True)
+    for k, hv in zip(in_keys, hin):
+        hv.copy_(s0_[k].cpu())
+    din_flat, din = packed([(tuple(s0_[k].shape), s0_[k].dtype) for k in in_keys], dev)
+    e2e_set = dict(zip(in_keys, din), W=s0_["W"], b=s0_["b"], Z=s0_["Z"])
+    hz = torch.empty(s0_["Z"].shape, dtype=s0_["Z"].dtype).pin_memory()
+
+    def e2e_call():
+        din_flat.copy_(hin_flat, non_blocking=True)
+        call(e2e_set)
+        hz.copy_(e2e_set["Z"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_call()
+    torch.cuda.synchronize(dev)
+    e2e_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(e2e_graph):
+        for _ in range(per_graph):
+            e2e_call()
+    e2e_graph.replay()
+    torch.cuda.synchronize(dev)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(replays):
+        e2e_graph.replay()
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(world, s0.elapsed_time(s1)) / n_calls
+    e2e_value = world * cfg.B * T / (e2e_ms * 1e-3)
+    clocks.stop()
+
+    peaks = load_peaks()
+    achieved = alg_bytes / (ms_step * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peaks["source"],
+            "kernel": "ttt_linear_decode" if d == 64 else "ttt_linear_generic",
+            "algorithmic_bytes": alg_bytes, "algorithmic_flops": alg_flops,
+            "roofline_ms": alg_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 1
+        rate, sample = oracle_rate(dcfg, x, args.cpu_seconds, threads)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": sample.replace("scans at full", "decode calls of")}
+    if rank == 0:
+        line = {"metric": "TTT-Linear decode tokens/s (one token at a time from a carried "
+                          "state) at 1 B300 and % of roofline",
+                "value": value, "unit": "tokens/s", "n_gpus": world, "steps": n_calls,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if cfg.io == "bf16" else "f32", "data": "synthetic",
+                "config": {"workload": f"decode_{cfg.name}_T{T}", "kind": "linear_decode",
+                           "B": cfg.B, "H": cfg.H, "tokens_per_call": T, "d": d, "io": cfg.io,
+                           "state": "f32", "residual_ln": cfg.ln,
+                           "l2": f"calls rotate over {n_sets} (inputs, state) sets "
+                                 f"({n_sets * (state_bytes + io_bytes) / 1e6:.0f} MB > L2)",
+                           "parallelism": f"replica x{world}, one warp per (batch, head)"},
+                "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": "tokens/s",
+                        "h2d_bytes_per_step": hin_flat.numel(),
+                        "d2h_bytes_per_step": hz.numel() * hz.element_size(),
+                        "schedule": "per call: one host->device copy of the tokens, the call, "
+                                    "one device->host copy of Z; the state stays on the device; "
+                                    "CUDA graph of the calls"},
+                "gpu_launches": n_calls, "clocks": clk,
+                "launch": f"CUDA graph of {per_graph} calls, replayed {replays} times"}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -471,6 +622,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="reference arm: host time spread over warm-up and timed steps")
+    ap.add_argument("--decode", type=int, default=0, metavar="T",
+                    help="time the decode step instead: T tokens per call, one at a time, from a "
+                         "state carried between calls (a linear workload's B, H, d)")
     ap.add_argument("--soak-ms", type=float, default=1500.0,
                     help="untimed load before the timed region, so the clock samples describe "
                          "this workload (0 under a profiler)")
@@ -482,6 +636,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, cfg, world, rank)
+        elif args.decode > 0:
+            run_decode(args, cfg, world, rank, local)
         else:
             run_ours(args, cfg, world, rank, local)
     finally:

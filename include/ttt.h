@@ -109,6 +109,26 @@ TTT_API ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *
                        float *b2_f, ttt_stream_t stream);
 
 /*
+ * TTT-Linear decode step (the state carried between calls, like a cache).
+ * The desc->L tokens of every (batch, head) are processed one at a time: the
+ * mini-batch form with desc->mini_batch == 1 (required), which is the per-token
+ * recurrence itself.  The state is per (batch, head) and updated in place:
+ *   in : Q, K, V [B,H,L,d] (io_dtype); eta [B,H,L]; gamma, beta [H, d] (NULL
+ *        allowed without LN);
+ *   in/out: W [B,H,d,d], b [B,H,d] (float): read as the state before the first
+ *        token, overwritten with the state after the last one;
+ *   out: Z [B,H,L,d] (io_dtype), z_t = f(q_t; W_t, c_t) after token t's update.
+ * Calling it T times with one token each gives the same result as one call
+ * with the T tokens.  desc->init_per_batch is ignored (the state is always
+ * [B, H, ...]).  Supported: any d <= 128; d = 64 runs the decode kernel (one
+ * warp per (batch, head), FP32), other d the generic kernel.  Z must not alias
+ * an input, and W, b must not alias any other buffer.
+ */
+TTT_API ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const void *K, const void *V,
+                                   const float *eta, float *W, float *b, const float *gamma,
+                                   const float *beta, void *Z, ttt_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports TTT_ERR_CUDA if a CUDA error is pending
  * and TTT_ERR_TIMEOUT if any kernel launched by this library on the current
  * device since the previous ttt_sync_status call gave up on a bounded wait

@@ -17,7 +17,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["TTTError", "Desc", "load", "library_path", "ttt_linear_fwd", "ttt_mlp_fwd",
+__all__ = ["TTTError", "Desc", "load", "library_path", "ttt_linear_fwd", "ttt_mlp_fwd", "ttt_linear_step",
            "ttt_sync_status", "kernel_name", "version", "STATUS", "set_wait_timeout_ns",
            "debug_withhold_loads"]
 
@@ -60,6 +60,8 @@ def load():
             vp, dp = ctypes.c_void_p, ctypes.POINTER(Desc)
             lib.ttt_linear_fwd.restype = ctypes.c_int
             lib.ttt_linear_fwd.argtypes = [dp] + [vp] * 12
+            lib.ttt_linear_step.restype = ctypes.c_int
+            lib.ttt_linear_step.argtypes = [dp] + [vp] * 10
             lib.ttt_mlp_fwd.restype = ctypes.c_int
             lib.ttt_mlp_fwd.argtypes = [dp] + [vp] * 16
             lib.ttt_sync_status.restype = ctypes.c_int
@@ -150,6 +152,32 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: i
                               _ptr(beta if residual_ln else None), _ptr(Z), _ptr(Wf), _ptr(bf),
                               _stream_handle(stream)))
     return Z, Wf, bf
+
+
+def ttt_linear_step(Q, K, V, eta, W, b, gamma=None, beta=None, *, residual_ln: bool = False,
+                    ln_eps: float = 1e-6, out=None, stream=None):
+    """TTT-Linear decode on the GPU: the L tokens of Q, K, V [B,H,L,d] one at a time from
+    the state W [B,H,d,d], b [B,H,d] (float32), which is updated in place.  Returns Z
+    [B,H,L,d]; pass ``out=Z`` to reuse a buffer.  Asynchronous on ``stream``."""
+    import torch
+    lib = load()
+    desc = make_desc(Q, 1, residual_ln, ln_eps, True)
+    dev = Q.device
+    for n, t in (("K", K), ("V", V)):
+        _check_tensor(n, t, Q.dtype, dev)
+    for n, t in (("eta", eta), ("W", W), ("b", b)):
+        _check_tensor(n, t, torch.float32, dev)
+    if residual_ln:
+        _check_tensor("gamma", gamma, torch.float32, dev)
+        _check_tensor("beta", beta, torch.float32, dev)
+    B, H, L, d = Q.shape
+    if tuple(W.shape) != (B, H, d, d) or tuple(b.shape) != (B, H, d):
+        raise ValueError("W must be [B,H,d,d] and b [B,H,d]")
+    Z = torch.empty_like(Q) if out is None else out
+    _check(lib.ttt_linear_step(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta), _ptr(W),
+                               _ptr(b), _ptr(gamma if residual_ln else None),
+                               _ptr(beta if residual_ln else None), _ptr(Z), _stream_handle(stream)))
+    return Z
 
 
 def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_batch: int = 16,

@@ -194,6 +194,55 @@ ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, co
     return ok();
 }
 
+ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const void *K, const void *V,
+                           const float *eta, float *W, float *b, const float *gamma,
+                           const float *beta, void *Z, ttt_stream_t stream)
+{
+    ttt_status st = check_desc(desc, false);
+    if (st != TTT_OK) return st;
+    ttt_desc s = *desc;
+    if (s.mini_batch != 1) return fail(TTT_ERR_INVALID_ARG, "ttt_linear_step needs mini_batch == 1");
+    s.init_per_batch = 1;
+    const void *ptrs[] = {Q, K, V, eta, W, b, Z};
+    const char *names[] = {"Q", "K", "V", "eta", "W", "b", "Z"};
+    for (int i = 0; i < 7; ++i)
+        if ((st = check_ptr(ptrs[i], names[i])) != TTT_OK) return st;
+    if (s.residual_ln) {
+        if ((st = check_ptr(gamma, "gamma")) != TTT_OK) return st;
+        if ((st = check_ptr(beta, "beta")) != TTT_OK) return st;
+    }
+    const size_t es = s.io_dtype == TTT_BF16 ? 2 : 4;
+    const size_t BH = (size_t)s.B * s.H, tok = BH * s.L * s.d;
+    const Range rq = range_of(Q, tok * es), rk = range_of(K, tok * es), rv = range_of(V, tok * es),
+                re = range_of(eta, BH * s.L * 4), rw = range_of(W, BH * s.d * s.d * 4),
+                rb = range_of(b, BH * s.d * 4), rz = range_of(Z, tok * es),
+                rg = range_of(gamma, s.residual_ln ? s.H * s.d * 4 : 0),
+                rbe = range_of(beta, s.residual_ln ? s.H * s.d * 4 : 0);
+    const Range all[] = {rq, rk, rv, re, rw, rb, rz, rg, rbe};
+    for (int i = 0; i < 9; ++i)
+        for (int j = i + 1; j < 9; ++j) {
+            const bool in_in = i < 4 && j < 4;   // inputs may share memory with each other
+            const bool params = i >= 7 && j >= 7;
+            if (!in_in && !params && overlap(all[i], all[j]))
+                return fail(TTT_ERR_INVALID_ARG, "W, b and Z must not overlap another buffer");
+        }
+    ttt::LinearArgs la{s, Q, K, V, eta, W, b, gamma, beta, Z, W, b,
+                       reinterpret_cast<cudaStream_t>(stream), nullptr};
+    if (!ttt::linear_decode_supported(s) && !ttt::linear_generic_smem_bytes(s))
+        return fail(TTT_ERR_UNSUPPORTED, "no decode kernel for d=%d", s.d);
+    la.status = failure_flag(&st);
+    if (st != TTT_OK) return st;
+    cudaError_t e;
+    if (ttt::linear_decode_supported(s)) {
+        ttt::DecodeArgs a{s, Q, K, V, eta, W, b, gamma, beta, Z, la.stream};
+        e = ttt::launch_linear_decode(a);
+    } else {
+        e = ttt::launch_linear_generic(la);   // reads its state slice before writing it back
+    }
+    if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
                        const float *eta, const float *W1_0, const float *b1_0,
                        const float *W2_0, const float *b2_0, const float *gamma,

@@ -1,0 +1,227 @@
+// ttt_decode.cu -- TTT-Linear decode: the tokens of a call are processed one at a time
+// (mini-batch size 1) from a fast-weight state (W, c) that lives in device memory between
+// calls and is updated in place.
+//
+// Per token t of every (batch, head) -- the update/apply recurrence of the damodev.csdn.net
+// TTT article, section 3.1 (the output reads the weights after the token's own update), with
+// mini-batch size 1 of sections 4.1-4.2 and the residual LayerNorm of the lryc.cn article,
+// section 2.1:
+//   z = k_t W + c
+//   g = z - v_t                      (plain)   or   g = LNbwd(z; v_t - k_t)   (residual LN)
+//   W -= eta_t k_t^T g,   c -= eta_t g
+//   o = q_t W + c,   Z_t = o   or   Z_t = q_t + LN(o)
+// with LNbwd the gradient of 1/2 |gamma xhat + beta - y|^2, xhat = (z - mu) r, through the
+// LayerNorm: g = r (gx - mean(gx) - xhat mean(gx xhat)), gx = gamma (gamma xhat + beta - y).
+//
+// B300 design.  A decode step is a chain of 64 x 64 matrix-vector products on a 16 KB state
+// per (batch, head): latency- and launch-bound work that suits FP32 FMA, not tensor cores.
+//   * one warp per (batch, head), four per CTA (one per SM sub-partition);
+//   * lane j holds columns 2j, 2j + 1 of W (128 registers) for all the call's tokens: W is
+//     read and written once per call;
+//   * each token's q and k rows are staged in a per-warp shared-memory row, so every lane
+//     reads k_i and q_i as 16-byte broadcasts;
+//   * sums over the 64 features are warp butterflies.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "ttt_internal.h"
+
+namespace ttt {
+namespace {
+
+constexpr int D = 64;
+constexpr int kWarps = 4;
+
+struct DecodeParams {
+    int BH, H, T;
+    float eps;
+    const void *Q, *K, *V;
+    const float *eta;
+    float *W, *b;
+    const float *gamma, *beta;
+    void *Z;
+};
+
+template <bool BF16>
+__device__ __forceinline__ float2 load_pair(const void *base, size_t idx)   // elements idx, idx + 1
+{
+    if (BF16) {
+        const uint32_t u = reinterpret_cast<const uint32_t *>(base)[idx >> 1];
+        return make_float2(ptx::bf16_lo(u), ptx::bf16_hi(u));
+    }
+    return reinterpret_cast<const float2 *>(base)[idx >> 1];
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store_pair(void *base, size_t idx, float x, float y)
+{
+    if (BF16)
+        reinterpret_cast<uint32_t *>(base)[idx >> 1] = ptx::pack_bf16(x, y);
+    else
+        reinterpret_cast<float2 *>(base)[idx >> 1] = make_float2(x, y);
+}
+
+__device__ __forceinline__ float2 warp_sum2(float a, float b)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+    return make_float2(a, b);
+}
+
+template <bool BF16, bool LN>
+__global__ void __launch_bounds__(kWarps * 32)
+linear_decode_kernel(DecodeParams p)
+{
+    __shared__ float4 rows[kWarps][2][D / 4];   // per warp: q and k of the current token
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x * kWarps + warp;
+    if (bh >= p.BH) return;   // whole warps leave; the kernel uses no block-wide barrier
+    const int h = bh % p.H;
+    const int j0 = 2 * lane;  // this lane's two features / columns of W
+
+    float w[D][2];
+    float *Wg = p.W + (size_t)bh * D * D;
+#pragma unroll
+    for (int i = 0; i < D; ++i) {
+        const float2 v = *reinterpret_cast<const float2 *>(Wg + i * D + j0);
+        w[i][0] = v.x;
+        w[i][1] = v.y;
+    }
+    float *bg = p.b + (size_t)bh * D;
+    float c0 = bg[j0], c1 = bg[j0 + 1];
+    float ga0 = 1.f, ga1 = 1.f, be0 = 0.f, be1 = 0.f;
+    if (LN) {
+        ga0 = p.gamma[(size_t)h * D + j0];
+        ga1 = p.gamma[(size_t)h * D + j0 + 1];
+        be0 = p.beta[(size_t)h * D + j0];
+        be1 = p.beta[(size_t)h * D + j0 + 1];
+    }
+    float *qs = reinterpret_cast<float *>(rows[warp][0]);
+    float *ks = reinterpret_cast<float *>(rows[warp][1]);
+
+    // x W for the row staged at xs (16-byte broadcasts), as four partial sums per column
+    auto row_times_w = [&](const float4 *xs, float &r0, float &r1) {
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i4 = 0; i4 < D / 4; ++i4) {
+            const float4 x = xs[i4];
+            a0[0] = fmaf(x.x, w[4 * i4][0], a0[0]);
+            a1[0] = fmaf(x.x, w[4 * i4][1], a1[0]);
+            a0[1] = fmaf(x.y, w[4 * i4 + 1][0], a0[1]);
+            a1[1] = fmaf(x.y, w[4 * i4 + 1][1], a1[1]);
+            a0[2] = fmaf(x.z, w[4 * i4 + 2][0], a0[2]);
+            a1[2] = fmaf(x.z, w[4 * i4 + 2][1], a1[2]);
+            a0[3] = fmaf(x.w, w[4 * i4 + 3][0], a0[3]);
+            a1[3] = fmaf(x.w, w[4 * i4 + 3][1], a1[3]);
+        }
+        r0 = (a0[0] + a0[1]) + (a0[2] + a0[3]);
+        r1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
+    };
+
+    // the next token's inputs are loaded while the current one is computed
+    const size_t row0 = (size_t)bh * p.T;
+    float2 qn = load_pair<BF16>(p.Q, row0 * D + j0), kn = load_pair<BF16>(p.K, row0 * D + j0),
+           vn = load_pair<BF16>(p.V, row0 * D + j0);
+    float en = p.eta[row0];
+    for (int t = 0; t < p.T; ++t) {
+        const size_t base = (row0 + t) * D + j0;
+        const float2 q = qn, k = kn, v = vn;
+        const float et = en;
+        if (t + 1 < p.T) {
+            qn = load_pair<BF16>(p.Q, base + D);
+            kn = load_pair<BF16>(p.K, base + D);
+            vn = load_pair<BF16>(p.V, base + D);
+            en = p.eta[row0 + t + 1];
+        }
+        *reinterpret_cast<float2 *>(qs + j0) = q;
+        *reinterpret_cast<float2 *>(ks + j0) = k;
+        __syncwarp();
+
+        // key-side forward and the token's gradient at the current weights
+        float z0, z1;
+        row_times_w(rows[warp][1], z0, z1);
+        z0 += c0;
+        z1 += c1;
+        float g0, g1;
+        if (LN) {
+            const float2 s = warp_sum2(z0 + z1, fmaf(z0, z0, z1 * z1));
+            const float mu = s.x * (1.f / D);
+            const float r = rsqrtf(fmaxf(s.y * (1.f / D) - mu * mu, 0.f) + p.eps);
+            const float xh0 = (z0 - mu) * r, xh1 = (z1 - mu) * r;
+            const float gx0 = ga0 * (fmaf(ga0, xh0, be0) - (v.x - k.x));
+            const float gx1 = ga1 * (fmaf(ga1, xh1, be1) - (v.y - k.y));
+            const float2 m = warp_sum2(gx0 + gx1, fmaf(gx0, xh0, gx1 * xh1));
+            const float m1 = m.x * (1.f / D), m2 = m.y * (1.f / D);
+            g0 = r * (gx0 - m1 - xh0 * m2);
+            g1 = r * (gx1 - m1 - xh1 * m2);
+        } else {
+            g0 = z0 - v.x;
+            g1 = z1 - v.y;
+        }
+
+        // W -= eta k^T g,  c -= eta g
+        const float eg0 = et * g0, eg1 = et * g1;
+#pragma unroll
+        for (int i4 = 0; i4 < D / 4; ++i4) {
+            const float4 x = rows[warp][1][i4];
+            w[4 * i4][0] = fmaf(-eg0, x.x, w[4 * i4][0]);
+            w[4 * i4][1] = fmaf(-eg1, x.x, w[4 * i4][1]);
+            w[4 * i4 + 1][0] = fmaf(-eg0, x.y, w[4 * i4 + 1][0]);
+            w[4 * i4 + 1][1] = fmaf(-eg1, x.y, w[4 * i4 + 1][1]);
+            w[4 * i4 + 2][0] = fmaf(-eg0, x.z, w[4 * i4 + 2][0]);
+            w[4 * i4 + 2][1] = fmaf(-eg1, x.z, w[4 * i4 + 2][1]);
+            w[4 * i4 + 3][0] = fmaf(-eg0, x.w, w[4 * i4 + 3][0]);
+            w[4 * i4 + 3][1] = fmaf(-eg1, x.w, w[4 * i4 + 3][1]);
+        }
+        c0 -= eg0;
+        c1 -= eg1;
+
+        // the output with the weights after this token's update
+        float o0, o1;
+        row_times_w(rows[warp][0], o0, o1);
+        o0 += c0;
+        o1 += c1;
+        if (LN) {
+            const float2 s = warp_sum2(o0 + o1, fmaf(o0, o0, o1 * o1));
+            const float mu = s.x * (1.f / D);
+            const float r = rsqrtf(fmaxf(s.y * (1.f / D) - mu * mu, 0.f) + p.eps);
+            o0 = q.x + fmaf(ga0 * (o0 - mu), r, be0);
+            o1 = q.y + fmaf(ga1 * (o1 - mu), r, be1);
+        }
+        store_pair<BF16>(p.Z, base, o0, o1);
+        __syncwarp();   // every lane is done with the staged rows before the next token
+    }
+
+#pragma unroll
+    for (int i = 0; i < D; ++i) *reinterpret_cast<float2 *>(Wg + i * D + j0) = make_float2(w[i][0], w[i][1]);
+    bg[j0] = c0;
+    bg[j0 + 1] = c1;
+}
+
+}  // namespace
+
+bool linear_decode_supported(const ttt_desc &d) { return d.d == D && d.mini_batch == 1; }
+
+cudaError_t launch_linear_decode(const DecodeArgs &a)
+{
+    const ttt_desc &d = a.desc;
+    const int BH = d.B * d.H;
+    DecodeParams p{BH, d.H, d.L, d.ln_eps, a.Q, a.K, a.V, a.eta, a.W, a.b, a.gamma, a.beta, a.Z};
+    const int grid = (BH + kWarps - 1) / kWarps;
+    const bool bf16 = d.io_dtype == TTT_BF16;
+    if (bf16 && d.residual_ln)
+        linear_decode_kernel<true, true><<<grid, kWarps * 32, 0, a.stream>>>(p);
+    else if (bf16)
+        linear_decode_kernel<true, false><<<grid, kWarps * 32, 0, a.stream>>>(p);
+    else if (d.residual_ln)
+        linear_decode_kernel<false, true><<<grid, kWarps * 32, 0, a.stream>>>(p);
+    else
+        linear_decode_kernel<false, false><<<grid, kWarps * 32, 0, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ttt

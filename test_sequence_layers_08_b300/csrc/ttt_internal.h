@@ -30,6 +30,17 @@ struct MlpArgs {
     unsigned int *status;
 };
 
+// One TTT-Linear decode call: tokens one at a time from the state (W, b), updated in place.
+struct DecodeArgs {
+    ttt_desc desc;  // desc.L = tokens of this call, desc.mini_batch = 1
+    const void *Q, *K, *V;
+    const float *eta;
+    float *W, *b;
+    const float *gamma, *beta;
+    void *Z;
+    cudaStream_t stream;
+};
+
 // Generic kernels: one CTA per (batch, head), fp32 FFMA arithmetic, state in
 // shared memory.  *_smem_bytes returns 0 when the shape does not fit.
 size_t linear_generic_smem_bytes(const ttt_desc &d);
@@ -40,6 +51,9 @@ cudaError_t launch_mlp_generic(const MlpArgs &a);
 // Tensor-core TTT-Linear kernel (bf16 I/O, d = 64, b = 16).
 bool linear_tc_supported(const ttt_desc &d);
 cudaError_t launch_linear_tc(const LinearArgs &a);
+// TTT-Linear decode kernel (d = 64, fp32 or bf16 I/O, FP32 arithmetic, one warp per head).
+bool linear_decode_supported(const ttt_desc &d);
+cudaError_t launch_linear_decode(const DecodeArgs &a);
 // Tensor-core TTT-MLP kernel (bf16 I/O, d = 64, d_hidden = 256, b = 16).
 bool mlp_tc_supported(const ttt_desc &d);
 cudaError_t launch_mlp_tc(const MlpArgs &a);

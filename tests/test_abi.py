@@ -109,3 +109,36 @@ def test_kernel_choice(lib):
     assert m(io_dtype=0) == "ttt_mlp_generic"
     assert m(d_hidden=128) == "ttt_mlp_generic"
     assert m(d_hidden=4096) is None
+
+
+def call_step(lib, dsc, ptrs=None):
+    p = [FAKE + i * (1 << 30) for i in range(9)] if ptrs is None else ptrs
+    return lib.ttt_linear_step(ctypes.byref(dsc), *[ctypes.c_void_p(x) if x else None for x in p],
+                               None)
+
+
+def test_step_declared_and_checked(lib):
+    assert "ttt_linear_step" in header_functions()
+    # the decode step is the mini-batch-1 recurrence: any other mini_batch is rejected
+    assert call_step(lib, desc(mini_batch=16)) == 1
+    assert "mini_batch" in lib.ttt_last_error().decode()
+    assert call_step(lib, desc(mini_batch=1, L=0)) == 1
+    base = [FAKE + i * (1 << 30) for i in range(9)]
+    for i in (0, 1, 2, 3, 4, 5, 8):            # Q K V eta W b Z
+        p = list(base)
+        p[i] = 0
+        assert call_step(lib, desc(mini_batch=1), p) == 1
+        p[i] = base[i] + 8
+        assert call_step(lib, desc(mini_batch=1), p) == 1
+    p = list(base)
+    p[6] = 0                                   # gamma needed with the residual LayerNorm
+    assert call_step(lib, desc(mini_batch=1, residual_ln=1), p) == 1
+
+
+def test_step_aliasing_rules(lib):
+    base = [FAKE + i * (1 << 30) for i in range(9)]
+    for i, j in ((8, 0), (4, 2), (5, 4), (4, 8)):   # Z on Q, W on V, b on W, W on Z
+        p = list(base)
+        p[i] = p[j]
+        assert call_step(lib, desc(mini_batch=1), p) == 1, (i, j)
+    assert call_step(lib, desc(mini_batch=1, d=256)) == 2   # no kernel for that width
