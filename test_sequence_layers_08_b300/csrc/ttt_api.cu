@@ -218,14 +218,14 @@ ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const void *K, c
                 rb = range_of(b, BH * s.d * 4), rz = range_of(Z, tok * es),
                 rg = range_of(gamma, s.residual_ln ? s.H * s.d * 4 : 0),
                 rbe = range_of(beta, s.residual_ln ? s.H * s.d * 4 : 0);
+    // the written buffers (W, b, Z) may overlap nothing; the read-only ones may share memory
+    const Range written[] = {rw, rb, rz};
     const Range all[] = {rq, rk, rv, re, rw, rb, rz, rg, rbe};
-    for (int i = 0; i < 9; ++i)
-        for (int j = i + 1; j < 9; ++j) {
-            const bool in_in = i < 4 && j < 4;   // inputs may share memory with each other
-            const bool params = i >= 7 && j >= 7;
-            if (!in_in && !params && overlap(all[i], all[j]))
-                return fail(TTT_ERR_INVALID_ARG, "W, b and Z must not overlap another buffer");
-        }
+    const char *wnames[] = {"W", "b", "Z"};
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 9; ++j)
+            if (j != 4 + i && overlap(written[i], all[j]))
+                return fail(TTT_ERR_INVALID_ARG, "%s overlaps another buffer", wnames[i]);
     ttt::LinearArgs la{s, Q, K, V, eta, W, b, gamma, beta, Z, W, b,
                        reinterpret_cast<cudaStream_t>(stream), nullptr};
     if (!ttt::linear_decode_supported(s) && !ttt::linear_generic_smem_bytes(s))

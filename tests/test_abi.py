@@ -142,3 +142,4 @@ def test_step_aliasing_rules(lib):
         p[i] = p[j]
         assert call_step(lib, desc(mini_batch=1), p) == 1, (i, j)
     assert call_step(lib, desc(mini_batch=1, d=256)) == 2   # no kernel for that width
+
