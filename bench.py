@@ -3,13 +3,17 @@ GPU under torchrun), plus roofline fraction, clocks, an end-to-end number
 through host buffers and the CPU oracle as a reported baseline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference]
+                    [--impl ours|reference] [--decode T]
 
 A step is one call of the library entry point over one batch of the workload
 (the whole hot path: every mini-batch of every (batch, head) scan).  Inputs are
 synthetic (seeded, see test_sequence_layers_08_b300/inputs.py) and resident in
 HBM; consecutive steps rotate through enough input/output copies that their
 union exceeds the 126 MB L2, so no step starts with its inputs in L2.
+
+--decode T times the decode step instead (ttt_linear_step: T tokens per call, one
+at a time, from a state carried in device memory between calls) on a linear
+workload's batch, heads and head width.
 """
 from __future__ import annotations
 
