@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 
 from test_sequence_layers_08_b300.inputs import CONFIGS, make_inputs  # noqa: E402
 
-DEFAULT_WORKLOAD = "linear_bf16_B8_H12_L2048"
+DEFAULT_WORKLOAD = "linear_ln_bf16_B4_H16_L8192"
 L2_BYTES = 126 * 2 ** 20
 METRIC = "TTT-layer fwd tokens/s at 1 B300 and % of roofline (TC peak vs HBM GB/s)"
 

@@ -76,7 +76,7 @@ typedef struct {
     int mini_batch;     /* b, tokens per mini-batch                            */
     ttt_dtype io_dtype; /* element type of Q, K, V and Z; state is always float */
     int residual_ln;    /* 0: f = f_res;  1: f(k) = k + LN(f_res(k))           */
-    float ln_eps;       /* LayerNorm eps (used iff residual_ln)                */
+    float ln_eps;       /* LayerNorm eps, finite and > 0 when residual_ln      */
     int init_per_batch; /* 0: initial state [H, ...];  1: [B, H, ...]          */
 } ttt_desc;
 
@@ -130,9 +130,12 @@ TTT_API ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const vo
 
 /*
  * Synchronises `stream`, then reports TTT_ERR_CUDA if a CUDA error is pending
- * and TTT_ERR_TIMEOUT if any kernel launched by this library on the current
- * device since the previous ttt_sync_status call gave up on a bounded wait
- * (its outputs are then unspecified).  Clears the device-side flag it read.
+ * and TTT_ERR_TIMEOUT if any kernel launched by this library on the stream's
+ * device (the current device for the legacy default stream) since the previous
+ * ttt_sync_status call gave up on a bounded wait (its outputs are then
+ * unspecified).  Clears the device-side flag it read.  The flag is one word per
+ * device, shared by every stream on it: a timeout on one stream is reported to
+ * whichever caller synchronises first.
  */
 TTT_API ttt_status ttt_sync_status(ttt_stream_t stream);
 

@@ -118,31 +118,75 @@ def kernel_name(desc: Desc, mlp: bool = False):
     return None if n is None else n.decode()
 
 
-def _check_tensor(name, t, dtype, device):
-    if t.dtype != dtype or t.device != device or not t.is_contiguous():
-        raise TypeError(f"{name} must be a contiguous {dtype} tensor on {device}")
+def _expect(name, t, shape, dtype, device):
+    """Raise unless ``t`` is a contiguous tensor of exactly ``shape``, ``dtype`` and ``device``.
+    Shape is checked first, so a wrong shape is reported even for host tensors."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if t.device != device:
+        raise TypeError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _io_shape(Q):
+    """Validate Q itself and return (B, H, L, d)."""
+    import torch
+    if not isinstance(Q, torch.Tensor) or Q.dim() != 4:
+        raise ValueError("Q must be a [B, H, L, d] tensor")
+    if Q.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"unsupported I/O dtype {Q.dtype}")
+    _expect("Q", Q, Q.shape, Q.dtype, Q.device)
+    return tuple(Q.shape)
+
+
+def _check_sequence(Q, K, V, eta, gamma, beta, residual_ln):
+    """Shapes, dtypes, device and contiguity of the per-token inputs and the LayerNorm
+    parameters; returns (B, H, L, d, device)."""
+    import torch
+    B, H, L, d = _io_shape(Q)
+    dev = Q.device
+    _expect("K", K, (B, H, L, d), Q.dtype, dev)
+    _expect("V", V, (B, H, L, d), Q.dtype, dev)
+    _expect("eta", eta, (B, H, L), torch.float32, dev)
+    if residual_ln:
+        _expect("gamma", gamma, (H, d), torch.float32, dev)
+        _expect("beta", beta, (H, d), torch.float32, dev)
+    return B, H, L, d, dev
+
+
+def _require_cuda(dev):
+    if dev.type != "cuda":
+        raise TypeError(f"tensors must be on a CUDA device, got {dev}")
 
 
 def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: int = 16,
                    residual_ln: bool = False, ln_eps: float = 1e-6, init_per_batch: bool = False,
                    out=None, stream=None):
     """TTT-Linear forward on the GPU.  Q,K,V: [B,H,L,d] (float32 or bfloat16);
-    eta [B,H,L] float32; W0 [H,d,d] (or [B,H,d,d]); b0 [H,d] (or [B,H,d]);
-    gamma, beta [H,d] float32 (residual LayerNorm only).  Returns (Z, W_final,
-    b_final); pass ``out=(Z, W_final, b_final)`` to reuse buffers.  The call is
-    asynchronous on ``stream`` (default: torch's current stream)."""
+    eta [B,H,L] float32; W0 [H,d,d] (or [B,H,d,d] with init_per_batch); b0 [H,d]
+    (or [B,H,d]); gamma, beta [H,d] float32 (residual LayerNorm only).  Returns
+    (Z, W_final, b_final); pass ``out=(Z, W_final, b_final)`` to reuse buffers.
+    Every operand is checked (shape, dtype, device, contiguity) before the C call.
+    The call is asynchronous on ``stream`` (default: torch's current stream)."""
     import torch
+    B, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln)
+    lead = (B, H) if init_per_batch else (H,)
+    _expect("W0", W0, lead + (d, d), torch.float32, dev)
+    _expect("b0", b0, lead + (d,), torch.float32, dev)
+    if out is not None:
+        Z, Wf, bf = out
+        _expect("out Z", Z, (B, H, L, d), Q.dtype, dev)
+        _expect("out W_final", Wf, (B, H, d, d), torch.float32, dev)
+        _expect("out b_final", bf, (B, H, d), torch.float32, dev)
+    _require_cuda(dev)
     lib = load()
     desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch)
-    dev = Q.device
-    for n, t in (("K", K), ("V", V)):
-        _check_tensor(n, t, Q.dtype, dev)
-    for n, t in (("eta", eta), ("W0", W0), ("b0", b0)):
-        _check_tensor(n, t, torch.float32, dev)
-    if residual_ln:
-        _check_tensor("gamma", gamma, torch.float32, dev)
-        _check_tensor("beta", beta, torch.float32, dev)
-    B, H, L, d = Q.shape
     if out is None:
         out = (torch.empty_like(Q), torch.empty((B, H, d, d), device=dev, dtype=torch.float32),
                torch.empty((B, H, d), device=dev, dtype=torch.float32))
@@ -160,19 +204,14 @@ def ttt_linear_step(Q, K, V, eta, W, b, gamma=None, beta=None, *, residual_ln: b
     the state W [B,H,d,d], b [B,H,d] (float32), which is updated in place.  Returns Z
     [B,H,L,d]; pass ``out=Z`` to reuse a buffer.  Asynchronous on ``stream``."""
     import torch
+    B, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln)
+    _expect("W", W, (B, H, d, d), torch.float32, dev)
+    _expect("b", b, (B, H, d), torch.float32, dev)
+    if out is not None:
+        _expect("out Z", out, (B, H, L, d), Q.dtype, dev)
+    _require_cuda(dev)
     lib = load()
     desc = make_desc(Q, 1, residual_ln, ln_eps, True)
-    dev = Q.device
-    for n, t in (("K", K), ("V", V)):
-        _check_tensor(n, t, Q.dtype, dev)
-    for n, t in (("eta", eta), ("W", W), ("b", b)):
-        _check_tensor(n, t, torch.float32, dev)
-    if residual_ln:
-        _check_tensor("gamma", gamma, torch.float32, dev)
-        _check_tensor("beta", beta, torch.float32, dev)
-    B, H, L, d = Q.shape
-    if tuple(W.shape) != (B, H, d, d) or tuple(b.shape) != (B, H, d):
-        raise ValueError("W must be [B,H,d,d] and b [B,H,d]")
     Z = torch.empty_like(Q) if out is None else out
     _check(lib.ttt_linear_step(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta), _ptr(W),
                                _ptr(b), _ptr(gamma if residual_ln else None),
@@ -184,20 +223,28 @@ def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_bat
                 residual_ln: bool = False, ln_eps: float = 1e-6, init_per_batch: bool = False,
                 out=None, stream=None):
     """TTT-MLP forward on the GPU.  W1 [H,d,dh], b1 [H,dh], W2 [H,dh,d], b2 [H,d]
-    (leading B when init_per_batch).  Returns (Z, W1_f, b1_f, W2_f, b2_f)."""
+    (leading B when init_per_batch).  Returns (Z, W1_f, b1_f, W2_f, b2_f).  Every
+    operand is checked before the C call."""
     import torch
-    lib = load()
+    B, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln)
+    if not isinstance(b1, torch.Tensor) or b1.dim() < 1:
+        raise ValueError("b1 must be a [H, dh] (or [B, H, dh]) tensor")
     dh = b1.shape[-1]
+    lead = (B, H) if init_per_batch else (H,)
+    _expect("W1", W1, lead + (d, dh), torch.float32, dev)
+    _expect("b1", b1, lead + (dh,), torch.float32, dev)
+    _expect("W2", W2, lead + (dh, d), torch.float32, dev)
+    _expect("b2", b2, lead + (d,), torch.float32, dev)
+    if out is not None:
+        Z, W1f, b1f, W2f, b2f = out
+        _expect("out Z", Z, (B, H, L, d), Q.dtype, dev)
+        _expect("out W1_f", W1f, (B, H, d, dh), torch.float32, dev)
+        _expect("out b1_f", b1f, (B, H, dh), torch.float32, dev)
+        _expect("out W2_f", W2f, (B, H, dh, d), torch.float32, dev)
+        _expect("out b2_f", b2f, (B, H, d), torch.float32, dev)
+    _require_cuda(dev)
+    lib = load()
     desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, d_hidden=dh)
-    dev = Q.device
-    for n, t in (("K", K), ("V", V)):
-        _check_tensor(n, t, Q.dtype, dev)
-    for n, t in (("eta", eta), ("W1", W1), ("b1", b1), ("W2", W2), ("b2", b2)):
-        _check_tensor(n, t, torch.float32, dev)
-    if residual_ln:
-        _check_tensor("gamma", gamma, torch.float32, dev)
-        _check_tensor("beta", beta, torch.float32, dev)
-    B, H, L, d = Q.shape
     if out is None:
         f32 = dict(device=dev, dtype=torch.float32)
         out = (torch.empty_like(Q), torch.empty((B, H, d, dh), **f32), torch.empty((B, H, dh), **f32),

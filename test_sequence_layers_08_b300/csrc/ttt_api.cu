@@ -4,6 +4,7 @@
 // 4-byte failure flag below, which the module loader places in the image.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -60,8 +61,8 @@ ttt_status check_desc(const ttt_desc *s, bool mlp)
         return fail(TTT_ERR_INVALID_ARG, "residual_ln must be 0 or 1");
     if (s->init_per_batch != 0 && s->init_per_batch != 1)
         return fail(TTT_ERR_INVALID_ARG, "init_per_batch must be 0 or 1");
-    if (s->residual_ln && !(std::isfinite(s->ln_eps) && s->ln_eps >= 0.f))
-        return fail(TTT_ERR_INVALID_ARG, "ln_eps must be finite and >= 0");
+    if (s->residual_ln && !(std::isfinite(s->ln_eps) && s->ln_eps > 0.f))
+        return fail(TTT_ERR_INVALID_ARG, "ln_eps must be finite and > 0 with the residual LayerNorm");
     if (mlp && s->d_hidden < 0) return fail(TTT_ERR_INVALID_ARG, "d_hidden must be >= 0");
     if ((long long)s->B * s->H > 0x7fffffffLL)
         return fail(TTT_ERR_INVALID_ARG, "B * H exceeds the grid limit");
@@ -76,26 +77,31 @@ ttt_status check_ptr(const void *p, const char *name)
     return TTT_OK;
 }
 
-// Pointer to this device's failure flag (looked up once per device).
+constexpr int kMaxDevices = 64;
+
+// Pointer to this device's failure flag, looked up once per device.  Host threads may race
+// on the first lookup; each entry is an atomic, and every racer stores the same address.
 unsigned int *failure_flag(ttt_status *st)
 {
-    static unsigned int *cache[64] = {};
+    static std::atomic<unsigned int *> cache[kMaxDevices];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         *st = fail(TTT_ERR_CUDA, "cudaGetDevice failed");
         return nullptr;
     }
-    if (!cache[dev]) {
+    unsigned int *flag = cache[dev].load(std::memory_order_acquire);
+    if (!flag) {
         void *ptr = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&ptr, g_ttt_failure_flag);
         if (e != cudaSuccess) {
             *st = fail(TTT_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
             return nullptr;
         }
-        cache[dev] = static_cast<unsigned int *>(ptr);
+        flag = static_cast<unsigned int *>(ptr);
+        cache[dev].store(flag, std::memory_order_release);
     }
     *st = TTT_OK;
-    return cache[dev];
+    return flag;
 }
 
 const char *linear_kernel(const ttt_desc &s)
@@ -304,16 +310,32 @@ void ttt_debug_withhold_loads(int on) { ttt::set_withhold_loads(on); }
 
 ttt_status ttt_sync_status(ttt_stream_t stream)
 {
-    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(cs);
     if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    // the flag read is the one of the stream's device (the legacy default stream belongs to
+    // the current device); the current device is restored afterwards
+    int cur = 0, dev = 0;
+    if ((e = cudaGetDevice(&cur)) != cudaSuccess)
+        return fail(TTT_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    dev = cur;
+    if (cs != nullptr && (e = cudaStreamGetDevice(cs, &dev)) != cudaSuccess)
+        return fail(TTT_ERR_CUDA, "cudaStreamGetDevice: %s", cudaGetErrorString(e));
+    if (dev != cur && (e = cudaSetDevice(dev)) != cudaSuccess)
+        return fail(TTT_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(e));
     unsigned int flag = 0;
+    cudaError_t e_clear = cudaSuccess;
     e = cudaMemcpyFromSymbol(&flag, g_ttt_failure_flag, sizeof(flag));
-    if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "reading the failure flag: %s", cudaGetErrorString(e));
-    if (flag != ttt::kStatusOk) {
+    if (e == cudaSuccess && flag != ttt::kStatusOk) {
         const unsigned int zero = 0;
-        cudaMemcpyToSymbol(g_ttt_failure_flag, &zero, sizeof(zero));
-        return fail(TTT_ERR_TIMEOUT, "a kernel gave up on a bounded wait (flag 0x%x)", flag);
+        e_clear = cudaMemcpyToSymbol(g_ttt_failure_flag, &zero, sizeof(zero));
     }
+    if (dev != cur) cudaSetDevice(cur);
+    if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "reading the failure flag: %s", cudaGetErrorString(e));
+    if (e_clear != cudaSuccess)
+        return fail(TTT_ERR_CUDA, "clearing the failure flag (0x%x): %s", flag, cudaGetErrorString(e_clear));
+    if (flag != ttt::kStatusOk)
+        return fail(TTT_ERR_TIMEOUT, "a kernel gave up on a bounded wait (flag 0x%x)", flag);
     return ok();
 }
 

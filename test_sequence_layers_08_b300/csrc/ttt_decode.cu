@@ -94,11 +94,18 @@ linear_decode_kernel(DecodeParams p)
     float *bg = p.b + (size_t)bh * D;
     float c0 = bg[j0], c1 = bg[j0 + 1];
     float ga0 = 1.f, ga1 = 1.f, be0 = 0.f, be1 = 0.f;
+    // LayerNorm pivot: LN and its backward do not see a common shift of z, so with the residual
+    // LayerNorm the tokens run on c - p, p = mean(c), and p is added back when c is stored; the
+    // one-pass sums of z and z^2 then stay free of cancellation when c has a large offset.
+    float pivot = 0.f;
     if (LN) {
         ga0 = p.gamma[(size_t)h * D + j0];
         ga1 = p.gamma[(size_t)h * D + j0 + 1];
         be0 = p.beta[(size_t)h * D + j0];
         be1 = p.beta[(size_t)h * D + j0 + 1];
+        pivot = warp_sum2(c0 + c1, 0.f).x * (1.f / D);
+        c0 -= pivot;
+        c1 -= pivot;
     }
     float *qs = reinterpret_cast<float *>(rows[warp][0]);
     float *ks = reinterpret_cast<float *>(rows[warp][1]);
@@ -198,8 +205,8 @@ linear_decode_kernel(DecodeParams p)
 
 #pragma unroll
     for (int i = 0; i < D; ++i) *reinterpret_cast<float2 *>(Wg + i * D + j0) = make_float2(w[i][0], w[i][1]);
-    bg[j0] = c0;
-    bg[j0 + 1] = c1;
+    bg[j0] = c0 + pivot;
+    bg[j0 + 1] = c1 + pivot;
 }
 
 }  // namespace

@@ -186,20 +186,34 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     float cb0 = p.b0[init * D + j0];
     float cb1 = p.b0[init * D + j1];
     float ga0 = 1.f, ga1 = 1.f, be0 = 0.f, be1 = 0.f, C1 = 0.f;
+    // LayerNorm pivot: LN(z - p 1) = LN(z) and its backward is unchanged, so with the residual
+    // LayerNorm the scan runs on c - p with p = mean(b0), and p is added back to b_final.  The
+    // one-pass sums of z and z^2 then see values near zero even when b0 has a large common
+    // offset (no cancellation in S2 / D - mu^2).
+    float pivot = 0.f;
     if (LN) {
         ga0 = p.gamma[(size_t)h * D + j0];
         ga1 = p.gamma[(size_t)h * D + j1];
         be0 = p.beta[(size_t)h * D + j0];
         be1 = p.beta[(size_t)h * D + j1];
-        // sum of gamma^2 over all features: this thread's two, then the warp, then the warps
-        float part = ga0 * ga0 + ga1 * ga1;
-        part += __shfl_xor_sync(0xffffffffu, part, 4);
-        part += __shfl_xor_sync(0xffffffffu, part, 8);
-        part += __shfl_xor_sync(0xffffffffu, part, 16);
-        if (lane == 0) s.red[0][0][warp] = part;
+        // sums of gamma^2 and of b0 over all features: this thread's two, the warp, the warps
+        float part = ga0 * ga0 + ga1 * ga1, pb = cb0 + cb1;
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+            part += __shfl_xor_sync(0xffffffffu, part, o);
+            pb += __shfl_xor_sync(0xffffffffu, pb, o);
+        }
+        if (lane == 0) {
+            s.red[0][0][warp] = part;
+            s.red[0][1][warp] = pb;
+        }
         ptx::named_bar(1, kMathThreads);
         const float4 w4 = *reinterpret_cast<const float4 *>(s.red[0][0]);
+        const float4 p4 = *reinterpret_cast<const float4 *>(s.red[0][1]);
         C1 = (w4.x + w4.y) + (w4.z + w4.w);
+        pivot = ((p4.x + p4.y) + (p4.z + p4.w)) * (1.f / D);
+        cb0 -= pivot;
+        cb1 -= pivot;
         ptx::named_bar(1, kMathThreads);
     }
     const float g20 = ga0 * ga0, g21 = ga1 * ga1;
@@ -634,8 +648,8 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             Wf[(i + 1) * D + j1] = wt[pt][3];
         }
         if (c == 0) {
-            p.bf[(size_t)bh * D + j0] = cb0;
-            p.bf[(size_t)bh * D + j1] = cb1;
+            p.bf[(size_t)bh * D + j0] = cb0 + pivot;
+            p.bf[(size_t)bh * D + j1] = cb1 + pivot;
         }
     }
 }

@@ -223,6 +223,10 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
     }
     float b2r[2] = {0.f, 0.f}, ga0 = 1.f, ga1 = 1.f, be0 = 0.f, be1 = 0.f, C1 = 0.f;
+    // LayerNorm pivot: with the residual LayerNorm the scan runs on b2 - p, p = mean(b2) (LN and
+    // its backward do not see a common shift of Z2), and p is added back to b2_final; the
+    // one-pass sums of z and z^2 then stay free of cancellation when b2 has a large offset.
+    float pivot = 0.f;
     if (lnw) {
         b2r[0] = p.b2[init * D + o0];
         b2r[1] = p.b2[init * D + o1];
@@ -231,14 +235,23 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             ga1 = p.gamma[(size_t)h * D + o1];
             be0 = p.beta[(size_t)h * D + o0];
             be1 = p.beta[(size_t)h * D + o1];
-            float part = ga0 * ga0 + ga1 * ga1;
-            part += __shfl_xor_sync(0xffffffffu, part, 4);
-            part += __shfl_xor_sync(0xffffffffu, part, 8);
-            part += __shfl_xor_sync(0xffffffffu, part, 16);
-            if (lane == 0) s.red[0][0][warp] = part;
+            float part = ga0 * ga0 + ga1 * ga1, pb = b2r[0] + b2r[1];
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+                part += __shfl_xor_sync(0xffffffffu, part, o);
+                pb += __shfl_xor_sync(0xffffffffu, pb, o);
+            }
+            if (lane == 0) {
+                s.red[0][0][warp] = part;
+                s.red[0][1][warp] = pb;
+            }
             ptx::named_bar(kBarLn, 128);
             const float4 w4 = *reinterpret_cast<const float4 *>(s.red[0][0]);
+            const float4 p4 = *reinterpret_cast<const float4 *>(s.red[0][1]);
             C1 = (w4.x + w4.y) + (w4.z + w4.w);
+            pivot = ((p4.x + p4.y) + (p4.z + p4.w)) * (1.f / D);
+            b2r[0] -= pivot;
+            b2r[1] -= pivot;
             ptx::named_bar(kBarLn, 128);
         }
     }
@@ -788,8 +801,8 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
     }
     if (lnw && c == 0) {
-        p.b2f[(size_t)bh * D + o0] = b2r[0];
-        p.b2f[(size_t)bh * D + o1] = b2r[1];
+        p.b2f[(size_t)bh * D + o0] = b2r[0] + pivot;
+        p.b2f[(size_t)bh * D + o1] = b2r[1] + pivot;
     }
 }
 

@@ -64,7 +64,8 @@ def call_linear(lib, dsc, ptrs=None):
 
 @pytest.mark.parametrize("kw", [dict(B=0), dict(H=-1), dict(L=0), dict(d=0), dict(mini_batch=0),
                                 dict(L=40), dict(io_dtype=7), dict(residual_ln=2),
-                                dict(init_per_batch=3), dict(residual_ln=1, ln_eps=-1.0)])
+                                dict(init_per_batch=3), dict(residual_ln=1, ln_eps=-1.0),
+                                dict(residual_ln=1, ln_eps=0.0), dict(residual_ln=1, ln_eps=float('nan'))])
 def test_bad_descriptor_is_invalid_arg(lib, kw):
     assert call_linear(lib, desc(**kw)) == 1
     assert lib.ttt_last_error().decode() != ""

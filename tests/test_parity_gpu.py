@@ -93,10 +93,7 @@ def test_state_carry_in_place(kind):
     out = (torch.empty_like(d2["Q"]),) + tuple(state)   # final state written over the initial
     second = run_gpu(half, d2, out=out, init_per_batch=True)
     z = np.concatenate([first[0], second[0]], axis=2)
-    tol = TOL[cfg.io]
-    assert rel_l2(z, full[0]) <= tol
-    for a, b in zip(second[1:], full[1:]):
-        assert rel_l2(a, b) <= tol
+    compare_all(cfg, [z] + list(second[1:]), full)
 
 
 def test_non_default_stream_and_reuse():
