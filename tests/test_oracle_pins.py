@@ -17,7 +17,15 @@ import torch
 import oracle
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-torch.set_default_dtype(torch.float64)
+
+
+@pytest.fixture(autouse=True)
+def _float64_default():
+    """torch's default dtype is float64 inside this module's tests only."""
+    old = torch.get_default_dtype()
+    torch.set_default_dtype(torch.float64)
+    yield
+    torch.set_default_dtype(old)
 
 
 def rand_problem(rng, B=1, H=2, L=32, d=8, ln=False, mlp=False, dh=None, eta_scale=0.3,
