@@ -65,6 +65,8 @@ def _load():
             lib.oracle_mlp_token_grad.restype = None
             lib.oracle_mlp_token_grad.argtypes = [dp, dp, dp, dp, dp, dp, i, i, i, dp, dp, d,
                                                   dp, dp, dp, dp]
+            lib.oracle_eta_gate.restype = i
+            lib.oracle_eta_gate.argtypes = [i, i, i, i, d, dp, dp, dp]
             for name in ("oracle_ttt_linear", "oracle_ttt_linear_dual"):
                 fn = getattr(lib, name)
                 fn.restype = i
@@ -85,6 +87,25 @@ def _p(a):
     if a is None:
         return None
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+# --------------------------------------------------------------------------
+# per-token learning rate
+# --------------------------------------------------------------------------
+
+def eta_gate(x, theta, eta_base: float):
+    """eta [B, H, L] = eta_base * sigmoid(theta[h] . x[b, t]) for the layer input
+    x [B, L, Dx] and the per-head gate vectors theta [H, Dx] (float64)."""
+    x, theta = _f64(x), _f64(theta)
+    B, L, Dx = x.shape
+    H = theta.shape[0]
+    if theta.shape != (H, Dx):
+        raise ValueError("theta must be [H, Dx]")
+    eta = np.empty((B, H, L))
+    rc = _load().oracle_eta_gate(B, H, L, Dx, float(eta_base), _p(x), _p(theta), _p(eta))
+    if rc != 0:
+        raise ValueError(f"oracle_eta_gate returned {rc}")
+    return eta
 
 
 # --------------------------------------------------------------------------

@@ -19,6 +19,8 @@
  *   [I]  same article, section 4.3: W1 is [heads, d, d] row-major, b1 [heads, 1, d].
  *   [F]  lryc.cn "测试时学习（TTT）" article, section 2.1: TTT-MLP is d -> 4d
  *        GELU -> d; residual form f(x) = x + LN(f_res(x)).
+ *   [G]  same lryc.cn article, section 2.2: the learnable per-token learning
+ *        rate eta(x) = eta_base * sigmoid(theta_lr . x).
  *
  * Readings where the pages are silent (all of them are also listed in the
  * design notes):
@@ -45,6 +47,29 @@
 #define ORACLE_OK 0
 #define ORACLE_BAD_ARG 1
 #define ORACLE_NO_MEM 2
+
+/* ------------------------------------------------------------------------ */
+/* Per-token learning rate [G]                                               */
+/* ------------------------------------------------------------------------ */
+
+/* eta[b, h, t] = eta_base * sigmoid(theta[h] . x[b, t]) for x [B, L, Dx] (the
+ * layer's input tokens) and theta [H, Dx] (one gate vector per head); eta is
+ * [B, H, L].  sigmoid(u) = 1 / (1 + exp(-u)). */
+int oracle_eta_gate(int B, int H, int L, int Dx, double eta_base, const double *x,
+                    const double *theta, double *eta)
+{
+    if (B <= 0 || H <= 0 || L <= 0 || Dx <= 0 || !x || !theta || !eta) return ORACLE_BAD_ARG;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int t = 0; t < L; ++t) {
+                const double *xt = x + ((size_t)b * L + t) * Dx;
+                const double *th = theta + (size_t)h * Dx;
+                double u = 0.0;
+                for (int k = 0; k < Dx; ++k) u += th[k] * xt[k];
+                eta[((size_t)b * H + h) * L + t] = eta_base / (1.0 + exp(-u));
+            }
+    return ORACLE_OK;
+}
 
 /* ------------------------------------------------------------------------ */
 /* Elementwise pieces                                                        */

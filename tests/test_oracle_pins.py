@@ -397,3 +397,45 @@ def test_bad_arguments_rejected():
     p = rand_problem(rng, B=1, H=1, L=20, d=4)
     with pytest.raises(ValueError):
         run_linear(p, 16, False)   # L % b != 0
+
+
+# --------------------------------------------------------------------------
+# the per-token learning-rate gate (lryc.cn TTT article, section 2.2)
+# --------------------------------------------------------------------------
+
+def test_gate_zero_theta_is_half_the_base_rate():
+    rng = np.random.default_rng(71)
+    x = rng.standard_normal((2, 5, 12))
+    eta = oracle.eta_gate(x, np.zeros((3, 12)), 0.3)
+    np.testing.assert_array_equal(eta, np.full((2, 3, 5), 0.15))
+
+
+def test_gate_hand_value():
+    """sigmoid(ln 3) = 3/4 exactly: one feature, theta = 1, x = ln 3."""
+    eta = oracle.eta_gate(np.array([[[np.log(3.0)], [-np.log(3.0)]]]), np.array([[1.0]]), 2.0)
+    np.testing.assert_allclose(eta[0, 0], [1.5, 0.5], rtol=1e-15)
+
+
+def test_gate_matches_library_sigmoid():
+    """Against scipy's expit of a numpy contraction, with every dimension distinct so that a
+    transposed index fails."""
+    from scipy.special import expit
+    rng = np.random.default_rng(72)
+    B, L, Dx, H = 2, 7, 33, 5
+    x = rng.standard_normal((B, L, Dx))
+    theta = rng.standard_normal((H, Dx)) * 0.3
+    ref = 0.125 * expit(np.einsum("blk,hk->bhl", x, theta))
+    np.testing.assert_allclose(oracle.eta_gate(x, theta, 0.125), ref, rtol=1e-13, atol=0)
+
+
+def test_gate_symmetry_and_saturation():
+    """sigmoid(u) + sigmoid(-u) = 1, and large |u| saturates without overflow."""
+    rng = np.random.default_rng(73)
+    x = rng.standard_normal((1, 9, 16))
+    theta = rng.standard_normal((2, 16))
+    s = oracle.eta_gate(x, theta, 1.0) + oracle.eta_gate(-x, theta, 1.0)
+    np.testing.assert_allclose(s, 1.0, rtol=1e-15)
+    big = oracle.eta_gate(np.full((1, 2, 1), 800.0) * np.array([1.0, -1.0])[None, :, None],
+                          np.ones((1, 1)), 0.5)
+    assert np.isfinite(big).all()
+    np.testing.assert_allclose(big[0, 0], [0.5, 0.0], atol=1e-300)
