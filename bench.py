@@ -191,11 +191,23 @@ def max_over_ranks(world, value: float) -> float:
 # CPU oracle (reported baseline / reference arm)
 # ---------------------------------------------------------------------------
 
+def oracle_inputs(x):
+    """The workload's inputs for the oracle: eta given, or from the oracle's own gate."""
+    import oracle
+    if "eta" in x:
+        return x
+    y = dict(x)
+    y["eta"] = oracle.eta_gate(x["x"], x["theta"], x["eta_base"])
+    return y
+
+
 def oracle_rate(cfg, x, budget_s: float, threads: int):
     """Time the oracle as it stands on whole (batch, head) scans of the
     workload, in chunks of at least one scan per thread, until the time budget
-    is spent (cycling over the workload's scans).  Returns (tokens/s, text)."""
+    is spent (cycling over the workload's scans).  Returns (tokens/s, text).
+    eta is computed (by the oracle's gate, for gated workloads) before timing."""
     import oracle
+    x = oracle_inputs(x)
     pairs = [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
     kw = dict(mini_batch=cfg.mini_batch, ln=cfg.ln, eps=cfg.eps)
     chunk = max(threads, min(len(pairs), 2 * threads))
@@ -272,12 +284,22 @@ def run_ours(args, cfg, world, rank, local):
     io = torch.bfloat16 if cfg.io == "bf16" else torch.float32
     state_keys = ["W0", "b0"] if cfg.kind == "linear" else ["W1", "b1", "W2", "b2"]
 
+    gated = "eta" not in x
+    if gated:   # the gate's inputs on the device; eta from the library's gate
+        x_dev = torch.from_numpy(x["x"]).to(dev).to(io)
+        theta_dev = torch.from_numpy(x["theta"]).to(dev)
+        eta_dev = ttt.ttt_eta_gate(x_dev, theta_dev, x["eta_base"])
+        ttt.ttt_sync_status()
+    else:
+        eta_dev = torch.from_numpy(x["eta"]).to(dev)
+
     def dev_inputs():
         d = {}
         for k in ("Q", "K", "V"):
             d[k] = torch.from_numpy(x[k]).to(dev).to(io)
-        for k in ["eta", "gamma", "beta"] + state_keys:
+        for k in ["gamma", "beta"] + state_keys:
             d[k] = None if x[k] is None else torch.from_numpy(x[k]).to(dev)
+        d["eta"] = eta_dev.clone()
         return d
 
     per_set = algorithmic_bytes(cfg)
@@ -288,6 +310,8 @@ def run_ours(args, cfg, world, rank, local):
 
     def step(i):
         s = sets[i % n_sets]
+        if args.gated:   # the learning-rate gate is part of the step
+            ttt.ttt_eta_gate(x_dev, theta_dev, x["eta_base"], out=s["eta"], stream=stream)
         kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps,
                   out=outs[i % n_sets], stream=stream)
         if cfg.kind == "linear":
@@ -347,17 +371,23 @@ def run_ours(args, cfg, world, rank, local):
     # one call, one copy out.  The two copy directions and the kernel run on three streams over
     # two device buffer sets, so the copies of neighbouring steps overlap the kernel (a
     # streaming job's steady state).
-    in_keys = ["Q", "K", "V", "eta"] + state_keys
-    in_specs = [(tuple(sets[0][k].shape), sets[0][k].dtype) for k in in_keys]
+    # with --gated a step copies the layer input x (the gate computes eta on the device)
+    in_keys = ["Q", "K", "V", "x" if args.gated else "eta"] + state_keys
+    shapes = {k: (tuple(sets[0][k].shape), sets[0][k].dtype) for k in in_keys if k != "x"}
+    if args.gated:
+        shapes["x"] = (tuple(x_dev.shape), x_dev.dtype)
+    in_specs = [shapes[k] for k in in_keys]
     out_specs = [(tuple(o.shape), o.dtype) for o in outs[0]]
     hin_flat, hin = packed(in_specs, "cpu", pin=True)
     for k, hv in zip(in_keys, hin):
-        hv.copy_(torch.from_numpy(x[k]).to(hv.dtype))
+        hv.copy_(eta_dev.cpu() if k == "eta" else torch.from_numpy(x[k]).to(hv.dtype))
     dsets, douts, din_flat, dout_flat, hout_flat = [], [], [], [], []
     for _ in range(2):
         f, views = packed(in_specs, dev)
         d = dict(zip(in_keys, views))
         d["gamma"], d["beta"] = sets[0]["gamma"], sets[0]["beta"]
+        if args.gated:
+            d["eta"] = torch.empty_like(eta_dev)
         dsets.append(d)
         din_flat.append(f)
         f, views = packed(out_specs, dev)
@@ -373,6 +403,8 @@ def run_ours(args, cfg, world, rank, local):
 
     def run_on(b):
         s_ = dsets[b]
+        if args.gated:
+            ttt.ttt_eta_gate(s_["x"], theta_dev, x["eta_base"], out=s_["eta"], stream=stream)
         kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps,
                   out=douts[b], stream=stream)
         if cfg.kind == "linear":
@@ -421,6 +453,9 @@ def run_ours(args, cfg, world, rank, local):
     peaks = load_peaks()
     alg_bytes = algorithmic_bytes(cfg)
     alg_flops = flops_per_head_token(cfg) * cfg.head_tokens
+    if args.gated:   # the gate reads x and writes eta (the scan's read of eta is counted)
+        alg_bytes += x_dev.numel() * x_dev.element_size() + cfg.head_tokens * 4
+        alg_flops += 2.0 * x_dev.numel() * cfg.H
     achieved_gbs = alg_bytes / (ms_step * 1e-3) / 1e9
     achieved_tf = alg_flops / (ms_step * 1e-3) / 1e12
     t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
@@ -447,7 +482,10 @@ def run_ours(args, cfg, world, rank, local):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if cfg.io == "bf16" else "f32", "data": "synthetic",
-                "config": {"workload": cfg.name, "kind": cfg.kind, "B": cfg.B, "H": cfg.H,
+                "config": {"workload": cfg.name + ("+gate" if args.gated else ""),
+                           "kind": cfg.kind, "B": cfg.B, "H": cfg.H,
+                           "eta": ("gate in the step (ttt_eta_gate)" if args.gated else
+                                   "input (computed once by ttt_eta_gate)" if gated else "constant"),
                            "L": cfg.L, "d": cfg.d, "mini_batch": cfg.mini_batch,
                            "io": cfg.io, "state": "f32", "residual_ln": cfg.ln,
                            "l2": f"inputs rotate over {n_sets} copies "
@@ -459,7 +497,7 @@ def run_ours(args, cfg, world, rank, local):
                         "schedule": "per step: one host->device copy of the inputs, the call, one "
                                     "device->host copy of the outputs; three streams over two "
                                     "buffer sets"},
-                "gpu_launches": args.steps, "clocks": clk,
+                "gpu_launches": args.steps * (2 if args.gated else 1), "clocks": clk,
                 "wall_s_timed": t_wall1 - t_wall0}
         print(json.dumps(line), flush=True)
 
@@ -493,7 +531,12 @@ def run_decode(args, cfg, world, rank, local):
     gamma = None if x["gamma"] is None else torch.from_numpy(x["gamma"]).to(dev)
     beta = None if x["beta"] is None else torch.from_numpy(x["beta"]).to(dev)
     qkv = {k: torch.from_numpy(x[k]).to(dev).to(io) for k in ("Q", "K", "V")}
-    eta = torch.from_numpy(x["eta"]).to(dev)
+    if "eta" in x:
+        eta = torch.from_numpy(x["eta"]).to(dev)
+    else:
+        eta = ttt.ttt_eta_gate(torch.from_numpy(x["x"]).to(dev).to(io),
+                               torch.from_numpy(x["theta"]).to(dev), x["eta_base"])
+        ttt.ttt_sync_status()
     sets = []
     for _ in range(n_sets):
         sets.append(dict(Q=qkv["Q"].clone(), K=qkv["K"].clone(), V=qkv["V"].clone(),
@@ -629,6 +672,9 @@ def main():
     ap.add_argument("--decode", type=int, default=0, metavar="T",
                     help="time the decode step instead: T tokens per call, one at a time, from a "
                          "state carried between calls (a linear workload's B, H, d)")
+    ap.add_argument("--gated", action="store_true",
+                    help="each step also computes eta from the layer input with the learning-rate "
+                         "gate (ttt_eta_gate) before the scan")
     ap.add_argument("--soak-ms", type=float, default=1500.0,
                     help="untimed load before the timed region, so the clock samples describe "
                          "this workload (0 under a profiler)")
@@ -636,6 +682,8 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     cfg = CONFIGS[args.workload]
+    if args.gated and cfg.eta != "gate":
+        raise SystemExit("--gated needs a workload with the per-token gate")
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":

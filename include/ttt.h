@@ -17,8 +17,9 @@
  *   - optional residual LayerNorm f(k) = k + LN(f_res(k)) with per-head gamma,
  *     beta [H, d], biased variance and eps = ln_eps -- lryc.cn article, section 2.1;
  *     the loss target of f_res is then v - k (damodev article, section 4.2).
- * The per-token learning rate eta (the gate eta_base * sigmoid(theta_lr x) of
- * the lryc.cn article, section 2.2) is computed by the caller and passed in.
+ * The per-token learning rate eta, the gate eta_base * sigmoid(theta_lr . x) of
+ * the lryc.cn article, section 2.2, is an input of the scan entry points;
+ * ttt_eta_gate computes it on the GPU from the layer's input tokens.
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers (cudaMalloc or equivalent) owned
@@ -127,6 +128,21 @@ TTT_API ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *
 TTT_API ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const void *K, const void *V,
                                    const float *eta, float *W, float *b, const float *gamma,
                                    const float *beta, void *Z, ttt_stream_t stream);
+
+/*
+ * Per-token learning rate (the learnable gate of the lryc.cn TTT article,
+ * section 2.2): eta[b, h, t] = eta_base * sigmoid(theta[h] . x[b, t]).
+ *   in : x [B, L, d_model] (x_dtype), the layer's input tokens; theta [H, d_model]
+ *        float, one gate vector per head; eta_base, the base learning rate;
+ *   out: eta [B, H, L] float -- the eta the scan entry points take.
+ * The contraction is carried in fp32 (bf16 tokens meet theta split into two bf16
+ * parts, so theta keeps ~16 mantissa bits).  bf16 tokens need d_model % 8 == 0.
+ * eta must not overlap x or theta.  Errors as for the other entry points; a
+ * bounded wait that runs out is reported by ttt_sync_status.
+ */
+TTT_API ttt_status ttt_eta_gate(int B, int H, int L, int d_model, ttt_dtype x_dtype,
+                                float eta_base, const void *x, const float *theta, float *eta,
+                                ttt_stream_t stream);
 
 /*
  * Synchronises `stream`, then reports TTT_ERR_CUDA if a CUDA error is pending

@@ -6,6 +6,7 @@ used for device memory and streams.  There is no CPU fallback: if the
 library has not been built, or the GPU is missing, calls raise.
 
 Functions mirror the C entry points:
+    ttt_eta_gate(x, theta, eta_base) -> eta
     ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma, beta, ...) -> (Z, W_final, b_final)
     ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma, beta, ...) -> (Z, W1_f, b1_f, W2_f, b2_f)
     ttt_sync_status(stream=None)
@@ -17,7 +18,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["TTTError", "Desc", "load", "library_path", "ttt_linear_fwd", "ttt_mlp_fwd", "ttt_linear_step",
+__all__ = ["TTTError", "Desc", "load", "library_path", "ttt_eta_gate", "ttt_linear_fwd", "ttt_mlp_fwd", "ttt_linear_step",
            "ttt_sync_status", "kernel_name", "version", "STATUS", "set_wait_timeout_ns",
            "debug_withhold_loads"]
 
@@ -64,6 +65,8 @@ def load():
             lib.ttt_linear_step.argtypes = [dp] + [vp] * 10
             lib.ttt_mlp_fwd.restype = ctypes.c_int
             lib.ttt_mlp_fwd.argtypes = [dp] + [vp] * 16
+            lib.ttt_eta_gate.restype = ctypes.c_int
+            lib.ttt_eta_gate.argtypes = [ctypes.c_int] * 5 + [ctypes.c_float] + [vp] * 4
             lib.ttt_sync_status.restype = ctypes.c_int
             lib.ttt_sync_status.argtypes = [vp]
             lib.ttt_status_string.restype = ctypes.c_char_p
@@ -255,6 +258,33 @@ def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_bat
                            _ptr(beta if residual_ln else None), _ptr(Z), _ptr(W1f), _ptr(b1f),
                            _ptr(W2f), _ptr(b2f), _stream_handle(stream)))
     return Z, W1f, b1f, W2f, b2f
+
+
+def ttt_eta_gate(x, theta, eta_base: float, *, out=None, stream=None):
+    """Per-token learning rate on the GPU: eta [B,H,L] = eta_base * sigmoid(theta[h] . x[b,t])
+    for the layer input x [B,L,d_model] (float32 or bfloat16) and theta [H,d_model] float32.
+    Pass ``out=eta`` to reuse a buffer.  Asynchronous on ``stream``."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.dim() != 3:
+        raise ValueError("x must be a [B, L, d_model] tensor")
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"unsupported token dtype {x.dtype}")
+    B, L, Dx = x.shape
+    dev = x.device
+    _expect("x", x, (B, L, Dx), x.dtype, dev)
+    if not isinstance(theta, torch.Tensor) or theta.dim() != 2:
+        raise ValueError("theta must be a [H, d_model] tensor")
+    H = theta.shape[0]
+    _expect("theta", theta, (H, Dx), torch.float32, dev)
+    if out is not None:
+        _expect("out eta", out, (B, H, L), torch.float32, dev)
+    _require_cuda(dev)
+    lib = load()
+    eta = torch.empty((B, H, L), device=dev, dtype=torch.float32) if out is None else out
+    io = TTT_BF16 if x.dtype == torch.bfloat16 else TTT_F32
+    _check(lib.ttt_eta_gate(B, H, L, Dx, io, float(eta_base), _ptr(x), _ptr(theta), _ptr(eta),
+                            _stream_handle(stream)))
+    return eta
 
 
 def set_wait_timeout_ns(ns: int):

@@ -304,6 +304,36 @@ ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const
     return ok();
 }
 
+ttt_status ttt_eta_gate(int B, int H, int L, int d_model, ttt_dtype x_dtype, float eta_base,
+                        const void *x, const float *theta, float *eta, ttt_stream_t stream)
+{
+    if (B <= 0 || H <= 0 || L <= 0 || d_model <= 0)
+        return fail(TTT_ERR_INVALID_ARG, "B, H, L and d_model must be positive");
+    if (x_dtype != TTT_F32 && x_dtype != TTT_BF16)
+        return fail(TTT_ERR_INVALID_ARG, "x_dtype must be TTT_F32 or TTT_BF16");
+    if (!std::isfinite(eta_base)) return fail(TTT_ERR_INVALID_ARG, "eta_base must be finite");
+    if ((long long)B * L > 0x7fffffffLL || (long long)B * H * L > (1LL << 40))
+        return fail(TTT_ERR_INVALID_ARG, "B * L exceeds the supported size");
+    if (x_dtype == TTT_BF16 && d_model % 8 != 0)
+        return fail(TTT_ERR_INVALID_ARG, "d_model must be a multiple of 8 for bf16 tokens");
+    ttt_status st;
+    if ((st = check_ptr(x, "x")) != TTT_OK) return st;
+    if ((st = check_ptr(theta, "theta")) != TTT_OK) return st;
+    if ((st = check_ptr(eta, "eta")) != TTT_OK) return st;
+    const size_t es = x_dtype == TTT_BF16 ? 2 : 4;
+    const Range re = range_of(eta, (size_t)B * H * L * 4);
+    if (overlap(re, range_of(x, (size_t)B * L * d_model * es)) ||
+        overlap(re, range_of(theta, (size_t)H * d_model * 4)))
+        return fail(TTT_ERR_INVALID_ARG, "eta overlaps an input");
+    ttt::GateArgs a{B, H, L, d_model, x_dtype, eta_base, x, theta, eta,
+                    reinterpret_cast<cudaStream_t>(stream), nullptr};
+    a.status = failure_flag(&st);
+    if (st != TTT_OK) return st;
+    cudaError_t e = ttt::launch_eta_gate(a);
+    if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "eta gate launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 void ttt_set_wait_timeout_ns(long long ns) { ttt::set_wait_timeout_ns(ns); }
 
 void ttt_debug_withhold_loads(int on) { ttt::set_withhold_loads(on); }

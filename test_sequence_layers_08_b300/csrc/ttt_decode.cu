@@ -20,7 +20,8 @@
 //     read and written once per call;
 //   * each token's q and k rows are staged in a per-warp shared-memory row, so every lane
 //     reads k_i and q_i as 16-byte broadcasts;
-//   * sums over the 64 features are warp butterflies.
+//   * sums over the 64 features are warp butterflies; the LayerNorm statistics take two
+//     passes (the mean, then the centred second moment).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -62,6 +63,13 @@ __device__ __forceinline__ void store_pair(void *base, size_t idx, float x, floa
         reinterpret_cast<float2 *>(base)[idx >> 1] = make_float2(x, y);
 }
 
+__device__ __forceinline__ float warp_sum(float a)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    return a;
+}
+
 __device__ __forceinline__ float2 warp_sum2(float a, float b)
 {
 #pragma unroll
@@ -94,18 +102,11 @@ linear_decode_kernel(DecodeParams p)
     float *bg = p.b + (size_t)bh * D;
     float c0 = bg[j0], c1 = bg[j0 + 1];
     float ga0 = 1.f, ga1 = 1.f, be0 = 0.f, be1 = 0.f;
-    // LayerNorm pivot: LN and its backward do not see a common shift of z, so with the residual
-    // LayerNorm the tokens run on c - p, p = mean(c), and p is added back when c is stored; the
-    // one-pass sums of z and z^2 then stay free of cancellation when c has a large offset.
-    float pivot = 0.f;
     if (LN) {
         ga0 = p.gamma[(size_t)h * D + j0];
         ga1 = p.gamma[(size_t)h * D + j0 + 1];
         be0 = p.beta[(size_t)h * D + j0];
         be1 = p.beta[(size_t)h * D + j0 + 1];
-        pivot = warp_sum2(c0 + c1, 0.f).x * (1.f / D);
-        c0 -= pivot;
-        c1 -= pivot;
     }
     float *qs = reinterpret_cast<float *>(rows[warp][0]);
     float *ks = reinterpret_cast<float *>(rows[warp][1]);
@@ -155,10 +156,12 @@ linear_decode_kernel(DecodeParams p)
         z1 += c1;
         float g0, g1;
         if (LN) {
-            const float2 s = warp_sum2(z0 + z1, fmaf(z0, z0, z1 * z1));
-            const float mu = s.x * (1.f / D);
-            const float r = rsqrtf(fmaxf(s.y * (1.f / D) - mu * mu, 0.f) + p.eps);
-            const float xh0 = (z0 - mu) * r, xh1 = (z1 - mu) * r;
+            // two passes (mean, then the centred second moment): no cancellation when z has a
+            // common offset much larger than its spread
+            const float mu = warp_sum(z0 + z1) * (1.f / D);
+            const float zc0 = z0 - mu, zc1 = z1 - mu;
+            const float r = rsqrtf(warp_sum(fmaf(zc0, zc0, zc1 * zc1)) * (1.f / D) + p.eps);
+            const float xh0 = zc0 * r, xh1 = zc1 * r;
             const float gx0 = ga0 * (fmaf(ga0, xh0, be0) - (v.x - k.x));
             const float gx1 = ga1 * (fmaf(ga1, xh1, be1) - (v.y - k.y));
             const float2 m = warp_sum2(gx0 + gx1, fmaf(gx0, xh0, gx1 * xh1));
@@ -193,11 +196,11 @@ linear_decode_kernel(DecodeParams p)
         o0 += c0;
         o1 += c1;
         if (LN) {
-            const float2 s = warp_sum2(o0 + o1, fmaf(o0, o0, o1 * o1));
-            const float mu = s.x * (1.f / D);
-            const float r = rsqrtf(fmaxf(s.y * (1.f / D) - mu * mu, 0.f) + p.eps);
-            o0 = q.x + fmaf(ga0 * (o0 - mu), r, be0);
-            o1 = q.y + fmaf(ga1 * (o1 - mu), r, be1);
+            const float mu = warp_sum(o0 + o1) * (1.f / D);
+            const float oc0 = o0 - mu, oc1 = o1 - mu;
+            const float r = rsqrtf(warp_sum(fmaf(oc0, oc0, oc1 * oc1)) * (1.f / D) + p.eps);
+            o0 = q.x + fmaf(ga0 * oc0, r, be0);
+            o1 = q.y + fmaf(ga1 * oc1, r, be1);
         }
         store_pair<BF16>(p.Z, base, o0, o1);
         __syncwarp();   // every lane is done with the staged rows before the next token
@@ -205,8 +208,8 @@ linear_decode_kernel(DecodeParams p)
 
 #pragma unroll
     for (int i = 0; i < D; ++i) *reinterpret_cast<float2 *>(Wg + i * D + j0) = make_float2(w[i][0], w[i][1]);
-    bg[j0] = c0 + pivot;
-    bg[j0 + 1] = c1 + pivot;
+    bg[j0] = c0;
+    bg[j0 + 1] = c1;
 }
 
 }  // namespace

@@ -109,6 +109,19 @@ __device__ __forceinline__ float gelu_tanh_prime(float x)
     return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * s * (1.f + 3.f * 0.044715f * x * x);
 }
 
+// Subtract the mean of the n values v[0..n) (shared memory, just written by the block) from
+// each of them; returns the mean.  Every thread sums in the same order, so all agree on it.
+__device__ float shift_by_mean(float *v, int n)
+{
+    __syncthreads();
+    float s = 0.f;
+    for (int j = 0; j < n; ++j) s += v[j];
+    const float mean = s / n;
+    __syncthreads();
+    for (int j = threadIdx.x; j < n; j += blockDim.x) v[j] -= mean;
+    return mean;
+}
+
 struct LinearParams {
     int H, L, d, mb, ln, init_per_batch;
     float eps;
@@ -149,6 +162,11 @@ __global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p
             bet[j] = p.beta[(size_t)h * d + j];
         }
     }
+    // LayerNorm pivot: LN and its backward do not see a common shift of k W + c, so with the
+    // residual LayerNorm the scan runs on c - mean(b0) and the mean is added back to b_final.
+    // The shifted bias keeps its per-feature deviations at full fp32 precision when b0 has a
+    // large common offset (an unshifted fp32 c holds them only to ulp(|c|)).
+    const float pivot = LN ? shift_by_mean(c, d) : 0.f;
     const IO *Qg = static_cast<const IO *>(p.Q) + (size_t)bh * L * d;
     const IO *Kg = static_cast<const IO *>(p.K) + (size_t)bh * L * d;
     const IO *Vg = static_cast<const IO *>(p.V) + (size_t)bh * L * d;
@@ -227,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p
     }
     __syncthreads();
     for (int i = tid; i < d * d; i += kThreads) p.Wf[(size_t)bh * d * d + i] = W[i];
-    for (int j = tid; j < d; j += kThreads) p.bf[(size_t)bh * d + j] = c[j];
+    for (int j = tid; j < d; j += kThreads) p.bf[(size_t)bh * d + j] = c[j] + pivot;
 }
 
 // ---------------------------------------------------------------------------
@@ -279,6 +297,8 @@ __global__ void __launch_bounds__(kThreads) mlp_generic_kernel(MlpParams p)
             bet[j] = p.beta[(size_t)h * d + j];
         }
     }
+    // LayerNorm pivot (as in the linear kernel): the scan runs on b2 - mean(b2)
+    const float pivot = LN ? shift_by_mean(b2, d) : 0.f;
     const IO *Qg = static_cast<const IO *>(p.Q) + (size_t)bh * L * d;
     const IO *Kg = static_cast<const IO *>(p.K) + (size_t)bh * L * d;
     const IO *Vg = static_cast<const IO *>(p.V) + (size_t)bh * L * d;
@@ -404,7 +424,7 @@ __global__ void __launch_bounds__(kThreads) mlp_generic_kernel(MlpParams p)
         p.W2f[(size_t)bh * d * dh + i] = W2[i];
     }
     for (int m = tid; m < dh; m += kThreads) p.b1f[(size_t)bh * dh + m] = b1[m];
-    for (int j = tid; j < d; j += kThreads) p.b2f[(size_t)bh * d + j] = b2[j];
+    for (int j = tid; j < d; j += kThreads) p.b2f[(size_t)bh * d + j] = b2[j] + pivot;
 }
 
 constexpr size_t kMaxSmem = 227 * 1024;

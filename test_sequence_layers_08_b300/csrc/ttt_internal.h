@@ -41,6 +41,22 @@ struct DecodeArgs {
     cudaStream_t stream;
 };
 
+// One per-token learning-rate gate call: eta [B, H, L] from x [B, L, Dx] and theta [H, Dx].
+struct GateArgs {
+    int B, H, L, Dx;
+    ttt_dtype x_dtype;
+    float eta_base;
+    const void *x;
+    const float *theta;
+    float *eta;
+    cudaStream_t stream;
+    unsigned int *status;
+};
+
+// Gate kernels: warp-MMA kernel for bf16 tokens (H <= 32, Dx % 16 == 0), FP32 otherwise.
+bool gate_mma_supported(int H, int Dx, ttt_dtype x_dtype);
+cudaError_t launch_eta_gate(const GateArgs &a);
+
 // Generic kernels: one CTA per (batch, head), fp32 FFMA arithmetic, state in
 // shared memory.  *_smem_bytes returns 0 when the shape does not fit.
 size_t linear_generic_smem_bytes(const ttt_desc &d);

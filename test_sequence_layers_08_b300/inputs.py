@@ -1,9 +1,12 @@
 """Seeded synthetic inputs for the TTT inner-loop forward.
 
 This module draws random numbers and rounds them to the I/O precision; it
-holds none of the method's arithmetic (the per-token learning-rate gate that
-produces ``eta`` sits outside the library boundary: the caller passes eta).
-Both the CUDA path's tests/benchmark and the CPU oracle are fed from here.
+holds none of the method's arithmetic.  In particular it does not evaluate the
+per-token learning-rate gate: for the gated workloads it hands over the gate's
+inputs (the layer input x, the per-head gate vectors theta and eta_base), and
+the CUDA path (ttt_eta_gate) and the CPU oracle (oracle.eta_gate) each compute
+eta from them.  Both the CUDA path's tests/benchmark and the CPU oracle are fed
+from here.
 
 Recipe (numpy PCG64, one independent sub-stream per tensor, seed 0 unless
 overridden; values drawn in float32, then rounded to bfloat16 with
@@ -13,9 +16,10 @@ round-to-nearest-even when the I/O type is bf16):
     damodev.csdn.net TTT article, section 4.3), b0 ~ N(0, b0_std^2) ([H, d]).
   * TTT-MLP: W1 [H, d, dh], W2 [H, dh, d] ~ N(0, 0.02^2), b1 = b2 = 0.
   * residual LayerNorm: gamma ~ 1 + N(0, 0.02^2), beta ~ N(0, 0.02^2), [H, d].
-  * eta: either a constant, or the per-token gate eta = sigmoid(x . theta_h) / d
-    (lryc.cn TTT article, section 2.2, with eta_base = 1/d), where
-    x ~ N(0, 1)^768 per (batch, position) and theta_h ~ N(0, 0.02^2)^768 per head.
+  * eta: either a constant, or the inputs of the per-token gate
+    eta = eta_base * sigmoid(theta_h . x_t) (lryc.cn TTT article, section 2.2)
+    with eta_base = 1/d, x ~ N(0, 1)^768 per (batch, position) (rounded to bf16
+    for bf16 I/O: it is the layer's input) and theta_h ~ N(0, 0.02^2)^768 per head.
   * drift (long-context case): K and V get +0.1 * j / sqrt(d) added to every
     coordinate in segment j = floor(t / 4096).
 """
@@ -27,6 +31,7 @@ import numpy as np
 
 _STREAMS = ("Q", "K", "V", "W0", "b0", "x", "theta", "gamma", "beta", "W1", "b1", "W2",
             "b2")
+D_MODEL = 768   # width of the layer input x that the learning-rate gate reads
 
 
 @dataclasses.dataclass(frozen=True)
@@ -91,10 +96,18 @@ def bf16_bits(a: np.ndarray) -> np.ndarray:
     return (a.view(np.uint32) >> 16).astype(np.uint16)
 
 
+def uniform_eta(B: int, H: int, L: int, lo: float, hi: float, seed: int) -> np.ndarray:
+    """A learning rate drawn uniformly from [lo, hi) per (batch, head, token), float32
+    [B, H, L]: for cases that set eta directly instead of through the gate."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0x37A])))
+    return rng.uniform(lo, hi, (B, H, L)).astype(np.float32)
+
+
 def make_inputs(cfg: Config, seed: int = 0) -> dict:
     """All inputs of one workload as float32 numpy arrays (bf16-exact for bf16
-    I/O).  Keys: Q, K, V, eta, and W0, b0 (linear) or W1, b1, W2, b2 (MLP), and
-    gamma, beta (None without LayerNorm)."""
+    I/O).  Keys: Q, K, V; eta (constant-rate workloads) or x [B, L, 768], theta
+    [H, 768] and eta_base (gated workloads); W0, b0 (linear) or W1, b1, W2, b2
+    (MLP); gamma, beta (None without LayerNorm)."""
     ss = np.random.SeedSequence(seed).spawn(len(_STREAMS))
     rng = {name: np.random.Generator(np.random.PCG64(s)) for name, s in zip(_STREAMS, ss)}
     B, H, L, d = cfg.B, cfg.H, cfg.L, cfg.d
@@ -113,15 +126,14 @@ def make_inputs(cfg: Config, seed: int = 0) -> dict:
     if cfg.io == "bf16":
         Q, K, V = round_bf16(Q), round_bf16(K), round_bf16(V)
 
+    out = {"Q": Q, "K": K, "V": V}
     if cfg.eta == "const":
-        eta = np.full((B, H, L), cfg.eta_const, dtype=np.float32)
+        out["eta"] = np.full((B, H, L), cfg.eta_const, dtype=np.float32)
     else:
-        x = rng["x"].standard_normal((B, L, 768), dtype=np.float32)
-        theta = normal("theta", (H, 768), 0.02)
-        logits = np.einsum("blk,hk->bhl", x.astype(np.float64), theta.astype(np.float64))
-        eta = (1.0 / (1.0 + np.exp(-logits)) / d).astype(np.float32)
-
-    out = {"Q": Q, "K": K, "V": V, "eta": np.ascontiguousarray(eta)}
+        x = rng["x"].standard_normal((B, L, D_MODEL), dtype=np.float32)
+        out["x"] = round_bf16(x) if cfg.io == "bf16" else x
+        out["theta"] = normal("theta", (H, D_MODEL), 0.02)
+        out["eta_base"] = 1.0 / d
     if cfg.kind == "linear":
         out["W0"] = normal("W0", (H, d, d), 0.02)
         out["b0"] = (normal("b0", (H, d), cfg.b0_std) if cfg.b0_std > 0

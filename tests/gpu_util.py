@@ -20,16 +20,29 @@ def rel_l2(got, ref):
 
 
 def to_device(cfg, x, device="cuda:0"):
+    """The inputs on the GPU.  When the workload gives the gate's inputs (x, theta,
+    eta_base) instead of eta, eta is computed on the GPU by the library's gate."""
     io = torch.bfloat16 if cfg.io == "bf16" else torch.float32
     dev = {}
     for k, v in x.items():
-        if v is None:
-            dev[k] = None
-        elif k in ("Q", "K", "V"):
-            dev[k] = torch.from_numpy(v).to(device).to(io).contiguous()
+        if v is None or k == "eta_base":
+            dev[k] = v
+        elif k in ("Q", "K", "V", "x"):
+            dev[k] = torch.from_numpy(np.ascontiguousarray(v)).to(device).to(io).contiguous()
         else:
             dev[k] = torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(device)
+    if "eta" not in dev:
+        dev["eta"] = ttt.ttt_eta_gate(dev["x"], dev["theta"], dev["eta_base"])
     return dev
+
+
+def with_oracle_eta(x):
+    """The inputs with eta for the oracle: given, or computed by the oracle's own gate."""
+    if "eta" in x:
+        return x
+    y = dict(x)
+    y["eta"] = oracle.eta_gate(x["x"], x["theta"], x["eta_base"])
+    return y
 
 
 def run_gpu(cfg, dev, stream=None, out=None, init_per_batch=False):
@@ -47,6 +60,7 @@ def run_gpu(cfg, dev, stream=None, out=None, init_per_batch=False):
 
 def run_oracle(cfg, x, pairs=None, threads=None):
     """Oracle outputs, either for everything or for a list of (batch, head)."""
+    x = with_oracle_eta(x)
     kw = dict(mini_batch=cfg.mini_batch, ln=cfg.ln, eps=cfg.eps)
     if pairs is None:
         if cfg.kind == "linear":

@@ -144,3 +144,30 @@ def test_step_aliasing_rules(lib):
         assert call_step(lib, desc(mini_batch=1), p) == 1, (i, j)
     assert call_step(lib, desc(mini_batch=1, d=256)) == 2   # no kernel for that width
 
+
+
+def call_gate(lib, B=2, H=3, L=64, Dx=768, io=1, eta_base=0.5, ptrs=None):
+    p = [FAKE + i * (1 << 30) for i in range(3)] if ptrs is None else ptrs
+    return lib.ttt_eta_gate(B, H, L, Dx, io, eta_base,
+                            *[ctypes.c_void_p(x) if x else None for x in p], None)
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(L=-1), dict(Dx=0), dict(io=5),
+                                dict(Dx=20), dict(eta_base=float("inf"))])
+def test_gate_bad_arguments(lib, kw):
+    assert call_gate(lib, **kw) == 1
+    assert lib.ttt_last_error().decode() != ""
+
+
+def test_gate_null_misaligned_and_overlap(lib):
+    base = [FAKE + i * (1 << 30) for i in range(3)]
+    for i in range(3):
+        p = list(base)
+        p[i] = 0
+        assert call_gate(lib, ptrs=p) == 1
+        p[i] = base[i] + 8
+        assert call_gate(lib, ptrs=p) == 1
+    p = list(base)
+    p[2] = base[0] + 4096            # eta inside x
+    assert call_gate(lib, ptrs=p) == 1
+    assert "overlap" in lib.ttt_last_error().decode()

@@ -7,7 +7,7 @@ import torch
 import oracle
 import test_sequence_layers_08_b300 as ttt
 from test_sequence_layers_08_b300.inputs import CONFIGS
-from gpu_util import TOL, compare_all, inputs, rel_l2
+from gpu_util import TOL, compare_all, inputs, rel_l2, to_device, with_oracle_eta
 
 pytestmark = pytest.mark.gpu
 
@@ -24,11 +24,7 @@ def problem(io, ln, B, H, L, d=64, seed=3):
 
 
 def to_dev(cfg, x, W, b):
-    io = torch.bfloat16 if cfg.io == "bf16" else torch.float32
-    d = {k: torch.from_numpy(x[k]).cuda().to(io).contiguous() for k in ("Q", "K", "V")}
-    d["eta"] = torch.from_numpy(np.ascontiguousarray(x["eta"], np.float32)).cuda()
-    for k in ("gamma", "beta"):
-        d[k] = None if x[k] is None else torch.from_numpy(x[k]).cuda()
+    d = to_device(cfg, {k: v for k, v in x.items() if k not in ("W0", "b0")})
     d["W"] = torch.from_numpy(W.copy()).cuda()
     d["b"] = torch.from_numpy(b.copy()).cuda()
     return d
@@ -44,6 +40,7 @@ def step(cfg, d, sl=slice(None), out=None):
 
 
 def oracle_ref(cfg, x, W, b):
+    x = with_oracle_eta(x)
     return oracle.ttt_linear(x["Q"], x["K"], x["V"], x["eta"], W, b, x["gamma"], x["beta"],
                              mini_batch=1, ln=cfg.ln, eps=cfg.eps, init_per_batch=True)
 

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import test_sequence_layers_08_b300 as ttt
-from test_sequence_layers_08_b300.inputs import CONFIGS
+from test_sequence_layers_08_b300.inputs import CONFIGS, uniform_eta
 
 from gpu_util import compare_all, inputs, run_gpu, run_oracle, to_device
 
@@ -46,7 +46,7 @@ def test_fused_large_state_values():
     """Large eta: the state moves far from its start within a few mini-batches."""
     cfg = LIN_LN.with_(name="bigeta", B=1, H=4, L=512)
     x = inputs(cfg, seed=17)
-    x["eta"] = (x["eta"] * 64.0).astype(np.float32)   # eta up to ~1
+    x["eta"] = uniform_eta(cfg.B, cfg.H, cfg.L, 0.0, 1.0, seed=17)   # eta up to ~1
     compare_all(cfg, run_gpu(cfg, to_device(cfg, x)), run_oracle(cfg, x))
 
 

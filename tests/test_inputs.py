@@ -21,7 +21,7 @@ def test_inputs_are_deterministic_and_bf16_exact():
     a, b = make_inputs(cfg, 0), make_inputs(cfg, 0)
     for k in a:
         if a[k] is not None:
-            np.testing.assert_array_equal(a[k], b[k])
+            np.testing.assert_array_equal(np.asarray(a[k]), np.asarray(b[k]))
     for k in ("Q", "K", "V"):
         assert np.array_equal(round_bf16(a[k]), a[k])
     c = make_inputs(cfg, 1)
@@ -35,11 +35,22 @@ def test_input_statistics():
     assert abs(x["Q"].std() - 1 / 8) < 0.01
     assert abs(x["W0"].std() - 0.02) < 0.002
     assert abs(x["b0"].std() - 0.01) < 0.002
-    # sigmoid(x . theta) / d with logit std ~ 0.55 -> eta around 1/128
-    assert 0.0 < x["eta"].min() and x["eta"].max() < 1 / 64
-    assert abs(np.log(x["eta"] * 64 / (1 - x["eta"] * 64)).std() - 0.02 * np.sqrt(768)) < 0.03
-    assert abs(x["eta"].mean() - 1 / 128) < 5e-4
+    # the gate's inputs, not eta itself: x ~ N(0, 1) (bf16-exact), theta ~ N(0, 0.02^2)
+    assert "eta" not in x
+    assert x["x"].shape == (2, 1024, 768) and x["theta"].shape == (4, 768)
+    assert np.array_equal(round_bf16(x["x"]), x["x"])
+    assert abs(x["x"].std() - 1.0) < 0.01
+    assert abs(x["theta"].std() - 0.02) < 0.001
+    assert x["eta_base"] == 1 / 64
     assert x["gamma"] is None
+
+
+def test_uniform_eta_range_and_determinism():
+    from test_sequence_layers_08_b300.inputs import uniform_eta
+    a = uniform_eta(2, 3, 50, 0.2, 0.5, seed=4)
+    assert a.shape == (2, 3, 50) and a.dtype == np.float32
+    assert a.min() >= 0.2 and a.max() < 0.5
+    np.testing.assert_array_equal(a, uniform_eta(2, 3, 50, 0.2, 0.5, seed=4))
 
 
 def test_drift_shifts_k_and_v_only():

@@ -11,7 +11,7 @@ import pytest
 
 from test_sequence_layers_08_b300.inputs import CONFIGS, round_bf16
 
-from gpu_util import compare_all, inputs, run_gpu, run_oracle, to_device
+from gpu_util import compare_all, inputs, run_gpu, run_oracle, to_device, with_oracle_eta
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +55,7 @@ def test_linear_bias_offset_per_batch_state():
     x["b0"] = (4.0 + 0.01 * rng.standard_normal((cfg.B, cfg.H, cfg.d))).astype(np.float32)
     got = run_gpu(cfg, to_device(cfg, x), init_per_batch=True)
     import oracle
+    x = with_oracle_eta(x)
     ref = oracle.ttt_linear(x["Q"], x["K"], x["V"], x["eta"], x["W0"], x["b0"], x["gamma"],
                             x["beta"], mini_batch=cfg.mini_batch, ln=True, eps=cfg.eps,
                             init_per_batch=True)

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import test_sequence_layers_08_b300 as ttt
-from test_sequence_layers_08_b300.inputs import CONFIGS
+from test_sequence_layers_08_b300.inputs import CONFIGS, uniform_eta
 
 from gpu_util import compare_all, inputs, run_gpu, run_oracle, to_device
 
@@ -43,7 +43,7 @@ def test_fused_mlp_large_eta():
     (Per-(batch, head) initial state is covered by the state-carry test.)"""
     cfg = MLP.with_(name="bigeta", B=2, H=2, L=128)
     x = inputs(cfg, seed=31)
-    x["eta"] = (x["eta"] * 16.0).astype(np.float32)
+    x["eta"] = uniform_eta(cfg.B, cfg.H, cfg.L, 0.0, 0.25, seed=31)
     compare_all(cfg, run_gpu(cfg, to_device(cfg, x)), run_oracle(cfg, x))
 
 

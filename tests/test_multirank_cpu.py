@@ -59,6 +59,8 @@ def _shard_worker(rank, world, port, q):
     dist.init_process_group("gloo")
     cfg = CONFIGS["linear_ln_bf16_B4_H16_L8192"].with_(name="shard", B=2, H=3, L=64)
     x = make_inputs(cfg, 0)
+    if "eta" not in x:
+        x["eta"] = oracle.eta_gate(x["x"], x["theta"], x["eta_base"])
     pairs = [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
     mine = pairs[rank::world]                      # (batch, head) shard of this rank
     res = oracle.run_pairs(cfg.kind, x, mine, threads=1, mini_batch=cfg.mini_batch, ln=cfg.ln,
@@ -86,6 +88,8 @@ def test_head_shards_reassemble_the_single_process_result():
         assert p.exitcode == 0
     cfg = CONFIGS["linear_ln_bf16_B4_H16_L8192"].with_(name="shard", B=2, H=3, L=64)
     x = make_inputs(cfg, 0)
+    if "eta" not in x:
+        x["eta"] = oracle.eta_gate(x["x"], x["theta"], x["eta_base"])
     pairs = [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
     full = oracle.run_pairs(cfg.kind, x, pairs, threads=1, mini_batch=cfg.mini_batch, ln=cfg.ln,
                             eps=cfg.eps)

@@ -63,7 +63,7 @@ def test_generic_shapes(mb, d):
 def test_eta_zero_returns_initial_state(kind):
     cfg = (LIN_LN if kind == "linear" else MLP).with_(name="z", B=2, H=2, L=64)
     x = inputs(cfg, seed=6)
-    x["eta"][:] = 0.0
+    x["eta"] = np.zeros((cfg.B, cfg.H, cfg.L), np.float32)
     got = run_gpu(cfg, to_device(cfg, x))
     ref = run_oracle(cfg, x)
     compare_all(cfg, got, ref)
