@@ -670,8 +670,13 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode()
     return fn;
 }
 
+long long g_wait_ns = kDefaultWaitNs;
+int g_withhold_loads = 0;
+
+}  // namespace
+
 // [BH][L][64] bf16 viewed as a 3-D tensor; boxes of `rows` tokens, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, int L, int BH, int rows)
+bool make_bf16_tile_map(CUtensorMap *m, const void *base, int L, int BH, int rows)
 {
     auto enc = get_encode();
     if (!enc) return false;
@@ -684,11 +689,6 @@ bool make_map(CUtensorMap *m, const void *base, int L, int BH, int rows)
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
-
-long long g_wait_ns = kDefaultWaitNs;
-int g_withhold_loads = 0;
-
-}  // namespace
 
 void set_wait_timeout_ns(long long ns) { g_wait_ns = ns > 0 ? ns : kDefaultWaitNs; }
 void set_withhold_loads(int on) { g_withhold_loads = on != 0; }
@@ -705,8 +705,8 @@ cudaError_t launch_linear_tc(const LinearArgs &a)
     const ttt_desc &d = a.desc;
     const int BH = d.B * d.H;
     CUtensorMap mq, mk, mv, mz;
-    if (!make_map(&mq, a.Q, d.L, BH, ST) || !make_map(&mk, a.K, d.L, BH, ST) ||
-        !make_map(&mv, a.V, d.L, BH, ST) || !make_map(&mz, a.Z, d.L, BH, MB))
+    if (!make_bf16_tile_map(&mq, a.Q, d.L, BH, ST) || !make_bf16_tile_map(&mk, a.K, d.L, BH, ST) ||
+        !make_bf16_tile_map(&mv, a.V, d.L, BH, ST) || !make_bf16_tile_map(&mz, a.Z, d.L, BH, MB))
         return cudaErrorInvalidValue;
     Params p{d.H, d.L, d.residual_ln, d.ln_eps, g_wait_ns, g_withhold_loads, a.eta, a.W0, a.b0, a.gamma, a.beta,
              a.W_final, a.b_final, a.status, d.init_per_batch};
