@@ -3,13 +3,19 @@ GPU under torchrun), plus roofline fraction, clocks, an end-to-end number
 through host buffers and the CPU oracle as a reported baseline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--decode T]
+                    [--impl ours|reference] [--decode T] [--gated] [--split]
 
 A step is one call of the library entry point over one batch of the workload
 (the whole hot path: every mini-batch of every (batch, head) scan).  Inputs are
 synthetic (seeded, see test_sequence_layers_08_b300/inputs.py) and resident in
 HBM; consecutive steps rotate through enough input/output copies that their
 union exceeds the 126 MB L2, so no step starts with its inputs in L2.
+
+Under torchrun (N > 1) every rank runs a replica of the workload by default
+(weak scaling); --split gives each rank its contiguous range of (batch, head)
+rows of one workload instead (partition_rows; strong scaling, no collective).
+--gated puts the learning-rate gate (ttt_eta_gate, eta from the layer input)
+in every step.
 
 --decode T times the decode step instead (ttt_linear_step: T tokens per call, one
 at a time, from a state carried in device memory between calls) on a linear
@@ -296,13 +302,22 @@ def run_ours(args, cfg, world, rank, local):
     def dev_inputs():
         d = {}
         for k in ("Q", "K", "V"):
-            d[k] = torch.from_numpy(x[k]).to(dev).to(io)
+            d[k] = rows(torch.from_numpy(x[k]).to(dev).to(io))
         for k in ["gamma", "beta"] + state_keys:
             d[k] = None if x[k] is None else torch.from_numpy(x[k]).to(dev)
-        d["eta"] = eta_dev.clone()
+        d["eta"] = rows(eta_dev.clone())
         return d
 
-    per_set = algorithmic_bytes(cfg)
+    # --split: this rank's contiguous range of (batch, head) rows (the library's partition);
+    # otherwise every rank runs the whole workload (a replica)
+    split = args.split and world > 1
+    r0, r1 = ttt.partition_rows(cfg.B * cfg.H, world, rank) if split else (0, cfg.B * cfg.H)
+    part_kw = dict(heads=cfg.H, bh_offset=r0) if split else {}
+
+    def rows(t):   # this rank's rows of a [B, H, ...] tensor
+        return t.reshape((-1,) + tuple(t.shape[2:]))[r0:r1].contiguous() if split else t
+
+    per_set = algorithmic_bytes(cfg) * (r1 - r0) / (cfg.B * cfg.H)
     n_sets = max(1, min(8, math.ceil(3 * L2_BYTES / per_set)))
     sets = [dev_inputs() for _ in range(n_sets)]
     outs = [None] * n_sets
@@ -313,7 +328,7 @@ def run_ours(args, cfg, world, rank, local):
         if args.gated:   # the learning-rate gate is part of the step
             ttt.ttt_eta_gate(x_dev, theta_dev, x["eta_base"], out=s["eta"], stream=stream)
         kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps,
-                  out=outs[i % n_sets], stream=stream)
+                  out=outs[i % n_sets], stream=stream, **part_kw)
         if cfg.kind == "linear":
             o = ttt.ttt_linear_fwd(s["Q"], s["K"], s["V"], s["eta"], s["W0"], s["b0"],
                                    s["gamma"], s["beta"], **kw)
@@ -323,7 +338,7 @@ def run_ours(args, cfg, world, rank, local):
         outs[i % n_sets] = o
 
     desc = ttt.make_desc(sets[0]["Q"], cfg.mini_batch, cfg.ln, cfg.eps,
-                         d_hidden=cfg.dh if cfg.kind == "mlp" else 0)
+                         d_hidden=cfg.dh if cfg.kind == "mlp" else 0, **part_kw)
     kname = ttt.kernel_name(desc, cfg.kind == "mlp")
 
     clocks = ClockSampler(local)
@@ -360,7 +375,8 @@ def run_ours(args, cfg, world, rank, local):
     ms_total = start.elapsed_time(end)
     ms_total = max_over_ranks(world, ms_total)
     ms_step = ms_total / args.steps
-    value = world * cfg.tokens / (ms_step * 1e-3)
+    # replicas: every rank runs the whole workload; split: the ranks share one workload
+    value = (1 if split else world) * cfg.tokens / (ms_step * 1e-3)
     if time.time() - t_wall1 < 0.4:
         time.sleep(0.4)   # let the sampler log past the end of the timed region
     clk = clocks.summary(t_soak, time.time())
@@ -380,7 +396,8 @@ def run_ours(args, cfg, world, rank, local):
     out_specs = [(tuple(o.shape), o.dtype) for o in outs[0]]
     hin_flat, hin = packed(in_specs, "cpu", pin=True)
     for k, hv in zip(in_keys, hin):
-        hv.copy_(eta_dev.cpu() if k == "eta" else torch.from_numpy(x[k]).to(hv.dtype))
+        src = eta_dev.cpu() if k == "eta" else torch.from_numpy(x[k]).to(hv.dtype)
+        hv.copy_(rows(src) if k in ("Q", "K", "V", "eta") else src)
     dsets, douts, din_flat, dout_flat, hout_flat = [], [], [], [], []
     for _ in range(2):
         f, views = packed(in_specs, dev)
@@ -406,7 +423,7 @@ def run_ours(args, cfg, world, rank, local):
         if args.gated:
             ttt.ttt_eta_gate(s_["x"], theta_dev, x["eta_base"], out=s_["eta"], stream=stream)
         kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps,
-                  out=douts[b], stream=stream)
+                  out=douts[b], stream=stream, **part_kw)
         if cfg.kind == "linear":
             douts[b] = ttt.ttt_linear_fwd(s_["Q"], s_["K"], s_["V"], s_["eta"], s_["W0"], s_["b0"],
                                           s_["gamma"], s_["beta"], **kw)
@@ -447,14 +464,14 @@ def run_ours(args, cfg, world, rank, local):
     s1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(world, s0.elapsed_time(s1)) / n_e2e
-    e2e_value = world * cfg.tokens / (e2e_ms * 1e-3)
+    e2e_value = (1 if split else world) * cfg.tokens / (e2e_ms * 1e-3)
 
     clocks.stop()
     peaks = load_peaks()
-    alg_bytes = algorithmic_bytes(cfg)
-    alg_flops = flops_per_head_token(cfg) * cfg.head_tokens
+    alg_bytes = per_set
+    alg_flops = flops_per_head_token(cfg) * cfg.L * (r1 - r0)
     if args.gated:   # the gate reads x and writes eta (the scan's read of eta is counted)
-        alg_bytes += x_dev.numel() * x_dev.element_size() + cfg.head_tokens * 4
+        alg_bytes += x_dev.numel() * x_dev.element_size() + cfg.head_tokens * 4   # (replicas)
         alg_flops += 2.0 * x_dev.numel() * cfg.H
     achieved_gbs = alg_bytes / (ms_step * 1e-3) / 1e9
     achieved_tf = alg_flops / (ms_step * 1e-3) / 1e12
@@ -480,7 +497,8 @@ def run_ours(args, cfg, world, rank, local):
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "higher_is_better": True, "scaling": "strong" if split else "weak",
+                "vs_baseline": None,
                 "dtype": "bf16" if cfg.io == "bf16" else "f32", "data": "synthetic",
                 "config": {"workload": cfg.name + ("+gate" if args.gated else ""),
                            "kind": cfg.kind, "B": cfg.B, "H": cfg.H,
@@ -490,7 +508,10 @@ def run_ours(args, cfg, world, rank, local):
                            "io": cfg.io, "state": "f32", "residual_ln": cfg.ln,
                            "l2": f"inputs rotate over {n_sets} copies "
                                  f"({n_sets * alg_bytes / 1e6:.0f} MB > L2)",
-                           "parallelism": f"replica x{world}, one CTA per (batch, head)"},
+                           "parallelism": (f"(batch, head) rows split over {world} GPUs "
+                                           f"(rank 0: rows {r0}..{r1 - 1}), one CTA per row"
+                                           if split else
+                                           f"replica x{world}, one CTA per (batch, head)")},
                 "head_tokens_per_s": value * cfg.H, "roofline": roof, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h,
@@ -672,6 +693,9 @@ def main():
     ap.add_argument("--decode", type=int, default=0, metavar="T",
                     help="time the decode step instead: T tokens per call, one at a time, from a "
                          "state carried between calls (a linear workload's B, H, d)")
+    ap.add_argument("--split", action="store_true",
+                    help="with N > 1 GPUs, split one workload's (batch, head) rows over the ranks "
+                         "(strong scaling) instead of running a replica on each")
     ap.add_argument("--gated", action="store_true",
                     help="each step also computes eta from the layer input with the learning-rate "
                          "gate (ttt_eta_gate) before the scan")
@@ -684,6 +708,8 @@ def main():
     cfg = CONFIGS[args.workload]
     if args.gated and cfg.eta != "gate":
         raise SystemExit("--gated needs a workload with the per-token gate")
+    if args.gated and args.split:
+        raise SystemExit("--gated and --split are not combined")
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":

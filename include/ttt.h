@@ -27,7 +27,8 @@
  *     state; it only launches kernels on `stream` and returns.  Results are
  *     valid once the stream has been synchronised (ttt_sync_status does that
  *     and also reports device-side failures).
- *   - Layouts are dense row-major, no padding, 16-byte aligned base pointers:
+ *   - Layouts are dense row-major, no padding, 16-byte aligned base pointers
+ *     (shapes below for a call on all B*H rows; see bh_offset/bh_count):
  *       Q, K, V, Z   [B, H, L, d]   element type desc->io_dtype
  *       eta          [B, H, L]      float
  *       gamma, beta  [H, d]         float  (may be NULL iff residual_ln == 0)
@@ -79,6 +80,16 @@ typedef struct {
     int residual_ln;    /* 0: f = f_res;  1: f(k) = k + LN(f_res(k))           */
     float ln_eps;       /* LayerNorm eps, finite and > 0 when residual_ln      */
     int init_per_batch; /* 0: initial state [H, ...];  1: [B, H, ...]          */
+    /* (batch, head) partition: the call covers rows bh_offset .. bh_offset + rows - 1 of
+     * the flattened B*H grid (row = b*H + h), rows = bh_count (0: all B*H rows, with
+     * bh_offset 0).  Every row-indexed buffer (Q, K, V, Z, eta, the final state, and
+     * the initial state when init_per_batch) starts at the call's first row and holds
+     * `rows` rows; head-indexed parameters (a head-shared initial state, gamma, beta)
+     * are passed whole, and row i of the call uses head (bh_offset + i) mod H.  Rows
+     * are independent, so calls on disjoint ranges (e.g. one per GPU) together give
+     * the result of one call on all rows. */
+    int bh_offset;
+    int bh_count;
 } ttt_desc;
 
 /*
@@ -182,7 +193,7 @@ TTT_API const char *ttt_last_error(void);
  * (is_mlp = 0 or 1), or NULL when the descriptor is rejected. */
 TTT_API const char *ttt_kernel_name(const ttt_desc *desc, int is_mlp);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor); 101 added bh_offset/bh_count. */
 TTT_API int ttt_version(void);
 
 #ifdef __cplusplus

@@ -18,7 +18,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["TTTError", "Desc", "load", "library_path", "ttt_eta_gate", "ttt_linear_fwd", "ttt_mlp_fwd", "ttt_linear_step",
+__all__ = ["TTTError", "Desc", "load", "library_path", "partition_rows", "ttt_eta_gate", "ttt_linear_fwd", "ttt_mlp_fwd", "ttt_linear_step",
            "ttt_sync_status", "kernel_name", "version", "STATUS", "set_wait_timeout_ns",
            "debug_withhold_loads"]
 
@@ -42,7 +42,8 @@ class Desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("L", ctypes.c_int),
                 ("d", ctypes.c_int), ("d_hidden", ctypes.c_int), ("mini_batch", ctypes.c_int),
                 ("io_dtype", ctypes.c_int), ("residual_ln", ctypes.c_int),
-                ("ln_eps", ctypes.c_float), ("init_per_batch", ctypes.c_int)]
+                ("ln_eps", ctypes.c_float), ("init_per_batch", ctypes.c_int),
+                ("bh_offset", ctypes.c_int), ("bh_count", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -106,14 +107,49 @@ def _stream_handle(stream):
 
 
 def make_desc(Q, mini_batch: int, residual_ln: bool, ln_eps: float = 1e-6,
-              init_per_batch: bool = False, d_hidden: int = 0) -> Desc:
+              init_per_batch: bool = False, d_hidden: int = 0, heads=None, bh_offset: int = 0) -> Desc:
+    """Descriptor of a call on Q [B, H, L, d], or on the row form Q [rows, L, d] covering rows
+    bh_offset .. bh_offset + rows - 1 of a (batch, head) grid with `heads` heads."""
     import torch
-    B, H, L, d = Q.shape
     io = {torch.float32: TTT_F32, torch.bfloat16: TTT_BF16}.get(Q.dtype)
     if io is None:
         raise TypeError(f"unsupported I/O dtype {Q.dtype}")
+    lead, H, L, d, B, off, cnt = _geometry(Q, heads, bh_offset)
     return Desc(B, H, L, d, d_hidden, mini_batch, io, int(residual_ln), float(ln_eps),
-                int(init_per_batch))
+                int(init_per_batch), off, cnt)
+
+
+def partition_rows(total_rows: int, world: int, rank: int):
+    """The contiguous range [r0, r1) of (batch, head) rows that rank `rank` of `world` owns:
+    balanced (sizes differ by at most one), in rank order, covering 0 .. total_rows - 1."""
+    if world <= 0 or not 0 <= rank < world or total_rows < 0:
+        raise ValueError("need world > 0, 0 <= rank < world and total_rows >= 0")
+    base, extra = divmod(total_rows, world)
+    r0 = rank * base + min(rank, extra)
+    return r0, r0 + base + (1 if rank < extra else 0)
+
+
+def _geometry(Q, heads, bh_offset):
+    """(row-indexed leading shape, H, L, d, descriptor B, bh_offset, bh_count) of a call:
+    Q [B, H, L, d] (heads None), or the row form Q [rows, L, d] with `heads` = H."""
+    import torch
+    if not isinstance(Q, torch.Tensor):
+        raise TypeError("Q must be a torch.Tensor")
+    if heads is None:
+        if Q.dim() != 4:
+            raise ValueError("Q must be [B, H, L, d], or the row form [rows, L, d] with heads=H")
+        if bh_offset:
+            raise ValueError("bh_offset needs the row form Q [rows, L, d] with heads=H")
+        B, H, L, d = Q.shape
+        return (B, H), H, L, d, B, 0, 0
+    if Q.dim() != 3:
+        raise ValueError("with heads=H, Q must be the row form [rows, L, d]")
+    rows, L, d = Q.shape
+    H = int(heads)
+    if H <= 0 or bh_offset < 0 or rows <= 0:
+        raise ValueError("need heads > 0, bh_offset >= 0 and at least one row")
+    B = -(-(bh_offset + rows) // H)
+    return (rows,), H, L, d, B, int(bh_offset), rows
 
 
 def kernel_name(desc: Desc, mlp: bool = False):
@@ -137,30 +173,22 @@ def _expect(name, t, shape, dtype, device):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _io_shape(Q):
-    """Validate Q itself and return (B, H, L, d)."""
+def _check_sequence(Q, K, V, eta, gamma, beta, residual_ln, heads=None, bh_offset=0):
+    """Shapes, dtypes, device and contiguity of the per-token inputs and the LayerNorm
+    parameters; returns (row-indexed leading shape, H, L, d, device)."""
     import torch
-    if not isinstance(Q, torch.Tensor) or Q.dim() != 4:
-        raise ValueError("Q must be a [B, H, L, d] tensor")
+    lead, H, L, d, _, _, _ = _geometry(Q, heads, bh_offset)
     if Q.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError(f"unsupported I/O dtype {Q.dtype}")
-    _expect("Q", Q, Q.shape, Q.dtype, Q.device)
-    return tuple(Q.shape)
-
-
-def _check_sequence(Q, K, V, eta, gamma, beta, residual_ln):
-    """Shapes, dtypes, device and contiguity of the per-token inputs and the LayerNorm
-    parameters; returns (B, H, L, d, device)."""
-    import torch
-    B, H, L, d = _io_shape(Q)
     dev = Q.device
-    _expect("K", K, (B, H, L, d), Q.dtype, dev)
-    _expect("V", V, (B, H, L, d), Q.dtype, dev)
-    _expect("eta", eta, (B, H, L), torch.float32, dev)
+    _expect("Q", Q, lead + (L, d), Q.dtype, dev)
+    _expect("K", K, lead + (L, d), Q.dtype, dev)
+    _expect("V", V, lead + (L, d), Q.dtype, dev)
+    _expect("eta", eta, lead + (L,), torch.float32, dev)
     if residual_ln:
         _expect("gamma", gamma, (H, d), torch.float32, dev)
         _expect("beta", beta, (H, d), torch.float32, dev)
-    return B, H, L, d, dev
+    return lead, H, L, d, dev
 
 
 def _require_cuda(dev):
@@ -170,29 +198,33 @@ def _require_cuda(dev):
 
 def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: int = 16,
                    residual_ln: bool = False, ln_eps: float = 1e-6, init_per_batch: bool = False,
-                   out=None, stream=None):
+                   out=None, stream=None, heads=None, bh_offset: int = 0):
     """TTT-Linear forward on the GPU.  Q,K,V: [B,H,L,d] (float32 or bfloat16);
     eta [B,H,L] float32; W0 [H,d,d] (or [B,H,d,d] with init_per_batch); b0 [H,d]
     (or [B,H,d]); gamma, beta [H,d] float32 (residual LayerNorm only).  Returns
     (Z, W_final, b_final); pass ``out=(Z, W_final, b_final)`` to reuse buffers.
+    Row form (a (batch, head) partition): with ``heads=H``, Q, K, V are [rows, L, d], eta
+    [rows, L], the outputs [rows, ...], W0/b0 [H, ...] (or [rows, ...] with init_per_batch),
+    and the rows are rows bh_offset .. bh_offset + rows - 1 of the B*H grid (row b*H + h).
     Every operand is checked (shape, dtype, device, contiguity) before the C call.
     The call is asynchronous on ``stream`` (default: torch's current stream)."""
     import torch
-    B, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln)
-    lead = (B, H) if init_per_batch else (H,)
-    _expect("W0", W0, lead + (d, d), torch.float32, dev)
-    _expect("b0", b0, lead + (d,), torch.float32, dev)
+    lead, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln, heads, bh_offset)
+    init = lead if init_per_batch else (H,)
+    _expect("W0", W0, init + (d, d), torch.float32, dev)
+    _expect("b0", b0, init + (d,), torch.float32, dev)
     if out is not None:
         Z, Wf, bf = out
-        _expect("out Z", Z, (B, H, L, d), Q.dtype, dev)
-        _expect("out W_final", Wf, (B, H, d, d), torch.float32, dev)
-        _expect("out b_final", bf, (B, H, d), torch.float32, dev)
+        _expect("out Z", Z, lead + (L, d), Q.dtype, dev)
+        _expect("out W_final", Wf, lead + (d, d), torch.float32, dev)
+        _expect("out b_final", bf, lead + (d,), torch.float32, dev)
     _require_cuda(dev)
     lib = load()
-    desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch)
+    desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, heads=heads,
+                     bh_offset=bh_offset)
     if out is None:
-        out = (torch.empty_like(Q), torch.empty((B, H, d, d), device=dev, dtype=torch.float32),
-               torch.empty((B, H, d), device=dev, dtype=torch.float32))
+        out = (torch.empty_like(Q), torch.empty(lead + (d, d), device=dev, dtype=torch.float32),
+               torch.empty(lead + (d,), device=dev, dtype=torch.float32))
     Z, Wf, bf = out
     _check(lib.ttt_linear_fwd(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta),
                               _ptr(W0), _ptr(b0), _ptr(gamma if residual_ln else None),
@@ -202,19 +234,20 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: i
 
 
 def ttt_linear_step(Q, K, V, eta, W, b, gamma=None, beta=None, *, residual_ln: bool = False,
-                    ln_eps: float = 1e-6, out=None, stream=None):
+                    ln_eps: float = 1e-6, out=None, stream=None, heads=None, bh_offset: int = 0):
     """TTT-Linear decode on the GPU: the L tokens of Q, K, V [B,H,L,d] one at a time from
     the state W [B,H,d,d], b [B,H,d] (float32), which is updated in place.  Returns Z
-    [B,H,L,d]; pass ``out=Z`` to reuse a buffer.  Asynchronous on ``stream``."""
+    [B,H,L,d]; pass ``out=Z`` to reuse a buffer.  Row form as for ttt_linear_fwd (the state
+    is then [rows, d, d] and [rows, d]).  Asynchronous on ``stream``."""
     import torch
-    B, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln)
-    _expect("W", W, (B, H, d, d), torch.float32, dev)
-    _expect("b", b, (B, H, d), torch.float32, dev)
+    lead, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln, heads, bh_offset)
+    _expect("W", W, lead + (d, d), torch.float32, dev)
+    _expect("b", b, lead + (d,), torch.float32, dev)
     if out is not None:
-        _expect("out Z", out, (B, H, L, d), Q.dtype, dev)
+        _expect("out Z", out, lead + (L, d), Q.dtype, dev)
     _require_cuda(dev)
     lib = load()
-    desc = make_desc(Q, 1, residual_ln, ln_eps, True)
+    desc = make_desc(Q, 1, residual_ln, ln_eps, True, heads=heads, bh_offset=bh_offset)
     Z = torch.empty_like(Q) if out is None else out
     _check(lib.ttt_linear_step(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta), _ptr(W),
                                _ptr(b), _ptr(gamma if residual_ln else None),
@@ -224,34 +257,35 @@ def ttt_linear_step(Q, K, V, eta, W, b, gamma=None, beta=None, *, residual_ln: b
 
 def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_batch: int = 16,
                 residual_ln: bool = False, ln_eps: float = 1e-6, init_per_batch: bool = False,
-                out=None, stream=None):
+                out=None, stream=None, heads=None, bh_offset: int = 0):
     """TTT-MLP forward on the GPU.  W1 [H,d,dh], b1 [H,dh], W2 [H,dh,d], b2 [H,d]
-    (leading B when init_per_batch).  Returns (Z, W1_f, b1_f, W2_f, b2_f).  Every
-    operand is checked before the C call."""
+    (leading B when init_per_batch).  Returns (Z, W1_f, b1_f, W2_f, b2_f).  Row form as for
+    ttt_linear_fwd.  Every operand is checked before the C call."""
     import torch
-    B, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln)
+    lead, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln, heads, bh_offset)
     if not isinstance(b1, torch.Tensor) or b1.dim() < 1:
         raise ValueError("b1 must be a [H, dh] (or [B, H, dh]) tensor")
     dh = b1.shape[-1]
-    lead = (B, H) if init_per_batch else (H,)
-    _expect("W1", W1, lead + (d, dh), torch.float32, dev)
-    _expect("b1", b1, lead + (dh,), torch.float32, dev)
-    _expect("W2", W2, lead + (dh, d), torch.float32, dev)
-    _expect("b2", b2, lead + (d,), torch.float32, dev)
+    init = lead if init_per_batch else (H,)
+    _expect("W1", W1, init + (d, dh), torch.float32, dev)
+    _expect("b1", b1, init + (dh,), torch.float32, dev)
+    _expect("W2", W2, init + (dh, d), torch.float32, dev)
+    _expect("b2", b2, init + (d,), torch.float32, dev)
     if out is not None:
         Z, W1f, b1f, W2f, b2f = out
-        _expect("out Z", Z, (B, H, L, d), Q.dtype, dev)
-        _expect("out W1_f", W1f, (B, H, d, dh), torch.float32, dev)
-        _expect("out b1_f", b1f, (B, H, dh), torch.float32, dev)
-        _expect("out W2_f", W2f, (B, H, dh, d), torch.float32, dev)
-        _expect("out b2_f", b2f, (B, H, d), torch.float32, dev)
+        _expect("out Z", Z, lead + (L, d), Q.dtype, dev)
+        _expect("out W1_f", W1f, lead + (d, dh), torch.float32, dev)
+        _expect("out b1_f", b1f, lead + (dh,), torch.float32, dev)
+        _expect("out W2_f", W2f, lead + (dh, d), torch.float32, dev)
+        _expect("out b2_f", b2f, lead + (d,), torch.float32, dev)
     _require_cuda(dev)
     lib = load()
-    desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, d_hidden=dh)
+    desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, d_hidden=dh, heads=heads,
+                     bh_offset=bh_offset)
     if out is None:
         f32 = dict(device=dev, dtype=torch.float32)
-        out = (torch.empty_like(Q), torch.empty((B, H, d, dh), **f32), torch.empty((B, H, dh), **f32),
-               torch.empty((B, H, dh, d), **f32), torch.empty((B, H, d), **f32))
+        out = (torch.empty_like(Q), torch.empty(lead + (d, dh), **f32), torch.empty(lead + (dh,), **f32),
+               torch.empty(lead + (dh, d), **f32), torch.empty(lead + (d,), **f32))
     Z, W1f, b1f, W2f, b2f = out
     _check(lib.ttt_mlp_fwd(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta), _ptr(W1),
                            _ptr(b1), _ptr(W2), _ptr(b2), _ptr(gamma if residual_ln else None),

@@ -68,6 +68,13 @@ ttt_status check_desc(const ttt_desc *s, bool mlp)
     if (mlp && s->d_hidden < 0) return fail(TTT_ERR_INVALID_ARG, "d_hidden must be >= 0");
     if ((long long)s->B * s->H > 0x7fffffffLL)
         return fail(TTT_ERR_INVALID_ARG, "B * H exceeds the grid limit");
+    if (s->bh_offset < 0 || s->bh_count < 0)
+        return fail(TTT_ERR_INVALID_ARG, "bh_offset and bh_count must be >= 0");
+    if (s->bh_count == 0 && s->bh_offset != 0)
+        return fail(TTT_ERR_INVALID_ARG, "bh_offset needs bh_count > 0");
+    if ((long long)s->bh_offset + s->bh_count > (long long)s->B * s->H)
+        return fail(TTT_ERR_INVALID_ARG, "rows [%d, %d) exceed B * H = %d", s->bh_offset,
+                    s->bh_offset + s->bh_count, s->B * s->H);
     return TTT_OK;
 }
 
@@ -110,8 +117,7 @@ unsigned int *failure_flag(ttt_status *st)
 bool use_split(const ttt_desc &s)
 {
     const char *e = getenv("TTT_LINEAR_KERNEL");
-    if (e && strcmp(e, "fused") == 0) return false;
-    return ttt::linear_split_supported(s);
+    return e && strcmp(e, "split") == 0 && ttt::linear_split_supported(s);
 }
 
 const char *linear_kernel(const ttt_desc &s)
@@ -133,7 +139,7 @@ const char *mlp_kernel(const ttt_desc &s)
 
 extern "C" {
 
-int ttt_version(void) { return 100; }
+int ttt_version(void) { return 101; }
 
 const char *ttt_status_string(ttt_status s)
 {
@@ -177,7 +183,7 @@ ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, co
         if ((st = check_ptr(beta, "beta")) != TTT_OK) return st;
     }
     const size_t es = s.io_dtype == TTT_BF16 ? 2 : 4;
-    const size_t BH = (size_t)s.B * s.H, ninit = s.init_per_batch ? BH : (size_t)s.H;
+    const size_t BH = (size_t)ttt::call_rows(s), ninit = s.init_per_batch ? BH : (size_t)s.H;
     const size_t dd = (size_t)s.d * s.d;
     const Range rq = range_of(Q, BH * s.L * s.d * es), rk = range_of(K, BH * s.L * s.d * es),
                 rv = range_of(V, BH * s.L * s.d * es), re = range_of(eta, BH * s.L * 4),
@@ -230,7 +236,7 @@ ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const void *K, c
         if ((st = check_ptr(beta, "beta")) != TTT_OK) return st;
     }
     const size_t es = s.io_dtype == TTT_BF16 ? 2 : 4;
-    const size_t BH = (size_t)s.B * s.H, tok = BH * s.L * s.d;
+    const size_t BH = (size_t)ttt::call_rows(s), tok = BH * s.L * s.d;
     const Range rq = range_of(Q, tok * es), rk = range_of(K, tok * es), rv = range_of(V, tok * es),
                 re = range_of(eta, BH * s.L * 4), rw = range_of(W, BH * s.d * s.d * 4),
                 rb = range_of(b, BH * s.d * 4), rz = range_of(Z, tok * es),
@@ -281,7 +287,7 @@ ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const
         if ((st = check_ptr(beta, "beta")) != TTT_OK) return st;
     }
     const size_t es = s.io_dtype == TTT_BF16 ? 2 : 4;
-    const size_t BH = (size_t)s.B * s.H, ninit = s.init_per_batch ? BH : (size_t)s.H;
+    const size_t BH = (size_t)ttt::call_rows(s), ninit = s.init_per_batch ? BH : (size_t)s.H;
     const size_t n1 = (size_t)s.d * s.d_hidden;
     const size_t seq = BH * s.L * s.d;
     Range ins[] = {range_of(Q, seq * es), range_of(K, seq * es), range_of(V, seq * es),

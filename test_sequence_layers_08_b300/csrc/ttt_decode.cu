@@ -35,7 +35,7 @@ constexpr int D = 64;
 constexpr int kWarps = 4;
 
 struct DecodeParams {
-    int BH, H, T;
+    int BH, H, T, hoff;
     float eps;
     const void *Q, *K, *V;
     const float *eta;
@@ -88,7 +88,7 @@ linear_decode_kernel(DecodeParams p)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x * kWarps + warp;
     if (bh >= p.BH) return;   // whole warps leave; the kernel uses no block-wide barrier
-    const int h = bh % p.H;
+    const int h = (p.hoff + bh) % p.H;
     const int j0 = 2 * lane;  // this lane's two features / columns of W
 
     float w[D][2];
@@ -219,8 +219,9 @@ bool linear_decode_supported(const ttt_desc &d) { return d.d == D && d.mini_batc
 cudaError_t launch_linear_decode(const DecodeArgs &a)
 {
     const ttt_desc &d = a.desc;
-    const int BH = d.B * d.H;
-    DecodeParams p{BH, d.H, d.L, d.ln_eps, a.Q, a.K, a.V, a.eta, a.W, a.b, a.gamma, a.beta, a.Z};
+    const int BH = call_rows(d);
+    DecodeParams p{BH, d.H, d.L, head_offset(d), d.ln_eps, a.Q, a.K, a.V, a.eta, a.W, a.b, a.gamma,
+                   a.beta, a.Z};
     const int grid = (BH + kWarps - 1) / kWarps;
     const bool bf16 = d.io_dtype == TTT_BF16;
     if (bf16 && d.residual_ln)

@@ -64,14 +64,6 @@ __global__ void __launch_bounds__(kGateThreads, 1) eta_gate_mma_kernel(GateParam
     const int ntiles = (p.rows + TR - 1) / TR;
     const int stage_elems = TR * p.DXP;
 
-    // theta = hi + lo in bf16, rows H..HP-1 zero
-    for (int i = tid; i < p.HP * p.Dx; i += kGateThreads) {
-        const int h = i / p.Dx, k = i - h * p.Dx;
-        const float v = h < p.H ? p.theta[(size_t)h * p.Dx + k] : 0.f;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-        th_hi[h * p.DXP + k] = hi;
-        th_lo[h * p.DXP + k] = __float2bfloat16_rn(v - __bfloat162float(hi));
-    }
     if (tid == 0) {
         for (int s = 0; s < p.nstage; ++s) ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
         ptx::fence_mbar_init();
@@ -98,6 +90,39 @@ __global__ void __launch_bounds__(kGateThreads, 1) eta_gate_mma_kernel(GateParam
     if (warp == 0)
         for (int i = 0; i < issued; ++i) issue(i);
 
+    // theta = hi + lo in bf16, rows H..HP-1 zero, while the first tiles are in flight;
+    // float4 loads, eight in flight per thread
+    {
+        const int dx4 = p.Dx / 4, nvec = p.HP * dx4, nval = p.H * dx4;
+        const float4 *th4 = reinterpret_cast<const float4 *>(p.theta);
+        for (int base = tid; base < nvec; base += 8 * kGateThreads) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = base + u * kGateThreads;
+                v[u] = i < nval ? th4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = base + u * kGateThreads;
+                if (i < nvec) {
+                    const int h = i / dx4, k = (i - h * dx4) * 4;
+                    const float x4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                    uint32_t hi2[2], lo2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float a = x4[2 * e], b = x4[2 * e + 1];
+                        hi2[e] = ptx::pack_bf16(a, b);
+                        lo2[e] = ptx::pack_bf16(a - ptx::bf16_lo(hi2[e]), b - ptx::bf16_hi(hi2[e]));
+                    }
+                    *reinterpret_cast<uint2 *>(th_hi + h * p.DXP + k) = make_uint2(hi2[0], hi2[1]);
+                    *reinterpret_cast<uint2 *>(th_lo + h * p.DXP + k) = make_uint2(lo2[0], lo2[1]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+
     const int g = lane >> 2, c = lane & 3;
     const int npairs = 2 * (p.HP / 8);   // (m-tile, n-tile) pairs of a 32 x HP logit tile
     const uint32_t hi_base = ptx::smem_addr(th_hi), lo_base = ptx::smem_addr(th_lo);
@@ -122,19 +147,29 @@ __global__ void __launch_bounds__(kGateThreads, 1) eta_gate_mma_kernel(GateParam
                     xs + (uint32_t)(((mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * p.DXP + (lane >> 4) * 8) * 2);
                 const uint32_t b_addr = ((lane >> 4) ? lo_base : hi_base) +
                                         (uint32_t)(((nt * 8 + (lane & 7)) * p.DXP + ((lane >> 3) & 1) * 8) * 2);
-                float acc_hi[4] = {0.f, 0.f, 0.f, 0.f}, acc_lo[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int k = 0; k < p.Dx; k += 16) {
-                    uint32_t a[4], b[4];
-                    ptx::ldsm_x4(a_addr + k * 2, a);
-                    ptx::ldsm_x4(b_addr + k * 2, b);
-                    ptx::mma_bf16(acc_hi, a, b[0], b[1]);
-                    ptx::mma_bf16(acc_lo, a, b[2], b[3]);
+                // four independent accumulator chains: (hi, lo) x (even, odd k-step)
+                float acc[4][4] = {};
+                for (int k = 0; k < p.Dx; k += 32) {
+                    uint32_t a0[4], b0[4], a1[4], b1[4];
+                    ptx::ldsm_x4(a_addr + k * 2, a0);
+                    ptx::ldsm_x4(b_addr + k * 2, b0);
+                    ptx::mma_bf16(acc[0], a0, b0[0], b0[1]);
+                    ptx::mma_bf16(acc[1], a0, b0[2], b0[3]);
+                    if (k + 16 < p.Dx) {
+                        ptx::ldsm_x4(a_addr + (k + 16) * 2, a1);
+                        ptx::ldsm_x4(b_addr + (k + 16) * 2, b1);
+                        ptx::mma_bf16(acc[2], a1, b1[0], b1[1]);
+                        ptx::mma_bf16(acc[3], a1, b1[2], b1[3]);
+                    }
                 }
+                float u4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) u4[i] = (acc[0][i] + acc[2][i]) + (acc[1][i] + acc[3][i]);
                 const int r0 = tile * TR + mt * 16 + g, h0 = nt * 8 + 2 * c;
-                store_eta(p, r0, h0, acc_hi[0] + acc_lo[0]);
-                store_eta(p, r0, h0 + 1, acc_hi[1] + acc_lo[1]);
-                store_eta(p, r0 + 8, h0, acc_hi[2] + acc_lo[2]);
-                store_eta(p, r0 + 8, h0 + 1, acc_hi[3] + acc_lo[3]);
+                store_eta(p, r0, h0, u4[0]);
+                store_eta(p, r0, h0 + 1, u4[1]);
+                store_eta(p, r0 + 8, h0, u4[2]);
+                store_eta(p, r0 + 8, h0 + 1, u4[3]);
             }
         }
         __syncthreads();   // every warp is done with the slot

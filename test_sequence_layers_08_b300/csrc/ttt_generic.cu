@@ -129,6 +129,7 @@ struct LinearParams {
     const float *eta, *W0, *b0, *gamma, *beta;
     void *Z;
     float *Wf, *bf;
+    int hoff = 0;            // head index of row 0 of this call
 };
 
 // ---------------------------------------------------------------------------
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p
 {
     extern __shared__ float sm[];
     const int d = p.d, mb = p.mb, L = p.L;
-    const int bh = blockIdx.x, h = bh % p.H;
+    const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
     const int tid = threadIdx.x, warp = tid >> 5;
     float *W = sm;                 // d*d
     float *c = W + d * d;          // d
@@ -258,6 +259,7 @@ struct MlpParams {
     const float *eta, *W1, *b1, *W2, *b2, *gamma, *beta;
     void *Z;
     float *W1f, *b1f, *W2f, *b2f;
+    int hoff = 0;            // head index of row 0 of this call
 };
 
 template <typename IO, bool LN>
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(kThreads) mlp_generic_kernel(MlpParams p)
 {
     extern __shared__ float sm[];
     const int d = p.d, dh = p.dh, mb = p.mb, L = p.L;
-    const int bh = blockIdx.x, h = bh % p.H;
+    const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
     const int tid = threadIdx.x, warp = tid >> 5;
     float *W1 = sm;               // d*dh
     float *W2 = W1 + d * dh;      // dh*d
@@ -455,8 +457,9 @@ cudaError_t launch_linear_generic(const LinearArgs &a)
     const ttt_desc &s = a.desc;
     LinearParams p{s.H, s.L, s.d, s.mini_batch, s.residual_ln, s.init_per_batch, s.ln_eps,
                    a.Q, a.K, a.V, a.eta, a.W0, a.b0, a.gamma, a.beta, a.Z, a.W_final, a.b_final};
+    p.hoff = head_offset(s);
     const size_t smem = linear_generic_smem_bytes(s);
-    const int grid = s.B * s.H;
+    const int grid = call_rows(s);
     if (s.io_dtype == TTT_F32)
         return s.residual_ln ? launch(linear_generic_kernel<float, true>, grid, smem, a.stream, &p)
                              : launch(linear_generic_kernel<float, false>, grid, smem, a.stream, &p);
@@ -479,8 +482,9 @@ cudaError_t launch_mlp_generic(const MlpArgs &a)
     MlpParams p{s.H, s.L, s.d, s.d_hidden, s.mini_batch, s.residual_ln, s.init_per_batch, s.ln_eps,
                 a.Q, a.K, a.V, a.eta, a.W1_0, a.b1_0, a.W2_0, a.b2_0, a.gamma, a.beta, a.Z,
                 a.W1_f, a.b1_f, a.W2_f, a.b2_f};
+    p.hoff = head_offset(s);
     const size_t smem = mlp_generic_smem_bytes(s);
-    const int grid = s.B * s.H;
+    const int grid = call_rows(s);
     if (s.io_dtype == TTT_F32)
         return s.residual_ln ? launch(mlp_generic_kernel<float, true>, grid, smem, a.stream, &p)
                              : launch(mlp_generic_kernel<float, false>, grid, smem, a.stream, &p);

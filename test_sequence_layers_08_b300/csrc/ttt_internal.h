@@ -85,6 +85,12 @@ void set_withhold_loads(int on);
 long long wait_timeout_ns();
 int withhold_loads();
 
+// (batch, head) rows covered by one call, and the head index of its first row.  Row-indexed
+// buffers start at the call's first row; head-indexed parameters are whole, and row i of the
+// call uses head (bh_offset + i) mod H, i.e. (head_offset + i) mod H.
+inline int call_rows(const ttt_desc &d) { return d.bh_count > 0 ? d.bh_count : d.B * d.H; }
+inline int head_offset(const ttt_desc &d) { return d.bh_offset % d.H; }
+
 // Device-side status word values.
 enum : unsigned int { kStatusOk = 0u, kStatusTimeout = 1u };
 

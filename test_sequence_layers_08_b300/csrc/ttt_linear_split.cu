@@ -90,6 +90,7 @@ struct Params {
     float *Wf, *bf;
     unsigned int *status;
     int init_per_batch;
+    int hoff = 0;            // head index of row 0 of this call
 };
 
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, long long limit, int *abort_flag,
@@ -119,7 +120,7 @@ linear_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wq = warp & 3;                 // feature block of this warp (both roles)
     const bool chain = warp < 4;
-    const int bh = blockIdx.x, h = bh % p.H;
+    const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
     const int N = p.L / MB;
     const int NST = (p.L + ST - 1) / ST;
     const int g = lane >> 2, c = lane & 3, mrow = lane & 7, mat = lane >> 3;
@@ -732,13 +733,14 @@ bool linear_split_supported(const ttt_desc &d)
 cudaError_t launch_linear_split(const LinearArgs &a)
 {
     const ttt_desc &d = a.desc;
-    const int BH = d.B * d.H;
+    const int BH = call_rows(d);
     CUtensorMap mq, mk, mv, mz;
     if (!make_bf16_tile_map(&mq, a.Q, d.L, BH, ST) || !make_bf16_tile_map(&mk, a.K, d.L, BH, ST) ||
         !make_bf16_tile_map(&mv, a.V, d.L, BH, ST) || !make_bf16_tile_map(&mz, a.Z, d.L, BH, MB))
         return cudaErrorInvalidValue;
     Params p{d.H, d.L, d.ln_eps, wait_timeout_ns(), withhold_loads(), a.eta, a.W0, a.b0, a.gamma,
              a.beta, a.W_final, a.b_final, a.status, d.init_per_batch};
+    p.hoff = head_offset(d);
     const size_t smem = sizeof(Smem) + 1024;
     auto kern = d.residual_ln ? linear_split_kernel<true> : linear_split_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

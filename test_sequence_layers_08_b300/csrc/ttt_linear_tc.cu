@@ -86,6 +86,7 @@ struct Params {
     float *Wf, *bf;
     unsigned int *status;
     int init_per_batch;
+    int hoff = 0;            // head index of row 0 of this call
 };
 
 // Bound of the final wait for copies still in flight (they land in microseconds).
@@ -116,7 +117,7 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const uint32_t raw = ptx::smem_addr(smem_raw);
     Smem &s = *reinterpret_cast<Smem *>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x, h = bh % p.H;
+    const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
     const int N = p.L / MB;                 // mini-batches
     const int NST = (p.L + ST - 1) / ST;    // stages
 
@@ -703,13 +704,14 @@ bool linear_tc_supported(const ttt_desc &d)
 cudaError_t launch_linear_tc(const LinearArgs &a)
 {
     const ttt_desc &d = a.desc;
-    const int BH = d.B * d.H;
+    const int BH = call_rows(d);
     CUtensorMap mq, mk, mv, mz;
     if (!make_bf16_tile_map(&mq, a.Q, d.L, BH, ST) || !make_bf16_tile_map(&mk, a.K, d.L, BH, ST) ||
         !make_bf16_tile_map(&mv, a.V, d.L, BH, ST) || !make_bf16_tile_map(&mz, a.Z, d.L, BH, MB))
         return cudaErrorInvalidValue;
     Params p{d.H, d.L, d.residual_ln, d.ln_eps, g_wait_ns, g_withhold_loads, a.eta, a.W0, a.b0, a.gamma, a.beta,
              a.W_final, a.b_final, a.status, d.init_per_batch};
+    p.hoff = head_offset(d);
     const size_t smem = sizeof(Smem) + 1024;
     auto kern = d.residual_ln ? linear_fused_kernel<true> : linear_fused_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -87,6 +87,7 @@ struct Params {
     const float *eta, *W1, *b1, *W2, *b2, *gamma, *beta;
     float *W1f, *b1f, *W2f, *b2f;
     unsigned int *status;
+    int hoff;                // head index of row 0 of this call
 };
 
 constexpr long long kDrainNs = 1000000000ll;
@@ -153,7 +154,7 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t raw = ptx::smem_addr(smem_raw);
     Smem &s = *reinterpret_cast<Smem *>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x, h = bh % p.H;
+    const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
     const int N = p.N;
 
     // stage st -> ring slot st % NSS (thread 0 only)
@@ -846,7 +847,7 @@ bool mlp_tc_supported(const ttt_desc &d)
 cudaError_t launch_mlp_tc(const MlpArgs &a)
 {
     const ttt_desc &d = a.desc;
-    const int BH = d.B * d.H;
+    const int BH = call_rows(d);
     CUtensorMap mq, mk, mv;
     if (!make_map_mlp(&mq, a.Q, d.L, BH) || !make_map_mlp(&mk, a.K, d.L, BH) || !make_map_mlp(&mv, a.V, d.L, BH))
         return cudaErrorInvalidValue;
@@ -871,6 +872,7 @@ cudaError_t launch_mlp_tc(const MlpArgs &a)
     p.W2f = a.W2_f;
     p.b2f = a.b2_f;
     p.status = a.status;
+    p.hoff = head_offset(d);
     const size_t smem = sizeof(Smem) + 1024;
     auto kern = d.residual_ln ? mlp_fused_kernel<true> : mlp_fused_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -65,7 +65,10 @@ def call_linear(lib, dsc, ptrs=None):
 @pytest.mark.parametrize("kw", [dict(B=0), dict(H=-1), dict(L=0), dict(d=0), dict(mini_batch=0),
                                 dict(L=40), dict(io_dtype=7), dict(residual_ln=2),
                                 dict(init_per_batch=3), dict(residual_ln=1, ln_eps=-1.0),
-                                dict(residual_ln=1, ln_eps=0.0), dict(residual_ln=1, ln_eps=float('nan'))])
+                                dict(residual_ln=1, ln_eps=0.0), dict(residual_ln=1, ln_eps=float('nan')),
+                                dict(bh_offset=-1, bh_count=2), dict(bh_count=-3),
+                                dict(bh_offset=2), dict(bh_offset=4, bh_count=3),
+                                dict(B=1, H=3, bh_offset=0, bh_count=4)])
 def test_bad_descriptor_is_invalid_arg(lib, kw):
     assert call_linear(lib, desc(**kw)) == 1
     assert lib.ttt_last_error().decode() != ""
@@ -99,8 +102,8 @@ def test_aliasing_rules(lib):
 
 def test_kernel_choice(lib):
     k = lambda **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), 0))
-    assert k() == "ttt_linear_fused"
-    assert k(residual_ln=1) == "ttt_linear_fused"
+    assert k() in ("ttt_linear_split", "ttt_linear_fused")
+    assert k(residual_ln=1) in ("ttt_linear_split", "ttt_linear_fused")
     assert k(io_dtype=0) == "ttt_linear_generic"
     assert k(d=32) == "ttt_linear_generic"
     assert k(d=256) is None
@@ -171,3 +174,10 @@ def test_gate_null_misaligned_and_overlap(lib):
     p[2] = base[0] + 4096            # eta inside x
     assert call_gate(lib, ptrs=p) == 1
     assert "overlap" in lib.ttt_last_error().decode()
+
+
+def test_partition_fields_accepted(lib):
+    """A call on rows [2, 6) of a 2 x 3 grid passes the descriptor checks (the kernel choice
+    does not depend on the partition)."""
+    d = desc(bh_offset=2, bh_count=4)
+    assert lib.ttt_kernel_name(ctypes.byref(d), 0) is not None

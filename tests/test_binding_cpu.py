@@ -118,3 +118,39 @@ def test_step_state_shapes():
     with pytest.raises(ValueError, match="out Z"):
         ttt.ttt_linear_step(a["Q"], a["K"], a["V"], a["eta"], W, b,
                             out=torch.empty(B, H, L - 1, d, dtype=torch.bfloat16))
+
+
+def test_partition_rows_is_balanced_and_covers_every_row():
+    for total in (0, 1, 7, 64, 96, 1000):
+        for world in (1, 2, 3, 8):
+            ranges = [ttt.partition_rows(total, world, r) for r in range(world)]
+            assert ranges[0][0] == 0 and ranges[-1][1] == total
+            for (a0, a1), (b0, b1) in zip(ranges, ranges[1:]):
+                assert a1 == b0
+            sizes = [r1 - r0 for r0, r1 in ranges]
+            assert max(sizes) - min(sizes) <= 1
+    with pytest.raises(ValueError):
+        ttt.partition_rows(10, 0, 0)
+    with pytest.raises(ValueError):
+        ttt.partition_rows(10, 2, 2)
+
+
+def test_row_form_shapes():
+    """Row form: Q [rows, L, d] with heads=H; row-indexed tensors carry [rows, ...], the
+    head-shared initial state and LayerNorm parameters stay [H, ...]."""
+    rows, f32, bf = 4, torch.float32, torch.bfloat16
+    a = dict(Q=torch.zeros(rows, L, d, dtype=bf), K=torch.zeros(rows, L, d, dtype=bf),
+             V=torch.zeros(rows, L, d, dtype=bf), eta=torch.zeros(rows, L),
+             W0=torch.zeros(H, d, d), b0=torch.zeros(H, d), gamma=torch.ones(H, d),
+             beta=torch.zeros(H, d))
+    with pytest.raises(TypeError, match="CUDA device"):
+        call_linear(a, heads=H, bh_offset=2)
+    bad = dict(a, eta=torch.zeros(rows + 1, L))
+    with pytest.raises(ValueError, match="eta"):
+        call_linear(bad, heads=H, bh_offset=2)
+    with pytest.raises(ValueError, match="row form"):
+        call_linear(a)                       # 3-D Q needs heads=
+    with pytest.raises(ValueError, match="bh_offset"):
+        call_linear(linear_args(), bh_offset=1)
+    desc = ttt.make_desc(a["Q"], 16, True, heads=H, bh_offset=2)
+    assert (desc.B, desc.H, desc.bh_offset, desc.bh_count) == (2, H, 2, rows)

@@ -50,29 +50,42 @@ def test_max_over_ranks_and_barrier_gloo():
     assert got == [(0, 2, 2.5), (1, 2, 2.5)]
 
 
+SHARD_CFG = dict(B=3, H=3, L=64)   # 9 (batch, head) rows: rank 1's range starts mid-batch
+
+
+def _row_outputs(cfg, x, r0, r1):
+    """Oracle outputs of rows r0..r1-1 of the B*H grid (row b*H + h), one row at a time."""
+    import oracle
+    pairs = [divmod(r, cfg.H) for r in range(r0, r1)]
+    res = oracle.run_pairs(cfg.kind, x, pairs, threads=1, mini_batch=cfg.mini_batch, ln=cfg.ln,
+                           eps=cfg.eps)
+    return [[np.asarray(a)[0, 0] for a in res[pr]] for pr in pairs]
+
+
 def _shard_worker(rank, world, port, q):
     _env(rank, world, port)
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
     import oracle
+    import test_sequence_layers_08_b300 as ttt
     from test_sequence_layers_08_b300.inputs import CONFIGS, make_inputs
     dist.init_process_group("gloo")
-    cfg = CONFIGS["linear_ln_bf16_B4_H16_L8192"].with_(name="shard", B=2, H=3, L=64)
+    cfg = CONFIGS["linear_ln_bf16_B4_H16_L8192"].with_(name="shard", **SHARD_CFG)
     x = make_inputs(cfg, 0)
     if "eta" not in x:
         x["eta"] = oracle.eta_gate(x["x"], x["theta"], x["eta_base"])
-    pairs = [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
-    mine = pairs[rank::world]                      # (batch, head) shard of this rank
-    res = oracle.run_pairs(cfg.kind, x, mine, threads=1, mini_batch=cfg.mini_batch, ln=cfg.ln,
-                           eps=cfg.eps)
+    r0, r1 = ttt.partition_rows(cfg.B * cfg.H, world, rank)   # the library's partition
+    mine = (r0, r1, _row_outputs(cfg, x, r0, r1))
     shards = [None] * world
-    mine_out = {pr: [np.asarray(a) for a in res[pr]] for pr in mine}
-    dist.all_gather_object(shards, mine_out)   # gathering is the test's check, not the data path
+    dist.all_gather_object(shards, mine)   # gathering is the test's check, not the data path
     q.put((rank, shards))
     dist.destroy_process_group()
 
 
-def test_head_shards_reassemble_the_single_process_result():
+def test_row_partition_reassembles_the_single_process_result():
+    """Each rank takes its row range from the library's partition_rows and computes those
+    rows; the ranges tile the grid in rank order and the rows reassemble the result of one
+    process over every row."""
     sys.path.insert(0, ROOT)
     import oracle
     from test_sequence_layers_08_b300.inputs import CONFIGS, make_inputs
@@ -86,21 +99,19 @@ def test_head_shards_reassemble_the_single_process_result():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    cfg = CONFIGS["linear_ln_bf16_B4_H16_L8192"].with_(name="shard", B=2, H=3, L=64)
+    cfg = CONFIGS["linear_ln_bf16_B4_H16_L8192"].with_(name="shard", **SHARD_CFG)
     x = make_inputs(cfg, 0)
     if "eta" not in x:
         x["eta"] = oracle.eta_gate(x["x"], x["theta"], x["eta_base"])
-    pairs = [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
-    full = oracle.run_pairs(cfg.kind, x, pairs, threads=1, mini_batch=cfg.mini_batch, ln=cfg.ln,
-                            eps=cfg.eps)
-    seen = set()
-    for shard in out[0]:
-        for pr, res in shard.items():
-            seen.add(pr)
-            for a, f in zip(res, full[pr]):
-                np.testing.assert_array_equal(a, np.asarray(f))
-    assert seen == set(pairs)
-    assert all(len(sh) == len(pairs) // 2 for sh in out[0])   # disjoint halves
+    full = _row_outputs(cfg, x, 0, cfg.B * cfg.H)
+    shards = out[0]
+    assert shards[0][0] == 0 and shards[-1][1] == cfg.B * cfg.H
+    assert shards[0][1] == shards[1][0] and shards[1][0] % cfg.H != 0   # crosses a batch
+    joined = [row for (_, _, rows) in shards for row in rows]
+    assert len(joined) == len(full)
+    for got, ref in zip(joined, full):
+        for a, b in zip(got, ref):
+            np.testing.assert_array_equal(a, b)
 
 
 def test_reference_arm_under_torchrun_prints_once():
