@@ -187,5 +187,14 @@ __device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t *r)
                  : "memory");
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held one 32-bit pair per lane: lane 4r + q
+// gives row r, columns 2q, 2q + 1 and receives row r, columns 2q, 2q + 1 of the transpose.
+__device__ __forceinline__ uint32_t movm_t(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 }  // namespace ptx
 }  // namespace ttt

@@ -9,8 +9,6 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
-#include <cstdlib>
-#include <cstring>
 
 #include "ttt_internal.h"
 
@@ -113,16 +111,8 @@ unsigned int *failure_flag(ttt_status *st)
     return flag;
 }
 
-// Development switch between the two bf16 TTT-Linear kernels (removed once one is chosen).
-bool use_split(const ttt_desc &s)
-{
-    const char *e = getenv("TTT_LINEAR_KERNEL");
-    return e && strcmp(e, "split") == 0 && ttt::linear_split_supported(s);
-}
-
 const char *linear_kernel(const ttt_desc &s)
 {
-    if (use_split(s)) return "ttt_linear_split";
     if (ttt::linear_tc_supported(s)) return "ttt_linear_fused";
     if (ttt::linear_generic_smem_bytes(s)) return "ttt_linear_generic";
     return nullptr;
@@ -211,9 +201,8 @@ ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, co
                       reinterpret_cast<cudaStream_t>(stream), nullptr};
     a.status = failure_flag(&st);
     if (st != TTT_OK) return st;
-    cudaError_t e = use_split(s)                 ? ttt::launch_linear_split(a)
-                    : ttt::linear_tc_supported(s) ? ttt::launch_linear_tc(a)
-                                                  : ttt::launch_linear_generic(a);
+    cudaError_t e = ttt::linear_tc_supported(s) ? ttt::launch_linear_tc(a)
+                                                : ttt::launch_linear_generic(a);
     if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "%s launch: %s", kname, cudaGetErrorString(e));
     return ok();
 }

@@ -65,12 +65,9 @@ cudaError_t launch_linear_generic(const LinearArgs &a);
 size_t mlp_generic_smem_bytes(const ttt_desc &d);
 cudaError_t launch_mlp_generic(const MlpArgs &a);
 
-// Tensor-core TTT-Linear kernels (bf16 I/O, d = 64, b = 16): four warps doing every step in
-// order, and the eight-warp kernel with separate chain and state/output warps.
+// Tensor-core TTT-Linear kernel (bf16 I/O, d = 64, b = 16).
 bool linear_tc_supported(const ttt_desc &d);
 cudaError_t launch_linear_tc(const LinearArgs &a);
-bool linear_split_supported(const ttt_desc &d);
-cudaError_t launch_linear_split(const LinearArgs &a);
 // TMA map of a [BH][L][64] bf16 tensor: boxes of `rows` tokens x 64 features, 128-byte swizzle.
 bool make_bf16_tile_map(CUtensorMap *m, const void *base, int L, int BH, int rows);
 // TTT-Linear decode kernel (d = 64, fp32 or bf16 I/O, FP32 arithmetic, one warp per head).
