@@ -74,6 +74,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1, int c2)
 {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
@@ -185,15 +194,6 @@ __device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t *r)
     asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]),
                  "r"(r[1]), "r"(r[2]), "r"(r[3])
                  : "memory");
-}
-
-// Transpose of an 8x8 matrix of 16-bit elements held one 32-bit pair per lane: lane 4r + q
-// gives row r, columns 2q, 2q + 1 and receives row r, columns 2q, 2q + 1 of the transpose.
-__device__ __forceinline__ uint32_t movm_t(uint32_t a)
-{
-    uint32_t d;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
-    return d;
 }
 
 }  // namespace ptx

@@ -7,16 +7,16 @@
 // B300 design.  The gate is a skinny contraction ([B L, Dx] x [Dx, H], H <= 32) whose cost
 // is reading x once: it is HBM-bound, so the kernel streams x at copy speed and keeps the
 // arithmetic small.
-//   * persistent CTAs (one per SM), 4 warps; 32-token tiles of x arrive by per-row bulk
-//     copies (cp.async.bulk, one per token row, issued by the 32 lanes of warp 0) into a
-//     2-3 deep shared-memory ring; each row is padded by 16 bytes so that ldmatrix reads of
-//     eight consecutive rows hit eight different bank groups;
+//   * persistent CTAs (one per SM), 4 warps; 32-token tiles of x arrive as Dx / 64 TMA boxes
+//     of 32 rows x 64 features (128-byte swizzle, so ldmatrix reads of eight rows hit eight
+//     different bank groups) into a 2-4 deep shared-memory ring;
 //   * theta is split once per CTA into bf16 hi + lo parts (theta = hi + lo to ~2^-16
 //     relative), so bf16 tokens are contracted by warp MMAs (m16n8k16, fp32 accumulate)
 //     with no precision lost beyond that split: logits = x . hi + x . lo;
 //   * the epilogue applies eta_base / (1 + exp(-u)) and writes eta[b, h, t].
-// fp32 tokens, more than 32 heads or widths the ring cannot hold take a plain FP32 kernel
-// (one warp per token row).
+// fp32 tokens, more than 32 heads, widths that are no multiple of 64 or that the ring cannot
+// hold take a plain FP32 kernel (one warp per token row).
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,9 +40,10 @@ struct GateParams {
     long long wait_ns;
 };
 
-size_t mma_smem_bytes(int HP, int DXP, int nstage)
+size_t mma_smem_bytes(int HP, int Dx, int nstage)
 {
-    return 1024 + (size_t)2 * HP * DXP * 2 + (size_t)nstage * TR * DXP * 2;
+    // ring (1024-aligned), theta hi / lo (padded rows), mbarriers, alignment slack
+    return 1024 + (size_t)nstage * TR * Dx * 2 + (size_t)2 * HP * (Dx + 8) * 2 + 64;
 }
 
 __device__ __forceinline__ void store_eta(const GateParams &p, int row, int h, float u)
@@ -53,41 +54,44 @@ __device__ __forceinline__ void store_eta(const GateParams &p, int row, int h, f
     }
 }
 
-__global__ void __launch_bounds__(kGateThreads, 1) eta_gate_mma_kernel(GateParams p)
+// x tiles of TR tokens arrive as Dx / 64 TMA boxes of TR rows x 64 features (128-byte swizzle,
+// 4 KB each); theta hi / lo rows are padded by 16 bytes so ldmatrix reads of eight heads hit
+// eight different bank groups.
+__global__ void __launch_bounds__(kGateThreads, 1)
+eta_gate_mma_kernel(const __grid_constant__ CUtensorMap tmX, GateParams p)
 {
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned long long *full = reinterpret_cast<unsigned long long *>(smem);   // [nstage]
-    __nv_bfloat16 *th_hi = reinterpret_cast<__nv_bfloat16 *>(smem + 1024);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 1024-byte aligned
+    const int nbox = p.Dx / 64;
+    const uint32_t stage_bytes = (uint32_t)nbox * TR * 128;
+    unsigned char *ring = smem;                                            // [nstage][nbox][TR][128 B]
+    __nv_bfloat16 *th_hi = reinterpret_cast<__nv_bfloat16 *>(ring + (size_t)p.nstage * stage_bytes);
     __nv_bfloat16 *th_lo = th_hi + (size_t)p.HP * p.DXP;
-    __nv_bfloat16 *ring = th_lo + (size_t)p.HP * p.DXP;
+    unsigned long long *full = reinterpret_cast<unsigned long long *>(th_lo + (size_t)p.HP * p.DXP);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ntiles = (p.rows + TR - 1) / TR;
-    const int stage_elems = TR * p.DXP;
 
     if (tid == 0) {
         for (int s = 0; s < p.nstage; ++s) ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
         ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmX);
     }
     __syncthreads();
 
     // tile i of this CTA is global tile blockIdx.x + i * gridDim.x, in ring slot i % nstage
-    auto issue = [&](int i) {   // warp 0 only
+    auto issue = [&](int i) {   // one thread
         const int tile = blockIdx.x + i * gridDim.x;
         const int slot = i % p.nstage;
-        const int nrows = min(TR, p.rows - tile * TR);
         const uint32_t bar = ptx::smem_addr(&full[slot]);
-        if (lane == 0) ptx::mbar_arrive_expect_tx(bar, (uint32_t)(nrows * p.Dx * 2));
-        __syncwarp();
-        if (lane < nrows) {
-            const __nv_bfloat16 *src =
-                reinterpret_cast<const __nv_bfloat16 *>(p.x) + (size_t)(tile * TR + lane) * p.Dx;
-            ptx::bulk_load(ptx::smem_addr(ring + (size_t)slot * stage_elems + lane * p.DXP), src,
-                           (uint32_t)(p.Dx * 2), bar);
-        }
+        ptx::mbar_arrive_expect_tx(bar, stage_bytes);
+        const uint32_t dst = ptx::smem_addr(ring + (size_t)slot * stage_bytes);
+        for (int kb = 0; kb < nbox; ++kb)
+            ptx::tma_load_2d(dst + kb * TR * 128, &tmX, bar, kb * 64, tile * TR);
     };
     const int mine = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     int issued = min(p.nstage, mine);   // tiles handed to the copy engine (uniform in the CTA)
-    if (warp == 0)
+    if (tid == 0)
         for (int i = 0; i < issued; ++i) issue(i);
 
     // theta = hi + lo in bf16, rows H..HP-1 zero, while the first tiles are in flight;
@@ -123,8 +127,8 @@ __global__ void __launch_bounds__(kGateThreads, 1) eta_gate_mma_kernel(GateParam
     }
     __syncthreads();
 
-    const int g = lane >> 2, c = lane & 3;
-    const int npairs = 2 * (p.HP / 8);   // (m-tile, n-tile) pairs of a 32 x HP logit tile
+    const int g = lane >> 2, c = lane & 3, mrow = lane & 7;
+    const int npairs = (TR / 16) * (p.HP / 8);   // (m-tile, n-tile) pairs of a TR x HP logit tile
     const uint32_t hi_base = ptx::smem_addr(th_hi), lo_base = ptx::smem_addr(th_lo);
     bool ok = true;
     for (int i = 0; i < mine; ++i) {
@@ -138,43 +142,48 @@ __global__ void __launch_bounds__(kGateThreads, 1) eta_gate_mma_kernel(GateParam
             if (tid == 0) atomicOr(p.status, kStatusTimeout);
             break;
         }
-        {
-            const uint32_t xs = ptx::smem_addr(ring + (size_t)slot * stage_elems);
-            for (int pr = warp; pr < npairs; pr += 4) {
-                const int mt = pr & 1, nt = pr >> 1;
-                // A rows (tokens) of this lane's ldmatrix address; B rows (heads)
-                const uint32_t a_addr =
-                    xs + (uint32_t)(((mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * p.DXP + (lane >> 4) * 8) * 2);
-                const uint32_t b_addr = ((lane >> 4) ? lo_base : hi_base) +
-                                        (uint32_t)(((nt * 8 + (lane & 7)) * p.DXP + ((lane >> 3) & 1) * 8) * 2);
-                // four independent accumulator chains: (hi, lo) x (even, odd k-step)
-                float acc[4][4] = {};
-                for (int k = 0; k < p.Dx; k += 32) {
+        const uint32_t xs = ptx::smem_addr(ring + (size_t)slot * stage_bytes);
+        for (int pr = warp; pr < npairs; pr += 4) {
+            const int mt = pr % (TR / 16), nt = pr / (TR / 16);
+            // A: token row t of this lane's ldmatrix address (matrices: rows 0-7 / 8-15 x
+            // k 0-7 / 8-15 of a 16-wide k-step); B: head row of theta hi (lanes 0-15) / lo
+            const int t = mt * 16 + mrow + ((lane >> 3) & 1) * 8;
+            const uint32_t a_row = xs + (uint32_t)(t * 128);
+            const int a_half = lane >> 4;
+            const uint32_t b_addr = ((lane >> 4) ? lo_base : hi_base) +
+                                    (uint32_t)(((nt * 8 + mrow) * p.DXP + ((lane >> 3) & 1) * 8) * 2);
+            float acc[4][4] = {};
+            for (int kb = 0; kb < nbox; ++kb) {
+                const uint32_t a_box = a_row + (uint32_t)(kb * TR * 128);
+#pragma unroll
+                for (int ks = 0; ks < 4; ks += 2) {
                     uint32_t a0[4], b0[4], a1[4], b1[4];
-                    ptx::ldsm_x4(a_addr + k * 2, a0);
-                    ptx::ldsm_x4(b_addr + k * 2, b0);
+                    // 16-byte chunk (2 ks + a_half) of the 64-feature box row, swizzled
+                    ptx::ldsm_x4(a_box + (uint32_t)((((2 * ks + a_half) ^ (t & 7))) << 4), a0);
+                    ptx::ldsm_x4(b_addr + (uint32_t)((kb * 64 + ks * 16) * 2), b0);
+                    ptx::ldsm_x4(a_box + (uint32_t)((((2 * ks + 2 + a_half) ^ (t & 7))) << 4), a1);
+                    ptx::ldsm_x4(b_addr + (uint32_t)((kb * 64 + ks * 16 + 16) * 2), b1);
                     ptx::mma_bf16(acc[0], a0, b0[0], b0[1]);
                     ptx::mma_bf16(acc[1], a0, b0[2], b0[3]);
-                    if (k + 16 < p.Dx) {
-                        ptx::ldsm_x4(a_addr + (k + 16) * 2, a1);
-                        ptx::ldsm_x4(b_addr + (k + 16) * 2, b1);
-                        ptx::mma_bf16(acc[2], a1, b1[0], b1[1]);
-                        ptx::mma_bf16(acc[3], a1, b1[2], b1[3]);
-                    }
+                    ptx::mma_bf16(acc[2], a1, b1[0], b1[1]);
+                    ptx::mma_bf16(acc[3], a1, b1[2], b1[3]);
                 }
-                float u4[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) u4[i] = (acc[0][i] + acc[2][i]) + (acc[1][i] + acc[3][i]);
-                const int r0 = tile * TR + mt * 16 + g, h0 = nt * 8 + 2 * c;
-                store_eta(p, r0, h0, u4[0]);
-                store_eta(p, r0, h0 + 1, u4[1]);
-                store_eta(p, r0 + 8, h0, u4[2]);
-                store_eta(p, r0 + 8, h0 + 1, u4[3]);
             }
+            float u4[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) u4[k] = (acc[0][k] + acc[2][k]) + (acc[1][k] + acc[3][k]);
+            const int r0 = tile * TR + mt * 16 + g, h0 = nt * 8 + 2 * c;
+            store_eta(p, r0, h0, u4[0]);
+            store_eta(p, r0, h0 + 1, u4[1]);
+            store_eta(p, r0 + 8, h0, u4[2]);
+            store_eta(p, r0 + 8, h0 + 1, u4[3]);
         }
         __syncthreads();   // every warp is done with the slot
         if (i + p.nstage < mine) {
-            if (warp == 0) issue(i + p.nstage);
+            if (tid == 0) {
+                ptx::fence_proxy_async();
+                issue(i + p.nstage);
+            }
             ++issued;
         }
     }
@@ -214,9 +223,9 @@ __global__ void __launch_bounds__(256) eta_gate_generic_kernel(GateParams p)
 
 bool gate_mma_supported(int H, int Dx, ttt_dtype x_dtype)
 {
-    if (x_dtype != TTT_BF16 || H > 32 || Dx % 16 != 0) return false;
-    const int HP = H <= 16 ? 16 : 32, DXP = Dx + 8;
-    return mma_smem_bytes(HP, DXP, 2) <= kSmemLimit;
+    if (x_dtype != TTT_BF16 || H > 32 || Dx % 64 != 0) return false;
+    const int HP = H <= 16 ? 16 : 32;
+    return mma_smem_bytes(HP, Dx, 2) <= kSmemLimit;
 }
 
 cudaError_t launch_eta_gate(const GateArgs &a)
@@ -239,14 +248,17 @@ cudaError_t launch_eta_gate(const GateArgs &a)
     if (gate_mma_supported(a.H, a.Dx, a.x_dtype)) {
         p.HP = a.H <= 16 ? 16 : 32;
         p.DXP = a.Dx + 8;
-        p.nstage = 3;
-        while (p.nstage > 2 && mma_smem_bytes(p.HP, p.DXP, p.nstage) > kSmemLimit) --p.nstage;
-        const size_t smem = mma_smem_bytes(p.HP, p.DXP, p.nstage);
+        p.nstage = 4;
+        while (p.nstage > 2 && mma_smem_bytes(p.HP, a.Dx, p.nstage) > kSmemLimit) --p.nstage;
+        const size_t smem = mma_smem_bytes(p.HP, a.Dx, p.nstage);
         const int ntiles = (p.rows + TR - 1) / TR;
+        CUtensorMap mx;
+        if (!make_bf16_2d_map(&mx, a.x, (unsigned long long)p.rows, (unsigned long long)a.Dx, TR))
+            return cudaErrorInvalidValue;
         if ((e = cudaFuncSetAttribute(eta_gate_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem)) != cudaSuccess)
             return e;
-        eta_gate_mma_kernel<<<min(ntiles, sms), kGateThreads, smem, a.stream>>>(p);
+        eta_gate_mma_kernel<<<min(ntiles, sms), kGateThreads, smem, a.stream>>>(mx, p);
     } else {
         const int blocks = min((p.rows + 7) / 8, sms * 8);
         if (a.x_dtype == TTT_BF16)

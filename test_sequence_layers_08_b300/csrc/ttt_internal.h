@@ -68,6 +68,9 @@ cudaError_t launch_mlp_generic(const MlpArgs &a);
 // Tensor-core TTT-Linear kernel (bf16 I/O, d = 64, b = 16).
 bool linear_tc_supported(const ttt_desc &d);
 cudaError_t launch_linear_tc(const LinearArgs &a);
+// TMA map of a [rows][cols] bf16 matrix: boxes of box_rows rows x 64 columns, 128-byte swizzle.
+bool make_bf16_2d_map(CUtensorMap *m, const void *base, unsigned long long rows, unsigned long long cols,
+                      unsigned box_rows);
 // TMA map of a [BH][L][64] bf16 tensor: boxes of `rows` tokens x 64 features, 128-byte swizzle.
 bool make_bf16_tile_map(CUtensorMap *m, const void *base, int L, int BH, int rows);
 // TTT-Linear decode kernel (d = 64, fp32 or bf16 I/O, FP32 arithmetic, one warp per head).

@@ -676,6 +676,22 @@ int g_withhold_loads = 0;
 
 }  // namespace
 
+// [rows][cols] bf16 row-major as a 2-D tensor; boxes of box_rows x 64 columns, 128-byte swizzle.
+bool make_bf16_2d_map(CUtensorMap *m, const void *base, unsigned long long rows, unsigned long long cols,
+                      unsigned box_rows)
+{
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // [BH][L][64] bf16 viewed as a 3-D tensor; boxes of `rows` tokens, 128-byte swizzle.
 bool make_bf16_tile_map(CUtensorMap *m, const void *base, int L, int BH, int rows)
 {

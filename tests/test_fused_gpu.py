@@ -16,7 +16,7 @@ LIN = CONFIGS["linear_bf16_B8_H12_L2048"]
 LIN_LN = CONFIGS["linear_ln_bf16_B4_H16_L8192"]
 
 # names of the tensor-core TTT-Linear kernels the library may pick for bf16, d = 64, b = 16
-LINEAR_TC_KERNELS = ("ttt_linear_fused", "ttt_linear_cluster")
+LINEAR_TC_KERNELS = ("ttt_linear_fused",)
 
 
 @pytest.mark.parametrize("name", ["linear_bf16_B8_H12_L2048", "linear_ln_bf16_B4_H16_L8192",
