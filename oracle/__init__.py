@@ -56,25 +56,25 @@ def _load():
             lib.oracle_ln_fwd.argtypes = [dp, i, dp, dp, d, dp]
             lib.oracle_ln_l2_bwd.restype = None
             lib.oracle_ln_l2_bwd.argtypes = [dp, dp, i, dp, dp, d, dp]
-            lib.oracle_linear_token_loss.restype = d
-            lib.oracle_linear_token_loss.argtypes = [dp, dp, dp, dp, i, i, dp, dp, d]
-            lib.oracle_linear_token_grad.restype = None
-            lib.oracle_linear_token_grad.argtypes = [dp, dp, dp, dp, i, i, dp, dp, d, dp, dp]
-            lib.oracle_mlp_token_loss.restype = d
-            lib.oracle_mlp_token_loss.argtypes = [dp, dp, dp, dp, dp, dp, i, i, i, dp, dp, d]
-            lib.oracle_mlp_token_grad.restype = None
-            lib.oracle_mlp_token_grad.argtypes = [dp, dp, dp, dp, dp, dp, i, i, i, dp, dp, d,
-                                                  dp, dp, dp, dp]
+            lib.oracle_linear_token_loss_v.restype = d
+            lib.oracle_linear_token_loss_v.argtypes = [dp, dp, dp, dp, i, i, i, dp, dp, d]
+            lib.oracle_linear_token_grad_v.restype = None
+            lib.oracle_linear_token_grad_v.argtypes = [dp, dp, dp, dp, i, i, i, dp, dp, d, dp, dp]
+            lib.oracle_mlp_token_loss_v.restype = d
+            lib.oracle_mlp_token_loss_v.argtypes = [dp, dp, dp, dp, dp, dp, i, i, i, i, dp, dp, d]
+            lib.oracle_mlp_token_grad_v.restype = None
+            lib.oracle_mlp_token_grad_v.argtypes = [dp, dp, dp, dp, dp, dp, i, i, i, i, dp, dp, d,
+                                                    dp, dp, dp, dp]
             lib.oracle_eta_gate.restype = i
             lib.oracle_eta_gate.argtypes = [i, i, i, i, d, dp, dp, dp]
-            for name in ("oracle_ttt_linear", "oracle_ttt_linear_dual"):
+            for name in ("oracle_ttt_linear_v", "oracle_ttt_linear_dual_v"):
                 fn = getattr(lib, name)
                 fn.restype = i
-                fn.argtypes = [i, i, i, i, i, i, d, i] + [dp] * 11
-            for name in ("oracle_ttt_mlp", "oracle_ttt_mlp_dual"):
+                fn.argtypes = [i, i, i, i, i, i, d, i, i, d] + [dp] * 11
+            for name in ("oracle_ttt_mlp_v", "oracle_ttt_mlp_dual_v"):
                 fn = getattr(lib, name)
                 fn.restype = i
-                fn.argtypes = [i, i, i, i, i, i, i, d, i] + [dp] * 15
+                fn.argtypes = [i, i, i, i, i, i, i, d, i, i, d] + [dp] * 15
             _lib = lib
     return _lib
 
@@ -138,40 +138,50 @@ def ln_l2_bwd(z, y, gamma=None, beta=None, eps=1e-6):
     return out
 
 
-def linear_token_loss(k, v, W, c, ln=False, gamma=None, beta=None, eps=1e-6):
+LOSSES = {"mse": 0, "ip": 1}   # 1/2 ||f(k) - v||^2, or the inner product -<f(k), v>
+
+
+def _loss_id(loss: str) -> int:
+    if loss not in LOSSES:
+        raise ValueError(f"loss must be one of {sorted(LOSSES)}")
+    return LOSSES[loss]
+
+
+def linear_token_loss(k, v, W, c, ln=False, gamma=None, beta=None, eps=1e-6, loss="mse"):
     k, v, W, c = _f64(k), _f64(v), _f64(W), _f64(c)
     g = None if gamma is None else _f64(gamma)
     b = None if beta is None else _f64(beta)
-    return _load().oracle_linear_token_loss(_p(k), _p(v), _p(W), _p(c), k.size, int(ln),
-                                            _p(g), _p(b), eps)
+    return _load().oracle_linear_token_loss_v(_p(k), _p(v), _p(W), _p(c), k.size, int(ln),
+                                              _loss_id(loss), _p(g), _p(b), eps)
 
 
-def linear_token_grad(k, v, W, c, ln=False, gamma=None, beta=None, eps=1e-6):
+def linear_token_grad(k, v, W, c, ln=False, gamma=None, beta=None, eps=1e-6, loss="mse"):
     k, v, W, c = _f64(k), _f64(v), _f64(W), _f64(c)
     g = None if gamma is None else _f64(gamma)
     b = None if beta is None else _f64(beta)
     gW, gc = np.empty_like(W), np.empty_like(c)
-    _load().oracle_linear_token_grad(_p(k), _p(v), _p(W), _p(c), k.size, int(ln), _p(g),
-                                     _p(b), eps, _p(gW), _p(gc))
+    _load().oracle_linear_token_grad_v(_p(k), _p(v), _p(W), _p(c), k.size, int(ln),
+                                       _loss_id(loss), _p(g), _p(b), eps, _p(gW), _p(gc))
     return gW, gc
 
 
-def mlp_token_loss(k, v, W1, b1, W2, b2, ln=False, gamma=None, beta=None, eps=1e-6):
+def mlp_token_loss(k, v, W1, b1, W2, b2, ln=False, gamma=None, beta=None, eps=1e-6, loss="mse"):
     k, v, W1, b1, W2, b2 = map(_f64, (k, v, W1, b1, W2, b2))
     g = None if gamma is None else _f64(gamma)
     b = None if beta is None else _f64(beta)
-    return _load().oracle_mlp_token_loss(_p(k), _p(v), _p(W1), _p(b1), _p(W2), _p(b2),
-                                         k.size, b1.size, int(ln), _p(g), _p(b), eps)
+    return _load().oracle_mlp_token_loss_v(_p(k), _p(v), _p(W1), _p(b1), _p(W2), _p(b2),
+                                           k.size, b1.size, int(ln), _loss_id(loss), _p(g),
+                                           _p(b), eps)
 
 
-def mlp_token_grad(k, v, W1, b1, W2, b2, ln=False, gamma=None, beta=None, eps=1e-6):
+def mlp_token_grad(k, v, W1, b1, W2, b2, ln=False, gamma=None, beta=None, eps=1e-6, loss="mse"):
     k, v, W1, b1, W2, b2 = map(_f64, (k, v, W1, b1, W2, b2))
     g = None if gamma is None else _f64(gamma)
     b = None if beta is None else _f64(beta)
     gW1, gb1, gW2, gb2 = (np.empty_like(a) for a in (W1, b1, W2, b2))
-    _load().oracle_mlp_token_grad(_p(k), _p(v), _p(W1), _p(b1), _p(W2), _p(b2), k.size,
-                                  b1.size, int(ln), _p(g), _p(b), eps, _p(gW1), _p(gb1),
-                                  _p(gW2), _p(gb2))
+    _load().oracle_mlp_token_grad_v(_p(k), _p(v), _p(W1), _p(b1), _p(W2), _p(b2), k.size,
+                                    b1.size, int(ln), _loss_id(loss), _p(g), _p(b), eps,
+                                    _p(gW1), _p(gb1), _p(gW2), _p(gb2))
     return gW1, gb1, gW2, gb2
 
 
@@ -181,9 +191,10 @@ def mlp_token_grad(k, v, W1, b1, W2, b2, ln=False, gamma=None, beta=None, eps=1e
 
 def ttt_linear(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: int,
                ln: bool, eps: float = 1e-6, init_per_batch: bool = False,
-               dual: bool = False):
+               dual: bool = False, loss: str = "mse", weight_decay: float = 0.0):
     """TTT-Linear forward.  Q,K,V: [B,H,L,d]; eta: [B,H,L]; W0: [H,d,d] (or
     [B,H,d,d] if init_per_batch); b0: [H,d] (or [B,H,d]); gamma/beta: [H,d].
+    loss: "mse" (1/2 ||f(k) - v||^2) or "ip" (-<f(k), v>); weight_decay lambda on W.
     Returns (Z [B,H,L,d], W_final [B,H,d,d], b_final [B,H,d]) in float64."""
     Q, K, V, eta, W0, b0 = map(_f64, (Q, K, V, eta, W0, b0))
     B, H, L, d = Q.shape
@@ -192,8 +203,9 @@ def ttt_linear(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: int,
     Z = np.empty((B, H, L, d))
     Wf = np.empty((B, H, d, d))
     bf = np.empty((B, H, d))
-    fn = _load().oracle_ttt_linear_dual if dual else _load().oracle_ttt_linear
+    fn = _load().oracle_ttt_linear_dual_v if dual else _load().oracle_ttt_linear_v
     rc = fn(B, H, L, d, int(mini_batch), int(ln), float(eps), int(init_per_batch),
+            _loss_id(loss), float(weight_decay),
             _p(Q), _p(K), _p(V), _p(eta), _p(W0), _p(b0), _p(g), _p(b), _p(Z), _p(Wf), _p(bf))
     if rc != 0:
         raise ValueError(f"oracle_ttt_linear returned {rc}")
@@ -201,9 +213,11 @@ def ttt_linear(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: int,
 
 
 def ttt_mlp(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_batch: int,
-            ln: bool, eps: float = 1e-6, init_per_batch: bool = False, dual: bool = False):
+            ln: bool, eps: float = 1e-6, init_per_batch: bool = False, dual: bool = False,
+            loss: str = "mse", weight_decay: float = 0.0):
     """TTT-MLP forward.  W1: [H,d,dh], b1: [H,dh], W2: [H,dh,d], b2: [H,d] (or with
-    a leading B if init_per_batch).  Returns (Z, W1_f, b1_f, W2_f, b2_f)."""
+    a leading B if init_per_batch); loss and weight_decay as for ttt_linear.
+    Returns (Z, W1_f, b1_f, W2_f, b2_f)."""
     Q, K, V, eta, W1, b1, W2, b2 = map(_f64, (Q, K, V, eta, W1, b1, W2, b2))
     B, H, L, d = Q.shape
     dh = b1.shape[-1]
@@ -214,8 +228,9 @@ def ttt_mlp(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_batch: 
     b1f = np.empty((B, H, dh))
     W2f = np.empty((B, H, dh, d))
     b2f = np.empty((B, H, d))
-    fn = _load().oracle_ttt_mlp_dual if dual else _load().oracle_ttt_mlp
+    fn = _load().oracle_ttt_mlp_dual_v if dual else _load().oracle_ttt_mlp_v
     rc = fn(B, H, L, d, dh, int(mini_batch), int(ln), float(eps), int(init_per_batch),
+            _loss_id(loss), float(weight_decay),
             _p(Q), _p(K), _p(V), _p(eta), _p(W1), _p(b1), _p(W2), _p(b2), _p(g), _p(b),
             _p(Z), _p(W1f), _p(b1f), _p(W2f), _p(b2f))
     if rc != 0:

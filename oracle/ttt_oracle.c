@@ -21,6 +21,8 @@
  *        GELU -> d; residual form f(x) = x + LN(f_res(x)).
  *   [G]  same lryc.cn article, section 2.2: the learnable per-token learning
  *        rate eta(x) = eta_base * sigmoid(theta_lr . x).
+ *   [M]  ai-feeds "Modular TTT" page, method overview: the loss (MSE or inner
+ *        product) and weight decay are design dimensions of the inner learner.
  *
  * Readings where the pages are silent (all of them are also listed in the
  * design notes):
@@ -33,6 +35,11 @@
  *   - LayerNorm uses the biased variance and eps passed by the caller; the same
  *     gamma/beta serve the loss and the output;
  *   - GELU is the tanh form 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *   - [M] gives no formulas; the readings taken: the inner-product loss is
+ *     l = -<f(k), v>; weight decay lambda adds 1/2 lambda ||W||^2 to each
+ *     token's loss for the weight matrices (W; W1, W2), not the biases, so a
+ *     token's step is W -= eta_t (grad_W l_t + lambda W) with both terms taken
+ *     at the mini-batch's starting weights like every other gradient [MB].
  *
  * Parity pins (what ties this file to something other than itself) live in
  * the CPU tests: autograd brute force of the definition, b = 1 online GD, eta = 0,
@@ -143,6 +150,58 @@ void oracle_ln_l2_bwd(const double *z, const double *y, int n, const double *gam
     free(gx);
 }
 
+/* Gradient w.r.t. z of a loss whose gradient w.r.t. LN(z) is u, by hand:
+ *   xh = (z - mu) r,  gx = gamma u,  g = r (gx - mean(gx) - xh mean(gx xh)). */
+static void ln_bwd_upstream(const double *z, const double *u, int n, const double *gamma,
+                            double eps, double *g)
+{
+    double mu = 0.0, var = 0.0;
+    for (int i = 0; i < n; ++i) mu += z[i];
+    mu /= n;
+    for (int i = 0; i < n; ++i) var += (z[i] - mu) * (z[i] - mu);
+    var /= n;
+    double r = 1.0 / sqrt(var + eps);
+    double m1 = 0.0, m2 = 0.0;
+    for (int i = 0; i < n; ++i) {
+        double gx = (gamma ? gamma[i] : 1.0) * u[i];
+        m1 += gx;
+        m2 += gx * (z[i] - mu) * r;
+    }
+    m1 /= n;
+    m2 /= n;
+    for (int i = 0; i < n; ++i) {
+        double gx = (gamma ? gamma[i] : 1.0) * u[i];
+        g[i] = r * (gx - m1 - (z[i] - mu) * r * m2);
+    }
+}
+
+/* dl/dz of one token for the loss `loss` (0: 1/2 ||f(k) - v||^2, 1: -<f(k), v>) with
+ * f(k) = z (ln = 0) or k + LN(z) (ln = 1); y is scratch of n values. */
+static void token_dz(const double *z, const double *k, const double *v, int n, int ln, int loss,
+                     const double *gamma, const double *beta, double eps, double *y, double *g)
+{
+    if (loss == 1) {
+        for (int j = 0; j < n; ++j) y[j] = -v[j];
+        if (ln)
+            ln_bwd_upstream(z, y, n, gamma, eps, g);
+        else
+            memcpy(g, y, sizeof(double) * (size_t)n);
+    } else if (ln) {
+        for (int j = 0; j < n; ++j) y[j] = v[j] - k[j];
+        oracle_ln_l2_bwd(z, y, n, gamma, beta, eps, g);
+    } else {
+        for (int j = 0; j < n; ++j) g[j] = z[j] - v[j];
+    }
+}
+
+/* The token loss from the output o = f(k): 1/2 ||o - v||^2 or -<o, v>. */
+static double token_loss_value(const double *o, const double *v, int n, int loss)
+{
+    double l = 0.0;
+    for (int j = 0; j < n; ++j) l += loss == 1 ? -o[j] * v[j] : 0.5 * (o[j] - v[j]) * (o[j] - v[j]);
+    return l;
+}
+
 /* ------------------------------------------------------------------------ */
 /* TTT-Linear: f(k) = k W + c  (row-vector convention of [D]/[I]),            */
 /* residual form f(k) = k + LN(k W + c).                                      */
@@ -160,10 +219,10 @@ static void row_times(const double *x, const double *W, const double *c, int n_i
     }
 }
 
-/* Per-token reconstruction loss 1/2 ||f(k) - v||^2 at weights (W, c). */
-double oracle_linear_token_loss(const double *k, const double *v, const double *W,
-                                const double *c, int d, int ln, const double *gamma,
-                                const double *beta, double eps)
+/* Per-token loss (1/2 ||f(k) - v||^2 or -<f(k), v>) at weights (W, c). */
+double oracle_linear_token_loss_v(const double *k, const double *v, const double *W,
+                                  const double *c, int d, int ln, int loss, const double *gamma,
+                                  const double *beta, double eps)
 {
     double *z = (double *)malloc(sizeof(double) * (size_t)d);
     double *o = (double *)malloc(sizeof(double) * (size_t)d);
@@ -174,34 +233,42 @@ double oracle_linear_token_loss(const double *k, const double *v, const double *
     } else {
         memcpy(o, z, sizeof(double) * (size_t)d);
     }
-    double l = 0.0;
-    for (int j = 0; j < d; ++j) l += 0.5 * (o[j] - v[j]) * (o[j] - v[j]);
+    double l = token_loss_value(o, v, d, loss);
     free(z);
     free(o);
     return l;
 }
 
+double oracle_linear_token_loss(const double *k, const double *v, const double *W,
+                                const double *c, int d, int ln, const double *gamma,
+                                const double *beta, double eps)
+{
+    return oracle_linear_token_loss_v(k, v, W, c, d, ln, 0, gamma, beta, eps);
+}
+
 /* Hand gradient of the token loss: g = dl/dz; dl/dW = k^T g; dl/dc = g. */
-void oracle_linear_token_grad(const double *k, const double *v, const double *W,
-                              const double *c, int d, int ln, const double *gamma,
-                              const double *beta, double eps, double *gW, double *gc)
+void oracle_linear_token_grad_v(const double *k, const double *v, const double *W,
+                                const double *c, int d, int ln, int loss, const double *gamma,
+                                const double *beta, double eps, double *gW, double *gc)
 {
     double *z = (double *)malloc(sizeof(double) * (size_t)d);
     double *g = (double *)malloc(sizeof(double) * (size_t)d);
     double *y = (double *)malloc(sizeof(double) * (size_t)d);
     row_times(k, W, c, d, d, z);
-    if (ln) {
-        for (int j = 0; j < d; ++j) y[j] = v[j] - k[j];
-        oracle_ln_l2_bwd(z, y, d, gamma, beta, eps, g);
-    } else {
-        for (int j = 0; j < d; ++j) g[j] = z[j] - v[j];
-    }
+    token_dz(z, k, v, d, ln, loss, gamma, beta, eps, y, g);
     for (int i = 0; i < d; ++i)
         for (int j = 0; j < d; ++j) gW[(size_t)i * d + j] = k[i] * g[j];
     for (int j = 0; j < d; ++j) gc[j] = g[j];
     free(z);
     free(g);
     free(y);
+}
+
+void oracle_linear_token_grad(const double *k, const double *v, const double *W,
+                              const double *c, int d, int ln, const double *gamma,
+                              const double *beta, double eps, double *gW, double *gc)
+{
+    oracle_linear_token_grad_v(k, v, W, c, d, ln, 0, gamma, beta, eps, gW, gc);
 }
 
 /* Offsets of the initial state for (batch bi, head hi). */
@@ -219,11 +286,11 @@ static size_t init_index(int bi, int hi, int H, int per_batch)
  * then, token by token, W -= eta_t k_t^T g_t, c -= eta_t g_t, and the output is
  * f(q_t) at the updated weights.
  */
-int oracle_ttt_linear(int B, int H, int L, int d, int mb, int ln, double eps,
-                      int init_per_batch, const double *Q, const double *K,
-                      const double *V, const double *eta, const double *W0,
-                      const double *b0, const double *gamma, const double *beta,
-                      double *Z, double *W_final, double *b_final)
+int oracle_ttt_linear_v(int B, int H, int L, int d, int mb, int ln, double eps,
+                        int init_per_batch, int loss, double wd, const double *Q,
+                        const double *K, const double *V, const double *eta, const double *W0,
+                        const double *b0, const double *gamma, const double *beta,
+                        double *Z, double *W_final, double *b_final)
 {
     if (B <= 0 || H <= 0 || L <= 0 || d <= 0 || mb <= 0 || L % mb != 0) return ORACLE_BAD_ARG;
     size_t dd = (size_t)d * d;
@@ -250,8 +317,8 @@ int oracle_ttt_linear(int B, int H, int L, int d, int mb, int ln, double eps,
                 /* every gradient of the mini-batch at its starting weights [MB] */
                 for (int s = 0; s < mb; ++s) {
                     size_t row = (bh * L + n0 + s) * d;
-                    oracle_linear_token_grad(K + row, V + row, Ws, cs, d, ln, gm, bt, eps,
-                                             gW, G + (size_t)s * d);
+                    oracle_linear_token_grad_v(K + row, V + row, Ws, cs, d, ln, loss, gm, bt, eps,
+                                               gW, G + (size_t)s * d);
                 }
                 /* token-by-token update, then apply with the updated weights [R] */
                 for (int t = 0; t < mb; ++t) {
@@ -259,8 +326,10 @@ int oracle_ttt_linear(int B, int H, int L, int d, int mb, int ln, double eps,
                     double et = eta[bh * L + n0 + t];
                     const double *kt = K + row;
                     const double *gt = G + (size_t)t * d;
+                    /* W -= eta_t (k_t^T g_t + lambda W_start) */
                     for (int i = 0; i < d; ++i)
-                        for (int j = 0; j < d; ++j) W[(size_t)i * d + j] -= et * kt[i] * gt[j];
+                        for (int j = 0; j < d; ++j)
+                            W[(size_t)i * d + j] -= et * (kt[i] * gt[j] + wd * Ws[(size_t)i * d + j]);
                     for (int j = 0; j < d; ++j) c[j] -= et * gt[j];
                     row_times(Q + row, W, c, d, d, z);
                     if (ln) {
@@ -279,6 +348,16 @@ int oracle_ttt_linear(int B, int H, int L, int d, int mb, int ln, double eps,
     return ORACLE_OK;
 }
 
+int oracle_ttt_linear(int B, int H, int L, int d, int mb, int ln, double eps,
+                      int init_per_batch, const double *Q, const double *K,
+                      const double *V, const double *eta, const double *W0,
+                      const double *b0, const double *gamma, const double *beta,
+                      double *Z, double *W_final, double *b_final)
+{
+    return oracle_ttt_linear_v(B, H, L, d, mb, ln, eps, init_per_batch, 0, 0.0, Q, K, V, eta,
+                               W0, b0, gamma, beta, Z, W_final, b_final);
+}
+
 /*
  * TTT-Linear forward, dual form, written separately from the primal above and
  * used only to check primal == dual.  Per mini-batch ([D] section 4.2):
@@ -286,12 +365,14 @@ int oracle_ttt_linear(int B, int H, int L, int d, int mb, int ln, double eps,
  *   A    = tril(Q K^T + 1) with column s scaled by eta_s (diagonal included),
  *   Zbar = Q W + 1 c - A G,    W <- W - K^T diag(eta) G,   c <- c - eta^T G.
  * The "+1" carries the bias: c_t = c - sum_{s<=t} eta_s g_s.
+ * With weight decay lambda the Q W term of token t is scaled by
+ * 1 - lambda sum_{s<=t} eta_s, and the carry by 1 - lambda sum_s eta_s.
  */
-int oracle_ttt_linear_dual(int B, int H, int L, int d, int mb, int ln, double eps,
-                           int init_per_batch, const double *Q, const double *K,
-                           const double *V, const double *eta, const double *W0,
-                           const double *b0, const double *gamma, const double *beta,
-                           double *Z, double *W_final, double *b_final)
+int oracle_ttt_linear_dual_v(int B, int H, int L, int d, int mb, int ln, double eps,
+                             int init_per_batch, int loss, double wd, const double *Q,
+                             const double *K, const double *V, const double *eta,
+                             const double *W0, const double *b0, const double *gamma,
+                             const double *beta, double *Z, double *W_final, double *b_final)
 {
     if (B <= 0 || H <= 0 || L <= 0 || d <= 0 || mb <= 0 || L % mb != 0) return ORACLE_BAD_ARG;
     size_t dd = (size_t)d * d;
@@ -320,13 +401,8 @@ int oracle_ttt_linear_dual(int B, int H, int L, int d, int mb, int ln, double ep
                 /* Zk and G */
                 for (int s = 0; s < mb; ++s) {
                     row_times(Kn + (size_t)s * d, W, c, d, d, Zk + (size_t)s * d);
-                    if (ln) {
-                        for (int j = 0; j < d; ++j) y[j] = Vn[(size_t)s * d + j] - Kn[(size_t)s * d + j];
-                        oracle_ln_l2_bwd(Zk + (size_t)s * d, y, d, gm, bt, eps, G + (size_t)s * d);
-                    } else {
-                        for (int j = 0; j < d; ++j)
-                            G[(size_t)s * d + j] = Zk[(size_t)s * d + j] - Vn[(size_t)s * d + j];
-                    }
+                    token_dz(Zk + (size_t)s * d, Kn + (size_t)s * d, Vn + (size_t)s * d, d, ln, loss,
+                             gm, bt, eps, y, G + (size_t)s * d);
                 }
                 /* A = tril(Q K^T + 1) diag(eta) */
                 for (int t = 0; t < mb; ++t)
@@ -338,9 +414,12 @@ int oracle_ttt_linear_dual(int B, int H, int L, int d, int mb, int ln, double ep
                         }
                         A[(size_t)t * mb + s] = a;
                     }
-                /* outputs with the mini-batch's starting W */
+                /* outputs with the mini-batch's starting W (decay-scaled) */
+                double cum = 0.0;
                 for (int t = 0; t < mb; ++t) {
-                    row_times(Qn + (size_t)t * d, W, c, d, d, zb);
+                    cum += en[t];
+                    row_times(Qn + (size_t)t * d, W, NULL, d, d, zb);
+                    for (int j = 0; j < d; ++j) zb[j] = (1.0 - wd * cum) * zb[j] + c[j];
                     for (int s = 0; s <= t; ++s)
                         for (int j = 0; j < d; ++j) zb[j] -= A[(size_t)t * mb + s] * G[(size_t)s * d + j];
                     double *zo = Z + (bh * L + n0 + t) * d;
@@ -351,7 +430,8 @@ int oracle_ttt_linear_dual(int B, int H, int L, int d, int mb, int ln, double ep
                         memcpy(zo, zb, sizeof(double) * (size_t)d);
                     }
                 }
-                /* carry: W -= K^T diag(eta) G, c -= eta^T G */
+                /* carry: W <- (1 - lambda sum eta) W - K^T diag(eta) G, c -= eta^T G */
+                for (size_t i = 0; i < dd; ++i) W[i] *= 1.0 - wd * cum;
                 for (int s = 0; s < mb; ++s)
                     for (int i = 0; i < d; ++i) {
                         double ks = en[s] * Kn[(size_t)s * d + i];
@@ -366,6 +446,16 @@ int oracle_ttt_linear_dual(int B, int H, int L, int d, int mb, int ln, double ep
     }
     free(W); free(c); free(Zk); free(G); free(A); free(zb); free(y);
     return ORACLE_OK;
+}
+
+int oracle_ttt_linear_dual(int B, int H, int L, int d, int mb, int ln, double eps,
+                           int init_per_batch, const double *Q, const double *K,
+                           const double *V, const double *eta, const double *W0,
+                           const double *b0, const double *gamma, const double *beta,
+                           double *Z, double *W_final, double *b_final)
+{
+    return oracle_ttt_linear_dual_v(B, H, L, d, mb, ln, eps, init_per_batch, 0, 0.0, Q, K, V,
+                                    eta, W0, b0, gamma, beta, Z, W_final, b_final);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -413,18 +503,25 @@ static void mlp_row_forward(const double *x, const double *W1, const double *b1,
     }
 }
 
+double oracle_mlp_token_loss_v(const double *k, const double *v, const double *W1,
+                               const double *b1, const double *W2, const double *b2, int d,
+                               int dh, int ln, int loss, const double *gamma, const double *beta,
+                               double eps)
+{
+    mlp_scratch s;
+    if (!mlp_scratch_alloc(&s, d, dh)) return NAN;
+    mlp_row_forward(k, W1, b1, W2, b2, d, dh, ln, gamma, beta, eps, &s);
+    double l = token_loss_value(s.o, v, d, loss);
+    mlp_scratch_free(&s);
+    return l;
+}
+
 double oracle_mlp_token_loss(const double *k, const double *v, const double *W1,
                              const double *b1, const double *W2, const double *b2, int d,
                              int dh, int ln, const double *gamma, const double *beta,
                              double eps)
 {
-    mlp_scratch s;
-    if (!mlp_scratch_alloc(&s, d, dh)) return NAN;
-    mlp_row_forward(k, W1, b1, W2, b2, d, dh, ln, gamma, beta, eps, &s);
-    double l = 0.0;
-    for (int j = 0; j < d; ++j) l += 0.5 * (s.o[j] - v[j]) * (s.o[j] - v[j]);
-    mlp_scratch_free(&s);
-    return l;
+    return oracle_mlp_token_loss_v(k, v, W1, b1, W2, b2, d, dh, ln, 0, gamma, beta, eps);
 }
 
 /* Hand back-propagation through the fast-weight MLP for one token:
@@ -432,19 +529,14 @@ double oracle_mlp_token_loss(const double *k, const double *v, const double *W1,
  *   g1 = (g2 W2^T) * GELU'(z1),
  *   dW1 = k^T g1, db1 = g1, dW2 = x2^T g2, db2 = g2.
  * Outputs g1 (dh), g2 (d) and x2 (dh); the weight gradients are the outer
- * products above (formed by the callers). */
+ * products above (formed by the callers).  `loss` as for token_dz. */
 static void mlp_token_backward(const double *k, const double *v, const double *W1,
                                const double *b1, const double *W2, const double *b2,
-                               int d, int dh, int ln, const double *gamma,
+                               int d, int dh, int ln, int loss, const double *gamma,
                                const double *beta, double eps, mlp_scratch *s)
 {
     mlp_row_forward(k, W1, b1, W2, b2, d, dh, ln, gamma, beta, eps, s);
-    if (ln) {
-        for (int j = 0; j < d; ++j) s->y[j] = v[j] - k[j];
-        oracle_ln_l2_bwd(s->z2, s->y, d, gamma, beta, eps, s->g2);
-    } else {
-        for (int j = 0; j < d; ++j) s->g2[j] = s->z2[j] - v[j];
-    }
+    token_dz(s->z2, k, v, d, ln, loss, gamma, beta, eps, s->y, s->g2);
     for (int m = 0; m < dh; ++m) {
         double a = 0.0;
         const double *W2m = W2 + (size_t)m * d;
@@ -454,14 +546,14 @@ static void mlp_token_backward(const double *k, const double *v, const double *W
     }
 }
 
-void oracle_mlp_token_grad(const double *k, const double *v, const double *W1,
-                           const double *b1, const double *W2, const double *b2, int d,
-                           int dh, int ln, const double *gamma, const double *beta,
-                           double eps, double *gW1, double *gb1, double *gW2, double *gb2)
+void oracle_mlp_token_grad_v(const double *k, const double *v, const double *W1,
+                             const double *b1, const double *W2, const double *b2, int d,
+                             int dh, int ln, int loss, const double *gamma, const double *beta,
+                             double eps, double *gW1, double *gb1, double *gW2, double *gb2)
 {
     mlp_scratch s;
     if (!mlp_scratch_alloc(&s, d, dh)) return;
-    mlp_token_backward(k, v, W1, b1, W2, b2, d, dh, ln, gamma, beta, eps, &s);
+    mlp_token_backward(k, v, W1, b1, W2, b2, d, dh, ln, loss, gamma, beta, eps, &s);
     for (int i = 0; i < d; ++i)
         for (int m = 0; m < dh; ++m) gW1[(size_t)i * dh + m] = k[i] * s.g1[m];
     for (int m = 0; m < dh; ++m) gb1[m] = s.g1[m];
@@ -471,17 +563,26 @@ void oracle_mlp_token_grad(const double *k, const double *v, const double *W1,
     mlp_scratch_free(&s);
 }
 
+void oracle_mlp_token_grad(const double *k, const double *v, const double *W1,
+                           const double *b1, const double *W2, const double *b2, int d,
+                           int dh, int ln, const double *gamma, const double *beta,
+                           double eps, double *gW1, double *gb1, double *gW2, double *gb2)
+{
+    oracle_mlp_token_grad_v(k, v, W1, b1, W2, b2, d, dh, ln, 0, gamma, beta, eps, gW1, gb1, gW2,
+                            gb2);
+}
+
 /*
  * TTT-MLP forward, per-token primal form ([R] + [MB] + [F]).
  *   W1_0: [H,d,dh] (or [B,H,d,dh]), b1_0: [H,dh], W2_0: [H,dh,d], b2_0: [H,d];
  *   finals are [B,H,...].  Other arrays as for oracle_ttt_linear.
  */
-int oracle_ttt_mlp(int B, int H, int L, int d, int dh, int mb, int ln, double eps,
-                   int init_per_batch, const double *Q, const double *K, const double *V,
-                   const double *eta, const double *W1_0, const double *b1_0,
-                   const double *W2_0, const double *b2_0, const double *gamma,
-                   const double *beta, double *Z, double *W1_f, double *b1_f,
-                   double *W2_f, double *b2_f)
+int oracle_ttt_mlp_v(int B, int H, int L, int d, int dh, int mb, int ln, double eps,
+                     int init_per_batch, int loss, double wd, const double *Q, const double *K,
+                     const double *V, const double *eta, const double *W1_0,
+                     const double *b1_0, const double *W2_0, const double *b2_0,
+                     const double *gamma, const double *beta, double *Z, double *W1_f,
+                     double *b1_f, double *W2_f, double *b2_f)
 {
     if (B <= 0 || H <= 0 || L <= 0 || d <= 0 || dh <= 0 || mb <= 0 || L % mb != 0)
         return ORACLE_BAD_ARG;
@@ -519,8 +620,8 @@ int oracle_ttt_mlp(int B, int H, int L, int d, int dh, int mb, int ln, double ep
                 memcpy(b2s, b2, sizeof(double) * (size_t)d);
                 for (int t = 0; t < mb; ++t) {
                     size_t row = (bh * L + n0 + t) * d;
-                    mlp_token_backward(K + row, V + row, W1s, b1s, W2s, b2s, d, dh, ln, gm,
-                                       bt, eps, &s);
+                    mlp_token_backward(K + row, V + row, W1s, b1s, W2s, b2s, d, dh, ln, loss,
+                                       gm, bt, eps, &s);
                     memcpy(G1 + (size_t)t * dh, s.g1, sizeof(double) * (size_t)dh);
                     memcpy(G2 + (size_t)t * d, s.g2, sizeof(double) * (size_t)d);
                     memcpy(X2 + (size_t)t * dh, s.x2, sizeof(double) * (size_t)dh);
@@ -533,10 +634,12 @@ int oracle_ttt_mlp(int B, int H, int L, int d, int dh, int mb, int ln, double ep
                     const double *g2 = G2 + (size_t)t * d;
                     const double *x2 = X2 + (size_t)t * dh;
                     for (int i = 0; i < d; ++i)
-                        for (int m = 0; m < dh; ++m) W1[(size_t)i * dh + m] -= et * kt[i] * g1[m];
+                        for (int m = 0; m < dh; ++m)
+                            W1[(size_t)i * dh + m] -= et * (kt[i] * g1[m] + wd * W1s[(size_t)i * dh + m]);
                     for (int m = 0; m < dh; ++m) b1[m] -= et * g1[m];
                     for (int m = 0; m < dh; ++m)
-                        for (int j = 0; j < d; ++j) W2[(size_t)m * d + j] -= et * x2[m] * g2[j];
+                        for (int j = 0; j < d; ++j)
+                            W2[(size_t)m * d + j] -= et * (x2[m] * g2[j] + wd * W2s[(size_t)m * d + j]);
                     for (int j = 0; j < d; ++j) b2[j] -= et * g2[j];
                     mlp_row_forward(Q + row, W1, b1, W2, b2, d, dh, ln, gm, bt, eps, &s);
                     memcpy(Z + row, s.o, sizeof(double) * (size_t)d);
@@ -554,6 +657,17 @@ int oracle_ttt_mlp(int B, int H, int L, int d, int dh, int mb, int ln, double ep
     return ORACLE_OK;
 }
 
+int oracle_ttt_mlp(int B, int H, int L, int d, int dh, int mb, int ln, double eps,
+                   int init_per_batch, const double *Q, const double *K, const double *V,
+                   const double *eta, const double *W1_0, const double *b1_0,
+                   const double *W2_0, const double *b2_0, const double *gamma,
+                   const double *beta, double *Z, double *W1_f, double *b1_f,
+                   double *W2_f, double *b2_f)
+{
+    return oracle_ttt_mlp_v(B, H, L, d, dh, mb, ln, eps, init_per_batch, 0, 0.0, Q, K, V, eta,
+                            W1_0, b1_0, W2_0, b2_0, gamma, beta, Z, W1_f, b1_f, W2_f, b2_f);
+}
+
 /*
  * TTT-MLP forward, dual form (separately written; only for primal == dual).
  * Per mini-batch, with the starting weights:
@@ -562,13 +676,15 @@ int oracle_ttt_mlp(int B, int H, int L, int d, int dh, int mb, int ln, double ep
  *   Zb2 = Xb2 W2 + 1 b2 - (tril(Xb2 X2^T + 1) diag(eta)) G2,
  *   out = Q + LN(Zb2) (or Zb2);  then W1 -= K^T diag(eta) G1, b1 -= eta^T G1,
  *   W2 -= X2^T diag(eta) G2, b2 -= eta^T G2.
+ * With weight decay lambda, token t's Q W1 and Xb2 W2 terms are scaled by
+ * 1 - lambda sum_{s<=t} eta_s and the carried W1, W2 by 1 - lambda sum_s eta_s.
  */
-int oracle_ttt_mlp_dual(int B, int H, int L, int d, int dh, int mb, int ln, double eps,
-                        int init_per_batch, const double *Q, const double *K,
-                        const double *V, const double *eta, const double *W1_0,
-                        const double *b1_0, const double *W2_0, const double *b2_0,
-                        const double *gamma, const double *beta, double *Z, double *W1_f,
-                        double *b1_f, double *W2_f, double *b2_f)
+int oracle_ttt_mlp_dual_v(int B, int H, int L, int d, int dh, int mb, int ln, double eps,
+                          int init_per_batch, int loss, double wd, const double *Q,
+                          const double *K, const double *V, const double *eta,
+                          const double *W1_0, const double *b1_0, const double *W2_0,
+                          const double *b2_0, const double *gamma, const double *beta,
+                          double *Z, double *W1_f, double *b1_f, double *W2_f, double *b2_f)
 {
     if (B <= 0 || H <= 0 || L <= 0 || d <= 0 || dh <= 0 || mb <= 0 || L % mb != 0)
         return ORACLE_BAD_ARG;
@@ -611,13 +727,8 @@ int oracle_ttt_mlp_dual(int B, int H, int L, int d, int dh, int mb, int ln, doub
                     for (int m = 0; m < dh; ++m)
                         X2[(size_t)s * dh + m] = oracle_gelu(Z1[(size_t)s * dh + m]);
                     row_times(X2 + (size_t)s * dh, W2, b2, dh, d, Z2 + (size_t)s * d);
-                    if (ln) {
-                        for (int j = 0; j < d; ++j) y[j] = Vn[(size_t)s * d + j] - Kn[(size_t)s * d + j];
-                        oracle_ln_l2_bwd(Z2 + (size_t)s * d, y, d, gm, bt, eps, G2 + (size_t)s * d);
-                    } else {
-                        for (int j = 0; j < d; ++j)
-                            G2[(size_t)s * d + j] = Z2[(size_t)s * d + j] - Vn[(size_t)s * d + j];
-                    }
+                    token_dz(Z2 + (size_t)s * d, Kn + (size_t)s * d, Vn + (size_t)s * d, d, ln, loss,
+                             gm, bt, eps, y, G2 + (size_t)s * d);
                     for (int m = 0; m < dh; ++m) {
                         double a = 0.0;
                         for (int j = 0; j < d; ++j) a += G2[(size_t)s * d + j] * W2[(size_t)m * d + j];
@@ -634,8 +745,12 @@ int oracle_ttt_mlp_dual(int B, int H, int L, int d, int dh, int mb, int ln, doub
                         }
                         A[(size_t)t * mb + s] = a;
                     }
+                double cum = 0.0;
                 for (int t = 0; t < mb; ++t) {
-                    row_times(Qn + (size_t)t * d, W1, b1, d, dh, Zb1 + (size_t)t * dh);
+                    cum += en[t];
+                    row_times(Qn + (size_t)t * d, W1, NULL, d, dh, Zb1 + (size_t)t * dh);
+                    for (int m = 0; m < dh; ++m)
+                        Zb1[(size_t)t * dh + m] = (1.0 - wd * cum) * Zb1[(size_t)t * dh + m] + b1[m];
                     for (int s = 0; s <= t; ++s)
                         for (int m = 0; m < dh; ++m)
                             Zb1[(size_t)t * dh + m] -= A[(size_t)t * mb + s] * G1[(size_t)s * dh + m];
@@ -652,8 +767,12 @@ int oracle_ttt_mlp_dual(int B, int H, int L, int d, int dh, int mb, int ln, doub
                         }
                         A[(size_t)t * mb + s] = a;
                     }
+                cum = 0.0;
                 for (int t = 0; t < mb; ++t) {
-                    row_times(Xb2 + (size_t)t * dh, W2, b2, dh, d, Zb2 + (size_t)t * d);
+                    cum += en[t];
+                    row_times(Xb2 + (size_t)t * dh, W2, NULL, dh, d, Zb2 + (size_t)t * d);
+                    for (int j = 0; j < d; ++j)
+                        Zb2[(size_t)t * d + j] = (1.0 - wd * cum) * Zb2[(size_t)t * d + j] + b2[j];
                     for (int s = 0; s <= t; ++s)
                         for (int j = 0; j < d; ++j)
                             Zb2[(size_t)t * d + j] -= A[(size_t)t * mb + s] * G2[(size_t)s * d + j];
@@ -665,7 +784,11 @@ int oracle_ttt_mlp_dual(int B, int H, int L, int d, int dh, int mb, int ln, doub
                         memcpy(zo, Zb2 + (size_t)t * d, sizeof(double) * (size_t)d);
                     }
                 }
-                /* carry */
+                /* carry (cum is now the mini-batch's sum of eta) */
+                for (size_t i = 0; i < n1; ++i) {
+                    W1[i] *= 1.0 - wd * cum;
+                    W2[i] *= 1.0 - wd * cum;
+                }
                 for (int s = 0; s < mb; ++s) {
                     for (int i = 0; i < d; ++i) {
                         double ks = en[s] * Kn[(size_t)s * d + i];
@@ -688,4 +811,16 @@ int oracle_ttt_mlp_dual(int B, int H, int L, int d, int dh, int mb, int ln, doub
     free(W1); free(W2); free(b1); free(b2); free(Z1); free(X2); free(Z2); free(G1);
     free(G2); free(Zb1); free(Xb2); free(Zb2); free(A); free(y);
     return ORACLE_OK;
+}
+
+int oracle_ttt_mlp_dual(int B, int H, int L, int d, int dh, int mb, int ln, double eps,
+                        int init_per_batch, const double *Q, const double *K,
+                        const double *V, const double *eta, const double *W1_0,
+                        const double *b1_0, const double *W2_0, const double *b2_0,
+                        const double *gamma, const double *beta, double *Z, double *W1_f,
+                        double *b1_f, double *W2_f, double *b2_f)
+{
+    return oracle_ttt_mlp_dual_v(B, H, L, d, dh, mb, ln, eps, init_per_batch, 0, 0.0, Q, K, V,
+                                 eta, W1_0, b1_0, W2_0, b2_0, gamma, beta, Z, W1_f, b1_f, W2_f,
+                                 b2_f);
 }

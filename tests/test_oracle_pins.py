@@ -52,14 +52,14 @@ def rand_problem(rng, B=1, H=2, L=32, d=8, ln=False, mlp=False, dh=None, eta_sca
     return p
 
 
-def run_linear(p, mb, ln, dual=False, eps=1e-6):
+def run_linear(p, mb, ln, dual=False, eps=1e-6, **kw):
     return oracle.ttt_linear(p["Q"], p["K"], p["V"], p["eta"], p["W0"], p["b0"], p["gamma"],
-                             p["beta"], mini_batch=mb, ln=ln, eps=eps, dual=dual)
+                             p["beta"], mini_batch=mb, ln=ln, eps=eps, dual=dual, **kw)
 
 
-def run_mlp(p, mb, ln, dual=False, eps=1e-6):
+def run_mlp(p, mb, ln, dual=False, eps=1e-6, **kw):
     return oracle.ttt_mlp(p["Q"], p["K"], p["V"], p["eta"], p["W1"], p["b1"], p["W2"], p["b2"],
-                          p["gamma"], p["beta"], mini_batch=mb, ln=ln, eps=eps, dual=dual)
+                          p["gamma"], p["beta"], mini_batch=mb, ln=ln, eps=eps, dual=dual, **kw)
 
 
 # ---------------------------------------------------------------------------
@@ -81,10 +81,11 @@ def torch_f_mlp(x, W1, b1, W2, b2, ln, g, b, eps):
     return x + _ln(z2, g, b, eps) if ln else z2
 
 
-def brute_force(p, mb, ln, mlp, eps=1e-6):
+def brute_force(p, mb, ln, mlp, eps=1e-6, loss="mse", wd=0.0):
     """Mini-batch TTT from the definition: at each mini-batch start take every
-    token's gradient of 1/2||f(k_s) - v_s||^2 (autograd), then apply the
-    updates token by token and read the output with the updated weights."""
+    token's gradient of its loss (autograd) -- 1/2||f(k_s) - v_s||^2 or -<f(k_s), v_s>,
+    plus 1/2 wd ||W||^2 over the weight matrices -- then apply the updates token by
+    token and read the output with the updated weights."""
     T = lambda a: None if a is None else torch.tensor(a)
     Q, K, V, eta = T(p["Q"]), T(p["K"]), T(p["V"]), T(p["eta"])
     B, H, L, d = Q.shape
@@ -103,10 +104,13 @@ def brute_force(p, mb, ln, mlp, eps=1e-6):
             for n0 in range(0, L, mb):
                 start = [w.clone().requires_grad_(True) for w in params]
                 grads = []
+                mats = [start[0], start[2]] if mlp else [start[0]]
                 for s in range(mb):
                     k, v = K[bi, hi, n0 + s], V[bi, hi, n0 + s]
-                    loss = 0.5 * ((f(k, start) - v) ** 2).sum()
-                    grads.append(torch.autograd.grad(loss, start))
+                    fk = f(k, start)
+                    lo = 0.5 * ((fk - v) ** 2).sum() if loss == "mse" else -(fk * v).sum()
+                    lo = lo + 0.5 * wd * sum((w ** 2).sum() for w in mats)
+                    grads.append(torch.autograd.grad(lo, start))
                 cur = [w.detach().clone() for w in start]
                 for t in range(mb):
                     e = eta[bi, hi, n0 + t]
@@ -439,3 +443,115 @@ def test_gate_symmetry_and_saturation():
                           np.ones((1, 1)), 0.5)
     assert np.isfinite(big).all()
     np.testing.assert_allclose(big[0, 0], [0.5, 0.0], atol=1e-300)
+
+
+
+# --------------------------------------------------------------------------
+# inner-learner variants (ai-feeds "Modular TTT" page, method overview): the loss
+# (1/2 ||f(k) - v||^2 or the inner product -<f(k), v>) and weight decay
+# --------------------------------------------------------------------------
+
+VARIANTS = [("ip", 0.0), ("mse", 0.3), ("ip", 0.3)]
+
+
+@pytest.mark.parametrize("loss,wd", VARIANTS)
+@pytest.mark.parametrize("ln", [False, True])
+@pytest.mark.parametrize("mb", [1, 4])
+def test_linear_variants_match_autograd_brute_force(loss, wd, ln, mb):
+    rng = np.random.default_rng(81 + mb + 10 * ln + 100 * (loss == "ip"))
+    p = rand_problem(rng, B=1, H=2, L=16, d=6, ln=ln)
+    Z, Wf, bf = run_linear(p, mb, ln, loss=loss, weight_decay=wd)
+    Zr, fin = brute_force(p, mb, ln, mlp=False, loss=loss, wd=wd)
+    np.testing.assert_allclose(Z, Zr, rtol=1e-10, atol=1e-11)
+    for idx, (W, c) in enumerate(fin):
+        np.testing.assert_allclose(Wf[0, idx], W, rtol=1e-10, atol=1e-11)
+        np.testing.assert_allclose(bf[0, idx], c, rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("loss,wd", VARIANTS)
+@pytest.mark.parametrize("ln", [False, True])
+def test_mlp_variants_match_autograd_brute_force(loss, wd, ln):
+    rng = np.random.default_rng(91 + 10 * ln + 100 * (loss == "ip"))
+    p = rand_problem(rng, B=1, H=2, L=8, d=4, ln=ln, mlp=True, dh=16)
+    Z, W1f, b1f, W2f, b2f = run_mlp(p, 4, ln, loss=loss, weight_decay=wd)
+    Zr, fin = brute_force(p, 4, ln, mlp=True, loss=loss, wd=wd)
+    np.testing.assert_allclose(Z, Zr, rtol=1e-9, atol=1e-11)
+    for idx, (W1, b1, W2, b2) in enumerate(fin):
+        np.testing.assert_allclose(W1f[0, idx], W1, rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(W2f[0, idx], W2, rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(b1f[0, idx], b1, rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(b2f[0, idx], b2, rtol=1e-9, atol=1e-11)
+
+
+@pytest.mark.parametrize("loss,wd", VARIANTS)
+@pytest.mark.parametrize("ln", [False, True])
+def test_variants_primal_equals_dual(loss, wd, ln):
+    rng = np.random.default_rng(101 + 10 * ln)
+    p = rand_problem(rng, B=1, H=2, L=32, d=8, ln=ln)
+    for a, b in zip(run_linear(p, 8, ln, loss=loss, weight_decay=wd),
+                    run_linear(p, 8, ln, dual=True, loss=loss, weight_decay=wd)):
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+    q = rand_problem(rng, B=1, H=1, L=16, d=4, ln=ln, mlp=True, dh=8)
+    for a, b in zip(run_mlp(q, 4, ln, loss=loss, weight_decay=wd),
+                    run_mlp(q, 4, ln, dual=True, loss=loss, weight_decay=wd)):
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("mb", [1, 4, 16])
+def test_inner_product_loss_is_causal_linear_attention(mb):
+    """With the inner-product loss and no LayerNorm the gradient is -v whatever the
+    weights, so from W0 = 0, b0 = 0 every mini-batch size gives
+    z_t = sum_{s <= t} eta_s (q_t . k_s + 1) v_s over the whole sequence."""
+    rng = np.random.default_rng(111)
+    p = rand_problem(rng, B=1, H=2, L=32, d=5)
+    p["W0"] = np.zeros_like(p["W0"])
+    p["b0"] = np.zeros_like(p["b0"])
+    Z, Wf, bf = run_linear(p, mb, False, loss="ip")
+    for h in range(2):
+        Q, K, V, e = p["Q"][0, h], p["K"][0, h], p["V"][0, h], p["eta"][0, h]
+        A = np.tril((Q @ K.T + 1.0) * e[None, :])
+        np.testing.assert_allclose(Z[0, h], A @ V, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(Wf[0, h], K.T @ (e[:, None] * V), rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(bf[0, h], e @ V, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("mb", [1, 4])
+def test_weight_decay_with_zero_keys(mb):
+    """With all keys zero the gradient part of the weight update vanishes, so weight decay
+    alone shrinks W by 1 - lambda * (sum of the mini-batch's eta) per mini-batch."""
+    rng = np.random.default_rng(121)
+    p = rand_problem(rng, B=1, H=1, L=16, d=4)
+    p["K"] = np.zeros_like(p["K"])
+    lam = 0.7
+    _, Wf, _ = run_linear(p, mb, False, weight_decay=lam)
+    e = p["eta"][0, 0]
+    factor = np.prod([1.0 - lam * e[n:n + mb].sum() for n in range(0, 16, mb)])
+    np.testing.assert_allclose(Wf[0, 0], factor * p["W0"][0], rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("ln", [False, True])
+def test_inner_product_gradients_by_finite_differences(ln):
+    rng = np.random.default_rng(131 + ln)
+    d, dh, h = 5, 7, 1e-6
+    k, v = rng.standard_normal(d), rng.standard_normal(d)
+    W, c = rng.standard_normal((d, d)) * 0.4, rng.standard_normal(d) * 0.1
+    gm, bt = 1.0 + 0.2 * rng.standard_normal(d), 0.1 * rng.standard_normal(d)
+    kw = dict(ln=ln, gamma=gm, beta=bt, loss="ip")
+    gW, gc = oracle.linear_token_grad(k, v, W, c, **kw)
+    for (i, j) in [(0, 0), (2, 3), (4, 1)]:
+        Wp, Wm = W.copy(), W.copy()
+        Wp[i, j] += h
+        Wm[i, j] -= h
+        fd = (oracle.linear_token_loss(k, v, Wp, c, **kw) - oracle.linear_token_loss(k, v, Wm, c, **kw)) / (2 * h)
+        assert abs(fd - gW[i, j]) <= 1e-6 * max(1.0, abs(fd))
+    W1, b1 = rng.standard_normal((d, dh)) * 0.4, rng.standard_normal(dh) * 0.1
+    W2, b2 = rng.standard_normal((dh, d)) * 0.4, rng.standard_normal(d) * 0.1
+    g1, _, g2, _ = oracle.mlp_token_grad(k, v, W1, b1, W2, b2, **kw)
+    for (M, G, ij) in [(W1, g1, (1, 2)), (W2, g2, (3, 4))]:
+        Mp, Mm = M.copy(), M.copy()
+        Mp[ij] += h
+        Mm[ij] -= h
+        args_p = (W1 if M is not W1 else Mp, b1, W2 if M is not W2 else Mp, b2)
+        args_m = (W1 if M is not W1 else Mm, b1, W2 if M is not W2 else Mm, b2)
+        fd = (oracle.mlp_token_loss(k, v, *args_p, **kw) - oracle.mlp_token_loss(k, v, *args_m, **kw)) / (2 * h)
+        assert abs(fd - G[ij]) <= 1e-6 * max(1.0, abs(fd))
