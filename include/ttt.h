@@ -90,7 +90,17 @@ typedef struct {
      * the result of one call on all rows. */
     int bh_offset;
     int bh_count;
+    /* inner learner (the design dimensions of the ai-feeds "Modular TTT" page):
+     * loss TTT_LOSS_MSE (1/2 ||f(k) - v||^2, the default) or TTT_LOSS_INNER_PRODUCT
+     * (-<f(k), v>); weight_decay lambda >= 0 adds 1/2 lambda ||W||^2 over the weight
+     * matrices (W; W1, W2 -- not the biases) to every token's loss, taken at the
+     * mini-batch's starting weights like the gradient: inside a mini-batch
+     * W_t = (1 - lambda sum_{s<=t} eta_s) W_start - sum_{s<=t} eta_s grad l_s. */
+    int loss;
+    float weight_decay;
 } ttt_desc;
+
+enum { TTT_LOSS_MSE = 0, TTT_LOSS_INNER_PRODUCT = 1 };
 
 /*
  * TTT-Linear forward.
@@ -100,7 +110,7 @@ typedef struct {
  *        token t's update; W_final [B,H,d,d], b_final [B,H,d]: state after
  *        the last mini-batch.
  * Supported: any d <= 128 and b <= 64 (generic kernels, fp32 arithmetic);
- * bf16 I/O with d = 64, b = 16 runs the tensor-core kernel.
+ * bf16 I/O with d = 64, b = 16 runs the tensor-core kernel (every loss and decay).
  */
 TTT_API ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
                           const float *eta, const float *W0, const float *b0,
@@ -112,7 +122,9 @@ TTT_API ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const voi
  *   in : Q, K, V, eta as above; W1_0 [H or B,H, d, dh]; b1_0 [H or B,H, dh];
  *        W2_0 [H or B,H, dh, d]; b2_0 [H or B,H, d]; gamma, beta [H, d].
  *   out: Z [B,H,L,d]; W1_f [B,H,d,dh]; b1_f [B,H,dh]; W2_f [B,H,dh,d]; b2_f [B,H,d].
- * Supported: d <= 128, dh <= 512, b <= 64 while the state fits on chip.
+ * Supported: d <= 128, dh <= 512, b <= 64 while the state fits on chip; the
+ * tensor-core kernel (bf16, d = 64, dh = 256, b = 16) runs the default learner
+ * (MSE loss, no weight decay), the generic kernel every variant.
  */
 TTT_API ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
                        const float *eta, const float *W1_0, const float *b1_0,
@@ -193,7 +205,8 @@ TTT_API const char *ttt_last_error(void);
  * (is_mlp = 0 or 1), or NULL when the descriptor is rejected. */
 TTT_API const char *ttt_kernel_name(const ttt_desc *desc, int is_mlp);
 
-/* Library ABI version (major * 100 + minor); 101 added bh_offset/bh_count. */
+/* Library ABI version (major * 100 + minor); 101 added bh_offset/bh_count, 102 loss and
+ * weight_decay. */
 TTT_API int ttt_version(void);
 
 #ifdef __cplusplus

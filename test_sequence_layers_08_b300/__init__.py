@@ -8,6 +8,7 @@ library has not been built, or the GPU is missing, calls raise.
 Functions mirror the C entry points:
     ttt_eta_gate(x, theta, eta_base) -> eta
     ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma, beta, ...) -> (Z, W_final, b_final)
+      (every entry point takes loss="mse"|"ip" and weight_decay=lambda)
     ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma, beta, ...) -> (Z, W1_f, b1_f, W2_f, b2_f)
     ttt_sync_status(stream=None)
     kernel_name(...)
@@ -43,7 +44,10 @@ class Desc(ctypes.Structure):
                 ("d", ctypes.c_int), ("d_hidden", ctypes.c_int), ("mini_batch", ctypes.c_int),
                 ("io_dtype", ctypes.c_int), ("residual_ln", ctypes.c_int),
                 ("ln_eps", ctypes.c_float), ("init_per_batch", ctypes.c_int),
-                ("bh_offset", ctypes.c_int), ("bh_count", ctypes.c_int)]
+                ("bh_offset", ctypes.c_int), ("bh_count", ctypes.c_int),
+                ("loss", ctypes.c_int), ("weight_decay", ctypes.c_float)]
+
+LOSSES = {"mse": 0, "ip": 1}   # 1/2 ||f(k) - v||^2, or the inner product -<f(k), v>
 
 
 def library_path() -> str:
@@ -107,16 +111,20 @@ def _stream_handle(stream):
 
 
 def make_desc(Q, mini_batch: int, residual_ln: bool, ln_eps: float = 1e-6,
-              init_per_batch: bool = False, d_hidden: int = 0, heads=None, bh_offset: int = 0) -> Desc:
+              init_per_batch: bool = False, d_hidden: int = 0, heads=None, bh_offset: int = 0,
+              loss: str = "mse", weight_decay: float = 0.0) -> Desc:
     """Descriptor of a call on Q [B, H, L, d], or on the row form Q [rows, L, d] covering rows
-    bh_offset .. bh_offset + rows - 1 of a (batch, head) grid with `heads` heads."""
+    bh_offset .. bh_offset + rows - 1 of a (batch, head) grid with `heads` heads.  loss: "mse"
+    or "ip" (inner product); weight_decay: lambda on the weight matrices."""
     import torch
     io = {torch.float32: TTT_F32, torch.bfloat16: TTT_BF16}.get(Q.dtype)
     if io is None:
         raise TypeError(f"unsupported I/O dtype {Q.dtype}")
     lead, H, L, d, B, off, cnt = _geometry(Q, heads, bh_offset)
+    if loss not in LOSSES:
+        raise ValueError(f"loss must be one of {sorted(LOSSES)}")
     return Desc(B, H, L, d, d_hidden, mini_batch, io, int(residual_ln), float(ln_eps),
-                int(init_per_batch), off, cnt)
+                int(init_per_batch), off, cnt, LOSSES[loss], float(weight_decay))
 
 
 def partition_rows(total_rows: int, world: int, rank: int):
@@ -198,7 +206,8 @@ def _require_cuda(dev):
 
 def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: int = 16,
                    residual_ln: bool = False, ln_eps: float = 1e-6, init_per_batch: bool = False,
-                   out=None, stream=None, heads=None, bh_offset: int = 0):
+                   out=None, stream=None, heads=None, bh_offset: int = 0, loss: str = "mse",
+                   weight_decay: float = 0.0):
     """TTT-Linear forward on the GPU.  Q,K,V: [B,H,L,d] (float32 or bfloat16);
     eta [B,H,L] float32; W0 [H,d,d] (or [B,H,d,d] with init_per_batch); b0 [H,d]
     (or [B,H,d]); gamma, beta [H,d] float32 (residual LayerNorm only).  Returns
@@ -221,7 +230,7 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: i
     _require_cuda(dev)
     lib = load()
     desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, heads=heads,
-                     bh_offset=bh_offset)
+                     bh_offset=bh_offset, loss=loss, weight_decay=weight_decay)
     if out is None:
         out = (torch.empty_like(Q), torch.empty(lead + (d, d), device=dev, dtype=torch.float32),
                torch.empty(lead + (d,), device=dev, dtype=torch.float32))
@@ -234,7 +243,8 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: i
 
 
 def ttt_linear_step(Q, K, V, eta, W, b, gamma=None, beta=None, *, residual_ln: bool = False,
-                    ln_eps: float = 1e-6, out=None, stream=None, heads=None, bh_offset: int = 0):
+                    ln_eps: float = 1e-6, out=None, stream=None, heads=None, bh_offset: int = 0,
+                    loss: str = "mse", weight_decay: float = 0.0):
     """TTT-Linear decode on the GPU: the L tokens of Q, K, V [B,H,L,d] one at a time from
     the state W [B,H,d,d], b [B,H,d] (float32), which is updated in place.  Returns Z
     [B,H,L,d]; pass ``out=Z`` to reuse a buffer.  Row form as for ttt_linear_fwd (the state
@@ -247,7 +257,8 @@ def ttt_linear_step(Q, K, V, eta, W, b, gamma=None, beta=None, *, residual_ln: b
         _expect("out Z", out, lead + (L, d), Q.dtype, dev)
     _require_cuda(dev)
     lib = load()
-    desc = make_desc(Q, 1, residual_ln, ln_eps, True, heads=heads, bh_offset=bh_offset)
+    desc = make_desc(Q, 1, residual_ln, ln_eps, True, heads=heads, bh_offset=bh_offset, loss=loss,
+                     weight_decay=weight_decay)
     Z = torch.empty_like(Q) if out is None else out
     _check(lib.ttt_linear_step(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta), _ptr(W),
                                _ptr(b), _ptr(gamma if residual_ln else None),
@@ -257,7 +268,8 @@ def ttt_linear_step(Q, K, V, eta, W, b, gamma=None, beta=None, *, residual_ln: b
 
 def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_batch: int = 16,
                 residual_ln: bool = False, ln_eps: float = 1e-6, init_per_batch: bool = False,
-                out=None, stream=None, heads=None, bh_offset: int = 0):
+                out=None, stream=None, heads=None, bh_offset: int = 0, loss: str = "mse",
+                weight_decay: float = 0.0):
     """TTT-MLP forward on the GPU.  W1 [H,d,dh], b1 [H,dh], W2 [H,dh,d], b2 [H,d]
     (leading B when init_per_batch).  Returns (Z, W1_f, b1_f, W2_f, b2_f).  Row form as for
     ttt_linear_fwd.  Every operand is checked before the C call."""
@@ -281,7 +293,7 @@ def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_bat
     _require_cuda(dev)
     lib = load()
     desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, d_hidden=dh, heads=heads,
-                     bh_offset=bh_offset)
+                     bh_offset=bh_offset, loss=loss, weight_decay=weight_decay)
     if out is None:
         f32 = dict(device=dev, dtype=torch.float32)
         out = (torch.empty_like(Q), torch.empty(lead + (d, dh), **f32), torch.empty(lead + (dh,), **f32),

@@ -66,6 +66,10 @@ ttt_status check_desc(const ttt_desc *s, bool mlp)
     if (mlp && s->d_hidden < 0) return fail(TTT_ERR_INVALID_ARG, "d_hidden must be >= 0");
     if ((long long)s->B * s->H > 0x7fffffffLL)
         return fail(TTT_ERR_INVALID_ARG, "B * H exceeds the grid limit");
+    if (s->loss != TTT_LOSS_MSE && s->loss != TTT_LOSS_INNER_PRODUCT)
+        return fail(TTT_ERR_INVALID_ARG, "loss must be TTT_LOSS_MSE or TTT_LOSS_INNER_PRODUCT");
+    if (!(std::isfinite(s->weight_decay) && s->weight_decay >= 0.f))
+        return fail(TTT_ERR_INVALID_ARG, "weight_decay must be finite and >= 0");
     if (s->bh_offset < 0 || s->bh_count < 0)
         return fail(TTT_ERR_INVALID_ARG, "bh_offset and bh_count must be >= 0");
     if (s->bh_count == 0 && s->bh_offset != 0)
@@ -129,7 +133,7 @@ const char *mlp_kernel(const ttt_desc &s)
 
 extern "C" {
 
-int ttt_version(void) { return 101; }
+int ttt_version(void) { return 102; }
 
 const char *ttt_status_string(ttt_status s)
 {

@@ -12,6 +12,10 @@
 //   o = q_t W + c,   Z_t = o   or   Z_t = q_t + LN(o)
 // with LNbwd the gradient of 1/2 |gamma xhat + beta - y|^2, xhat = (z - mu) r, through the
 // LayerNorm: g = r (gx - mean(gx) - xhat mean(gx xhat)), gx = gamma (gamma xhat + beta - y).
+// The inner-learner variants of the ai-feeds Modular TTT page: with the inner-product loss
+// -<f(k), v>, g = -v (plain) or the LayerNorm backward of the upstream -v (gx = -gamma v);
+// with weight decay lambda the update is W <- (1 - eta_t lambda) W - eta_t k_t^T g (the bias
+// is not decayed).
 //
 // B300 design.  A decode step is a chain of 64 x 64 matrix-vector products on a 16 KB state
 // per (batch, head): latency- and launch-bound work that suits FP32 FMA, not tensor cores.
@@ -37,6 +41,8 @@ constexpr int kWarps = 4;
 struct DecodeParams {
     int BH, H, T, hoff;
     float eps;
+    int ip;       // inner-product loss
+    float wd;     // weight decay lambda
     const void *Q, *K, *V;
     const float *eta;
     float *W, *b;
@@ -162,30 +168,31 @@ linear_decode_kernel(DecodeParams p)
             const float zc0 = z0 - mu, zc1 = z1 - mu;
             const float r = rsqrtf(warp_sum(fmaf(zc0, zc0, zc1 * zc1)) * (1.f / D) + p.eps);
             const float xh0 = zc0 * r, xh1 = zc1 * r;
-            const float gx0 = ga0 * (fmaf(ga0, xh0, be0) - (v.x - k.x));
-            const float gx1 = ga1 * (fmaf(ga1, xh1, be1) - (v.y - k.y));
+            const float gx0 = p.ip ? -ga0 * v.x : ga0 * (fmaf(ga0, xh0, be0) - (v.x - k.x));
+            const float gx1 = p.ip ? -ga1 * v.y : ga1 * (fmaf(ga1, xh1, be1) - (v.y - k.y));
             const float2 m = warp_sum2(gx0 + gx1, fmaf(gx0, xh0, gx1 * xh1));
             const float m1 = m.x * (1.f / D), m2 = m.y * (1.f / D);
             g0 = r * (gx0 - m1 - xh0 * m2);
             g1 = r * (gx1 - m1 - xh1 * m2);
         } else {
-            g0 = z0 - v.x;
-            g1 = z1 - v.y;
+            g0 = p.ip ? -v.x : z0 - v.x;
+            g1 = p.ip ? -v.y : z1 - v.y;
         }
 
-        // W -= eta k^T g,  c -= eta g
+        // W <- (1 - eta lambda) W - eta k^T g,  c -= eta g   (the factor is 1 without decay)
         const float eg0 = et * g0, eg1 = et * g1;
+        const float dec = 1.f - et * p.wd;
 #pragma unroll
         for (int i4 = 0; i4 < D / 4; ++i4) {
             const float4 x = rows[warp][1][i4];
-            w[4 * i4][0] = fmaf(-eg0, x.x, w[4 * i4][0]);
-            w[4 * i4][1] = fmaf(-eg1, x.x, w[4 * i4][1]);
-            w[4 * i4 + 1][0] = fmaf(-eg0, x.y, w[4 * i4 + 1][0]);
-            w[4 * i4 + 1][1] = fmaf(-eg1, x.y, w[4 * i4 + 1][1]);
-            w[4 * i4 + 2][0] = fmaf(-eg0, x.z, w[4 * i4 + 2][0]);
-            w[4 * i4 + 2][1] = fmaf(-eg1, x.z, w[4 * i4 + 2][1]);
-            w[4 * i4 + 3][0] = fmaf(-eg0, x.w, w[4 * i4 + 3][0]);
-            w[4 * i4 + 3][1] = fmaf(-eg1, x.w, w[4 * i4 + 3][1]);
+            w[4 * i4][0] = fmaf(-eg0, x.x, dec * w[4 * i4][0]);
+            w[4 * i4][1] = fmaf(-eg1, x.x, dec * w[4 * i4][1]);
+            w[4 * i4 + 1][0] = fmaf(-eg0, x.y, dec * w[4 * i4 + 1][0]);
+            w[4 * i4 + 1][1] = fmaf(-eg1, x.y, dec * w[4 * i4 + 1][1]);
+            w[4 * i4 + 2][0] = fmaf(-eg0, x.z, dec * w[4 * i4 + 2][0]);
+            w[4 * i4 + 2][1] = fmaf(-eg1, x.z, dec * w[4 * i4 + 2][1]);
+            w[4 * i4 + 3][0] = fmaf(-eg0, x.w, dec * w[4 * i4 + 3][0]);
+            w[4 * i4 + 3][1] = fmaf(-eg1, x.w, dec * w[4 * i4 + 3][1]);
         }
         c0 -= eg0;
         c1 -= eg1;
@@ -220,8 +227,8 @@ cudaError_t launch_linear_decode(const DecodeArgs &a)
 {
     const ttt_desc &d = a.desc;
     const int BH = call_rows(d);
-    DecodeParams p{BH, d.H, d.L, head_offset(d), d.ln_eps, a.Q, a.K, a.V, a.eta, a.W, a.b, a.gamma,
-                   a.beta, a.Z};
+    DecodeParams p{BH, d.H, d.L, head_offset(d), d.ln_eps, d.loss == TTT_LOSS_INNER_PRODUCT,
+                   d.weight_decay, a.Q, a.K, a.V, a.eta, a.W, a.b, a.gamma, a.beta, a.Z};
     const int grid = (BH + kWarps - 1) / kWarps;
     const bool bf16 = d.io_dtype == TTT_BF16;
     if (bf16 && d.residual_ln)

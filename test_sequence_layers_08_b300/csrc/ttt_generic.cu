@@ -85,6 +85,37 @@ __device__ void ln_l2_bwd_row(float *z, const float *v, const float *k, const fl
     __syncwarp();
 }
 
+// In place: z <- d/dz of -< q + gamma * norm(z) + beta, v > (inner-product loss).
+__device__ void ln_ip_bwd_row(float *z, const float *v, const float *gam, int d, float eps)
+{
+    const int lane = threadIdx.x & 31;
+    float mu, r;
+    row_stats(z, d, eps, mu, r);
+    float m1 = 0.f, m2 = 0.f;
+    for (int j = lane; j < d; j += 32) {
+        float xh = (z[j] - mu) * r;
+        float gx = -gam[j] * v[j];
+        m1 += gx;
+        m2 += gx * xh;
+    }
+    m1 = warp_sum(m1) / d;
+    m2 = warp_sum(m2) / d;
+    __syncwarp();
+    for (int j = lane; j < d; j += 32) {
+        float xh = (z[j] - mu) * r;
+        z[j] = r * (-gam[j] * v[j] - m1 - xh * m2);
+    }
+    __syncwarp();
+}
+
+// Sum of eta over tokens 0..t of the staged mini-batch.
+__device__ __forceinline__ float eta_prefix(const float *et, int t)
+{
+    float a = 0.f;
+    for (int s = 0; s <= t; ++s) a += et[s];
+    return a;
+}
+
 // out_row = q + gamma * norm(z) + beta, written to global in the I/O type.
 template <typename IO>
 __device__ void ln_out_row(const float *z, const float *q, const float *gam,
@@ -125,6 +156,8 @@ __device__ float shift_by_mean(float *v, int n)
 struct LinearParams {
     int H, L, d, mb, ln, init_per_batch;
     float eps;
+    int ip;                  // inner-product loss
+    float wd;                // weight decay lambda
     const void *Q, *K, *V;
     const float *eta, *W0, *b0, *gamma, *beta;
     void *Z;
@@ -185,10 +218,11 @@ __global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p
         }
         for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
         __syncthreads();
-        // key- and query-side products at the mini-batch's starting weights
+        // key- and query-side products at the mini-batch's starting weights; with weight
+        // decay the query row t sees (1 - lambda sum_{s<=t} eta_s) W_start
         for (int i = tid; i < nt; i += kThreads) {
             const int s = i / d, j = i - s * d;
-            float ak = c[j], aq = c[j];
+            float ak = c[j], aq = 0.f;
             const float *kr = Kt + s * d, *qr = Qt + s * d;
             for (int u = 0; u < d; ++u) {
                 const float w = W[u * d + j];
@@ -196,7 +230,7 @@ __global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p
                 aq = fmaf(qr[u], w, aq);
             }
             G[i] = ak;
-            Zb[i] = aq;
+            Zb[i] = fmaf(1.f - p.wd * eta_prefix(et, s), aq, c[j]);
         }
         for (int i = tid; i < mb * mb; i += kThreads) {
             const int t = i / mb, s = i - t * mb;
@@ -210,10 +244,14 @@ __global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p
         }
         __syncthreads();
         if (LN) {
-            for (int s = warp; s < mb; s += kWarps)
-                ln_l2_bwd_row(G + s * d, Vt + s * d, Kt + s * d, gam, bet, d, p.eps);
+            for (int s = warp; s < mb; s += kWarps) {
+                if (p.ip)
+                    ln_ip_bwd_row(G + s * d, Vt + s * d, gam, d, p.eps);
+                else
+                    ln_l2_bwd_row(G + s * d, Vt + s * d, Kt + s * d, gam, bet, d, p.eps);
+            }
         } else {
-            for (int i = tid; i < nt; i += kThreads) G[i] -= Vt[i];
+            for (int i = tid; i < nt; i += kThreads) G[i] = p.ip ? -Vt[i] : G[i] - Vt[i];
         }
         __syncthreads();
         // dual-form outputs
@@ -226,12 +264,13 @@ __global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p
             else
                 store_io(Zg, (size_t)(n0 + t) * d + j, z);
         }
-        // carry: W -= K^T diag(eta) G, c -= eta^T G
+        // carry: W <- (1 - lambda sum eta) W - K^T diag(eta) G, c -= eta^T G
+        const float decay = 1.f - p.wd * eta_prefix(et, mb - 1);
         for (int i = tid; i < d * d; i += kThreads) {
             const int u = i / d, j = i - u * d;
             float acc = 0.f;
             for (int s = 0; s < mb; ++s) acc = fmaf(et[s] * Kt[s * d + u], G[s * d + j], acc);
-            W[i] -= acc;
+            W[i] = fmaf(decay, W[i], -acc);
         }
         for (int j = tid; j < d; j += kThreads) {
             float acc = 0.f;
@@ -255,6 +294,8 @@ __global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p
 struct MlpParams {
     int H, L, d, dh, mb, ln, init_per_batch;
     float eps;
+    int ip;                  // inner-product loss
+    float wd;                // weight decay lambda
     const void *Q, *K, *V;
     const float *eta, *W1, *b1, *W2, *b2, *gamma, *beta;
     void *Z;
@@ -321,7 +362,7 @@ __global__ void __launch_bounds__(kThreads) mlp_generic_kernel(MlpParams p)
         // first layer at the starting weights, key and query side
         for (int i = tid; i < nh; i += kThreads) {
             const int s = i / dh, m = i - s * dh;
-            float ak = b1[m], aq = b1[m];
+            float ak = b1[m], aq = 0.f;
             for (int u = 0; u < d; ++u) {
                 const float w = W1[u * dh + m];
                 ak = fmaf(Kt[s * d + u], w, ak);
@@ -329,7 +370,7 @@ __global__ void __launch_bounds__(kThreads) mlp_generic_kernel(MlpParams p)
             }
             Z1[i] = ak;
             X2[i] = gelu_tanh(ak);
-            Zb1[i] = aq;
+            Zb1[i] = fmaf(1.f - p.wd * eta_prefix(et, s), aq, b1[m]);
         }
         for (int i = tid; i < mb * mb; i += kThreads) {
             const int t = i / mb, s = i - t * mb;
@@ -350,10 +391,14 @@ __global__ void __launch_bounds__(kThreads) mlp_generic_kernel(MlpParams p)
         }
         __syncthreads();
         if (LN) {
-            for (int s = warp; s < mb; s += kWarps)
-                ln_l2_bwd_row(Z2 + s * d, Vt + s * d, Kt + s * d, gam, bet, d, p.eps);
+            for (int s = warp; s < mb; s += kWarps) {
+                if (p.ip)
+                    ln_ip_bwd_row(Z2 + s * d, Vt + s * d, gam, d, p.eps);
+                else
+                    ln_l2_bwd_row(Z2 + s * d, Vt + s * d, Kt + s * d, gam, bet, d, p.eps);
+            }
         } else {
-            for (int i = tid; i < nt; i += kThreads) Z2[i] -= Vt[i];
+            for (int i = tid; i < nt; i += kThreads) Z2[i] = p.ip ? -Vt[i] : Z2[i] - Vt[i];
         }
         __syncthreads();
         // G1 = (G2 W2^T) * GELU'(Z1), in place over Z1; query side of layer 1
@@ -383,8 +428,9 @@ __global__ void __launch_bounds__(kThreads) mlp_generic_kernel(MlpParams p)
         __syncthreads();
         for (int i = tid; i < nt; i += kThreads) {
             const int t = i / d, j = i - t * d;
-            float z = b2[j];
+            float z = 0.f;
             for (int m = 0; m < dh; ++m) z = fmaf(Zb1[t * dh + m], W2[m * d + j], z);
+            z = fmaf(1.f - p.wd * eta_prefix(et, t), z, b2[j]);
             for (int s = 0; s <= t; ++s) z = fmaf(-A[t * mb + s], Z2[s * d + j], z);
             if (LN)
                 Zb2[i] = z;
@@ -392,18 +438,19 @@ __global__ void __launch_bounds__(kThreads) mlp_generic_kernel(MlpParams p)
                 store_io(Zg, (size_t)(n0 + t) * d + j, z);
         }
         __syncthreads();
-        // carry
+        // carry (weight decay scales W1 and W2 by 1 - lambda sum eta)
+        const float decay = 1.f - p.wd * eta_prefix(et, mb - 1);
         for (int i = tid; i < d * dh; i += kThreads) {
             const int u = i / dh, m = i - u * dh;
             float acc = 0.f;
             for (int s = 0; s < mb; ++s) acc = fmaf(et[s] * Kt[s * d + u], Z1[s * dh + m], acc);
-            W1[i] -= acc;
+            W1[i] = fmaf(decay, W1[i], -acc);
         }
         for (int i = tid; i < dh * d; i += kThreads) {
             const int m = i / d, j = i - m * d;
             float acc = 0.f;
             for (int s = 0; s < mb; ++s) acc = fmaf(et[s] * X2[s * dh + m], Z2[s * d + j], acc);
-            W2[i] -= acc;
+            W2[i] = fmaf(decay, W2[i], -acc);
         }
         for (int m = tid; m < dh; m += kThreads) {
             float acc = 0.f;
@@ -456,6 +503,7 @@ cudaError_t launch_linear_generic(const LinearArgs &a)
 {
     const ttt_desc &s = a.desc;
     LinearParams p{s.H, s.L, s.d, s.mini_batch, s.residual_ln, s.init_per_batch, s.ln_eps,
+                   s.loss == TTT_LOSS_INNER_PRODUCT, s.weight_decay,
                    a.Q, a.K, a.V, a.eta, a.W0, a.b0, a.gamma, a.beta, a.Z, a.W_final, a.b_final};
     p.hoff = head_offset(s);
     const size_t smem = linear_generic_smem_bytes(s);
@@ -480,6 +528,7 @@ cudaError_t launch_mlp_generic(const MlpArgs &a)
 {
     const ttt_desc &s = a.desc;
     MlpParams p{s.H, s.L, s.d, s.d_hidden, s.mini_batch, s.residual_ln, s.init_per_batch, s.ln_eps,
+                s.loss == TTT_LOSS_INNER_PRODUCT, s.weight_decay,
                 a.Q, a.K, a.V, a.eta, a.W1_0, a.b1_0, a.W2_0, a.b2_0, a.gamma, a.beta, a.Z,
                 a.W1_f, a.b1_f, a.W2_f, a.b2_f};
     p.hoff = head_offset(s);

@@ -36,6 +36,17 @@
 //     z^2, g^2 z, g^2 z^2, g b' z, g b' with b' = beta - v + k), all in fp32;
 //   * Z tiles are transposed back with stmatrix into a swizzled staging ring
 //     and written by TMA stores.
+// Inner-learner variants (ai-feeds Modular TTT page: loss and weight decay):
+//   * inner-product loss -<f(k), v>: G = -V, or the LayerNorm backward of the upstream
+//     -V; the kernel keeps one code path and zeroes the coefficients of the terms the
+//     loss does not have (gamma^2 xhat, beta, k);
+//   * weight decay lambda (W only, gradient at the mini-batch's start):
+//     W_{n+1} = (1 - lambda S_n) W_n - K_n^T diag(eta_n) G_n with S_n the mini-batch's
+//     sum of eta, and query token t reads (1 - lambda cum_t) W_n, cum_t the prefix sum
+//     of eta up to t.  So the carried W^T is scaled before the deferred update, the
+//     output product Y_n and the re-associated key product X_{n+1} are scaled per token
+//     around the bias, and the chain is otherwise unchanged (a template switch: the
+//     default learner pays none of it).
 // Every mbarrier wait is bounded; a wait that runs out sets the library's
 // failure flag and the kernel finishes without waiting again.
 #include <cuda.h>
@@ -87,6 +98,8 @@ struct Params {
     unsigned int *status;
     int init_per_batch;
     int hoff = 0;            // head index of row 0 of this call
+    int ip = 0;              // inner-product loss
+    float wd = 0.f;          // weight decay lambda (read by the WD instantiation)
 };
 
 // Bound of the final wait for copies still in flight (they land in microseconds).
@@ -105,7 +118,7 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, long long 
     return false;
 }
 
-template <bool LN>
+template <bool LN, bool WD>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmZ,
@@ -211,13 +224,17 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         ptx::named_bar(1, kMathThreads);
         const float4 w4 = *reinterpret_cast<const float4 *>(s.red[0][0]);
         const float4 p4 = *reinterpret_cast<const float4 *>(s.red[0][1]);
-        C1 = (w4.x + w4.y) + (w4.z + w4.w);
+        C1 = p.ip ? 0.f : (w4.x + w4.y) + (w4.z + w4.w);
         pivot = ((p4.x + p4.y) + (p4.z + p4.w)) * (1.f / D);
         cb0 -= pivot;
         cb1 -= pivot;
         ptx::named_bar(1, kMathThreads);
     }
-    const float g20 = ga0 * ga0, g21 = ga1 * ga1;
+    // LayerNorm backward coefficients: the squared-error loss has gx = gamma (gamma xhat +
+    // beta - v + k); the inner-product loss has gx = -gamma v (no gamma^2, beta or k term)
+    const float g20 = p.ip ? 0.f : ga0 * ga0, g21 = p.ip ? 0.f : ga1 * ga1;
+    const float bx0 = p.ip ? 0.f : be0, bx1 = p.ip ? 0.f : be1;
+    const float kf = p.ip ? 0.f : 1.f;   // weight of k in gx, and of P in the plain G
 
     uint32_t wa[4][4];   // bf16 A fragments of W^T, k-steps of 16 input features
     auto pack_w = [&]() {
@@ -419,6 +436,15 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // carried between steps: the previous step's -eta G (deferred W update), its output
     float zprev[2][4] = {}, qprev[2][4] = {};
     uint32_t ngep[4] = {0u, 0u, 0u, 0u};
+    float dprev = 1.f;   // weight decay: 1 - lambda S_{n-1}, the factor of the deferred update
+
+    // weight decay: scale the carried W^T by 1 - lambda S before the deferred update
+    auto decay_w = [&](float f) {
+#pragma unroll
+        for (int pt = 0; pt < 8; ++pt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wt[pt][i] *= f;
+    };
 
     for (int n = 0; n < N; ++n) {
         const int par = n & 1;
@@ -429,8 +455,33 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // input blocks of the next mini-batch (independent of the state)
         if (LN) compute_sfrag(n + 1);
         // deferred update with G_{n-1} (zero fragments at n = 0): W_n, then its bf16 copy
+        if (WD) decay_w(dprev);
         update_w(ngep, max(n - 1, 0));
         pack_w();
+        // weight decay: per-token factors 1 - lambda cum_t for this lane's tokens 8u + 2c + e
+        // (prefix sums of eta within the mini-batch by a scan over the 4 lanes sharing g)
+        float fq[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, dn = 1.f;
+        if (WD) {
+            const float a0 = eta_at(n, 2 * c), a1 = eta_at(n, 2 * c + 1);
+            const float b0 = eta_at(n, 2 * c + 8), b1 = eta_at(n, 2 * c + 9);
+            float ia = a0 + a1, ib = b0 + b1;
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                const float ta = __shfl_up_sync(0xffffffffu, ia, o, 4);
+                const float tb = __shfl_up_sync(0xffffffffu, ib, o, 4);
+                if (c >= o) {
+                    ia += ta;
+                    ib += tb;
+                }
+            }
+            const float ta = __shfl_sync(0xffffffffu, ia, 3, 4);   // sum over tokens 0..7
+            const float tb = __shfl_sync(0xffffffffu, ib, 3, 4);
+            fq[0][0] = 1.f - p.wd * (ia - a1);
+            fq[0][1] = 1.f - p.wd * ia;
+            fq[1][0] = 1.f - p.wd * (ta + ib - b1);
+            fq[1][1] = 1.f - p.wd * (ta + ib);
+            dn = 1.f - p.wd * (ta + tb);
+        }
         // products from W_n: output Y_n = W_n^T Q_n^T + c_n, and the key product of the
         // next mini-batch (clamped at the end: unused)
         float yacc[2][4], xacc[2][4];
@@ -448,10 +499,10 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // b'_j = beta_j - (v - k); gb = gamma * b'
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                gb[u][0] = ga0 * (be0 - vt[u][0] + kt[u][0]);
-                gb[u][1] = ga0 * (be0 - vt[u][1] + kt[u][1]);
-                gb[u][2] = ga1 * (be1 - vt[u][2] + kt[u][2]);
-                gb[u][3] = ga1 * (be1 - vt[u][3] + kt[u][3]);
+                gb[u][0] = ga0 * fmaf(kt[u][0], kf, bx0 - vt[u][0]);
+                gb[u][1] = ga0 * fmaf(kt[u][1], kf, bx0 - vt[u][1]);
+                gb[u][2] = ga1 * fmaf(kt[u][2], kf, bx1 - vt[u][2]);
+                gb[u][3] = ga1 * fmaf(kt[u][3], kf, bx1 - vt[u][3]);
             }
             // per-token partial sums over this thread's two features
             float vs[24];
@@ -552,7 +603,7 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) gmat[u][i] = pacc[u][i] - vt[u][i];
+                for (int i = 0; i < 4; ++i) gmat[u][i] = fmaf(pacc[u][i], kf, -vt[u][i]);
         }
 
         // -G and -eta G as A fragments (rows = features, k = tokens)
@@ -564,9 +615,28 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         ng[1] = ptx::pack_bf16(-gmat[0][2], -gmat[0][3]);
         ng[2] = ptx::pack_bf16(-gmat[1][0], -gmat[1][1]);
         ng[3] = ptx::pack_bf16(-gmat[1][2], -gmat[1][3]);
-        // chain: P_{n+1} = X_{n+1} - G_n^T M^T
+        // chain: P_{n+1} = X_{n+1} - G_n^T M^T; with weight decay
+        // X_{n+1} = (1 - lambda S_n) K_{n+1} W_n + c_n
         uint32_t bf[2][2];
         read_sfrag(n, 0, bf);
+        if (WD) {
+            const float l0 = (1.f - dn) * cb0, l1 = (1.f - dn) * cb1;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                xacc[u][0] = fmaf(dn, xacc[u][0], l0);
+                xacc[u][1] = fmaf(dn, xacc[u][1], l0);
+                xacc[u][2] = fmaf(dn, xacc[u][2], l1);
+                xacc[u][3] = fmaf(dn, xacc[u][3], l1);
+                // Y_n: token t reads (1 - lambda cum_t) W_n
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float f = fq[u][e];
+                    yacc[u][e] = fmaf(f, yacc[u][e], (1.f - f) * cb0);
+                    yacc[u][2 + e] = fmaf(f, yacc[u][2 + e], (1.f - f) * cb1);
+                }
+            }
+            dprev = dn;
+        }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
 #pragma unroll
@@ -619,6 +689,7 @@ linear_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     }
 
     // ---- tail: last update, last output, final stores, final state
+    if (WD) decay_w(dprev);
     update_w(ngep, N - 1);
     {
         const int par = N & 1;
@@ -728,8 +799,12 @@ cudaError_t launch_linear_tc(const LinearArgs &a)
     Params p{d.H, d.L, d.residual_ln, d.ln_eps, g_wait_ns, g_withhold_loads, a.eta, a.W0, a.b0, a.gamma, a.beta,
              a.W_final, a.b_final, a.status, d.init_per_batch};
     p.hoff = head_offset(d);
+    p.ip = d.loss == TTT_LOSS_INNER_PRODUCT;
+    p.wd = d.weight_decay;
     const size_t smem = sizeof(Smem) + 1024;
-    auto kern = d.residual_ln ? linear_fused_kernel<true> : linear_fused_kernel<false>;
+    const bool wd = d.weight_decay != 0.f;
+    auto kern = d.residual_ln ? (wd ? linear_fused_kernel<true, true> : linear_fused_kernel<true, false>)
+                              : (wd ? linear_fused_kernel<false, true> : linear_fused_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<BH, kThreads, smem, a.stream>>>(mq, mk, mv, mz, p);

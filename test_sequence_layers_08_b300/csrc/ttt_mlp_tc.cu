@@ -841,6 +841,7 @@ bool make_map_mlp(CUtensorMap *m, const void *base, int L, int BH)
 
 bool mlp_tc_supported(const ttt_desc &d)
 {
+    if (d.loss != TTT_LOSS_MSE || d.weight_decay != 0.f) return false;   // default learner only
     return d.io_dtype == TTT_BF16 && d.d == D && d.d_hidden == DH && d.mini_batch == MB;
 }
 

@@ -45,9 +45,10 @@ def with_oracle_eta(x):
     return y
 
 
-def run_gpu(cfg, dev, stream=None, out=None, init_per_batch=False):
+def run_gpu(cfg, dev, stream=None, out=None, init_per_batch=False, **variant):
+    """The CUDA path; ``variant`` is the inner learner's loss= and weight_decay=."""
     kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps,
-              init_per_batch=init_per_batch, stream=stream, out=out)
+              init_per_batch=init_per_batch, stream=stream, out=out, **variant)
     if cfg.kind == "linear":
         res = ttt.ttt_linear_fwd(dev["Q"], dev["K"], dev["V"], dev["eta"], dev["W0"], dev["b0"],
                                  dev["gamma"], dev["beta"], **kw)
@@ -58,10 +59,10 @@ def run_gpu(cfg, dev, stream=None, out=None, init_per_batch=False):
     return [r.float().cpu().numpy().astype(np.float64) for r in res]
 
 
-def run_oracle(cfg, x, pairs=None, threads=None):
+def run_oracle(cfg, x, pairs=None, threads=None, **variant):
     """Oracle outputs, either for everything or for a list of (batch, head)."""
     x = with_oracle_eta(x)
-    kw = dict(mini_batch=cfg.mini_batch, ln=cfg.ln, eps=cfg.eps)
+    kw = dict(mini_batch=cfg.mini_batch, ln=cfg.ln, eps=cfg.eps, **variant)
     if pairs is None:
         if cfg.kind == "linear":
             return oracle.ttt_linear(x["Q"], x["K"], x["V"], x["eta"], x["W0"], x["b0"],

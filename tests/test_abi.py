@@ -71,7 +71,9 @@ def call_linear(lib, dsc, ptrs=None):
                                 dict(residual_ln=1, ln_eps=0.0), dict(residual_ln=1, ln_eps=float('nan')),
                                 dict(bh_offset=-1, bh_count=2), dict(bh_count=-3),
                                 dict(bh_offset=2), dict(bh_offset=4, bh_count=3),
-                                dict(B=1, H=3, bh_offset=0, bh_count=4)])
+                                dict(B=1, H=3, bh_offset=0, bh_count=4),
+                                dict(loss=2), dict(loss=-1), dict(weight_decay=-0.5),
+                                dict(weight_decay=float('nan')), dict(weight_decay=float('inf'))])
 def test_bad_descriptor_is_invalid_arg(lib, kw):
     assert call_linear(lib, desc(**kw)) == 1
     assert lib.ttt_last_error().decode() != ""
@@ -184,3 +186,14 @@ def test_partition_fields_accepted(lib):
     does not depend on the partition)."""
     d = desc(bh_offset=2, bh_count=4)
     assert lib.ttt_kernel_name(ctypes.byref(d), 0) is not None
+
+
+def test_variant_kernel_choice(lib):
+    """The fused TTT-Linear kernel runs both inner-learner variants; the fused TTT-MLP kernel
+    runs the default learner only, so MLP variants go to the generic kernel."""
+    k = lambda mlp, **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), mlp))
+    for var in (dict(loss=1), dict(weight_decay=0.1), dict(loss=1, weight_decay=0.1)):
+        assert k(0, **var) in LINEAR_TC_KERNELS
+        assert k(0, residual_ln=1, **var) in LINEAR_TC_KERNELS
+        assert k(1, **var) == "ttt_mlp_generic"
+        assert k(1, residual_ln=1, d_hidden=256, **var) == "ttt_mlp_generic"
