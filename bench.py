@@ -207,7 +207,7 @@ def oracle_inputs(x):
     return y
 
 
-def oracle_rate(cfg, x, budget_s: float, threads: int):
+def oracle_rate(cfg, x, budget_s: float, threads: int, variant=None):
     """Time the oracle as it stands on whole (batch, head) scans of the
     workload, in chunks of at least one scan per thread, until the time budget
     is spent (cycling over the workload's scans).  Returns (tokens/s, text).
@@ -215,7 +215,7 @@ def oracle_rate(cfg, x, budget_s: float, threads: int):
     import oracle
     x = oracle_inputs(x)
     pairs = [(b, h) for b in range(cfg.B) for h in range(cfg.H)]
-    kw = dict(mini_batch=cfg.mini_batch, ln=cfg.ln, eps=cfg.eps)
+    kw = dict(mini_batch=cfg.mini_batch, ln=cfg.ln, eps=cfg.eps, **(variant or {}))
     chunk = max(threads, min(len(pairs), 2 * threads))
     done, i = 0, 0
     t0 = time.perf_counter()
@@ -310,6 +310,10 @@ def run_ours(args, cfg, world, rank, local):
 
     # --split: this rank's contiguous range of (batch, head) rows (the library's partition);
     # otherwise every rank runs the whole workload (a replica)
+    # the inner learner (default: squared-error loss, no weight decay)
+    variant = dict(loss=args.loss, weight_decay=args.weight_decay)
+    learner_tag = ("" if args.loss == "mse" else f"+loss_{args.loss}") + \
+                  ("" if args.weight_decay == 0 else f"+wd{args.weight_decay:g}")
     split = args.split and world > 1
     r0, r1 = ttt.partition_rows(cfg.B * cfg.H, world, rank) if split else (0, cfg.B * cfg.H)
     part_kw = dict(heads=cfg.H, bh_offset=r0) if split else {}
@@ -328,7 +332,7 @@ def run_ours(args, cfg, world, rank, local):
         if args.gated:   # the learning-rate gate is part of the step
             ttt.ttt_eta_gate(x_dev, theta_dev, x["eta_base"], out=s["eta"], stream=stream)
         kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps,
-                  out=outs[i % n_sets], stream=stream, **part_kw)
+                  out=outs[i % n_sets], stream=stream, **part_kw, **variant)
         if cfg.kind == "linear":
             o = ttt.ttt_linear_fwd(s["Q"], s["K"], s["V"], s["eta"], s["W0"], s["b0"],
                                    s["gamma"], s["beta"], **kw)
@@ -338,7 +342,7 @@ def run_ours(args, cfg, world, rank, local):
         outs[i % n_sets] = o
 
     desc = ttt.make_desc(sets[0]["Q"], cfg.mini_batch, cfg.ln, cfg.eps,
-                         d_hidden=cfg.dh if cfg.kind == "mlp" else 0, **part_kw)
+                         d_hidden=cfg.dh if cfg.kind == "mlp" else 0, **part_kw, **variant)
     kname = ttt.kernel_name(desc, cfg.kind == "mlp")
 
     clocks = ClockSampler(local)
@@ -423,7 +427,7 @@ def run_ours(args, cfg, world, rank, local):
         if args.gated:
             ttt.ttt_eta_gate(s_["x"], theta_dev, x["eta_base"], out=s_["eta"], stream=stream)
         kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps,
-                  out=douts[b], stream=stream, **part_kw)
+                  out=douts[b], stream=stream, **part_kw, **variant)
         if cfg.kind == "linear":
             douts[b] = ttt.ttt_linear_fwd(s_["Q"], s_["K"], s_["V"], s_["eta"], s_["W0"], s_["b0"],
                                           s_["gamma"], s_["beta"], **kw)
@@ -490,7 +494,7 @@ def run_ours(args, cfg, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 1
-        rate, sample = oracle_rate(cfg, x, args.cpu_seconds, threads)
+        rate, sample = oracle_rate(cfg, x, args.cpu_seconds, threads, variant)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": sample}
 
@@ -500,12 +504,13 @@ def run_ours(args, cfg, world, rank, local):
                 "higher_is_better": True, "scaling": "strong" if split else "weak",
                 "vs_baseline": None,
                 "dtype": "bf16" if cfg.io == "bf16" else "f32", "data": "synthetic",
-                "config": {"workload": cfg.name + ("+gate" if args.gated else ""),
+                "config": {"workload": cfg.name + ("+gate" if args.gated else "") + learner_tag,
                            "kind": cfg.kind, "B": cfg.B, "H": cfg.H,
                            "eta": ("gate in the step (ttt_eta_gate)" if args.gated else
                                    "input (computed once by ttt_eta_gate)" if gated else "constant"),
                            "L": cfg.L, "d": cfg.d, "mini_batch": cfg.mini_batch,
                            "io": cfg.io, "state": "f32", "residual_ln": cfg.ln,
+                           "learner": {"loss": args.loss, "weight_decay": args.weight_decay},
                            "l2": f"inputs rotate over {n_sets} copies "
                                  f"({n_sets * alg_bytes / 1e6:.0f} MB > L2)",
                            "parallelism": (f"(batch, head) rows split over {world} GPUs "
@@ -696,6 +701,10 @@ def main():
     ap.add_argument("--split", action="store_true",
                     help="with N > 1 GPUs, split one workload's (batch, head) rows over the ranks "
                          "(strong scaling) instead of running a replica on each")
+    ap.add_argument("--loss", choices=["mse", "ip"], default="mse",
+                    help="inner-learner loss: squared error (default) or inner product")
+    ap.add_argument("--weight-decay", type=float, default=0.0,
+                    help="inner-learner weight decay lambda on the fast weights")
     ap.add_argument("--gated", action="store_true",
                     help="each step also computes eta from the layer input with the learning-rate "
                          "gate (ttt_eta_gate) before the scan")
