@@ -71,7 +71,8 @@ def algorithmic_bytes(cfg) -> float:
     return float(io + state * cfg.H + state * cfg.B * cfg.H + ln)
 
 
-KERNEL_SOURCES = {"ttt_linear_fused": "ttt_linear_tc.cu", "ttt_mlp_fused": "ttt_mlp_tc.cu",
+KERNEL_SOURCES = {"ttt_linear_fused": "ttt_linear_tc.cu", "ttt_linear_chunked": "ttt_linear_chunk.cu",
+                  "ttt_mlp_fused": "ttt_mlp_tc.cu",
                   "ttt_linear_generic": "ttt_generic.cu", "ttt_mlp_generic": "ttt_generic.cu"}
 
 

@@ -117,6 +117,7 @@ unsigned int *failure_flag(ttt_status *st)
 
 const char *linear_kernel(const ttt_desc &s)
 {
+    if (ttt::linear_chunk_supported(s)) return "ttt_linear_chunked";
     if (ttt::linear_tc_supported(s)) return "ttt_linear_fused";
     if (ttt::linear_generic_smem_bytes(s)) return "ttt_linear_generic";
     return nullptr;
@@ -205,8 +206,9 @@ ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, co
                       reinterpret_cast<cudaStream_t>(stream), nullptr};
     a.status = failure_flag(&st);
     if (st != TTT_OK) return st;
-    cudaError_t e = ttt::linear_tc_supported(s) ? ttt::launch_linear_tc(a)
-                                                : ttt::launch_linear_generic(a);
+    cudaError_t e = ttt::linear_chunk_supported(s) ? ttt::launch_linear_chunk(a)
+                    : ttt::linear_tc_supported(s)  ? ttt::launch_linear_tc(a)
+                                                   : ttt::launch_linear_generic(a);
     if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "%s launch: %s", kname, cudaGetErrorString(e));
     return ok();
 }

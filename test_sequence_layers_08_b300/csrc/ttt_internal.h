@@ -68,6 +68,10 @@ cudaError_t launch_mlp_generic(const MlpArgs &a);
 // Tensor-core TTT-Linear kernel (bf16 I/O, d = 64, b = 16).
 bool linear_tc_supported(const ttt_desc &d);
 cudaError_t launch_linear_tc(const LinearArgs &a);
+// Chunked tensor-core TTT-Linear kernel without the residual LayerNorm (bf16 I/O, d = 64,
+// b = 16, no weight decay): the state is carried across 64-token chunks.
+bool linear_chunk_supported(const ttt_desc &d);
+cudaError_t launch_linear_chunk(const LinearArgs &a);
 // TMA map of a [rows][cols] bf16 matrix: boxes of box_rows rows x 64 columns, 128-byte swizzle.
 bool make_bf16_2d_map(CUtensorMap *m, const void *base, unsigned long long rows, unsigned long long cols,
                       unsigned box_rows);

@@ -13,7 +13,7 @@ from test_sequence_layers_08_b300 import build as ttt_build
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # names of the tensor-core TTT-Linear kernels the library may pick for bf16, d = 64, b = 16
-LINEAR_TC_KERNELS = ("ttt_linear_fused",)
+LINEAR_TC_KERNELS = ("ttt_linear_fused", "ttt_linear_chunked")
 
 
 @pytest.fixture(scope="module")

@@ -1,6 +1,7 @@
-"""The fused TTT-Linear kernel (bf16 I/O, d = 64, b = 16): it is the kernel the
-library picks, it matches the oracle on edge shapes, and its bounded waits
-report a timeout instead of hanging."""
+"""The tensor-core TTT-Linear kernels (bf16 I/O, d = 64, b = 16): the fused kernel (residual
+LayerNorm, weight decay) and the chunked kernel (no LayerNorm) are the kernels the library
+picks, they match the oracle on edge shapes, and their bounded waits report a timeout
+instead of hanging."""
 import numpy as np
 import pytest
 import torch
@@ -16,7 +17,7 @@ LIN = CONFIGS["linear_bf16_B8_H12_L2048"]
 LIN_LN = CONFIGS["linear_ln_bf16_B4_H16_L8192"]
 
 # names of the tensor-core TTT-Linear kernels the library may pick for bf16, d = 64, b = 16
-LINEAR_TC_KERNELS = ("ttt_linear_fused",)
+LINEAR_TC_KERNELS = ("ttt_linear_fused", "ttt_linear_chunked")
 
 
 @pytest.mark.parametrize("name", ["linear_bf16_B8_H12_L2048", "linear_ln_bf16_B4_H16_L8192",
@@ -45,16 +46,18 @@ def test_fused_more_ctas_than_sms(ln):
     compare_all(cfg, run_gpu(cfg, to_device(cfg, x)), run_oracle(cfg, x))
 
 
-def test_fused_large_state_values():
+@pytest.mark.parametrize("ln", [False, True])
+def test_fused_large_state_values(ln):
     """Large eta: the state moves far from its start within a few mini-batches."""
-    cfg = LIN_LN.with_(name="bigeta", B=1, H=4, L=512)
+    cfg = (LIN_LN if ln else LIN).with_(name="bigeta", B=1, H=4, L=512)
     x = inputs(cfg, seed=17)
     x["eta"] = uniform_eta(cfg.B, cfg.H, cfg.L, 0.0, 1.0, seed=17)   # eta up to ~1
     compare_all(cfg, run_gpu(cfg, to_device(cfg, x)), run_oracle(cfg, x))
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
-    cfg = LIN_LN.with_(name="timeout", B=1, H=2, L=256)
+@pytest.mark.parametrize("ln", [False, True])   # the chunked and the fused kernel
+def test_bounded_wait_reports_timeout_and_context_survives(ln):
+    cfg = (LIN_LN if ln else LIN).with_(name="timeout", B=1, H=2, L=256)
     x = inputs(cfg, seed=19)
     dev = to_device(cfg, x)
     try:

@@ -41,7 +41,7 @@ def test_linear_variants(io, ln, variant):
     L = 1040 if io == "bf16" else 272
     cfg = (LIN_LN if ln else LIN).with_(name=f"lin_var_{io}", B=2, H=3, L=L, io=io)
     if io == "bf16":
-        assert kernel(cfg) == "ttt_linear_fused"
+        assert kernel(cfg) in ("ttt_linear_fused", "ttt_linear_chunked")
     x = inputs(cfg, seed=71)
     got = run_gpu(cfg, to_device(cfg, x), loss=loss, weight_decay=wd)
     compare_all(cfg, got, run_oracle(cfg, x, loss=loss, weight_decay=wd))
