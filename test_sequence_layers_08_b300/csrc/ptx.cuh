@@ -129,6 +129,13 @@ __device__ __forceinline__ void named_bar(int id, int threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Arrive on named barrier `id` without waiting (the producer half of a producer/consumer
+// pair: the consumers bar.sync on the same id with the same thread count).
+__device__ __forceinline__ void named_arrive(int id, int threads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ---------------------------------------------------------------- warp MMA (bf16)
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
@@ -148,6 +155,18 @@ __device__ __forceinline__ void mma_bf16(float *d, const uint32_t *a, uint32_t b
         "{%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D(16x8, f32) = A(16x16, bf16, row) * B(16x8, bf16, col) + C with C given separately
+__device__ __forceinline__ void mma_bf16_c(float *d, const uint32_t *a, uint32_t b0, uint32_t b1,
+                                           float c0, float c1, float c2, float c3)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2),
+          "f"(c3));
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t *r)
