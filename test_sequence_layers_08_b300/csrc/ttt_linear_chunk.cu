@@ -16,26 +16,23 @@
 // block-triangular correction L that keeps every gradient at its own mini-batch's state.
 // With the inner-product loss -<f(k), v> of the ai-feeds Modular TTT page, G_m = -V_m.
 //
-// B300 design.  The scan is latency-bound (each chunk of one (batch, head) waits on the
-// last), so the kernel shortens the chain per token and gives every SM sub-partition two
-// independent instruction streams.  One CTA per (batch, head), eight warps in two groups;
-// warp w and warp w + 4 own output features 16 (w mod 4) .. + 15 and share a sub-partition:
-//   * chain warps 0-3: the intra-chunk chain (G_m, then three dependent 16 x 16 x 16
-//     corrections), the state update W^T += (-eta G)^T K as a 64-token warp-MMA GEMM, and
-//     the key product of the next chunk from the new state.  W^T lives in their registers
-//     as fp32 accumulators for the whole scan;
-//   * output warps 4-7: the 16 input-only 16 x 16 blocks of the next chunk (6 chain blocks
-//     L_{ml}, 10 output blocks), the query product Q W + c of the current chunk, its causal
-//     correction with the chain's G, and the Z tile (stmatrix transpose, TMA store);
-//   * the groups hand over through double-buffered shared memory: the chain publishes -G
-//     of a chunk and the bf16 fragments of the new W^T with c, the output group publishes
-//     the blocks; named-barrier arrive/sync pairs order every buffer, so the chain runs up
-//     to one chunk ahead of the output side;
-//   * 64-token stages of Q, K, V (TMA, 128-byte swizzle) and eta (bulk copy) stream into a
-//     4-deep ring; an output-group thread refills a slot once both groups are past it.
-// Every mbarrier wait is bounded; a wait that runs out sets the library's failure flag and
-// the kernel finishes its chunks (the named-barrier protocol still completes) without
-// waiting again.
+// B300 design.  The scan is latency-bound (one chunk of one (batch, head) waits on the
+// last), so the kernel shortens the chain per token: the d x d state update, the key
+// product of the next chunk and the query product of this one are 64-token warp-MMA
+// GEMMs, and only the intra-chunk correction (three dependent 16 x 16 x 16 products)
+// sits between them.  One CTA per (batch, head), four warps:
+//   * 64-token stages of Q, K, V (TMA, 128-byte swizzle) and eta (bulk copy) stream into
+//     a 3-deep shared-memory ring; one thread refills a slot after the barrier that
+//     retires it;
+//   * warp w owns output features 16w..16w+15: W^T rows live in registers as fp32
+//     accumulators, and P, Zbar, G are 16 x 64 register tiles (features x tokens);
+//   * the 16 input-only 16 x 16 blocks of a chunk (6 chain blocks L_{ml}, 10 output
+//     blocks) are computed one chunk ahead, four per warp, and shared as ready-made bf16
+//     B fragments through shared memory;
+//   * one named barrier per chunk; Z tiles are transposed with stmatrix into a swizzled
+//     staging tile and written by a TMA store.
+// Every mbarrier wait is bounded; a wait that runs out sets the library's failure flag
+// and the kernel finishes without waiting again.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -50,30 +47,18 @@ constexpr int D = 64;           // head dim
 constexpr int MB = 16;          // mini-batch
 constexpr int CT = 64;          // tokens per chunk (= per pipeline stage)
 constexpr int NMB = CT / MB;    // mini-batches per chunk
-constexpr int NSS = 4;          // stages in the ring
-constexpr int kThreads = 256;
-constexpr int kGroup = 128;     // threads per group
-constexpr int kStoreTid = 128;  // output thread that issues the Z stores
-constexpr int kRefillTid = 224; // output thread that refills ring slots
+constexpr int NSS = 3;          // stages in the ring
+constexpr int kThreads = 128;
+constexpr int kRefill = 96;     // thread that refills ring slots (warp 3; warp 0 stores Z)
 constexpr uint32_t kTileBytes = CT * D * 2;   // 8 KB
 constexpr int kBlocks = 16;     // 6 chain blocks + 10 output blocks
-
-// named barriers (0 is __syncthreads)
-constexpr int BAR_OUT = 1;          // output group only (Z staging tile complete)
-constexpr int BAR_BLK_FULL = 2;     // + parity: blocks of a chunk written (output -> chain)
-constexpr int BAR_BLK_EMPTY = 4;    // + parity: blocks read by the chain (chain -> output)
-constexpr int BAR_PUB_FULL = 6;     // + parity: -G and the new state published (chain -> output)
-constexpr int BAR_PUB_EMPTY = 8;    // + parity: publication read (output -> chain)
 
 struct __align__(1024) Smem {
     __nv_bfloat16 q[NSS][CT * D];
     __nv_bfloat16 k[NSS][CT * D];
     __nv_bfloat16 v[NSS][CT * D];
     __nv_bfloat16 z[2][CT * D];
-    uint2 blk[2][kBlocks][2][32];        // [chunk parity][block][source half][lane]
-    uint4 ng[2][NMB][4][32];             // [chunk parity][mini-batch][warp][lane]: -G A fragments
-    uint4 wa[2][4][4][32];               // [state parity][k-step][warp][lane]: W^T A fragments
-    float cb[2][D];                      // [state parity][feature]: c
+    uint2 blk[2][kBlocks][2][32];   // [chunk parity][block][source half][lane]
     float eta[NSS][CT];
     unsigned long long full[NSS];
     int abort_flag;
@@ -117,11 +102,8 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const uint32_t raw = ptx::smem_addr(smem_raw);
     Smem &s = *reinterpret_cast<Smem *>(smem_raw + (((raw + 1023u) & ~1023u) - raw));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int fw = warp & 3;                 // feature block of this warp
-    const bool chain_group = warp < 4;
     const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
-    const int NC = (p.L + CT - 1) / CT;      // chunks (= stages)
-    const int tail = p.L - (NC - 1) * CT;    // tokens of the last chunk
+    const int NC = (p.L + CT - 1) / CT;   // chunks (= stages)
 
     const float *eta_bh = p.eta + (size_t)bh * p.L;
     auto issue_stage = [&](int st) {
@@ -144,9 +126,10 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         ptx::prefetch_tmap(&tmV);
         for (int st = 0; st < issued; ++st) issue_stage(st);
     }
+    __syncthreads();
 
     const int g = lane >> 2, c = lane & 3, mrow = lane & 7, mat = lane >> 3;
-    const int j0 = fw * 16 + g, j1 = j0 + 8;   // this thread's two features
+    const int j0 = warp * 16 + g, j1 = j0 + 8;   // this thread's two features
     bool aborted = false;
 
     auto wait_stage = [&](int st) {
@@ -160,29 +143,24 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     auto tile_addr = [&](const __nv_bfloat16 (*arr)[CT * D], int cc, int t, int ch) -> uint32_t {
         return ptx::smem_addr(arr[cc % NSS]) + (uint32_t)(t * 128 + ((ch ^ mrow) << 4));
     };
-    // eta of tokens t, t + 1 (t even) of chunk cc (the stale tail of a ragged last stage is
-    // zeroed before any reads)
+    // eta of tokens t, t + 1 (t even) of chunk cc
     auto eta2 = [&](int cc, int t) -> float2 {
         return *reinterpret_cast<const float2 *>(&s.eta[cc % NSS][t]);
     };
-
-    // ---- the chain group's state: W^T rows j0/j1 as fp32 accumulators, c
-    float wt[8][4];
-    float cb0 = 0.f, cb1 = 0.f;
-    const size_t init = p.init_per_batch ? (size_t)bh : (size_t)h;
-    auto publish_w = [&](int par) {   // bf16 A fragments of W^T and c for the output group
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            s.wa[par][q][fw][lane] = make_uint4(ptx::pack_bf16(wt[2 * q][0], wt[2 * q][1]),
-                                                ptx::pack_bf16(wt[2 * q][2], wt[2 * q][3]),
-                                                ptx::pack_bf16(wt[2 * q + 1][0], wt[2 * q + 1][1]),
-                                                ptx::pack_bf16(wt[2 * q + 1][2], wt[2 * q + 1][3]));
-        if (c == 0) {
-            s.cb[par][j0] = cb0;
-            s.cb[par][j1] = cb1;
+    // the slot of a ragged last stage holds stale eta past the sequence: every warp zeroes it
+    // (identical values) before its own first read of that stage
+    const int tail = p.L - (NC - 1) * CT;
+    auto zero_eta_tail = [&](int cc) {
+        if (cc == NC - 1 && tail < CT) {
+            for (int t = tail + lane; t < CT; t += 32) s.eta[cc % NSS][t] = 0.f;
+            __syncwarp();
         }
     };
-    if (chain_group) {
+
+    // ---- initial state: W^T rows j0/j1 as fp32 accumulators, c
+    float wt[8][4];
+    const size_t init = p.init_per_batch ? (size_t)bh : (size_t)h;
+    {
         const float *W0 = p.W0 + init * D * D;
 #pragma unroll
         for (int pt = 0; pt < 8; ++pt) {
@@ -192,16 +170,24 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             wt[pt][2] = W0[i * D + j1];
             wt[pt][3] = W0[(i + 1) * D + j1];
         }
-        cb0 = p.b0[init * D + j0];
-        cb1 = p.b0[init * D + j1];
-        publish_w(0);
     }
-    __syncthreads();   // mbarriers initialised, W_0 published
+    float cb0 = p.b0[init * D + j0];
+    float cb1 = p.b0[init * D + j1];
+    const float kf = p.ip ? 0.f : 1.f;   // weight of P in G (0: inner-product loss, G = -V)
 
-    // acc[nt] = W^T X^T + c over the 64 tokens of chunk cc (n-tile nt = tokens 8 nt..8 nt + 7),
-    // W^T given as bf16 A fragments
-    auto product = [&](float (*acc)[4], const uint32_t (*wa)[4], float c0, float c1,
-                       const __nv_bfloat16 (*arr)[CT * D], int cc) {
+    uint32_t wa[4][4];   // bf16 A fragments of W^T, k-steps of 16 input features
+    auto pack_w = [&]() {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            wa[q][0] = ptx::pack_bf16(wt[2 * q][0], wt[2 * q][1]);
+            wa[q][1] = ptx::pack_bf16(wt[2 * q][2], wt[2 * q][3]);
+            wa[q][2] = ptx::pack_bf16(wt[2 * q + 1][0], wt[2 * q + 1][1]);
+            wa[q][3] = ptx::pack_bf16(wt[2 * q + 1][2], wt[2 * q + 1][3]);
+        }
+    };
+
+    // acc[nt] = W^T X^T + c over the 64 tokens of chunk cc (n-tile nt = tokens 8 nt..8 nt + 7)
+    auto product = [&](float (*acc)[4], const __nv_bfloat16 (*arr)[CT * D], int cc) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
 #pragma unroll
@@ -210,8 +196,8 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 uint32_t r[4];
                 ptx::ldsm_x4(tile_addr(arr, cc, (2 * tb + (mat >> 1)) * 8 + mrow, 2 * q + (mat & 1)), r);
                 if (q == 0) {
-                    ptx::mma_bf16_c(acc[2 * tb], wa[q], r[0], r[1], c0, c0, c1, c1);
-                    ptx::mma_bf16_c(acc[2 * tb + 1], wa[q], r[2], r[3], c0, c0, c1, c1);
+                    ptx::mma_bf16_c(acc[2 * tb], wa[q], r[0], r[1], cb0, cb0, cb1, cb1);
+                    ptx::mma_bf16_c(acc[2 * tb + 1], wa[q], r[2], r[3], cb0, cb0, cb1, cb1);
                 } else {
                     ptx::mma_bf16(acc[2 * tb], wa[q], r[0], r[1]);
                     ptx::mma_bf16(acc[2 * tb + 1], wa[q], r[2], r[3]);
@@ -220,108 +206,186 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
     };
 
-    if (chain_group) {
-        // ================================================================ chain warps
-        uint32_t wa[4][4];
-        auto pack_w = [&]() {
+    // Input-only block: rows t = target tokens of mini-batch mt of X (Q or K), columns s =
+    // source tokens of mini-batch l of K; value eta_s (x_t . k_s + 1), masked to s <= t on a
+    // diagonal output block.  Stored as the lane's own B fragments (k = s, n = t).
+    auto block = [&](const __nv_bfloat16 (*X)[CT * D], int cc, int mt, int l, bool causal, int b) {
+        uint32_t a[4][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                wa[q][0] = ptx::pack_bf16(wt[2 * q][0], wt[2 * q][1]);
-                wa[q][1] = ptx::pack_bf16(wt[2 * q][2], wt[2 * q][3]);
-                wa[q][2] = ptx::pack_bf16(wt[2 * q + 1][0], wt[2 * q + 1][1]);
-                wa[q][3] = ptx::pack_bf16(wt[2 * q + 1][2], wt[2 * q + 1][3]);
-            }
-        };
-        const float kf = p.ip ? 0.f : 1.f;   // weight of P in G (0: inner-product loss, G = -V)
-        wait_stage(0);
-        pack_w();
-        float pacc[8][4];
-        product(pacc, wa, cb0, cb1, s.k, 0);
-
-        for (int cc = 0; cc < NC; ++cc) {
-            const int par = cc & 1;
-            ptx::named_bar(BAR_BLK_FULL + par, kThreads);   // blocks of chunk cc are in place
-            uint32_t ng[NMB][4];
-            float d0 = 0.f, d1 = 0.f;   // eta^T G for features j0, j1 (this thread's tokens)
+        for (int q = 0; q < 4; ++q)   // A: matrices (t0, ch 2q), (t1, 2q), (t0, 2q + 1), (t1, 2q + 1)
+            ptx::ldsm_x4(tile_addr(X, cc, mt * MB + (mat & 1) * 8 + mrow, 2 * q + (mat >> 1)), a[q]);
+        float acc[2][4], ac2[2][4];
 #pragma unroll
-            for (int m = 0; m < NMB; ++m) {
-                float vt[2][4];
-                {
-                    uint32_t r[4];   // V^T of mini-batch m: matrices (t0, j0), (t0, j1), (t1, j0), (t1, j1)
-                    ptx::ldsm_x4_t(tile_addr(s.v, cc, m * MB + (mat >> 1) * 8 + mrow, fw * 2 + (mat & 1)), r);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        vt[u][0] = ptx::bf16_lo(r[2 * u]);
-                        vt[u][1] = ptx::bf16_hi(r[2 * u]);
-                        vt[u][2] = ptx::bf16_lo(r[2 * u + 1]);
-                        vt[u][3] = ptx::bf16_hi(r[2 * u + 1]);
-                    }
-                }
-                float gm[2][4];
-#pragma unroll
-                for (int u = 0; u < 2; ++u)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) gm[u][i] = fmaf(pacc[2 * m + u][i], kf, -vt[u][i]);
-                ng[m][0] = ptx::pack_bf16(-gm[0][0], -gm[0][1]);
-                ng[m][1] = ptx::pack_bf16(-gm[0][2], -gm[0][3]);
-                ng[m][2] = ptx::pack_bf16(-gm[1][0], -gm[1][1]);
-                ng[m][3] = ptx::pack_bf16(-gm[1][2], -gm[1][3]);
-                // chain: P_{m'} -= G_m L_{m'm}^T for the later mini-batches
-#pragma unroll
-                for (int mp = m + 1; mp < NMB; ++mp) {
-                    const uint2 f0 = s.blk[par][chain_blk(mp, m)][0][lane];
-                    const uint2 f1 = s.blk[par][chain_blk(mp, m)][1][lane];
-                    ptx::mma_bf16(pacc[2 * mp], ng[m], f0.x, f1.x);
-                    ptx::mma_bf16(pacc[2 * mp + 1], ng[m], f0.y, f1.y);
-                }
-                // state update, k-step m: W^T += (-eta G_m)^T K_m
-                const float2 e0 = eta2(cc, m * MB + 2 * c), e1 = eta2(cc, m * MB + 2 * c + 8);
-                uint32_t nge[4];
-                nge[0] = ptx::pack_bf16(-e0.x * gm[0][0], -e0.y * gm[0][1]);
-                nge[1] = ptx::pack_bf16(-e0.x * gm[0][2], -e0.y * gm[0][3]);
-                nge[2] = ptx::pack_bf16(-e1.x * gm[1][0], -e1.y * gm[1][1]);
-                nge[3] = ptx::pack_bf16(-e1.x * gm[1][2], -e1.y * gm[1][3]);
-                d0 += e0.x * gm[0][0] + e0.y * gm[0][1] + e1.x * gm[1][0] + e1.y * gm[1][1];
-                d1 += e0.x * gm[0][2] + e0.y * gm[0][3] + e1.x * gm[1][2] + e1.y * gm[1][3];
-#pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    // matrices (s-block, i-chunk): (0, 2pp), (1, 2pp), (0, 2pp + 1), (1, 2pp + 1)
-                    uint32_t r[4];
-                    ptx::ldsm_x4_t(tile_addr(s.k, cc, m * MB + (mat & 1) * 8 + mrow, 2 * pp + (mat >> 1)), r);
-                    ptx::mma_bf16(wt[2 * pp], nge, r[0], r[1]);
-                    ptx::mma_bf16(wt[2 * pp + 1], nge, r[2], r[3]);
-                }
-            }
-            if (cc + 2 < NC) ptx::named_arrive(BAR_BLK_EMPTY + par, kThreads);
-            // c -= eta^T G over the chunk (sum over the four lanes sharing g)
-            d0 += __shfl_xor_sync(0xffffffffu, d0, 1);
-            d1 += __shfl_xor_sync(0xffffffffu, d1, 1);
-            d0 += __shfl_xor_sync(0xffffffffu, d0, 2);
-            d1 += __shfl_xor_sync(0xffffffffu, d1, 2);
-            cb0 -= d0;
-            cb1 -= d1;
-            pack_w();
-            // publish -G of chunk cc and the state W_{cc+1}, c_{cc+1}; the output group must be
-            // done with chunk cc - 1 (the buffers of that parity hold chunk cc - 2 / state cc - 1)
-            if (cc >= 1) ptx::named_bar(BAR_PUB_EMPTY + (par ^ 1), kThreads);
-#pragma unroll
-            for (int m = 0; m < NMB; ++m)
-                s.ng[par][m][fw][lane] = make_uint4(ng[m][0], ng[m][1], ng[m][2], ng[m][3]);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                s.wa[par ^ 1][q][fw][lane] = make_uint4(wa[q][0], wa[q][1], wa[q][2], wa[q][3]);
-            if (c == 0) {
-                s.cb[par ^ 1][j0] = cb0;
-                s.cb[par ^ 1][j1] = cb1;
-            }
-            ptx::named_arrive(BAR_PUB_FULL + par, kThreads);
-            // the next chunk's key product from the new state
-            if (cc + 1 < NC) {
-                wait_stage(cc + 1);
-                product(pacc, wa, cb0, cb1, s.k, cc + 1);
+        for (int q = 0; q < 4; ++q) {
+            // B: source rows s: matrices (half 0, ch 2q), (half 0, 2q + 1), (half 1, 2q), (half 1, 2q + 1)
+            uint32_t r[4];
+            ptx::ldsm_x4(tile_addr(s.k, cc, l * MB + (mat >> 1) * 8 + mrow, 2 * q + (mat & 1)), r);
+            float (*dst)[4] = (q & 1) ? ac2 : acc;
+            if (q < 2) {
+                ptx::mma_bf16_c(dst[0], a[q], r[0], r[1], 0.f, 0.f, 0.f, 0.f);
+                ptx::mma_bf16_c(dst[1], a[q], r[2], r[3], 0.f, 0.f, 0.f, 0.f);
+            } else {
+                ptx::mma_bf16(dst[0], a[q], r[0], r[1]);
+                ptx::mma_bf16(dst[1], a[q], r[2], r[3]);
             }
         }
-        // final state
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            // rows t = g, g + 8; columns s = 8 hf + 2c, +1
+            const int s0 = hf * 8 + 2 * c;
+            const float2 e = eta2(cc, l * MB + s0);
+            const float e0 = e.x, e1 = e.y;
+            const float x0 = acc[hf][0] + ac2[hf][0], x1 = acc[hf][1] + ac2[hf][1];
+            const float x2 = acc[hf][2] + ac2[hf][2], x3 = acc[hf][3] + ac2[hf][3];
+            const float v0 = (causal && s0 > g) ? 0.f : e0 * (x0 + 1.f);
+            const float v1 = (causal && s0 + 1 > g) ? 0.f : e1 * (x1 + 1.f);
+            const float v2 = (causal && s0 > g + 8) ? 0.f : e0 * (x2 + 1.f);
+            const float v3 = (causal && s0 + 1 > g + 8) ? 0.f : e1 * (x3 + 1.f);
+            s.blk[cc & 1][b][hf][lane] = make_uint2(ptx::pack_bf16(v0, v1), ptx::pack_bf16(v2, v3));
+        }
+    };
+    // this warp's four blocks of chunk cc: the output blocks of target mini-batch w and the
+    // chain blocks of target mini-batch 3 - w
+    auto blocks = [&](int cc) {
+        zero_eta_tail(cc);
+        for (int l = 0; l <= warp; ++l) block(s.q, cc, warp, l, l == warp, out_blk(warp, l));
+        const int mc = NMB - 1 - warp;
+        for (int l = 0; l < mc; ++l) block(s.k, cc, mc, l, false, chain_blk(mc, l));
+    };
+    // both n-tiles of a block: (f0.x, f1.x) for target tokens 0-7, (f0.y, f1.y) for 8-15
+    auto read_blk = [&](int cc, int b, uint2 &f0, uint2 &f1) {
+        f0 = s.blk[cc & 1][b][0][lane];
+        f1 = s.blk[cc & 1][b][1][lane];
+    };
+
+    // ---- prologue: P_0 = K_0 W_0 + c_0 and the blocks of chunk 0
+    wait_stage(0);
+    pack_w();
+    float pacc[8][4];
+    product(pacc, s.k, 0);
+    blocks(0);
+    ptx::named_bar(1, kThreads);
+
+    for (int cc = 0; cc < NC; ++cc) {
+        const bool more = cc + 1 < NC;
+        if (more) wait_stage(cc + 1);
+
+        // query-side product with the chunk's starting state
+        float yacc[8][4];
+        product(yacc, s.q, cc);
+
+        // intra-chunk chain: G_m, then its corrections to the later mini-batches' P and to Zbar,
+        // and its k-step of the state update
+        uint32_t ng[NMB][4];
+        float d0 = 0.f, d1 = 0.f;   // eta^T G for features j0, j1 (this thread's tokens)
+#pragma unroll
+        for (int m = 0; m < NMB; ++m) {
+            float vt[2][4];
+            {
+                uint32_t r[4];   // V^T of mini-batch m: matrices (t0, j0), (t0, j1), (t1, j0), (t1, j1)
+                ptx::ldsm_x4_t(tile_addr(s.v, cc, m * MB + (mat >> 1) * 8 + mrow, warp * 2 + (mat & 1)), r);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    vt[u][0] = ptx::bf16_lo(r[2 * u]);
+                    vt[u][1] = ptx::bf16_hi(r[2 * u]);
+                    vt[u][2] = ptx::bf16_lo(r[2 * u + 1]);
+                    vt[u][3] = ptx::bf16_hi(r[2 * u + 1]);
+                }
+            }
+            float gm[2][4];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) gm[u][i] = fmaf(pacc[2 * m + u][i], kf, -vt[u][i]);
+            ng[m][0] = ptx::pack_bf16(-gm[0][0], -gm[0][1]);
+            ng[m][1] = ptx::pack_bf16(-gm[0][2], -gm[0][3]);
+            ng[m][2] = ptx::pack_bf16(-gm[1][0], -gm[1][1]);
+            ng[m][3] = ptx::pack_bf16(-gm[1][2], -gm[1][3]);
+            // chain: P_{m'} -= G_m L_{m'm}^T for the later mini-batches
+#pragma unroll
+            for (int mp = m + 1; mp < NMB; ++mp) {
+                uint2 f0, f1;
+                read_blk(cc, chain_blk(mp, m), f0, f1);
+                ptx::mma_bf16(pacc[2 * mp], ng[m], f0.x, f1.x);
+                ptx::mma_bf16(pacc[2 * mp + 1], ng[m], f0.y, f1.y);
+            }
+            // outputs: Zbar_{m'} -= G_m B_{m'm}^T for m' >= m (independent accumulators)
+#pragma unroll
+            for (int mp = m; mp < NMB; ++mp) {
+                uint2 f0, f1;
+                read_blk(cc, out_blk(mp, m), f0, f1);
+                ptx::mma_bf16(yacc[2 * mp], ng[m], f0.x, f1.x);
+                ptx::mma_bf16(yacc[2 * mp + 1], ng[m], f0.y, f1.y);
+            }
+            // state update, k-step m: W^T += (-eta G_m)^T K_m
+            const int s0 = m * MB + 2 * c;
+            const float2 ea = eta2(cc, s0), eb = eta2(cc, s0 + 8);
+            const float e00 = ea.x, e01 = ea.y, e10 = eb.x, e11 = eb.y;
+            uint32_t nge[4];
+            nge[0] = ptx::pack_bf16(-e00 * gm[0][0], -e01 * gm[0][1]);
+            nge[1] = ptx::pack_bf16(-e00 * gm[0][2], -e01 * gm[0][3]);
+            nge[2] = ptx::pack_bf16(-e10 * gm[1][0], -e11 * gm[1][1]);
+            nge[3] = ptx::pack_bf16(-e10 * gm[1][2], -e11 * gm[1][3]);
+            d0 += e00 * gm[0][0] + e01 * gm[0][1] + e10 * gm[1][0] + e11 * gm[1][1];
+            d1 += e00 * gm[0][2] + e01 * gm[0][3] + e10 * gm[1][2] + e11 * gm[1][3];
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                // matrices (s-block, i-chunk): (0, 2pp), (1, 2pp), (0, 2pp + 1), (1, 2pp + 1)
+                uint32_t r[4];
+                ptx::ldsm_x4_t(tile_addr(s.k, cc, m * MB + (mat & 1) * 8 + mrow, 2 * pp + (mat >> 1)), r);
+                ptx::mma_bf16(wt[2 * pp], nge, r[0], r[1]);
+                ptx::mma_bf16(wt[2 * pp + 1], nge, r[2], r[3]);
+            }
+        }
+        // c -= eta^T G over the chunk (sum over the four lanes sharing g)
+        d0 += __shfl_xor_sync(0xffffffffu, d0, 1);
+        d1 += __shfl_xor_sync(0xffffffffu, d1, 1);
+        d0 += __shfl_xor_sync(0xffffffffu, d0, 2);
+        d1 += __shfl_xor_sync(0xffffffffu, d1, 2);
+        cb0 -= d0;
+        cb1 -= d1;
+        pack_w();
+
+        // next chunk: its key product from the new state, and its input-only blocks
+        if (more) {
+            product(pacc, s.k, cc + 1);
+            blocks(cc + 1);
+        }
+
+        // Zbar -> bf16 staging tile cc % 2 (rows = tokens), TMA-stored after the barrier
+        {
+            const uint32_t zaddr = ptx::smem_addr(s.z[cc & 1]);
+#pragma unroll
+            for (int m = 0; m < NMB; ++m) {
+                uint32_t r[4];
+                r[0] = ptx::pack_bf16(yacc[2 * m][0], yacc[2 * m][1]);
+                r[1] = ptx::pack_bf16(yacc[2 * m][2], yacc[2 * m][3]);
+                r[2] = ptx::pack_bf16(yacc[2 * m + 1][0], yacc[2 * m + 1][1]);
+                r[3] = ptx::pack_bf16(yacc[2 * m + 1][2], yacc[2 * m + 1][3]);
+                // matrices (j-block, t-block): (0,0), (1,0), (0,1), (1,1)
+                ptx::stsm_x4_t(zaddr + ptx::sw128(m * MB + (mat >> 1) * 8 + mrow, warp * 2 + (mat & 1)), r);
+            }
+            ptx::fence_proxy_async();
+        }
+        // the store of chunk cc - 1 has read its tile (which chunk cc + 1 overwrites)
+        if (tid == 0) ptx::bulk_wait_read<0>();
+        ptx::named_bar(1, kThreads);
+        if (tid == 0) {
+            ptx::tma_store_3d(&tmZ, ptx::smem_addr(s.z[cc & 1]), 0, cc * CT, bh);
+            ptx::bulk_commit();
+        }
+        if (tid == kRefill && cc + NSS < nissue && !aborted) {
+            // stage cc is no longer read: refill its slot with stage cc + NSS
+            ptx::fence_proxy_async();
+            issue_stage(cc + NSS);
+            issued = cc + NSS + 1;
+        }
+    }
+    if (tid == 0) ptx::bulk_wait<0>();
+    if (tid == kRefill)   // copies still in flight (only after a wait ran out) land before exit
+        for (int st = max(0, issued - NSS); st < issued; ++st)
+            ptx::mbar_wait_bounded(ptx::smem_addr(&s.full[st % NSS]), (st / NSS) & 1, kDrainNs);
+    {
         float *Wf = p.Wf + (size_t)bh * D * D;
 #pragma unroll
         for (int pt = 0; pt < 8; ++pt) {
@@ -335,125 +399,6 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             p.bf[(size_t)bh * D + j0] = cb0;
             p.bf[(size_t)bh * D + j1] = cb1;
         }
-    } else {
-        // ================================================================ output warps
-        const int ow = fw;   // 0..3
-        // Input-only block: rows t = target tokens of mini-batch mt of X (Q or K), columns s =
-        // source tokens of mini-batch l of K; value eta_s (x_t . k_s + 1), masked to s <= t on
-        // a diagonal output block.  Stored as the lane's own B fragments (k = s, n = t).
-        auto block = [&](const __nv_bfloat16 (*X)[CT * D], int cc, int mt, int l, bool causal, int b) {
-            uint32_t a[4][4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)   // A: matrices (t0, ch 2q), (t1, 2q), (t0, 2q + 1), (t1, 2q + 1)
-                ptx::ldsm_x4(tile_addr(X, cc, mt * MB + (mat & 1) * 8 + mrow, 2 * q + (mat >> 1)), a[q]);
-            float acc[2][4], ac2[2][4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                // B: source rows s: matrices (half 0, ch 2q), (half 0, 2q + 1), (half 1, 2q), (half 1, 2q + 1)
-                uint32_t r[4];
-                ptx::ldsm_x4(tile_addr(s.k, cc, l * MB + (mat >> 1) * 8 + mrow, 2 * q + (mat & 1)), r);
-                float (*dst)[4] = (q & 1) ? ac2 : acc;
-                if (q < 2) {
-                    ptx::mma_bf16_c(dst[0], a[q], r[0], r[1], 0.f, 0.f, 0.f, 0.f);
-                    ptx::mma_bf16_c(dst[1], a[q], r[2], r[3], 0.f, 0.f, 0.f, 0.f);
-                } else {
-                    ptx::mma_bf16(dst[0], a[q], r[0], r[1]);
-                    ptx::mma_bf16(dst[1], a[q], r[2], r[3]);
-                }
-            }
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                // rows t = g, g + 8; columns s = 8 hf + 2c, +1
-                const int s0 = hf * 8 + 2 * c;
-                const float2 e = eta2(cc, l * MB + s0);
-                const float x0 = acc[hf][0] + ac2[hf][0], x1 = acc[hf][1] + ac2[hf][1];
-                const float x2 = acc[hf][2] + ac2[hf][2], x3 = acc[hf][3] + ac2[hf][3];
-                const float v0 = (causal && s0 > g) ? 0.f : e.x * (x0 + 1.f);
-                const float v1 = (causal && s0 + 1 > g) ? 0.f : e.y * (x1 + 1.f);
-                const float v2 = (causal && s0 > g + 8) ? 0.f : e.x * (x2 + 1.f);
-                const float v3 = (causal && s0 + 1 > g + 8) ? 0.f : e.y * (x3 + 1.f);
-                s.blk[cc & 1][b][hf][lane] = make_uint2(ptx::pack_bf16(v0, v1), ptx::pack_bf16(v2, v3));
-            }
-        };
-        // this warp's four blocks of chunk cc: the output blocks of target mini-batch ow and
-        // the chain blocks of target mini-batch 3 - ow
-        auto blocks = [&](int cc) {
-            wait_stage(cc);
-            if (cc == NC - 1 && tail < CT) {
-                // the ring slot past the sequence holds stale eta: zero it before any reads
-                if (ow == 0)
-                    for (int t = tail + lane; t < CT; t += 32) s.eta[cc % NSS][t] = 0.f;
-                ptx::named_bar(BAR_OUT, kGroup);
-            }
-            if (cc >= 2) ptx::named_bar(BAR_BLK_EMPTY + (cc & 1), kThreads);
-            for (int l = 0; l <= ow; ++l) block(s.q, cc, ow, l, l == ow, out_blk(ow, l));
-            const int mc = NMB - 1 - ow;
-            for (int l = 0; l < mc; ++l) block(s.k, cc, mc, l, false, chain_blk(mc, l));
-            ptx::named_arrive(BAR_BLK_FULL + (cc & 1), kThreads);
-        };
-
-        blocks(0);
-        for (int cc = 0; cc < NC; ++cc) {
-            const int par = cc & 1;
-            if (cc + 1 < NC) blocks(cc + 1);
-            // query-side product with the chunk's starting state (published one chunk earlier)
-            float yacc[8][4];
-            {
-                uint32_t wa[4][4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 w4 = s.wa[par][q][ow][lane];
-                    wa[q][0] = w4.x; wa[q][1] = w4.y; wa[q][2] = w4.z; wa[q][3] = w4.w;
-                }
-                product(yacc, wa, s.cb[par][j0], s.cb[par][j1], s.q, cc);
-            }
-            // the chain's -G of this chunk: Zbar_m = Y_m - sum_{l <= m} G_l B_{ml}^T
-            ptx::named_bar(BAR_PUB_FULL + par, kThreads);
-#pragma unroll
-            for (int m = 0; m < NMB; ++m)
-#pragma unroll
-                for (int l = 0; l <= m; ++l) {
-                    const uint4 n4 = s.ng[par][l][ow][lane];
-                    const uint32_t ng[4] = {n4.x, n4.y, n4.z, n4.w};
-                    const uint2 f0 = s.blk[par][out_blk(m, l)][0][lane];
-                    const uint2 f1 = s.blk[par][out_blk(m, l)][1][lane];
-                    ptx::mma_bf16(yacc[2 * m], ng, f0.x, f1.x);
-                    ptx::mma_bf16(yacc[2 * m + 1], ng, f0.y, f1.y);
-                }
-            if (cc + 1 < NC) ptx::named_arrive(BAR_PUB_EMPTY + par, kThreads);
-            // both groups are past stage cc: refill its slot
-            if (tid == kRefillTid && cc + NSS < nissue && !aborted) {
-                ptx::fence_proxy_async();
-                issue_stage(cc + NSS);
-                issued = cc + NSS + 1;
-            }
-            // Zbar -> bf16 staging tile cc % 2 (rows = tokens) -> TMA store
-            {
-                const uint32_t zaddr = ptx::smem_addr(s.z[par]);
-#pragma unroll
-                for (int m = 0; m < NMB; ++m) {
-                    uint32_t r[4];
-                    r[0] = ptx::pack_bf16(yacc[2 * m][0], yacc[2 * m][1]);
-                    r[1] = ptx::pack_bf16(yacc[2 * m][2], yacc[2 * m][3]);
-                    r[2] = ptx::pack_bf16(yacc[2 * m + 1][0], yacc[2 * m + 1][1]);
-                    r[3] = ptx::pack_bf16(yacc[2 * m + 1][2], yacc[2 * m + 1][3]);
-                    // matrices (j-block, t-block): (0,0), (1,0), (0,1), (1,1)
-                    ptx::stsm_x4_t(zaddr + ptx::sw128(m * MB + (mat >> 1) * 8 + mrow, ow * 2 + (mat & 1)), r);
-                }
-                ptx::fence_proxy_async();
-            }
-            // the store of chunk cc - 1 has read its tile (which chunk cc + 1 overwrites)
-            if (tid == kStoreTid) ptx::bulk_wait_read<0>();
-            ptx::named_bar(BAR_OUT, kGroup);
-            if (tid == kStoreTid) {
-                ptx::tma_store_3d(&tmZ, ptx::smem_addr(s.z[par]), 0, cc * CT, bh);
-                ptx::bulk_commit();
-            }
-        }
-        if (tid == kStoreTid) ptx::bulk_wait<0>();
-        if (tid == kRefillTid)   // copies still in flight (only after a wait ran out) land before exit
-            for (int st = max(0, issued - NSS); st < issued; ++st)
-                ptx::mbar_wait_bounded(ptx::smem_addr(&s.full[st % NSS]), (st / NSS) & 1, kDrainNs);
     }
 }
 
