@@ -109,8 +109,10 @@ enum { TTT_LOSS_MSE = 0, TTT_LOSS_INNER_PRODUCT = 1 };
  *   out: Z [B,H,L,d] (io_dtype): z_t = f(q_t; W_t, c_t) with the weights after
  *        token t's update; W_final [B,H,d,d], b_final [B,H,d]: state after
  *        the last mini-batch.
- * Supported: any d <= 128 and b <= 64 (generic kernels, fp32 arithmetic);
- * bf16 I/O with d = 64, b = 16 runs the tensor-core kernel (every loss and decay).
+ * Supported: d <= 128 with d a multiple of 4, and b <= 64 (generic kernel, fp32
+ * arithmetic); bf16 I/O with d = 64, b = 16 runs a tensor-core kernel: without the
+ * residual LayerNorm and weight decay the chunked kernel (the state carried across
+ * 64-token chunks), otherwise the fused kernel (every loss and decay).
  */
 TTT_API ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
                           const float *eta, const float *W0, const float *b0,
@@ -144,8 +146,8 @@ TTT_API ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *
  *   out: Z [B,H,L,d] (io_dtype), z_t = f(q_t; W_t, c_t) after token t's update.
  * Calling it T times with one token each gives the same result as one call
  * with the T tokens.  desc->init_per_batch is ignored (the state is always
- * [B, H, ...]).  Supported: any d <= 128; d = 64 runs the decode kernel (one
- * warp per (batch, head), FP32), other d the generic kernel.  Z must not alias
+ * [B, H, ...]).  Supported: d <= 128 with d a multiple of 4; d = 64 runs the decode
+ * kernel (one warp per (batch, head), FP32), other d the generic kernel.  Z must not alias
  * an input, and W, b must not alias any other buffer.
  */
 TTT_API ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const void *K, const void *V,

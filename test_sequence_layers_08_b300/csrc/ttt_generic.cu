@@ -167,14 +167,59 @@ struct LinearParams {
 
 // ---------------------------------------------------------------------------
 // TTT-Linear
+//
+// The d x d products are register-tiled: a thread owns 4 consecutive features (a float4 of
+// a W row) of one token, or a 4 x 4 block of W for the update, and reads its operands as
+// 16-byte shared-memory loads.  When the next mini-batch's K, Q, V fit in four 16-byte
+// registers per thread, they are loaded from global memory while the current one computes.
+// d must be a multiple of 4 (checked at launch).
 // ---------------------------------------------------------------------------
-template <typename IO, bool LN>
-__global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p)
+constexpr int kLinThreads = 256;  // threads of the TTT-Linear kernel
+constexpr int kLinWarps = kLinThreads / 32;
+constexpr int kPrefetchVec = 4;   // 16-byte vectors of K, Q, V a thread may hold in registers
+
+template <typename IO> struct Vec4;
+template <> struct Vec4<float> {
+    using T = float4;
+    static __device__ __forceinline__ float4 load(const float *p, size_t i)
+    {
+        return *reinterpret_cast<const float4 *>(p + i);
+    }
+    static __device__ __forceinline__ float4 to_f32(float4 v) { return v; }
+};
+template <> struct Vec4<__nv_bfloat16> {
+    using T = uint2;
+    static __device__ __forceinline__ uint2 load(const __nv_bfloat16 *p, size_t i)
+    {
+        return *reinterpret_cast<const uint2 *>(p + i);
+    }
+    static __device__ __forceinline__ float4 to_f32(uint2 v)
+    {
+        return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+    }
+};
+
+__device__ __forceinline__ float4 f4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void fma4(float4 &a, float s, float4 b)
 {
-    extern __shared__ float sm[];
-    const int d = p.d, mb = p.mb, L = p.L;
+    a.x = fmaf(s, b.x, a.x);
+    a.y = fmaf(s, b.y, a.y);
+    a.z = fmaf(s, b.z, a.z);
+    a.w = fmaf(s, b.w, a.w);
+}
+
+// DC: the head dim as a compile-time constant (0: taken from the parameters at run time)
+template <typename IO, bool LN, int DC>
+__global__ void __launch_bounds__(kLinThreads) linear_generic_kernel(LinearParams p)
+{
+    constexpr int kThreads = kLinThreads, kWarps = kLinWarps;
+    extern __shared__ float4 sm4[];
+    float *sm = reinterpret_cast<float *>(sm4);
+    const int d = DC ? DC : p.d, mb = p.mb, L = p.L;
     const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int d4 = d >> 2;
     float *W = sm;                 // d*d
     float *c = W + d * d;          // d
     float *Kt = c + d;             // mb*d
@@ -206,39 +251,91 @@ __global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p
     const IO *Vg = static_cast<const IO *>(p.V) + (size_t)bh * L * d;
     IO *Zg = static_cast<IO *>(p.Z) + (size_t)bh * L * d;
     const float *eg = p.eta + (size_t)bh * L;
-    const int nt = mb * d;
+    const int nt = mb * d, nt4 = nt >> 2;
 
-    for (int n0 = 0; n0 < L; n0 += mb) {
-        __syncthreads();
-        for (int i = tid; i < nt; i += kThreads) {
-            size_t gi = (size_t)n0 * d + i;
-            Kt[i] = load_io(Kg, gi);
-            Qt[i] = load_io(Qg, gi);
-            Vt[i] = load_io(Vg, gi);
-        }
-        for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
-        __syncthreads();
-        // key- and query-side products at the mini-batch's starting weights; with weight
-        // decay the query row t sees (1 - lambda sum_{s<=t} eta_s) W_start
-        for (int i = tid; i < nt; i += kThreads) {
-            const int s = i / d, j = i - s * d;
-            float ak = c[j], aq = 0.f;
-            const float *kr = Kt + s * d, *qr = Qt + s * d;
-            for (int u = 0; u < d; ++u) {
-                const float w = W[u * d + j];
-                ak = fmaf(kr[u], w, ak);
-                aq = fmaf(qr[u], w, aq);
+    // K, Q, V of a mini-batch: 3 nt4 vectors of 4 elements; vector v of the three tiles
+    const bool prefetch = 3 * nt4 <= kPrefetchVec * kThreads;
+    using V4 = Vec4<IO>;
+    typename V4::T pre[kPrefetchVec];
+    float pre_eta = 0.f;
+    auto fetch = [&](int n0) {   // this thread's vectors (and eta) of mini-batch n0 into registers
+        if (tid < mb) pre_eta = eg[n0 + tid];
+#pragma unroll
+        for (int r = 0; r < kPrefetchVec; ++r) {
+            const int v = tid + r * kThreads;
+            if (v < 3 * nt4) {
+                const int which = v / nt4, i = (v - which * nt4) * 4;
+                const IO *src = which == 0 ? Kg : which == 1 ? Qg : Vg;
+                pre[r] = V4::load(src, (size_t)n0 * d + i);
             }
-            G[i] = ak;
-            Zb[i] = fmaf(1.f - p.wd * eta_prefix(et, s), aq, c[j]);
         }
+    };
+    auto stage = [&](int n0) {   // K, Q, V, eta of mini-batch n0 into shared memory (fp32)
+        if (prefetch) {
+#pragma unroll
+            for (int r = 0; r < kPrefetchVec; ++r) {
+                const int v = tid + r * kThreads;
+                if (v < 3 * nt4) {
+                    const int which = v / nt4, i = (v - which * nt4) * 4;
+                    float *dst = which == 0 ? Kt : which == 1 ? Qt : Vt;
+                    *reinterpret_cast<float4 *>(dst + i) = V4::to_f32(pre[r]);
+                }
+            }
+            if (tid < mb) et[tid] = pre_eta;
+        } else {
+            for (int v = tid; v < 3 * nt4; v += kThreads) {
+                const int which = v / nt4, i = (v - which * nt4) * 4;
+                const IO *src = which == 0 ? Kg : which == 1 ? Qg : Vg;
+                float *dst = which == 0 ? Kt : which == 1 ? Qt : Vt;
+                *reinterpret_cast<float4 *>(dst + i) = V4::to_f32(V4::load(src, (size_t)n0 * d + i));
+            }
+            for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
+        }
+    };
+
+    if (prefetch) fetch(0);
+    for (int n0 = 0; n0 < L; n0 += mb) {
+        __syncthreads();   // the previous mini-batch is done with the tiles
+        stage(n0);
+        __syncthreads();
+        if (prefetch && n0 + mb < L) fetch(n0 + mb);
+        // key- and query-side products at the mini-batch's starting weights: thread tile =
+        // 4 features of one token, both sides; with weight decay the query row t sees
+        // (1 - lambda sum_{s<=t} eta_s) W_start
+        for (int tile = tid; tile < nt4; tile += kThreads) {
+            const int t = tile / d4, j = (tile - t * d4) * 4;
+            float4 ak = f4(c + j), aq = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float *kr = Kt + t * d, *qr = Qt + t * d;
+#pragma unroll(DC ? DC / 4 : 1)
+            for (int u = 0; u < d; u += 4) {
+                const float4 k4 = f4(kr + u), q4 = f4(qr + u);
+                const float4 w0 = f4(W + u * d + j), w1 = f4(W + (u + 1) * d + j);
+                const float4 w2 = f4(W + (u + 2) * d + j), w3 = f4(W + (u + 3) * d + j);
+                fma4(ak, k4.x, w0); fma4(ak, k4.y, w1); fma4(ak, k4.z, w2); fma4(ak, k4.w, w3);
+                fma4(aq, q4.x, w0); fma4(aq, q4.y, w1); fma4(aq, q4.z, w2); fma4(aq, q4.w, w3);
+            }
+            *reinterpret_cast<float4 *>(G + t * d + j) = ak;
+            const float f = 1.f - p.wd * eta_prefix(et, t);
+            const float4 cj = f4(c + j);
+            *reinterpret_cast<float4 *>(Zb + t * d + j) =
+                make_float4(fmaf(f, aq.x, cj.x), fmaf(f, aq.y, cj.y), fmaf(f, aq.z, cj.z), fmaf(f, aq.w, cj.w));
+        }
+        // A[t, s] = eta_s (q_t . k_s + 1), s <= t
         for (int i = tid; i < mb * mb; i += kThreads) {
             const int t = i / mb, s = i - t * mb;
             float a = 0.f;
             if (s <= t) {
                 const float *qr = Qt + t * d, *kr = Kt + s * d;
-                for (int u = 0; u < d; ++u) a = fmaf(qr[u], kr[u], a);
-                a = (a + 1.f) * et[s];
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll(DC ? DC / 4 : 1)
+                for (int u = 0; u < d; u += 4) {
+                    const float4 q4 = f4(qr + u), k4 = f4(kr + u);
+                    a0 = fmaf(q4.x, k4.x, a0);
+                    a1 = fmaf(q4.y, k4.y, a1);
+                    a0 = fmaf(q4.z, k4.z, a0);
+                    a1 = fmaf(q4.w, k4.w, a1);
+                }
+                a = (a0 + a1 + 1.f) * et[s];
             }
             A[i] = a;
         }
@@ -254,23 +351,45 @@ __global__ void __launch_bounds__(kThreads) linear_generic_kernel(LinearParams p
             for (int i = tid; i < nt; i += kThreads) G[i] = p.ip ? -Vt[i] : G[i] - Vt[i];
         }
         __syncthreads();
-        // dual-form outputs
-        for (int i = tid; i < nt; i += kThreads) {
-            const int t = i / d, j = i - t * d;
-            float z = Zb[i];
-            for (int s = 0; s <= t; ++s) z = fmaf(-A[t * mb + s], G[s * d + j], z);
-            if (LN)
-                Zb[i] = z;
-            else
-                store_io(Zg, (size_t)(n0 + t) * d + j, z);
+        // dual-form outputs: Zb[t] -= sum_{s <= t} A[t, s] G[s]   (4 features of one token)
+        for (int tile = tid; tile < nt4; tile += kThreads) {
+            const int t = tile / d4, j = (tile - t * d4) * 4;
+            float4 z = f4(Zb + t * d + j);
+            for (int s = 0; s <= t; ++s) fma4(z, -A[t * mb + s], f4(G + s * d + j));
+            if (LN) {
+                *reinterpret_cast<float4 *>(Zb + t * d + j) = z;
+            } else {
+                const size_t o = (size_t)(n0 + t) * d + j;
+                store_io(Zg, o, z.x);
+                store_io(Zg, o + 1, z.y);
+                store_io(Zg, o + 2, z.z);
+                store_io(Zg, o + 3, z.w);
+            }
         }
-        // carry: W <- (1 - lambda sum eta) W - K^T diag(eta) G, c -= eta^T G
+        // carry: W <- (1 - lambda sum eta) W - K^T diag(eta) G (4 x 4 blocks of W),
+        // c -= eta^T G
         const float decay = 1.f - p.wd * eta_prefix(et, mb - 1);
-        for (int i = tid; i < d * d; i += kThreads) {
-            const int u = i / d, j = i - u * d;
-            float acc = 0.f;
-            for (int s = 0; s < mb; ++s) acc = fmaf(et[s] * Kt[s * d + u], G[s * d + j], acc);
-            W[i] = fmaf(decay, W[i], -acc);
+        for (int tile = tid; tile < d4 * d4; tile += kThreads) {
+            const int u = (tile / d4) * 4, j = (tile - (tile / d4) * d4) * 4;
+            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+            for (int s = 0; s < mb; ++s) {
+                const float e = et[s];
+                const float4 k4 = f4(Kt + s * d + u), g4 = f4(G + s * d + j);
+                fma4(a0, e * k4.x, g4);
+                fma4(a1, e * k4.y, g4);
+                fma4(a2, e * k4.z, g4);
+                fma4(a3, e * k4.w, g4);
+            }
+            const float4 acc[4] = {a0, a1, a2, a3};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float4 x = *reinterpret_cast<float4 *>(W + (u + r) * d + j);
+                x.x = fmaf(decay, x.x, -acc[r].x);
+                x.y = fmaf(decay, x.y, -acc[r].y);
+                x.z = fmaf(decay, x.z, -acc[r].z);
+                x.w = fmaf(decay, x.w, -acc[r].w);
+                *reinterpret_cast<float4 *>(W + (u + r) * d + j) = x;
+            }
         }
         for (int j = tid; j < d; j += kThreads) {
             float acc = 0.f;
@@ -492,7 +611,7 @@ cudaError_t launch(K kernel, int grid, size_t smem, cudaStream_t stream, const v
 
 size_t linear_generic_smem_bytes(const ttt_desc &s)
 {
-    if (s.d > 128 || s.mini_batch > 64) return 0;
+    if (s.d > 128 || s.d % 4 != 0 || s.mini_batch > 64) return 0;
     size_t d = s.d, mb = s.mini_batch;
     size_t n = d * d + d + 5 * mb * d + mb * mb + mb + 2 * d;
     size_t bytes = n * sizeof(float);
@@ -508,11 +627,18 @@ cudaError_t launch_linear_generic(const LinearArgs &a)
     p.hoff = head_offset(s);
     const size_t smem = linear_generic_smem_bytes(s);
     const int grid = call_rows(s);
-    if (s.io_dtype == TTT_F32)
-        return s.residual_ln ? launch(linear_generic_kernel<float, true>, grid, smem, a.stream, &p)
-                             : launch(linear_generic_kernel<float, false>, grid, smem, a.stream, &p);
-    return s.residual_ln ? launch(linear_generic_kernel<__nv_bfloat16, true>, grid, smem, a.stream, &p)
-                         : launch(linear_generic_kernel<__nv_bfloat16, false>, grid, smem, a.stream, &p);
+    const bool f32 = s.io_dtype == TTT_F32, ln = s.residual_ln != 0, d64 = s.d == 64;
+    auto pick = [&](auto k64, auto kany) { return d64 ? (const void *)k64 : (const void *)kany; };
+    const void *k = f32 ? (ln ? pick(linear_generic_kernel<float, true, 64>, linear_generic_kernel<float, true, 0>)
+                              : pick(linear_generic_kernel<float, false, 64>, linear_generic_kernel<float, false, 0>))
+                        : (ln ? pick(linear_generic_kernel<__nv_bfloat16, true, 64>,
+                                     linear_generic_kernel<__nv_bfloat16, true, 0>)
+                              : pick(linear_generic_kernel<__nv_bfloat16, false, 64>,
+                                     linear_generic_kernel<__nv_bfloat16, false, 0>));
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    void *args[] = {&p};
+    return cudaLaunchKernel(k, dim3(grid), dim3(kLinThreads), args, smem, a.stream);
 }
 
 size_t mlp_generic_smem_bytes(const ttt_desc &s)

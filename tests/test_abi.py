@@ -112,6 +112,7 @@ def test_kernel_choice(lib):
     assert k(io_dtype=0) == "ttt_linear_generic"
     assert k(d=32) == "ttt_linear_generic"
     assert k(d=256) is None
+    assert k(d=6, io_dtype=0) is None   # the generic kernel takes d a multiple of 4
     m = lambda **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), 1))
     assert m() == "ttt_mlp_fused"                    # d_hidden 0 -> 4 d = 256
     assert m(residual_ln=1, d_hidden=256) == "ttt_mlp_fused"
