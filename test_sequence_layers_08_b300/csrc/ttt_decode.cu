@@ -10,6 +10,12 @@
 //   g = z - v_t                      (plain)   or   g = LNbwd(z; v_t - k_t)   (residual LN)
 //   W -= eta_t k_t^T g,   c -= eta_t g
 //   o = q_t W + c,   Z_t = o   or   Z_t = q_t + LN(o)
+// With the residual LayerNorm the output is taken from the products with the state before
+// the update, o = q_t W_old + c_new - eta_t (q_t . k_t) g  ((1 - eta_t lambda) q_t W_old with
+// decay), so one sweep over W gives both k_t W_old and q_t W_old and a token costs two
+// sweeps (products, update) instead of three; the q . k butterfly hides under the
+// LayerNorm's.  Without the LayerNorm the chain per token is short and three sweeps with
+// more independent partial sums are faster (B300: 17.2 against 18.1 us for 16 tokens).
 // with LNbwd the gradient of 1/2 |gamma xhat + beta - y|^2, xhat = (z - mu) r, through the
 // LayerNorm: g = r (gx - mean(gx) - xhat mean(gx xhat)), gx = gamma (gamma xhat + beta - y).
 // The inner-learner variants of the ai-feeds Modular TTT page: with the inner-product loss
@@ -86,7 +92,7 @@ __device__ __forceinline__ float2 warp_sum2(float a, float b)
     return make_float2(a, b);
 }
 
-template <bool BF16, bool LN>
+template <bool BF16, bool LN, bool WD>
 __global__ void __launch_bounds__(kWarps * 32)
 linear_decode_kernel(DecodeParams p)
 {
@@ -123,17 +129,37 @@ linear_decode_kernel(DecodeParams p)
 #pragma unroll
         for (int i4 = 0; i4 < D / 4; ++i4) {
             const float4 x = xs[i4];
-            a0[0] = fmaf(x.x, w[4 * i4][0], a0[0]);
-            a1[0] = fmaf(x.x, w[4 * i4][1], a1[0]);
-            a0[1] = fmaf(x.y, w[4 * i4 + 1][0], a0[1]);
-            a1[1] = fmaf(x.y, w[4 * i4 + 1][1], a1[1]);
-            a0[2] = fmaf(x.z, w[4 * i4 + 2][0], a0[2]);
-            a1[2] = fmaf(x.z, w[4 * i4 + 2][1], a1[2]);
-            a0[3] = fmaf(x.w, w[4 * i4 + 3][0], a0[3]);
-            a1[3] = fmaf(x.w, w[4 * i4 + 3][1], a1[3]);
+            const float xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                a0[e] = fmaf(xv[e], w[4 * i4 + e][0], a0[e]);
+                a1[e] = fmaf(xv[e], w[4 * i4 + e][1], a1[e]);
+            }
         }
         r0 = (a0[0] + a0[1]) + (a0[2] + a0[3]);
         r1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
+    };
+    // k W and q W for the rows staged at ks4, qs4 (16-byte broadcasts), four partial sums each
+    auto rows_times_w = [&](const float4 *ks4, const float4 *qs4, float &z0, float &z1, float &y0,
+                            float &y1) {
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+        float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i4 = 0; i4 < D / 4; ++i4) {
+            const float4 x = ks4[i4], y = qs4[i4];
+            const float xv[4] = {x.x, x.y, x.z, x.w}, yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                a0[e] = fmaf(xv[e], w[4 * i4 + e][0], a0[e]);
+                a1[e] = fmaf(xv[e], w[4 * i4 + e][1], a1[e]);
+                b0[e] = fmaf(yv[e], w[4 * i4 + e][0], b0[e]);
+                b1[e] = fmaf(yv[e], w[4 * i4 + e][1], b1[e]);
+            }
+        }
+        z0 = (a0[0] + a0[1]) + (a0[2] + a0[3]);
+        z1 = (a1[0] + a1[1]) + (a1[2] + a1[3]);
+        y0 = (b0[0] + b0[1]) + (b0[2] + b0[3]);
+        y1 = (b1[0] + b1[1]) + (b1[2] + b1[3]);
     };
 
     // the next token's inputs are loaded while the current one is computed
@@ -155,9 +181,15 @@ linear_decode_kernel(DecodeParams p)
         *reinterpret_cast<float2 *>(ks + j0) = k;
         __syncwarp();
 
-        // key-side forward and the token's gradient at the current weights
-        float z0, z1;
-        row_times_w(rows[warp][1], z0, z1);
+        // key-side product with the state before this token's update (with the LayerNorm also
+        // the query-side product and q . k)
+        float z0, z1, y0 = 0.f, y1 = 0.f, qk = 0.f;
+        if (LN) {
+            rows_times_w(rows[warp][1], rows[warp][0], z0, z1, y0, y1);
+            qk = warp_sum(fmaf(q.x, k.x, q.y * k.y));
+        } else {
+            row_times_w(rows[warp][1], z0, z1);
+        }
         z0 += c0;
         z1 += c1;
         float g0, g1;
@@ -181,27 +213,32 @@ linear_decode_kernel(DecodeParams p)
 
         // W <- (1 - eta lambda) W - eta k^T g,  c -= eta g   (the factor is 1 without decay)
         const float eg0 = et * g0, eg1 = et * g1;
-        const float dec = 1.f - et * p.wd;
+        const float dec = WD ? 1.f - et * p.wd : 1.f;
 #pragma unroll
         for (int i4 = 0; i4 < D / 4; ++i4) {
             const float4 x = rows[warp][1][i4];
-            w[4 * i4][0] = fmaf(-eg0, x.x, dec * w[4 * i4][0]);
-            w[4 * i4][1] = fmaf(-eg1, x.x, dec * w[4 * i4][1]);
-            w[4 * i4 + 1][0] = fmaf(-eg0, x.y, dec * w[4 * i4 + 1][0]);
-            w[4 * i4 + 1][1] = fmaf(-eg1, x.y, dec * w[4 * i4 + 1][1]);
-            w[4 * i4 + 2][0] = fmaf(-eg0, x.z, dec * w[4 * i4 + 2][0]);
-            w[4 * i4 + 2][1] = fmaf(-eg1, x.z, dec * w[4 * i4 + 2][1]);
-            w[4 * i4 + 3][0] = fmaf(-eg0, x.w, dec * w[4 * i4 + 3][0]);
-            w[4 * i4 + 3][1] = fmaf(-eg1, x.w, dec * w[4 * i4 + 3][1]);
+            w[4 * i4][0] = fmaf(-eg0, x.x, WD ? dec * w[4 * i4][0] : w[4 * i4][0]);
+            w[4 * i4][1] = fmaf(-eg1, x.x, WD ? dec * w[4 * i4][1] : w[4 * i4][1]);
+            w[4 * i4 + 1][0] = fmaf(-eg0, x.y, WD ? dec * w[4 * i4 + 1][0] : w[4 * i4 + 1][0]);
+            w[4 * i4 + 1][1] = fmaf(-eg1, x.y, WD ? dec * w[4 * i4 + 1][1] : w[4 * i4 + 1][1]);
+            w[4 * i4 + 2][0] = fmaf(-eg0, x.z, WD ? dec * w[4 * i4 + 2][0] : w[4 * i4 + 2][0]);
+            w[4 * i4 + 2][1] = fmaf(-eg1, x.z, WD ? dec * w[4 * i4 + 2][1] : w[4 * i4 + 2][1]);
+            w[4 * i4 + 3][0] = fmaf(-eg0, x.w, WD ? dec * w[4 * i4 + 3][0] : w[4 * i4 + 3][0]);
+            w[4 * i4 + 3][1] = fmaf(-eg1, x.w, WD ? dec * w[4 * i4 + 3][1] : w[4 * i4 + 3][1]);
         }
         c0 -= eg0;
         c1 -= eg1;
 
         // the output with the weights after this token's update
         float o0, o1;
-        row_times_w(rows[warp][0], o0, o1);
-        o0 += c0;
-        o1 += c1;
+        if (LN) {   // q W_new + c_new = dec (q W_old) - eta (q . k) g + c_new
+            o0 = fmaf(-eg0, qk, fmaf(dec, y0, c0));
+            o1 = fmaf(-eg1, qk, fmaf(dec, y1, c1));
+        } else {
+            row_times_w(rows[warp][0], o0, o1);
+            o0 += c0;
+            o1 += c1;
+        }
         if (LN) {
             const float mu = warp_sum(o0 + o1) * (1.f / D);
             const float oc0 = o0 - mu, oc1 = o1 - mu;
@@ -230,15 +267,13 @@ cudaError_t launch_linear_decode(const DecodeArgs &a)
     DecodeParams p{BH, d.H, d.L, head_offset(d), d.ln_eps, d.loss == TTT_LOSS_INNER_PRODUCT,
                    d.weight_decay, a.Q, a.K, a.V, a.eta, a.W, a.b, a.gamma, a.beta, a.Z};
     const int grid = (BH + kWarps - 1) / kWarps;
-    const bool bf16 = d.io_dtype == TTT_BF16;
-    if (bf16 && d.residual_ln)
-        linear_decode_kernel<true, true><<<grid, kWarps * 32, 0, a.stream>>>(p);
-    else if (bf16)
-        linear_decode_kernel<true, false><<<grid, kWarps * 32, 0, a.stream>>>(p);
-    else if (d.residual_ln)
-        linear_decode_kernel<false, true><<<grid, kWarps * 32, 0, a.stream>>>(p);
-    else
-        linear_decode_kernel<false, false><<<grid, kWarps * 32, 0, a.stream>>>(p);
+    const bool bf16 = d.io_dtype == TTT_BF16, ln = d.residual_ln != 0, wd = d.weight_decay != 0.f;
+    using K = void (*)(DecodeParams);
+    const K table[2][2][2] = {{{linear_decode_kernel<false, false, false>, linear_decode_kernel<false, false, true>},
+                               {linear_decode_kernel<false, true, false>, linear_decode_kernel<false, true, true>}},
+                              {{linear_decode_kernel<true, false, false>, linear_decode_kernel<true, false, true>},
+                               {linear_decode_kernel<true, true, false>, linear_decode_kernel<true, true, true>}}};
+    table[bf16][ln][wd]<<<grid, kWarps * 32, 0, a.stream>>>(p);
     return cudaGetLastError();
 }
 
