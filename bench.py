@@ -72,7 +72,7 @@ def algorithmic_bytes(cfg) -> float:
 
 
 KERNEL_SOURCES = {"ttt_linear_fused": "ttt_linear_tc.cu", "ttt_linear_chunked": "ttt_linear_chunk.cu",
-                  "ttt_mlp_fused": "ttt_mlp_tc.cu",
+                  "ttt_mlp_fused": "ttt_mlp_tc.cu", "ttt_linear_decode": "ttt_decode.cu",
                   "ttt_linear_generic": "ttt_generic.cu", "ttt_mlp_generic": "ttt_generic.cu"}
 
 
@@ -649,9 +649,11 @@ def run_decode(args, cfg, world, rank, local):
 
     peaks = load_peaks()
     achieved = alg_bytes / (ms_step * 1e-3) / 1e9
+    dkname = "ttt_linear_decode" if d == 64 else "ttt_linear_generic"
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peaks["source"],
-            "kernel": "ttt_linear_decode" if d == 64 else "ttt_linear_generic",
+            "frac": achieved / peaks["hbm_gbs"],
+            "traffic": measured_traffic(dkname, f"decode_{cfg.name}_T{T}"),
+            "peak_source": peaks["source"], "kernel": dkname,
             "algorithmic_bytes": alg_bytes, "algorithmic_flops": alg_flops,
             "roofline_ms": alg_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3}
     cpu = None
