@@ -1,4 +1,4 @@
-"""Python binding of libttt.so: the TTT inner-loop forward on B300 (sm_103a).
+"""Python binding of libttt.so: the TTT inner loop on B300 (sm_103a).
 
 Argument marshalling only: every step of the computation runs in the CUDA
 kernels behind the C ABI declared in ``include/ttt.h``.  Torch tensors are
@@ -10,6 +10,9 @@ Functions mirror the C entry points:
     ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma, beta, ...) -> (Z, W_final, b_final)
       (every entry point takes loss="mse"|"ip" and weight_decay=lambda)
     ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma, beta, ...) -> (Z, W1_f, b1_f, W2_f, b2_f)
+    ttt_linear_step(Q, K, V, eta, W, b, gamma, beta, ...) -> Z   (decode, state in place)
+    ttt_linear_bwd(Q, K, V, eta, W0, b0, dZ, dW_final, db_final, ...)
+        -> (dQ, dK, dV, deta, dW0, db0)
     ttt_sync_status(stream=None)
     kernel_name(...)
 """
@@ -20,6 +23,7 @@ import os
 import threading
 
 __all__ = ["TTTError", "Desc", "load", "library_path", "partition_rows", "ttt_eta_gate", "ttt_linear_fwd", "ttt_mlp_fwd", "ttt_linear_step",
+           "ttt_linear_bwd", "ttt_linear_bwd_workspace_size",
            "ttt_sync_status", "kernel_name", "version", "STATUS", "set_wait_timeout_ns",
            "debug_withhold_loads"]
 
@@ -70,6 +74,10 @@ def load():
             lib.ttt_linear_step.argtypes = [dp] + [vp] * 10
             lib.ttt_mlp_fwd.restype = ctypes.c_int
             lib.ttt_mlp_fwd.argtypes = [dp] + [vp] * 16
+            lib.ttt_linear_bwd.restype = ctypes.c_int
+            lib.ttt_linear_bwd.argtypes = [dp] + [vp] * 16 + [ctypes.c_size_t, vp]
+            lib.ttt_linear_bwd_workspace_size.restype = ctypes.c_size_t
+            lib.ttt_linear_bwd_workspace_size.argtypes = [dp]
             lib.ttt_eta_gate.restype = ctypes.c_int
             lib.ttt_eta_gate.argtypes = [ctypes.c_int] * 5 + [ctypes.c_float] + [vp] * 4
             lib.ttt_sync_status.restype = ctypes.c_int
@@ -240,6 +248,58 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: i
                               _ptr(beta if residual_ln else None), _ptr(Z), _ptr(Wf), _ptr(bf),
                               _stream_handle(stream)))
     return Z, Wf, bf
+
+
+def ttt_linear_bwd_workspace_size(Q, *, mini_batch: int = 16, init_per_batch: bool = False,
+                                  heads=None, bh_offset: int = 0, loss: str = "mse") -> int:
+    """Bytes of device workspace ttt_linear_bwd needs for inputs shaped like Q (0 when the
+    shape is not supported)."""
+    desc = make_desc(Q, mini_batch, False, 1e-6, init_per_batch, heads=heads, bh_offset=bh_offset,
+                     loss=loss)
+    return int(load().ttt_linear_bwd_workspace_size(ctypes.byref(desc)))
+
+
+def ttt_linear_bwd(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, *, mini_batch: int = 16,
+                   init_per_batch: bool = False, loss: str = "mse", out=None, workspace=None,
+                   stream=None, heads=None, bh_offset: int = 0):
+    """TTT-Linear backward on the GPU (no residual LayerNorm, no weight decay): the gradients
+    of F = <Z, dZ> + <W_final, dW_final> + <b_final, db_final> for the forward
+    ttt_linear_fwd(Q, K, V, eta, W0, b0, ...).  Returns (dQ, dK, dV, deta, dW0, db0); dW0, db0
+    are shaped like W0, b0.  ``workspace``: a uint8 CUDA tensor of at least
+    ttt_linear_bwd_workspace_size(...) bytes (allocated here when None).  ``out`` reuses
+    output buffers.  Row form as for ttt_linear_fwd.  Asynchronous on ``stream``."""
+    import torch
+    lead, H, L, d, dev = _check_sequence(Q, K, V, eta, None, None, False, heads, bh_offset)
+    init = lead if init_per_batch else (H,)
+    _expect("W0", W0, init + (d, d), torch.float32, dev)
+    _expect("b0", b0, init + (d,), torch.float32, dev)
+    _expect("dZ", dZ, lead + (L, d), Q.dtype, dev)
+    if dW_final is not None:
+        _expect("dW_final", dW_final, lead + (d, d), torch.float32, dev)
+    if db_final is not None:
+        _expect("db_final", db_final, lead + (d,), torch.float32, dev)
+    _require_cuda(dev)
+    lib = load()
+    desc = make_desc(Q, mini_batch, False, 1e-6, init_per_batch, heads=heads, bh_offset=bh_offset,
+                     loss=loss)
+    need = int(lib.ttt_linear_bwd_workspace_size(ctypes.byref(desc)))
+    if need == 0:
+        raise TTTError(2, "ttt_linear_bwd: shape not supported")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _expect("workspace", workspace, (workspace.numel(),), torch.uint8, dev)
+    if out is None:
+        out = (torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V), torch.empty_like(eta),
+               torch.empty_like(W0), torch.empty_like(b0))
+    else:
+        for name, t, ref in zip(("dQ", "dK", "dV", "deta", "dW0", "db0"), out, (Q, K, V, eta, W0, b0)):
+            _expect("out " + name, t, tuple(ref.shape), ref.dtype, dev)
+    dQ, dK, dV, deta, dW0, db0 = out
+    _check(lib.ttt_linear_bwd(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta), _ptr(W0),
+                              _ptr(b0), _ptr(dZ), _ptr(dW_final), _ptr(db_final), _ptr(dQ), _ptr(dK),
+                              _ptr(dV), _ptr(deta), _ptr(dW0), _ptr(db0), _ptr(workspace),
+                              ctypes.c_size_t(workspace.numel()), _stream_handle(stream)))
+    return dQ, dK, dV, deta, dW0, db0
 
 
 def ttt_linear_step(Q, K, V, eta, W, b, gamma=None, beta=None, *, residual_ln: bool = False,

@@ -1,0 +1,394 @@
+// ttt_backward.cu -- backward pass of the TTT-Linear inner loop (no residual LayerNorm).
+//
+// Training through the inner loop (the meta-learning gradient of the damodev.csdn.net TTT
+// article, section 6.1) needs the vector-Jacobian product of the mini-batch scan of
+// sections 4.1-4.2: given dZ and the gradients dW_final, db_final of the final state,
+// the gradients of Q, K, V, eta, W0, b0.  Per mini-batch n, with E = diag(eta_n), the
+// causal mask M (s <= t) and the forward
+//   P = K W + 1 c,  G = P - V  (inner-product loss: G = -V),
+//   A = M . (Q K^T + 1) E,  Z = Q W + 1 c - A G,
+//   W' = W - K^T E G,  c' = c - G^T eta,
+// the reverse step from the gradients dW', dc' of the state after the mini-batch is
+//   dG  = -A^T dZ - E K dW' - eta dc'^T,          D = M . (dZ G^T)
+//   dQ  = dZ W^T - D E K
+//   dK  = dG W^T - E G dW'^T - E D^T Q             (the dG W^T term: squared-error loss)
+//   dV  = -dG
+//   deta_s = -(K dW')_s . g_s - g_s . dc' - sum_t D[t, s] (q_t . k_s + 1)
+//   dW  = dW' + Q^T dZ + K^T dG,   dc = dc' + 1^T dZ + 1^T dG   (K^T dG, 1^T dG: squared error)
+// and dW, dc are the gradients of the state before the mini-batch.  The scan reads the
+// states in reverse, so the kernel first re-runs the forward and checkpoints the state
+// every `ck` mini-batches in the workspace; the reverse pass restores a chunk's states
+// from its checkpoint in shared memory and walks its mini-batches backwards.
+//
+// B300 design: one CTA per (batch, head), 256 threads, fp32 FFMA on shared-memory tiles
+// (register-tiled loops with 16-byte loads).  The gradients of a head-shared initial state
+// are summed over the batch by a second kernel, in a fixed order (deterministic).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ttt_internal.h"
+
+namespace ttt {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float load_io(const float *p, size_t i) { return p[i]; }
+__device__ __forceinline__ float load_io(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void store_io(float *p, size_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void store_io(__nv_bfloat16 *p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float4 f4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void fma4(float4 &a, float s, float4 b)
+{
+    a.x = fmaf(s, b.x, a.x);
+    a.y = fmaf(s, b.y, a.y);
+    a.z = fmaf(s, b.z, a.z);
+    a.w = fmaf(s, b.w, a.w);
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b) { return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w))); }
+
+// out[r][j..j+3] = init[j..j+3] + sum_u X[r][u] Y[u][j..j+3]   (X: m x k, Y: k x n, row-major;
+// n, k multiples of 4; init may be null)
+__device__ void mm_xy(float *out, const float *X, const float *Y, const float *init, int m, int k, int n)
+{
+    const int n4 = n >> 2;
+    for (int tile = threadIdx.x; tile < m * n4; tile += kThreads) {
+        const int r = tile / n4, j = (tile - r * n4) * 4;
+        float4 a = init ? f4(init + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float *xr = X + r * k;
+        for (int u = 0; u < k; u += 4) {
+            const float4 x = f4(xr + u);
+            fma4(a, x.x, f4(Y + u * n + j));
+            fma4(a, x.y, f4(Y + (u + 1) * n + j));
+            fma4(a, x.z, f4(Y + (u + 2) * n + j));
+            fma4(a, x.w, f4(Y + (u + 3) * n + j));
+        }
+        st4(out + r * n + j, a);
+    }
+}
+
+// out[r][i] = sum_j X[r][j] Y[i][j]   (X Y^T; X: m x k, Y: n x k; k a multiple of 4)
+__device__ void mm_xyt(float *out, const float *X, const float *Y, int m, int k, int n)
+{
+    for (int idx = threadIdx.x; idx < m * n; idx += kThreads) {
+        const int r = idx / n, i = idx - r * n;
+        const float *xr = X + r * k, *yr = Y + i * k;
+        float a0 = 0.f, a1 = 0.f;
+        for (int u = 0; u < k; u += 8) {
+            a0 += dot4(f4(xr + u), f4(yr + u));
+            if (u + 4 < k) a1 += dot4(f4(xr + u + 4), f4(yr + u + 4));
+        }
+        out[idx] = a0 + a1;
+    }
+}
+
+// acc[u][j..j+3] += sum_s w_s X[s][u] Y[s][j..j+3]   (X^T diag(w) Y, 4 x 4 blocks; X: m x k,
+// Y: m x n; w may be null (1); sign -1 subtracts)
+__device__ void mm_xty_acc(float *acc, const float *X, const float *Y, const float *w, float sign, int m,
+                           int k, int n)
+{
+    const int n4 = n >> 2, k4 = k >> 2;
+    for (int tile = threadIdx.x; tile < k4 * n4; tile += kThreads) {
+        const int u = (tile / n4) * 4, j = (tile - (tile / n4) * n4) * 4;
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+        for (int s = 0; s < m; ++s) {
+            const float e = w ? w[s] : 1.f;
+            const float4 x = f4(X + s * k + u), y = f4(Y + s * n + j);
+            fma4(a0, e * x.x, y);
+            fma4(a1, e * x.y, y);
+            fma4(a2, e * x.z, y);
+            fma4(a3, e * x.w, y);
+        }
+        const float4 a[4] = {a0, a1, a2, a3};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float4 o = f4(acc + (u + r) * n + j);
+            o.x = fmaf(sign, a[r].x, o.x);
+            o.y = fmaf(sign, a[r].y, o.y);
+            o.z = fmaf(sign, a[r].z, o.z);
+            o.w = fmaf(sign, a[r].w, o.w);
+            st4(acc + (u + r) * n + j, o);
+        }
+    }
+}
+
+struct BwdParams {
+    int H, L, d, mb, ck;      // ck: mini-batches per checkpoint
+    int init_per_batch, ip;
+    const void *Q, *K, *V, *dZ;
+    const float *eta, *W0, *b0, *dWf, *dbf;
+    void *dQ, *dK, *dV;
+    float *deta, *dW0, *db0;  // dW0/db0: per (batch, head) (the partials when the state is head-shared)
+    float *ckpt;              // [rows][nck][d d + d]
+    int hoff;
+};
+
+template <typename IO>
+__device__ void load_tile(float *dst, const IO *src, int n)
+{
+    for (int i = threadIdx.x; i < n; i += kThreads) dst[i] = load_io(src, i);
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
+{
+    extern __shared__ float4 sm4[];
+    float *sm = reinterpret_cast<float *>(sm4);
+    const int d = p.d, mb = p.mb, L = p.L, ck = p.ck, dd = d * d;
+    const int sd = dd + d;                        // one state: W then c
+    const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
+    const int tid = threadIdx.x;
+    const int nmb = L / mb, nck = (nmb + ck - 1) / ck;
+    const int nt = mb * d;
+    const float kf = p.ip ? 0.f : 1.f;
+
+    float *S = sm;                  // ck states [ck][d d + d]
+    float *dW = S + ck * sd;        // d d, then dc (d)
+    float *dc = dW + dd;
+    float *Kt = dc + d;             // mb d each
+    float *Qt = Kt + nt;
+    float *Vt = Qt + nt;
+    float *dZt = Vt + nt;
+    float *G = dZt + nt;
+    float *dG = G + nt;
+    float *T1 = dG + nt;            // dZ W^T, later dG W^T
+    float *T2 = T1 + nt;            // K dW'
+    float *T3 = T2 + nt;            // G dW'^T
+    float *A = T3 + nt;             // mb mb: R = M . (Q K^T + 1) (A = R E)
+    float *Dm = A + mb * mb;        // mb mb
+    float *et = Dm + mb * mb;       // mb
+
+    const IO *Qg = static_cast<const IO *>(p.Q) + (size_t)bh * L * d;
+    const IO *Kg = static_cast<const IO *>(p.K) + (size_t)bh * L * d;
+    const IO *Vg = static_cast<const IO *>(p.V) + (size_t)bh * L * d;
+    const IO *dZg = static_cast<const IO *>(p.dZ) + (size_t)bh * L * d;
+    const float *eg = p.eta + (size_t)bh * L;
+    float *ck_base = p.ckpt + (size_t)bh * nck * sd;
+
+    // one forward mini-batch on the state X (in place): G = kf (K W + c) - V, W -= K^T E G, c -= G^T eta
+    auto forward_step = [&](float *X, int n0) {
+        __syncthreads();
+        load_tile(Kt, Kg + (size_t)n0 * d, nt);
+        load_tile(Vt, Vg + (size_t)n0 * d, nt);
+        for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
+        __syncthreads();
+        mm_xy(G, Kt, X, X + dd, mb, d, d);
+        __syncthreads();
+        for (int i = tid; i < nt; i += kThreads) G[i] = fmaf(G[i], kf, -Vt[i]);
+        __syncthreads();
+        mm_xty_acc(X, Kt, G, et, -1.f, mb, d, d);
+        for (int j = tid; j < d; j += kThreads) {
+            float a = 0.f;
+            for (int s = 0; s < mb; ++s) a = fmaf(et[s], G[s * d + j], a);
+            X[dd + j] -= a;
+        }
+    };
+
+    // ---- pass 1: forward, checkpoint the state at the start of every ck mini-batches
+    const size_t init = p.init_per_batch ? (size_t)bh : (size_t)h;
+    for (int i = tid; i < dd; i += kThreads) S[i] = p.W0[init * dd + i];
+    for (int j = tid; j < d; j += kThreads) S[dd + j] = p.b0[init * d + j];
+    for (int n = 0; n < nmb; ++n) {
+        if (n % ck == 0) {
+            __syncthreads();
+            float *dst = ck_base + (size_t)(n / ck) * sd;
+            for (int i = tid; i < sd; i += kThreads) dst[i] = S[i];
+        }
+        if (n + 1 < nmb) forward_step(S, n * mb);   // the last state is never needed
+    }
+
+    // ---- pass 2: reverse
+    for (int i = tid; i < dd; i += kThreads) dW[i] = p.dWf ? p.dWf[(size_t)bh * dd + i] : 0.f;
+    for (int j = tid; j < d; j += kThreads) dc[j] = p.dbf ? p.dbf[(size_t)bh * d + j] : 0.f;
+    for (int ci = nck - 1; ci >= 0; --ci) {
+        const int m0 = ci * ck, mcount = min(ck, nmb - m0);
+        // restore the chunk's states S[0..mcount)
+        __syncthreads();
+        const float *src = ck_base + (size_t)ci * sd;
+        for (int i = tid; i < sd; i += kThreads) S[i] = src[i];
+        for (int m = 1; m < mcount; ++m) {
+            __syncthreads();
+            for (int i = tid; i < sd; i += kThreads) S[m * sd + i] = S[(m - 1) * sd + i];
+            forward_step(S + m * sd, (m0 + m - 1) * mb);
+        }
+        for (int m = mcount - 1; m >= 0; --m) {
+            const int n0 = (m0 + m) * mb;
+            const float *W = S + m * sd, *c = W + dd;
+            __syncthreads();
+            load_tile(Kt, Kg + (size_t)n0 * d, nt);
+            load_tile(Qt, Qg + (size_t)n0 * d, nt);
+            load_tile(Vt, Vg + (size_t)n0 * d, nt);
+            load_tile(dZt, dZg + (size_t)n0 * d, nt);
+            for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
+            __syncthreads();
+            // G (pre-loss), dZ W^T, K dW', R = M . (Q K^T + 1)
+            mm_xy(G, Kt, W, c, mb, d, d);
+            mm_xyt(T1, dZt, W, mb, d, d);
+            mm_xy(T2, Kt, dW, nullptr, mb, d, d);
+            for (int i = tid; i < mb * mb; i += kThreads) {
+                const int t = i / mb, s = i - t * mb;
+                float a = 0.f;
+                if (s <= t) {
+                    float x = 0.f;
+                    for (int u = 0; u < d; u += 4) x += dot4(f4(Qt + t * d + u), f4(Kt + s * d + u));
+                    a = x + 1.f;
+                }
+                A[i] = a;
+            }
+            __syncthreads();
+            for (int i = tid; i < nt; i += kThreads) G[i] = fmaf(G[i], kf, -Vt[i]);
+            __syncthreads();
+            // G dW'^T, D = M . (dZ G^T), dG = -A^T dZ - E K dW' - eta dc'^T
+            mm_xyt(T3, G, dW, mb, d, d);
+            for (int i = tid; i < mb * mb; i += kThreads) {
+                const int t = i / mb, s = i - t * mb;
+                float x = 0.f;
+                if (s <= t)
+                    for (int u = 0; u < d; u += 4) x += dot4(f4(dZt + t * d + u), f4(G + s * d + u));
+                Dm[i] = x;
+            }
+            for (int tile = tid; tile < nt / 4; tile += kThreads) {
+                const int s = tile / (d / 4), j = (tile - s * (d / 4)) * 4;
+                float4 a = f4(T2 + s * d + j);
+                const float4 dcj = f4(dc + j);
+                a.x = -et[s] * (a.x + dcj.x);
+                a.y = -et[s] * (a.y + dcj.y);
+                a.z = -et[s] * (a.z + dcj.z);
+                a.w = -et[s] * (a.w + dcj.w);
+                for (int t = s; t < mb; ++t) fma4(a, -et[s] * A[t * mb + s], f4(dZt + t * d + j));
+                st4(dG + s * d + j, a);
+            }
+            __syncthreads();
+            // dQ = dZ W^T - D E K;  dV = -dG;  deta;  then T1 <- dG W^T
+            IO *dQg = static_cast<IO *>(p.dQ) + (size_t)bh * L * d + (size_t)n0 * d;
+            IO *dKg = static_cast<IO *>(p.dK) + (size_t)bh * L * d + (size_t)n0 * d;
+            IO *dVg = static_cast<IO *>(p.dV) + (size_t)bh * L * d + (size_t)n0 * d;
+            for (int tile = tid; tile < nt / 4; tile += kThreads) {
+                const int t = tile / (d / 4), j = (tile - t * (d / 4)) * 4;
+                float4 a = f4(T1 + t * d + j);
+                for (int s = 0; s <= t; ++s) fma4(a, -Dm[t * mb + s] * et[s], f4(Kt + s * d + j));
+                store_io(dQg, t * d + j, a.x);
+                store_io(dQg, t * d + j + 1, a.y);
+                store_io(dQg, t * d + j + 2, a.z);
+                store_io(dQg, t * d + j + 3, a.w);
+                const float4 g = f4(dG + t * d + j);
+                store_io(dVg, t * d + j, -g.x);
+                store_io(dVg, t * d + j + 1, -g.y);
+                store_io(dVg, t * d + j + 2, -g.z);
+                store_io(dVg, t * d + j + 3, -g.w);
+            }
+            // deta_s = -(K dW')_s . g_s - g_s . dc' - sum_{t >= s} D[t, s] (q_t . k_s + 1)
+            for (int s = tid; s < mb; s += kThreads) {
+                float a = 0.f;
+                for (int u = 0; u < d; u += 4) {
+                    const float4 g = f4(G + s * d + u);
+                    a -= dot4(f4(T2 + s * d + u), g) + dot4(g, f4(dc + u));
+                }
+                for (int t = s; t < mb; ++t) a -= Dm[t * mb + s] * A[t * mb + s];
+                p.deta[(size_t)bh * L + n0 + s] = a;
+            }
+            __syncthreads();
+            mm_xyt(T1, dG, W, mb, d, d);   // dG W^T
+            __syncthreads();
+            // dK = kf dG W^T - E G dW'^T - E D^T Q
+            for (int tile = tid; tile < nt / 4; tile += kThreads) {
+                const int s = tile / (d / 4), j = (tile - s * (d / 4)) * 4;
+                const float4 t1 = f4(T1 + s * d + j), t3 = f4(T3 + s * d + j);
+                float4 a = make_float4(kf * t1.x - et[s] * t3.x, kf * t1.y - et[s] * t3.y,
+                                       kf * t1.z - et[s] * t3.z, kf * t1.w - et[s] * t3.w);
+                for (int t = s; t < mb; ++t) fma4(a, -et[s] * Dm[t * mb + s], f4(Qt + t * d + j));
+                store_io(dKg, s * d + j, a.x);
+                store_io(dKg, s * d + j + 1, a.y);
+                store_io(dKg, s * d + j + 2, a.z);
+                store_io(dKg, s * d + j + 3, a.w);
+            }
+            // dW += Q^T dZ + kf K^T dG;  dc += 1^T dZ + kf 1^T dG
+            mm_xty_acc(dW, Qt, dZt, nullptr, 1.f, mb, d, d);
+            if (kf != 0.f) mm_xty_acc(dW, Kt, dG, nullptr, 1.f, mb, d, d);
+            for (int j = tid; j < d; j += kThreads) {
+                float a = 0.f;
+                for (int s = 0; s < mb; ++s) a += dZt[s * d + j] + kf * dG[s * d + j];
+                dc[j] += a;
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < dd; i += kThreads) p.dW0[(size_t)bh * dd + i] = dW[i];
+    for (int j = tid; j < d; j += kThreads) p.db0[(size_t)bh * d + j] = dc[j];
+}
+
+// out[h] = sum of part[i] over the call's rows i of head h = (hoff + i) mod H, in row order
+// (deterministic), for a head-shared initial state; heads without a row get 0
+__global__ void sum_over_rows_kernel(const float *part, float *out, int rows, int H, int hoff, int n)
+{
+    const size_t total = (size_t)H * n;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int hh = (int)(i / n);
+        const size_t e = i - (size_t)hh * n;
+        const int first = ((hh - hoff) % H + H) % H;   // the first row of head hh
+        float a = 0.f;
+        for (int r = first; r < rows; r += H) a += part[(size_t)r * n + e];
+        out[i] = a;
+    }
+}
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+size_t smem_for(const ttt_desc &s, int ck)
+{
+    const size_t d = s.d, mb = s.mini_batch;
+    const size_t n = ck * (d * d + d) + d * d + d + 10 * mb * d + 2 * mb * mb + 2 * mb;
+    return n * sizeof(float);
+}
+
+}  // namespace
+
+int linear_bwd_checkpoint_every(const ttt_desc &s)
+{
+    if (s.d > 128 || s.d % 4 != 0 || s.mini_batch > 64 || s.residual_ln || s.weight_decay != 0.f) return 0;
+    for (int ck : {4, 2, 1})
+        if (smem_for(s, ck) <= kMaxSmem) return ck;
+    return 0;
+}
+
+size_t linear_bwd_workspace_bytes(const ttt_desc &s)
+{
+    const int ck = linear_bwd_checkpoint_every(s);
+    if (!ck) return 0;
+    const size_t rows = call_rows(s), d = s.d;
+    const size_t nmb = s.L / s.mini_batch, nck = (nmb + ck - 1) / ck;
+    size_t bytes = rows * nck * (d * d + d) * sizeof(float);
+    if (!s.init_per_batch) bytes += rows * (d * d + d) * sizeof(float);   // per-(batch, head) partials
+    return (bytes + 255) / 256 * 256;
+}
+
+cudaError_t launch_linear_bwd(const LinearBwdArgs &a)
+{
+    const ttt_desc &s = a.desc;
+    const int ck = linear_bwd_checkpoint_every(s);
+    const int rows = call_rows(s);
+    const size_t d = s.d, nmb = s.L / s.mini_batch, nck = (nmb + ck - 1) / ck;
+    float *ckpt = static_cast<float *>(a.workspace);
+    float *part = ckpt + (size_t)rows * nck * (d * d + d);
+    BwdParams p{s.H, s.L, s.d, s.mini_batch, ck, s.init_per_batch, s.loss == TTT_LOSS_INNER_PRODUCT,
+                a.Q, a.K, a.V, a.dZ, a.eta, a.W0, a.b0, a.dW_final, a.db_final, a.dQ, a.dK, a.dV,
+                a.deta, s.init_per_batch ? a.dW0 : part, s.init_per_batch ? a.db0 : part + (size_t)rows * d * d,
+                ckpt, head_offset(s)};
+    const size_t smem = smem_for(s, ck);
+    const void *k = s.io_dtype == TTT_F32 ? (const void *)linear_bwd_kernel<float>
+                                          : (const void *)linear_bwd_kernel<__nv_bfloat16>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    void *args[] = {&p};
+    e = cudaLaunchKernel(k, dim3(rows), dim3(kThreads), args, smem, a.stream);
+    if (e != cudaSuccess || s.init_per_batch) return e;
+    // head-shared initial state: sum the per-(batch, head) gradients over the call's rows
+    sum_over_rows_kernel<<<148, 256, 0, a.stream>>>(part, a.dW0, rows, s.H, head_offset(s), (int)(d * d));
+    sum_over_rows_kernel<<<148, 256, 0, a.stream>>>(part + (size_t)rows * d * d, a.db0, rows, s.H,
+                                                   head_offset(s), (int)d);
+    return cudaGetLastError();
+}
+
+}  // namespace ttt

@@ -42,6 +42,25 @@ struct DecodeArgs {
     cudaStream_t stream;
 };
 
+// One TTT-Linear backward call (pointers already checked; the workspace holds
+// linear_bwd_workspace_bytes(desc) bytes, 256-byte aligned).
+struct LinearBwdArgs {
+    ttt_desc desc;
+    const void *Q, *K, *V, *dZ;
+    const float *eta, *W0, *b0, *dW_final, *db_final;   // dW_final, db_final may be null (0)
+    void *dQ, *dK, *dV;
+    float *deta, *dW0, *db0;
+    void *workspace;
+    cudaStream_t stream;
+};
+
+// TTT-Linear backward (no residual LayerNorm, no weight decay; d <= 128, d % 4 == 0,
+// b <= 64).  *_checkpoint_every returns the mini-batches per state checkpoint (0: the
+// shape is not supported).
+int linear_bwd_checkpoint_every(const ttt_desc &d);
+size_t linear_bwd_workspace_bytes(const ttt_desc &d);
+cudaError_t launch_linear_bwd(const LinearBwdArgs &a);
+
 // One per-token learning-rate gate call: eta [B, H, L] from x [B, L, Dx] and theta [H, Dx].
 struct GateArgs {
     int B, H, L, Dx;
