@@ -73,6 +73,7 @@ def algorithmic_bytes(cfg) -> float:
 
 KERNEL_SOURCES = {"ttt_linear_fused": "ttt_linear_tc.cu", "ttt_linear_chunked": "ttt_linear_chunk.cu",
                   "ttt_mlp_fused": "ttt_mlp_tc.cu", "ttt_linear_decode": "ttt_decode.cu",
+                  "ttt_linear_bwd": "ttt_backward.cu",
                   "ttt_linear_generic": "ttt_generic.cu", "ttt_mlp_generic": "ttt_generic.cu"}
 
 
@@ -687,6 +688,166 @@ def run_decode(args, cfg, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_backward(args, cfg, world, rank, local):
+    """Backward: `ttt_linear_bwd` (the vector-Jacobian product of the TTT-Linear forward) on
+    a linear workload without LayerNorm, with a seeded random dZ, dW_final, db_final.  Each
+    step is one library call (the backward kernel and, for the head-shared initial state,
+    the two per-head sums); consecutive steps rotate over input/output/workspace sets whose
+    union exceeds L2.  FP32 FFMA arithmetic: the roofline is the FP32 ALU peak derived from
+    the SM count and the maximum clock (148 SMs x 128 lanes x 2 FLOP x 2.032 GHz)."""
+    import torch
+    import test_sequence_layers_08_b300 as ttt
+    if cfg.kind != "linear" or cfg.ln:
+        raise SystemExit("--backward runs the TTT-Linear backward: pick a linear workload without LN")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    x = make_inputs(cfg, 0)
+    io = torch.bfloat16 if cfg.io == "bf16" else torch.float32
+    es = 2 if cfg.io == "bf16" else 4
+    if "eta" not in x:   # eta from the library's gate
+        eta_dev = ttt.ttt_eta_gate(torch.from_numpy(x["x"]).to(dev).to(io),
+                                   torch.from_numpy(x["theta"]).to(dev), x["eta_base"])
+        ttt.ttt_sync_status()
+    else:
+        eta_dev = torch.from_numpy(x["eta"]).to(dev)
+    rng = np.random.default_rng(1)
+    B, H, L, d = cfg.B, cfg.H, cfg.L, cfg.d
+    dZ_h = rng.standard_normal((B, H, L, d)).astype(np.float32)
+    dWf_h = rng.standard_normal((B, H, d, d)).astype(np.float32)
+    dbf_h = rng.standard_normal((B, H, d)).astype(np.float32)
+    seq = B * H * L
+    alg_bytes = float(seq * (7 * d * es + 8) + 2 * H * (d * d + d) * 4 + 2 * B * H * (d * d + d) * 4)
+    alg_flops = float(2 * (11 * d * d + 4 * cfg.mini_batch * d) * seq)
+    n_sets = max(1, min(4, math.ceil(3 * L2_BYTES / alg_bytes)))
+
+    def make_set():
+        t = {k: torch.from_numpy(x[k]).to(dev).to(io) for k in ("Q", "K", "V")}
+        t["dZ"] = torch.from_numpy(dZ_h).to(dev).to(io)
+        t["eta"] = eta_dev.clone()
+        t["W0"], t["b0"] = torch.from_numpy(x["W0"]).to(dev), torch.from_numpy(x["b0"]).to(dev)
+        t["dWf"], t["dbf"] = torch.from_numpy(dWf_h).to(dev), torch.from_numpy(dbf_h).to(dev)
+        t["ws"] = torch.empty(ttt.ttt_linear_bwd_workspace_size(t["Q"], mini_batch=cfg.mini_batch),
+                              dtype=torch.uint8, device=dev)
+        t["out"] = (torch.empty_like(t["Q"]), torch.empty_like(t["K"]), torch.empty_like(t["V"]),
+                    torch.empty_like(t["eta"]), torch.empty_like(t["W0"]), torch.empty_like(t["b0"]))
+        return t
+    sets = [make_set() for _ in range(n_sets)]
+    stream = torch.cuda.current_stream(dev)
+
+    def call(t, strm):
+        ttt.ttt_linear_bwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], t["b0"], t["dZ"], t["dWf"],
+                           t["dbf"], mini_batch=cfg.mini_batch, out=t["out"], workspace=t["ws"],
+                           stream=strm)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(args.warmup):
+        call(sets[i % n_sets], stream)
+    ttt.ttt_sync_status(stream)
+    t_soak = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    call(sets[0], stream)
+    e1.record(stream)
+    e1.synchronize()
+    soak_n = int(min(2000, max(0, args.soak_ms / max(e0.elapsed_time(e1), 1e-3))))
+    for i in range(soak_n):
+        call(sets[i % n_sets], stream)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        call(sets[i % n_sets], stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ttt.ttt_sync_status(stream)
+    ms_step = max_over_ranks(world, start.elapsed_time(end)) / args.steps
+    value = world * cfg.tokens / (ms_step * 1e-3)
+    time.sleep(0.4)
+    clk = clocks.summary(t_soak, time.time())
+
+    # end to end: every step copies its inputs in from pinned host memory and its gradients out
+    t0 = sets[0]
+    in_keys = ["Q", "K", "V", "eta", "dZ", "dWf", "dbf"]
+    hin_flat, hin = packed([(tuple(t0[k].shape), t0[k].dtype) for k in in_keys], "cpu", pin=True)
+    for k, hv in zip(in_keys, hin):
+        hv.copy_(t0[k].cpu())
+    din_flat, din = packed([(tuple(t0[k].shape), t0[k].dtype) for k in in_keys], dev)
+    e2e = dict(t0)
+    e2e.update(zip(in_keys, din))
+    out_specs = [(tuple(o.shape), o.dtype) for o in t0["out"]]
+    dout_flat, dout = packed(out_specs, dev)
+    hout_flat = packed(out_specs, "cpu", pin=True)[0]
+    e2e["out"] = tuple(dout)
+    n_e2e = max(3, min(args.steps, 20))
+    for _ in range(2):
+        din_flat.copy_(hin_flat, non_blocking=True)
+        call(e2e, stream)
+        hout_flat.copy_(dout_flat, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(n_e2e):
+        din_flat.copy_(hin_flat, non_blocking=True)
+        call(e2e, stream)
+        hout_flat.copy_(dout_flat, non_blocking=True)
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(world, s0.elapsed_time(s1)) / n_e2e
+    e2e_value = world * cfg.tokens / (e2e_ms * 1e-3)
+    clocks.stop()
+
+    peaks = load_peaks()
+    alu_peak = 148 * 128 * 2 * 2.032e9 / 1e12
+    achieved = alg_flops / (ms_step * 1e-3) / 1e12
+    roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+            "frac": achieved / alu_peak, "traffic": measured_traffic("ttt_linear_bwd", cfg.name),
+            "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 FLOP x 2.032 GHz",
+            "kernel": "ttt_linear_bwd", "algorithmic_bytes": alg_bytes, "algorithmic_flops": alg_flops,
+            "hbm_frac": alg_bytes / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "roofline_ms": alg_flops / (alu_peak * 1e12) * 1e3}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle.backward import ttt_linear_grad
+        threads = torch.get_num_threads()
+        eta_h = eta_dev.cpu().numpy()
+        t_start, done = time.perf_counter(), 0
+        while True:   # whole (batch, head) scans at full L, one at a time
+            bi, hi = divmod(done % (B * H), H)
+            sl = lambda a: a[bi:bi + 1, hi:hi + 1]
+            ttt_linear_grad(sl(x["Q"]), sl(x["K"]), sl(x["V"]), sl(eta_h), x["W0"][hi:hi + 1],
+                            x["b0"][hi:hi + 1], None, None, sl(dZ_h), sl(dWf_h), sl(dbf_h),
+                            mini_batch=cfg.mini_batch)
+            done += 1
+            dt = time.perf_counter() - t_start
+            if dt >= args.cpu_seconds:
+                break
+        cpu = {"value": done * L / H / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{done} (batch, head) backward scans at full L={L} in {dt:.1f} s "
+                         f"(torch autograd, float64); tokens/s = head-tokens/s / H"}
+    if rank == 0:
+        line = {"metric": "TTT-Linear backward tokens/s at 1 B300 and % of roofline (FP32 ALU)",
+                "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic",
+                "config": {"workload": cfg.name + "+backward", "kind": "linear_backward",
+                           "B": B, "H": H, "L": L, "d": d, "mini_batch": cfg.mini_batch, "io": cfg.io,
+                           "l2": f"inputs rotate over {n_sets} sets "
+                                 f"({n_sets * alg_bytes / 1e6:.0f} MB of I/O, plus the checkpoint "
+                                 f"workspaces)",
+                           "parallelism": f"replica x{world}, one CTA per (batch, head)"},
+                "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": "tokens/s",
+                        "h2d_bytes_per_step": hin_flat.numel(), "d2h_bytes_per_step": hout_flat.numel(),
+                        "schedule": "per step: one host->device copy of the inputs and dZ, the call, "
+                                    "one device->host copy of the gradients, one stream"},
+                "gpu_launches": args.steps * 3, "clocks": clk}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -701,6 +862,9 @@ def main():
     ap.add_argument("--decode", type=int, default=0, metavar="T",
                     help="time the decode step instead: T tokens per call, one at a time, from a "
                          "state carried between calls (a linear workload's B, H, d)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the TTT-Linear backward pass (ttt_linear_bwd) instead; the default "
+                         "workload is then linear_bf16_B8_H12_L2048 (the backward has no LN)")
     ap.add_argument("--split", action="store_true",
                     help="with N > 1 GPUs, split one workload's (batch, head) rows over the ranks "
                          "(strong scaling) instead of running a replica on each")
@@ -717,6 +881,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.backward and args.workload == DEFAULT_WORKLOAD:
+        args.workload = "linear_bf16_B8_H12_L2048"
     cfg = CONFIGS[args.workload]
     if args.gated and cfg.eta != "gate":
         raise SystemExit("--gated needs a workload with the per-token gate")
@@ -728,6 +894,8 @@ def main():
             run_reference(args, cfg, world, rank)
         elif args.decode > 0:
             run_decode(args, cfg, world, rank, local)
+        elif args.backward:
+            run_backward(args, cfg, world, rank, local)
         else:
             run_ours(args, cfg, world, rank, local)
     finally:
