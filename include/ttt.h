@@ -185,6 +185,27 @@ TTT_API ttt_status ttt_linear_bwd(const ttt_desc *desc, const void *Q, const voi
                                   size_t workspace_bytes, ttt_stream_t stream);
 
 /*
+ * ttt_linear_bwd on the library's own static device scratch (no counterpart on the pages:
+ * an interface for callers that must not allocate device memory, e.g. a serving or
+ * training process whose device memory is fixed at start-up, or a C caller without a
+ * device allocator of its own).  Same arguments, results and errors as ttt_linear_bwd
+ * without the workspace; it allocates nothing.  The scratch is a 64 MiB file-scope device
+ * array per device (ttt_linear_bwd_static_scratch_bytes()); a call whose
+ * ttt_linear_bwd_workspace_size exceeds it fails with TTT_ERR_INVALID_ARG.  Nothing in it
+ * needs to start at zero.  The first call on a device, with that device current, resolves
+ * the scratch address (cudaGetSymbolAddress, which may load the library's module); make it
+ * before any stream capture.  All calls on a device share the one scratch: calls whose
+ * execution overlaps in time (other streams, other host threads) race on it and give
+ * undefined results, so serialise them (one stream, or synchronise between calls).
+ */
+TTT_API size_t ttt_linear_bwd_static_scratch_bytes(void);
+TTT_API ttt_status ttt_linear_bwd_static(const ttt_desc *desc, const void *Q, const void *K,
+                                         const void *V, const float *eta, const float *W0,
+                                         const float *b0, const void *dZ, const float *dW_final,
+                                         const float *db_final, void *dQ, void *dK, void *dV,
+                                         float *deta, float *dW0, float *db0, ttt_stream_t stream);
+
+/*
  * Per-token learning rate (the learnable gate of the lryc.cn TTT article,
  * section 2.2): eta[b, h, t] = eta_base * sigmoid(theta[h] . x[b, t]).
  *   in : x [B, L, d_model] (x_dtype), the layer's input tokens; theta [H, d_model]

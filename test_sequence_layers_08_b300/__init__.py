@@ -23,7 +23,7 @@ import os
 import threading
 
 __all__ = ["TTTError", "Desc", "load", "library_path", "partition_rows", "ttt_eta_gate", "ttt_linear_fwd", "ttt_mlp_fwd", "ttt_linear_step",
-           "ttt_linear_bwd", "ttt_linear_bwd_workspace_size",
+           "ttt_linear_bwd", "ttt_linear_bwd_workspace_size", "ttt_linear_bwd_static",
            "ttt_sync_status", "kernel_name", "version", "STATUS", "set_wait_timeout_ns",
            "debug_withhold_loads"]
 
@@ -76,6 +76,10 @@ def load():
             lib.ttt_mlp_fwd.argtypes = [dp] + [vp] * 16
             lib.ttt_linear_bwd.restype = ctypes.c_int
             lib.ttt_linear_bwd.argtypes = [dp] + [vp] * 16 + [ctypes.c_size_t, vp]
+            lib.ttt_linear_bwd_static.restype = ctypes.c_int
+            lib.ttt_linear_bwd_static.argtypes = [dp] + [vp] * 16
+            lib.ttt_linear_bwd_static_scratch_bytes.restype = ctypes.c_size_t
+            lib.ttt_linear_bwd_static_scratch_bytes.argtypes = []
             lib.ttt_linear_bwd_workspace_size.restype = ctypes.c_size_t
             lib.ttt_linear_bwd_workspace_size.argtypes = [dp]
             lib.ttt_eta_gate.restype = ctypes.c_int
@@ -300,6 +304,36 @@ def ttt_linear_bwd(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, *, mi
                               _ptr(dV), _ptr(deta), _ptr(dW0), _ptr(db0), _ptr(workspace),
                               ctypes.c_size_t(workspace.numel()), _stream_handle(stream)))
     return dQ, dK, dV, deta, dW0, db0
+
+
+def ttt_linear_bwd_static(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, *, out,
+                          mini_batch: int = 16, init_per_batch: bool = False, loss: str = "mse",
+                          stream=None, heads=None, bh_offset: int = 0):
+    """ttt_linear_bwd on the library's static device scratch: allocates nothing, so the
+    output buffers ``out=(dQ, dK, dV, deta, dW0, db0)`` are required.  Calls on one device
+    share the scratch and must not overlap in time.  Returns ``out``."""
+    import torch
+    lead, H, L, d, dev = _check_sequence(Q, K, V, eta, None, None, False, heads, bh_offset)
+    init = lead if init_per_batch else (H,)
+    _expect("W0", W0, init + (d, d), torch.float32, dev)
+    _expect("b0", b0, init + (d,), torch.float32, dev)
+    _expect("dZ", dZ, lead + (L, d), Q.dtype, dev)
+    if dW_final is not None:
+        _expect("dW_final", dW_final, lead + (d, d), torch.float32, dev)
+    if db_final is not None:
+        _expect("db_final", db_final, lead + (d,), torch.float32, dev)
+    for name, t, ref in zip(("dQ", "dK", "dV", "deta", "dW0", "db0"), out, (Q, K, V, eta, W0, b0)):
+        _expect("out " + name, t, tuple(ref.shape), ref.dtype, dev)
+    _require_cuda(dev)
+    lib = load()
+    desc = make_desc(Q, mini_batch, False, 1e-6, init_per_batch, heads=heads, bh_offset=bh_offset,
+                     loss=loss)
+    dQ, dK, dV, deta, dW0, db0 = out
+    _check(lib.ttt_linear_bwd_static(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta),
+                                     _ptr(W0), _ptr(b0), _ptr(dZ), _ptr(dW_final), _ptr(db_final),
+                                     _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(deta), _ptr(dW0), _ptr(db0),
+                                     _stream_handle(stream)))
+    return out
 
 
 def ttt_linear_step(Q, K, V, eta, W, b, gamma=None, beta=None, *, residual_ln: bool = False,

@@ -35,6 +35,23 @@ ttt_status ok()
     return TTT_OK;
 }
 
+}  // namespace
+
+namespace ttt {
+// Error reports of ttt_linear_bwd_static (its own translation unit), in this file's format.
+ttt_status fail_static_scratch(size_t need, size_t have)
+{
+    return fail(TTT_ERR_INVALID_ARG, "the call needs %zu bytes of scratch, the static scratch holds %zu",
+                need, have);
+}
+ttt_status fail_cuda(const char *what, cudaError_t e)
+{
+    return fail(TTT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+}  // namespace ttt
+
+namespace {
+
 struct Range {
     uintptr_t lo, hi;  // [lo, hi)
 };

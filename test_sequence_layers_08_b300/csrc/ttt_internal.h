@@ -114,6 +114,10 @@ int withhold_loads();
 inline int call_rows(const ttt_desc &d) { return d.bh_count > 0 ? d.bh_count : d.B * d.H; }
 inline int head_offset(const ttt_desc &d) { return d.bh_offset % d.H; }
 
+// Error reports of ttt_linear_bwd_static (set ttt_last_error, return the status).
+ttt_status fail_static_scratch(size_t need, size_t have);
+ttt_status fail_cuda(const char *what, cudaError_t e);
+
 // Device-side status word values.
 enum : unsigned int { kStatusOk = 0u, kStatusTimeout = 1u };
 
