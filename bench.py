@@ -690,15 +690,16 @@ def run_decode(args, cfg, world, rank, local):
 
 def run_backward(args, cfg, world, rank, local):
     """Backward: `ttt_linear_bwd` (the vector-Jacobian product of the TTT-Linear forward) on
-    a linear workload without LayerNorm, with a seeded random dZ, dW_final, db_final.  Each
+    a linear workload (with its residual LayerNorm if it has one), with a seeded random dZ,
+    dW_final, db_final.  Each
     step is one library call (the backward kernel and, for the head-shared initial state,
     the two per-head sums); consecutive steps rotate over input/output/workspace sets whose
     union exceeds L2.  FP32 FFMA arithmetic: the roofline is the FP32 ALU peak derived from
     the SM count and the maximum clock (148 SMs x 128 lanes x 2 FLOP x 2.032 GHz)."""
     import torch
     import test_sequence_layers_08_b300 as ttt
-    if cfg.kind != "linear" or cfg.ln:
-        raise SystemExit("--backward runs the TTT-Linear backward: pick a linear workload without LN")
+    if cfg.kind != "linear":
+        raise SystemExit("--backward runs the TTT-Linear backward: pick a linear workload")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     x = make_inputs(cfg, 0)
@@ -717,7 +718,7 @@ def run_backward(args, cfg, world, rank, local):
     dbf_h = rng.standard_normal((B, H, d)).astype(np.float32)
     seq = B * H * L
     alg_bytes = float(seq * (7 * d * es + 8) + 2 * H * (d * d + d) * 4 + 2 * B * H * (d * d + d) * 4)
-    alg_flops = float(2 * (11 * d * d + 4 * cfg.mini_batch * d) * seq)
+    alg_flops = float(2 * ((12 if cfg.ln else 11) * d * d + 4 * cfg.mini_batch * d) * seq)
     n_sets = max(1, min(4, math.ceil(3 * L2_BYTES / alg_bytes)))
 
     def make_set():
@@ -725,18 +726,24 @@ def run_backward(args, cfg, world, rank, local):
         t["dZ"] = torch.from_numpy(dZ_h).to(dev).to(io)
         t["eta"] = eta_dev.clone()
         t["W0"], t["b0"] = torch.from_numpy(x["W0"]).to(dev), torch.from_numpy(x["b0"]).to(dev)
+        t["gamma"] = None if x["gamma"] is None else torch.from_numpy(x["gamma"]).to(dev)
+        t["beta"] = None if x["beta"] is None else torch.from_numpy(x["beta"]).to(dev)
         t["dWf"], t["dbf"] = torch.from_numpy(dWf_h).to(dev), torch.from_numpy(dbf_h).to(dev)
-        t["ws"] = torch.empty(ttt.ttt_linear_bwd_workspace_size(t["Q"], mini_batch=cfg.mini_batch),
+        t["ws"] = torch.empty(ttt.ttt_linear_bwd_workspace_size(t["Q"], mini_batch=cfg.mini_batch,
+                                                               residual_ln=cfg.ln, ln_eps=cfg.eps),
                               dtype=torch.uint8, device=dev)
         t["out"] = (torch.empty_like(t["Q"]), torch.empty_like(t["K"]), torch.empty_like(t["V"]),
                     torch.empty_like(t["eta"]), torch.empty_like(t["W0"]), torch.empty_like(t["b0"]))
+        if cfg.ln:
+            t["out"] += (torch.empty_like(t["gamma"]), torch.empty_like(t["beta"]))
         return t
     sets = [make_set() for _ in range(n_sets)]
     stream = torch.cuda.current_stream(dev)
 
     def call(t, strm):
         ttt.ttt_linear_bwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], t["b0"], t["dZ"], t["dWf"],
-                           t["dbf"], mini_batch=cfg.mini_batch, out=t["out"], workspace=t["ws"],
+                           t["dbf"], t["gamma"], t["beta"], mini_batch=cfg.mini_batch,
+                           residual_ln=cfg.ln, ln_eps=cfg.eps, out=t["out"], workspace=t["ws"],
                            stream=strm)
 
     clocks = ClockSampler(local)
@@ -818,8 +825,10 @@ def run_backward(args, cfg, world, rank, local):
             bi, hi = divmod(done % (B * H), H)
             sl = lambda a: a[bi:bi + 1, hi:hi + 1]
             ttt_linear_grad(sl(x["Q"]), sl(x["K"]), sl(x["V"]), sl(eta_h), x["W0"][hi:hi + 1],
-                            x["b0"][hi:hi + 1], None, None, sl(dZ_h), sl(dWf_h), sl(dbf_h),
-                            mini_batch=cfg.mini_batch)
+                            x["b0"][hi:hi + 1],
+                            None if x["gamma"] is None else x["gamma"][hi:hi + 1],
+                            None if x["beta"] is None else x["beta"][hi:hi + 1], sl(dZ_h), sl(dWf_h),
+                            sl(dbf_h), mini_batch=cfg.mini_batch, ln=cfg.ln, eps=cfg.eps)
             done += 1
             dt = time.perf_counter() - t_start
             if dt >= args.cpu_seconds:
@@ -844,7 +853,7 @@ def run_backward(args, cfg, world, rank, local):
                         "h2d_bytes_per_step": hin_flat.numel(), "d2h_bytes_per_step": hout_flat.numel(),
                         "schedule": "per step: one host->device copy of the inputs and dZ, the call, "
                                     "one device->host copy of the gradients, one stream"},
-                "gpu_launches": args.steps * 3, "clocks": clk}
+                "gpu_launches": args.steps * (5 if cfg.ln else 3), "clocks": clk}
         print(json.dumps(line), flush=True)
 
 
@@ -863,8 +872,8 @@ def main():
                     help="time the decode step instead: T tokens per call, one at a time, from a "
                          "state carried between calls (a linear workload's B, H, d)")
     ap.add_argument("--backward", action="store_true",
-                    help="time the TTT-Linear backward pass (ttt_linear_bwd) instead; the default "
-                         "workload is then linear_bf16_B8_H12_L2048 (the backward has no LN)")
+                    help="time the TTT-Linear backward pass (ttt_linear_bwd) instead (a linear "
+                         "workload, with or without its residual LayerNorm)")
     ap.add_argument("--split", action="store_true",
                     help="with N > 1 GPUs, split one workload's (batch, head) rows over the ranks "
                          "(strong scaling) instead of running a replica on each")
@@ -881,8 +890,6 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.backward and args.workload == DEFAULT_WORKLOAD:
-        args.workload = "linear_bf16_B8_H12_L2048"
     cfg = CONFIGS[args.workload]
     if args.gated and cfg.eta != "gate":
         raise SystemExit("--gated needs a workload with the per-token gate")

@@ -160,28 +160,33 @@ TTT_API ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const vo
 /*
  * TTT-Linear backward: the vector-Jacobian product of ttt_linear_fwd, the gradient that
  * training through the inner loop needs (the meta-learning gradient of the damodev.csdn.net
- * TTT article, section 6.1, taken through the mini-batch scan of sections 4.1-4.2).  For
- * the outer loss F = <Z, dZ> + <W_final, dW_final> + <b_final, db_final> it writes
+ * TTT article, section 6.1, taken through the mini-batch scan of sections 4.1-4.2, with the
+ * residual LayerNorm of the lryc.cn TTT article, section 2.1).  For the outer loss
+ * F = <Z, dZ> + <W_final, dW_final> + <b_final, db_final> it writes
  *   dQ, dK, dV [B,H,L,d] (io_dtype), deta [B,H,L] float,
  *   dW0 [H or B,H, d, d], db0 [H or B,H, d] float (shaped like W0, b0: with a head-shared
  *        initial state, the sum over the call's rows of each head; a head with no row in
- *        the call gets 0).
- *   in : Q, K, V, dZ [B,H,L,d] (io_dtype); eta [B,H,L]; W0, b0 as the forward;
- *        dW_final [B,H,d,d], db_final [B,H,d] float, or NULL for zero.
+ *        the call gets 0),
+ *   dgamma, dbeta [H, d] float with the residual LayerNorm (the same per-head sums; NULL
+ *        allowed without it).
+ *   in : Q, K, V, dZ [B,H,L,d] (io_dtype); eta [B,H,L]; W0, b0, gamma, beta as the forward
+ *        (gamma, beta NULL allowed without LN); dW_final [B,H,d,d], db_final [B,H,d]
+ *        float, or NULL for zero.
  *   workspace: device memory of at least ttt_linear_bwd_workspace_size(desc) bytes,
  *        256-byte aligned, owned by the caller; the call overwrites it (state checkpoints
  *        of a forward re-run and per-row partial gradients).  Calls that share a workspace
  *        must not overlap in time.
- * Supported: no residual LayerNorm, no weight decay (desc->residual_ln == 0,
- * desc->weight_decay == 0), either loss, d <= 128 with d a multiple of 4, b <= 64; fp32
- * arithmetic.  Otherwise TTT_ERR_UNSUPPORTED.  Outputs may overlap neither each other,
- * the workspace nor an input.
+ * Supported: with or without the residual LayerNorm, either loss, no weight decay
+ * (desc->weight_decay == 0), d <= 128 with d a multiple of 4, b <= 64; fp32 arithmetic.
+ * Otherwise TTT_ERR_UNSUPPORTED.  Outputs may overlap neither each other, the workspace
+ * nor an input.
  */
 TTT_API size_t ttt_linear_bwd_workspace_size(const ttt_desc *desc);   /* 0: invalid or unsupported */
 TTT_API ttt_status ttt_linear_bwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
-                                  const float *eta, const float *W0, const float *b0, const void *dZ,
-                                  const float *dW_final, const float *db_final, void *dQ, void *dK,
-                                  void *dV, float *deta, float *dW0, float *db0, void *workspace,
+                                  const float *eta, const float *W0, const float *b0, const float *gamma,
+                                  const float *beta, const void *dZ, const float *dW_final,
+                                  const float *db_final, void *dQ, void *dK, void *dV, float *deta,
+                                  float *dW0, float *db0, float *dgamma, float *dbeta, void *workspace,
                                   size_t workspace_bytes, ttt_stream_t stream);
 
 /*
@@ -201,9 +206,10 @@ TTT_API ttt_status ttt_linear_bwd(const ttt_desc *desc, const void *Q, const voi
 TTT_API size_t ttt_linear_bwd_static_scratch_bytes(void);
 TTT_API ttt_status ttt_linear_bwd_static(const ttt_desc *desc, const void *Q, const void *K,
                                          const void *V, const float *eta, const float *W0,
-                                         const float *b0, const void *dZ, const float *dW_final,
-                                         const float *db_final, void *dQ, void *dK, void *dV,
-                                         float *deta, float *dW0, float *db0, ttt_stream_t stream);
+                                         const float *b0, const float *gamma, const float *beta,
+                                         const void *dZ, const float *dW_final, const float *db_final,
+                                         void *dQ, void *dK, void *dV, float *deta, float *dW0,
+                                         float *db0, float *dgamma, float *dbeta, ttt_stream_t stream);
 
 /*
  * Per-token learning rate (the learnable gate of the lryc.cn TTT article,
@@ -259,7 +265,8 @@ TTT_API const char *ttt_last_error(void);
 TTT_API const char *ttt_kernel_name(const ttt_desc *desc, int is_mlp);
 
 /* Library ABI version (major * 100 + minor); 101 added bh_offset/bh_count, 102 loss and
- * weight_decay, 103 ttt_linear_bwd. */
+ * weight_decay, 103 ttt_linear_bwd, 104 its residual-LayerNorm form (gamma, beta, dgamma,
+ * dbeta arguments). */
 TTT_API int ttt_version(void);
 
 #ifdef __cplusplus

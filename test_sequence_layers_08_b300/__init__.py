@@ -75,9 +75,9 @@ def load():
             lib.ttt_mlp_fwd.restype = ctypes.c_int
             lib.ttt_mlp_fwd.argtypes = [dp] + [vp] * 16
             lib.ttt_linear_bwd.restype = ctypes.c_int
-            lib.ttt_linear_bwd.argtypes = [dp] + [vp] * 16 + [ctypes.c_size_t, vp]
+            lib.ttt_linear_bwd.argtypes = [dp] + [vp] * 20 + [ctypes.c_size_t, vp]
             lib.ttt_linear_bwd_static.restype = ctypes.c_int
-            lib.ttt_linear_bwd_static.argtypes = [dp] + [vp] * 16
+            lib.ttt_linear_bwd_static.argtypes = [dp] + [vp] * 20
             lib.ttt_linear_bwd_static_scratch_bytes.restype = ctypes.c_size_t
             lib.ttt_linear_bwd_static_scratch_bytes.argtypes = []
             lib.ttt_linear_bwd_workspace_size.restype = ctypes.c_size_t
@@ -255,25 +255,26 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: i
 
 
 def ttt_linear_bwd_workspace_size(Q, *, mini_batch: int = 16, init_per_batch: bool = False,
-                                  heads=None, bh_offset: int = 0, loss: str = "mse") -> int:
+                                  heads=None, bh_offset: int = 0, loss: str = "mse",
+                                  residual_ln: bool = False, ln_eps: float = 1e-6) -> int:
     """Bytes of device workspace ttt_linear_bwd needs for inputs shaped like Q (0 when the
     shape is not supported)."""
-    desc = make_desc(Q, mini_batch, False, 1e-6, init_per_batch, heads=heads, bh_offset=bh_offset,
-                     loss=loss)
+    desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, heads=heads,
+                     bh_offset=bh_offset, loss=loss)
     return int(load().ttt_linear_bwd_workspace_size(ctypes.byref(desc)))
 
 
-def ttt_linear_bwd(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, *, mini_batch: int = 16,
-                   init_per_batch: bool = False, loss: str = "mse", out=None, workspace=None,
-                   stream=None, heads=None, bh_offset: int = 0):
-    """TTT-Linear backward on the GPU (no residual LayerNorm, no weight decay): the gradients
-    of F = <Z, dZ> + <W_final, dW_final> + <b_final, db_final> for the forward
-    ttt_linear_fwd(Q, K, V, eta, W0, b0, ...).  Returns (dQ, dK, dV, deta, dW0, db0); dW0, db0
-    are shaped like W0, b0.  ``workspace``: a uint8 CUDA tensor of at least
-    ttt_linear_bwd_workspace_size(...) bytes (allocated here when None).  ``out`` reuses
-    output buffers.  Row form as for ttt_linear_fwd.  Asynchronous on ``stream``."""
+def _bwd_outputs(Q, K, V, eta, W0, b0, gamma, residual_ln):
     import torch
-    lead, H, L, d, dev = _check_sequence(Q, K, V, eta, None, None, False, heads, bh_offset)
+    o = (torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V), torch.empty_like(eta),
+         torch.empty_like(W0), torch.empty_like(b0))
+    return o + ((torch.empty_like(gamma), torch.empty_like(gamma)) if residual_ln else ())
+
+
+def _bwd_check(Q, K, V, eta, W0, b0, gamma, beta, dZ, dW_final, db_final, out, residual_ln,
+               init_per_batch, heads, bh_offset):
+    import torch
+    lead, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln, heads, bh_offset)
     init = lead if init_per_batch else (H,)
     _expect("W0", W0, init + (d, d), torch.float32, dev)
     _expect("b0", b0, init + (d,), torch.float32, dev)
@@ -282,10 +283,34 @@ def ttt_linear_bwd(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, *, mi
         _expect("dW_final", dW_final, lead + (d, d), torch.float32, dev)
     if db_final is not None:
         _expect("db_final", db_final, lead + (d,), torch.float32, dev)
+    if out is not None:
+        refs = (Q, K, V, eta, W0, b0) + ((gamma, beta) if residual_ln else ())
+        names = ("dQ", "dK", "dV", "deta", "dW0", "db0", "dgamma", "dbeta")
+        if len(out) != len(refs):
+            raise ValueError(f"out must hold {len(refs)} tensors")
+        for name, t, ref in zip(names, out, refs):
+            _expect("out " + name, t, tuple(ref.shape), ref.dtype, dev)
     _require_cuda(dev)
+    return dev
+
+
+def ttt_linear_bwd(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, gamma=None, beta=None,
+                   *, mini_batch: int = 16, residual_ln: bool = False, ln_eps: float = 1e-6,
+                   init_per_batch: bool = False, loss: str = "mse", out=None, workspace=None,
+                   stream=None, heads=None, bh_offset: int = 0):
+    """TTT-Linear backward on the GPU (no weight decay): the gradients of
+    F = <Z, dZ> + <W_final, dW_final> + <b_final, db_final> for the forward
+    ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma, beta, ...).  Returns (dQ, dK, dV, deta, dW0,
+    db0), plus (dgamma, dbeta) with the residual LayerNorm; dW0, db0 are shaped like W0, b0.
+    ``workspace``: a uint8 CUDA tensor of at least ttt_linear_bwd_workspace_size(...) bytes
+    (allocated here when None).  ``out`` reuses output buffers.  Row form as for
+    ttt_linear_fwd.  Asynchronous on ``stream``."""
+    import torch
+    dev = _bwd_check(Q, K, V, eta, W0, b0, gamma, beta, dZ, dW_final, db_final, out, residual_ln,
+                     init_per_batch, heads, bh_offset)
     lib = load()
-    desc = make_desc(Q, mini_batch, False, 1e-6, init_per_batch, heads=heads, bh_offset=bh_offset,
-                     loss=loss)
+    desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, heads=heads,
+                     bh_offset=bh_offset, loss=loss)
     need = int(lib.ttt_linear_bwd_workspace_size(ctypes.byref(desc)))
     if need == 0:
         raise TTTError(2, "ttt_linear_bwd: shape not supported")
@@ -293,45 +318,35 @@ def ttt_linear_bwd(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, *, mi
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     _expect("workspace", workspace, (workspace.numel(),), torch.uint8, dev)
     if out is None:
-        out = (torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V), torch.empty_like(eta),
-               torch.empty_like(W0), torch.empty_like(b0))
-    else:
-        for name, t, ref in zip(("dQ", "dK", "dV", "deta", "dW0", "db0"), out, (Q, K, V, eta, W0, b0)):
-            _expect("out " + name, t, tuple(ref.shape), ref.dtype, dev)
-    dQ, dK, dV, deta, dW0, db0 = out
+        out = _bwd_outputs(Q, K, V, eta, W0, b0, gamma, residual_ln)
+    dgam, dbet = (out[6], out[7]) if residual_ln else (None, None)
     _check(lib.ttt_linear_bwd(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta), _ptr(W0),
-                              _ptr(b0), _ptr(dZ), _ptr(dW_final), _ptr(db_final), _ptr(dQ), _ptr(dK),
-                              _ptr(dV), _ptr(deta), _ptr(dW0), _ptr(db0), _ptr(workspace),
+                              _ptr(b0), _ptr(gamma if residual_ln else None),
+                              _ptr(beta if residual_ln else None), _ptr(dZ), _ptr(dW_final),
+                              _ptr(db_final), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _ptr(out[3]),
+                              _ptr(out[4]), _ptr(out[5]), _ptr(dgam), _ptr(dbet), _ptr(workspace),
                               ctypes.c_size_t(workspace.numel()), _stream_handle(stream)))
-    return dQ, dK, dV, deta, dW0, db0
+    return tuple(out)
 
 
-def ttt_linear_bwd_static(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, *, out,
-                          mini_batch: int = 16, init_per_batch: bool = False, loss: str = "mse",
+def ttt_linear_bwd_static(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, gamma=None,
+                          beta=None, *, out, mini_batch: int = 16, residual_ln: bool = False,
+                          ln_eps: float = 1e-6, init_per_batch: bool = False, loss: str = "mse",
                           stream=None, heads=None, bh_offset: int = 0):
     """ttt_linear_bwd on the library's static device scratch: allocates nothing, so the
-    output buffers ``out=(dQ, dK, dV, deta, dW0, db0)`` are required.  Calls on one device
-    share the scratch and must not overlap in time.  Returns ``out``."""
-    import torch
-    lead, H, L, d, dev = _check_sequence(Q, K, V, eta, None, None, False, heads, bh_offset)
-    init = lead if init_per_batch else (H,)
-    _expect("W0", W0, init + (d, d), torch.float32, dev)
-    _expect("b0", b0, init + (d,), torch.float32, dev)
-    _expect("dZ", dZ, lead + (L, d), Q.dtype, dev)
-    if dW_final is not None:
-        _expect("dW_final", dW_final, lead + (d, d), torch.float32, dev)
-    if db_final is not None:
-        _expect("db_final", db_final, lead + (d,), torch.float32, dev)
-    for name, t, ref in zip(("dQ", "dK", "dV", "deta", "dW0", "db0"), out, (Q, K, V, eta, W0, b0)):
-        _expect("out " + name, t, tuple(ref.shape), ref.dtype, dev)
-    _require_cuda(dev)
+    output buffers ``out=(dQ, dK, dV, deta, dW0, db0[, dgamma, dbeta])`` are required.  Calls
+    on one device share the scratch and must not overlap in time.  Returns ``out``."""
+    _bwd_check(Q, K, V, eta, W0, b0, gamma, beta, dZ, dW_final, db_final, out, residual_ln,
+               init_per_batch, heads, bh_offset)
     lib = load()
-    desc = make_desc(Q, mini_batch, False, 1e-6, init_per_batch, heads=heads, bh_offset=bh_offset,
-                     loss=loss)
-    dQ, dK, dV, deta, dW0, db0 = out
+    desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, heads=heads,
+                     bh_offset=bh_offset, loss=loss)
+    dgam, dbet = (out[6], out[7]) if residual_ln else (None, None)
     _check(lib.ttt_linear_bwd_static(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta),
-                                     _ptr(W0), _ptr(b0), _ptr(dZ), _ptr(dW_final), _ptr(db_final),
-                                     _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(deta), _ptr(dW0), _ptr(db0),
+                                     _ptr(W0), _ptr(b0), _ptr(gamma if residual_ln else None),
+                                     _ptr(beta if residual_ln else None), _ptr(dZ), _ptr(dW_final),
+                                     _ptr(db_final), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                                     _ptr(out[3]), _ptr(out[4]), _ptr(out[5]), _ptr(dgam), _ptr(dbet),
                                      _stream_handle(stream)))
     return out
 

@@ -151,7 +151,7 @@ const char *mlp_kernel(const ttt_desc &s)
 
 extern "C" {
 
-int ttt_version(void) { return 103; }
+int ttt_version(void) { return 104; }
 
 const char *ttt_status_string(ttt_status s)
 {
@@ -237,18 +237,25 @@ size_t ttt_linear_bwd_workspace_size(const ttt_desc *desc)
 }
 
 ttt_status ttt_linear_bwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
-                          const float *eta, const float *W0, const float *b0, const void *dZ,
-                          const float *dW_final, const float *db_final, void *dQ, void *dK,
-                          void *dV, float *deta, float *dW0, float *db0, void *workspace,
+                          const float *eta, const float *W0, const float *b0, const float *gamma,
+                          const float *beta, const void *dZ, const float *dW_final,
+                          const float *db_final, void *dQ, void *dK, void *dV, float *deta,
+                          float *dW0, float *db0, float *dgamma, float *dbeta, void *workspace,
                           size_t workspace_bytes, ttt_stream_t stream)
 {
     ttt_status st = check_desc(desc, false);
     if (st != TTT_OK) return st;
     const ttt_desc &s = *desc;
-    if (s.residual_ln || s.weight_decay != 0.f || !ttt::linear_bwd_checkpoint_every(s))
+    if (s.weight_decay != 0.f || !ttt::linear_bwd_checkpoint_every(s))
         return fail(TTT_ERR_UNSUPPORTED,
-                    "the backward pass takes no residual LayerNorm, no weight decay, d <= 128 "
-                    "(a multiple of 4) and mini_batch <= 64");
+                    "the backward pass takes no weight decay, d <= 128 (a multiple of 4) and "
+                    "mini_batch <= 64");
+    if (s.residual_ln) {
+        const void *lp[] = {gamma, beta, dgamma, dbeta};
+        const char *ln_names[] = {"gamma", "beta", "dgamma", "dbeta"};
+        for (int i = 0; i < 4; ++i)
+            if ((st = check_ptr(lp[i], ln_names[i])) != TTT_OK) return st;
+    }
     const void *ptrs[] = {Q, K, V, eta, W0, b0, dZ, dQ, dK, dV, deta, dW0, db0, workspace};
     const char *names[] = {"Q", "K", "V", "eta", "W0", "b0", "dZ", "dQ", "dK", "dV", "deta",
                            "dW0", "db0", "workspace"};
@@ -264,21 +271,26 @@ ttt_status ttt_linear_bwd(const ttt_desc *desc, const void *Q, const void *K, co
     const size_t es = s.io_dtype == TTT_BF16 ? 2 : 4;
     const size_t BH = (size_t)ttt::call_rows(s), ninit = s.init_per_batch ? BH : (size_t)s.H;
     const size_t tok = BH * s.L * s.d, dd = (size_t)s.d * s.d;
+    const size_t lnb = s.residual_ln ? (size_t)s.H * s.d * 4 : 0;
     const Range ins[] = {range_of(Q, tok * es), range_of(K, tok * es), range_of(V, tok * es),
                          range_of(eta, BH * s.L * 4), range_of(W0, ninit * dd * 4),
                          range_of(b0, ninit * s.d * 4), range_of(dZ, tok * es),
                          range_of(dW_final, dW_final ? BH * dd * 4 : 0),
-                         range_of(db_final, db_final ? BH * s.d * 4 : 0)};
+                         range_of(db_final, db_final ? BH * s.d * 4 : 0),
+                         range_of(gamma, lnb), range_of(beta, lnb)};
     const Range outs[] = {range_of(dQ, tok * es), range_of(dK, tok * es), range_of(dV, tok * es),
                           range_of(deta, BH * s.L * 4), range_of(dW0, ninit * dd * 4),
-                          range_of(db0, ninit * s.d * 4), range_of(workspace, need)};
-    for (int o = 0; o < 7; ++o) {
-        for (int o2 = o + 1; o2 < 7; ++o2)
+                          range_of(db0, ninit * s.d * 4), range_of(workspace, need),
+                          range_of(dgamma, lnb), range_of(dbeta, lnb)};
+    for (int o = 0; o < 9; ++o) {
+        for (int o2 = o + 1; o2 < 9; ++o2)
             if (overlap(outs[o], outs[o2])) return fail(TTT_ERR_INVALID_ARG, "output buffers overlap");
         for (const Range &r : ins)
             if (overlap(outs[o], r)) return fail(TTT_ERR_INVALID_ARG, "an output overlaps an input");
     }
-    ttt::LinearBwdArgs a{s, Q, K, V, dZ, eta, W0, b0, dW_final, db_final, dQ, dK, dV, deta, dW0, db0,
+    const bool ln = s.residual_ln != 0;
+    ttt::LinearBwdArgs a{s, Q, K, V, dZ, eta, W0, b0, ln ? gamma : nullptr, ln ? beta : nullptr, dW_final,
+                         db_final, dQ, dK, dV, deta, dW0, db0, ln ? dgamma : nullptr, ln ? dbeta : nullptr,
                          workspace, reinterpret_cast<cudaStream_t>(stream)};
     cudaError_t e = ttt::launch_linear_bwd(a);
     if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "ttt_linear_bwd launch: %s", cudaGetErrorString(e));

@@ -117,10 +117,12 @@ __device__ void mm_xty_acc(float *acc, const float *X, const float *Y, const flo
 struct BwdParams {
     int H, L, d, mb, ck;      // ck: mini-batches per checkpoint
     int init_per_batch, ip;
+    float eps;
     const void *Q, *K, *V, *dZ;
-    const float *eta, *W0, *b0, *dWf, *dbf;
+    const float *eta, *W0, *b0, *gamma, *beta, *dWf, *dbf;
     void *dQ, *dK, *dV;
     float *deta, *dW0, *db0;  // dW0/db0: per (batch, head) (the partials when the state is head-shared)
+    float *dgb;               // LN: per-row partials [rows][2 d] of dgamma, dbeta
     float *ckpt;              // [rows][nck][d d + d]
     int hoff;
 };
@@ -131,7 +133,89 @@ __device__ void load_tile(float *dst, const IO *src, int n)
     for (int i = threadIdx.x; i < n; i += kThreads) dst[i] = load_io(src, i);
 }
 
-template <typename IO>
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+constexpr int kMaxPerLane = 4;   // d <= 128: features lane, lane + 32, ... of a row
+
+// Per-token LayerNorm quantities of a row z (d features, lane owns j = lane + 32 i):
+// xh = (z - mu) r with two-pass statistics.
+struct LnRow {
+    float xh[kMaxPerLane];
+    float r;
+};
+__device__ __forceinline__ LnRow ln_row(const float *z, int d, float eps)
+{
+    const int lane = threadIdx.x & 31;
+    LnRow o;
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+        const int j = lane + 32 * i;
+        if (j < d) s += z[j];
+    }
+    const float mu = warp_sum(s) / d;
+    float v = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+        const int j = lane + 32 * i;
+        o.xh[i] = j < d ? z[j] - mu : 0.f;
+        v += o.xh[i] * o.xh[i];
+    }
+    o.r = rsqrtf(warp_sum(v) / d + eps);
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) o.xh[i] *= o.r;
+    return o;
+}
+
+// Pi w = w - mean(w) - xh mean(xh w), in place over the lane's features
+__device__ __forceinline__ void ln_pi(float *w, const float *xh, int d)
+{
+    const int lane = threadIdx.x & 31;
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i)
+        if (lane + 32 * i < d) {
+            s1 += w[i];
+            s2 += xh[i] * w[i];
+        }
+    s1 = warp_sum(s1) / d;
+    s2 = warp_sum(s2) / d;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) w[i] = w[i] - s1 - xh[i] * s2;
+}
+
+// The per-token gradient with the residual LayerNorm, for the row z = k W + c:
+// G = r Pi gx with gx = a xh + c0, a = gamma^2, c0 = gamma (beta - (v - k)) (squared error) or
+// a = 0, c0 = -gamma v (inner product).  Returns gx in gxo when asked.
+__device__ __forceinline__ void ln_grad_row(float *G, const float *z, const float *k, const float *v,
+                                            const float *gam, const float *bet, int d, float eps, bool ip,
+                                            const LnRow &ln, float *gxo)
+{
+    const int lane = threadIdx.x & 31;
+    float w[kMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+        const int j = lane + 32 * i;
+        float gx = 0.f;
+        if (j < d) gx = ip ? -gam[j] * v[j] : gam[j] * (gam[j] * ln.xh[i] + bet[j] - (v[j] - k[j]));
+        w[i] = gx;
+        if (gxo) gxo[i] = gx;
+    }
+    ln_pi(w, ln.xh, d);
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+        const int j = lane + 32 * i;
+        if (j < d) G[j] = ln.r * w[i];
+    }
+    (void)z;
+}
+
+template <typename IO, bool LN>
 __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
 {
     extern __shared__ float4 sm4[];
@@ -139,7 +223,8 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
     const int d = p.d, mb = p.mb, L = p.L, ck = p.ck, dd = d * d;
     const int sd = dd + d;                        // one state: W then c
     const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int kWarps = kThreads / 32;
     const int nmb = L / mb, nck = (nmb + ck - 1) / ck;
     const int nt = mb * d;
     const float kf = p.ip ? 0.f : 1.f;
@@ -149,16 +234,24 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
     float *dc = dW + dd;
     float *Kt = dc + d;             // mb d each
     float *Qt = Kt + nt;
-    float *Vt = Qt + nt;
+    float *Vt = Qt + nt;            // V; with LN later dy (dV)
     float *dZt = Vt + nt;
     float *G = dZt + nt;
     float *dG = G + nt;
-    float *T1 = dG + nt;            // dZ W^T, later dG W^T
-    float *T2 = T1 + nt;            // K dW'
+    float *T1 = dG + nt;            // dZbar W^T, later dP W^T
+    float *T2 = T1 + nt;            // K dW', later dP
     float *T3 = T2 + nt;            // G dW'^T
     float *A = T3 + nt;             // mb mb: R = M . (Q K^T + 1) (A = R E)
     float *Dm = A + mb * mb;        // mb mb
     float *et = Dm + mb * mb;       // mb
+    float *Pz = et + mb;            // LN: P = K W + c
+    float *dZb = Pz + nt;           // LN: Zbar, then dZbar (without LN: dZ itself)
+    float *gam = dZb + nt;          // LN: d
+    float *bet = gam + d;           // LN: d
+    // kWarps x 2 d for the final dgamma / dbeta reduction: the state area once the scan is
+    // done, or its own area when the states are smaller (d < 16)
+    float *red = (2 * d * kWarps <= ck * sd) ? S : bet + d;
+    if (!LN) dZb = dZt;
 
     const IO *Qg = static_cast<const IO *>(p.Q) + (size_t)bh * L * d;
     const IO *Kg = static_cast<const IO *>(p.K) + (size_t)bh * L * d;
@@ -166,17 +259,35 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
     const IO *dZg = static_cast<const IO *>(p.dZ) + (size_t)bh * L * d;
     const float *eg = p.eta + (size_t)bh * L;
     float *ck_base = p.ckpt + (size_t)bh * nck * sd;
+    if (LN)
+        for (int j = tid; j < d; j += kThreads) {
+            gam[j] = p.gamma[(size_t)h * d + j];
+            bet[j] = p.beta[(size_t)h * d + j];
+        }
 
-    // one forward mini-batch on the state X (in place): G = kf (K W + c) - V, W -= K^T E G, c -= G^T eta
+    // G = dl/dz of the tile's rows, from P (in G on entry for the plain loss; in src for LN)
+    auto gradient_rows = [&](float *Gout, const float *src) {
+        if (LN) {
+            for (int s = warp; s < mb; s += kWarps) {
+                const LnRow ln = ln_row(src + s * d, d, p.eps);
+                ln_grad_row(Gout + s * d, src + s * d, Kt + s * d, Vt + s * d, gam, bet, d, p.eps, p.ip != 0, ln,
+                            nullptr);
+            }
+        } else {
+            for (int i = tid; i < nt; i += kThreads) Gout[i] = fmaf(src[i], kf, -Vt[i]);
+        }
+    };
+
+    // one forward mini-batch on the state X (in place): G, W -= K^T E G, c -= G^T eta
     auto forward_step = [&](float *X, int n0) {
         __syncthreads();
         load_tile(Kt, Kg + (size_t)n0 * d, nt);
         load_tile(Vt, Vg + (size_t)n0 * d, nt);
         for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
         __syncthreads();
-        mm_xy(G, Kt, X, X + dd, mb, d, d);
+        mm_xy(LN ? Pz : G, Kt, X, X + dd, mb, d, d);
         __syncthreads();
-        for (int i = tid; i < nt; i += kThreads) G[i] = fmaf(G[i], kf, -Vt[i]);
+        gradient_rows(G, LN ? Pz : G);
         __syncthreads();
         mm_xty_acc(X, Kt, G, et, -1.f, mb, d, d);
         for (int j = tid; j < d; j += kThreads) {
@@ -200,6 +311,9 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
     }
 
     // ---- pass 2: reverse
+    float dgam_acc[kMaxPerLane], dbet_acc[kMaxPerLane];   // this warp's tokens (LN)
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) dgam_acc[i] = dbet_acc[i] = 0.f;
     for (int i = tid; i < dd; i += kThreads) dW[i] = p.dWf ? p.dWf[(size_t)bh * dd + i] : 0.f;
     for (int j = tid; j < d; j += kThreads) dc[j] = p.dbf ? p.dbf[(size_t)bh * d + j] : 0.f;
     for (int ci = nck - 1; ci >= 0; --ci) {
@@ -223,10 +337,10 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
             load_tile(dZt, dZg + (size_t)n0 * d, nt);
             for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
             __syncthreads();
-            // G (pre-loss), dZ W^T, K dW', R = M . (Q K^T + 1)
-            mm_xy(G, Kt, W, c, mb, d, d);
-            mm_xyt(T1, dZt, W, mb, d, d);
+            // P (LN: kept in Pz), K dW', R = M . (Q K^T + 1); LN: Q W + c into dZb
+            mm_xy(LN ? Pz : G, Kt, W, c, mb, d, d);
             mm_xy(T2, Kt, dW, nullptr, mb, d, d);
+            if (LN) mm_xy(dZb, Qt, W, c, mb, d, d);
             for (int i = tid; i < mb * mb; i += kThreads) {
                 const int t = i / mb, s = i - t * mb;
                 float a = 0.f;
@@ -238,15 +352,47 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
                 A[i] = a;
             }
             __syncthreads();
-            for (int i = tid; i < nt; i += kThreads) G[i] = fmaf(G[i], kf, -Vt[i]);
+            gradient_rows(G, LN ? Pz : G);
             __syncthreads();
-            // G dW'^T, D = M . (dZ G^T), dG = -A^T dZ - E K dW' - eta dc'^T
+            if (LN) {
+                // Zbar = Q W + c - A G, then dZbar = r Pi(gamma dZ) (output LayerNorm backward);
+                // dgamma += dZ . xh_o, dbeta += dZ
+                for (int tile = tid; tile < nt / 4; tile += kThreads) {
+                    const int t = tile / (d / 4), j = (tile - t * (d / 4)) * 4;
+                    float4 z = f4(dZb + t * d + j);
+                    for (int s = 0; s <= t; ++s) fma4(z, -et[s] * A[t * mb + s], f4(G + s * d + j));
+                    st4(dZb + t * d + j, z);
+                }
+                __syncthreads();
+                for (int t = warp; t < mb; t += kWarps) {
+                    const LnRow lo = ln_row(dZb + t * d, d, p.eps);
+                    float w[kMaxPerLane];
+#pragma unroll
+                    for (int i = 0; i < kMaxPerLane; ++i) {
+                        const int j = lane + 32 * i;
+                        const float dz = j < d ? dZt[t * d + j] : 0.f;
+                        w[i] = j < d ? gam[j] * dz : 0.f;
+                        dgam_acc[i] = fmaf(dz, lo.xh[i], dgam_acc[i]);
+                        dbet_acc[i] += dz;
+                    }
+                    ln_pi(w, lo.xh, d);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < kMaxPerLane; ++i) {
+                        const int j = lane + 32 * i;
+                        if (j < d) dZb[t * d + j] = lo.r * w[i];
+                    }
+                }
+                __syncthreads();
+            }
+            // dZbar W^T, G dW'^T, D = M . (dZbar G^T), dG = -A^T dZbar - E K dW' - eta dc'^T
+            mm_xyt(T1, dZb, W, mb, d, d);
             mm_xyt(T3, G, dW, mb, d, d);
             for (int i = tid; i < mb * mb; i += kThreads) {
                 const int t = i / mb, s = i - t * mb;
                 float x = 0.f;
                 if (s <= t)
-                    for (int u = 0; u < d; u += 4) x += dot4(f4(dZt + t * d + u), f4(G + s * d + u));
+                    for (int u = 0; u < d; u += 4) x += dot4(f4(dZb + t * d + u), f4(G + s * d + u));
                 Dm[i] = x;
             }
             for (int tile = tid; tile < nt / 4; tile += kThreads) {
@@ -257,27 +403,26 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
                 a.y = -et[s] * (a.y + dcj.y);
                 a.z = -et[s] * (a.z + dcj.z);
                 a.w = -et[s] * (a.w + dcj.w);
-                for (int t = s; t < mb; ++t) fma4(a, -et[s] * A[t * mb + s], f4(dZt + t * d + j));
+                for (int t = s; t < mb; ++t) fma4(a, -et[s] * A[t * mb + s], f4(dZb + t * d + j));
                 st4(dG + s * d + j, a);
             }
             __syncthreads();
-            // dQ = dZ W^T - D E K;  dV = -dG;  deta;  then T1 <- dG W^T
+            // dQ = dZ (residual LN) + dZbar W^T - D E K
             IO *dQg = static_cast<IO *>(p.dQ) + (size_t)bh * L * d + (size_t)n0 * d;
             IO *dKg = static_cast<IO *>(p.dK) + (size_t)bh * L * d + (size_t)n0 * d;
             IO *dVg = static_cast<IO *>(p.dV) + (size_t)bh * L * d + (size_t)n0 * d;
             for (int tile = tid; tile < nt / 4; tile += kThreads) {
                 const int t = tile / (d / 4), j = (tile - t * (d / 4)) * 4;
                 float4 a = f4(T1 + t * d + j);
+                if (LN) {
+                    const float4 z = f4(dZt + t * d + j);
+                    a.x += z.x; a.y += z.y; a.z += z.z; a.w += z.w;
+                }
                 for (int s = 0; s <= t; ++s) fma4(a, -Dm[t * mb + s] * et[s], f4(Kt + s * d + j));
                 store_io(dQg, t * d + j, a.x);
                 store_io(dQg, t * d + j + 1, a.y);
                 store_io(dQg, t * d + j + 2, a.z);
                 store_io(dQg, t * d + j + 3, a.w);
-                const float4 g = f4(dG + t * d + j);
-                store_io(dVg, t * d + j, -g.x);
-                store_io(dVg, t * d + j + 1, -g.y);
-                store_io(dVg, t * d + j + 2, -g.z);
-                store_io(dVg, t * d + j + 3, -g.w);
             }
             // deta_s = -(K dW')_s . g_s - g_s . dc' - sum_{t >= s} D[t, s] (q_t . k_s + 1)
             for (int s = tid; s < mb; s += kThreads) {
@@ -290,26 +435,94 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
                 p.deta[(size_t)bh * L + n0 + s] = a;
             }
             __syncthreads();
-            mm_xyt(T1, dG, W, mb, d, d);   // dG W^T
+            // dP (into T2) and dV: through G's dependence on P and on v (and k)
+            if (LN) {
+                for (int s = warp; s < mb; s += kWarps) {
+                    const float *z = Pz + s * d;
+                    const LnRow ln = ln_row(z, d, p.eps);
+                    float gx[kMaxPerLane], Gv[kMaxPerLane], u[kMaxPerLane];
+                    ln_grad_row(T3 + s * d, z, Kt + s * d, Vt + s * d, gam, bet, d, p.eps, p.ip != 0, ln, gx);
+                    // T3 row s now holds G again (the same values as G); u = dG row
+                    float su = 0.f, suG = 0.f, sxg = 0.f, sux = 0.f;
+#pragma unroll
+                    for (int i = 0; i < kMaxPerLane; ++i) {
+                        const int j = lane + 32 * i;
+                        u[i] = j < d ? dG[s * d + j] : 0.f;
+                        Gv[i] = j < d ? G[s * d + j] : 0.f;
+                        su += u[i];
+                        suG += u[i] * Gv[i];
+                        sxg += ln.xh[i] * gx[i];
+                        sux += u[i] * ln.xh[i];
+                    }
+                    su = warp_sum(su);
+                    suG = warp_sum(suG);
+                    sxg = warp_sum(sxg);
+                    sux = warp_sum(sux);
+                    float f[kMaxPerLane], w[kMaxPerLane];
+#pragma unroll
+                    for (int i = 0; i < kMaxPerLane; ++i) {
+                        const int j = lane + 32 * i;
+                        const float a = (j < d && !p.ip) ? gam[j] * gam[j] : 0.f;
+                        f[i] = ln.r * (a * u[i] - su * a / d - (u[i] * sxg + sux * (gx[i] + a * ln.xh[i])) / d);
+                        w[i] = u[i];
+                    }
+                    ln_pi(f, ln.xh, d);
+                    ln_pi(w, ln.xh, d);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < kMaxPerLane; ++i) {
+                        const int j = lane + 32 * i;
+                        if (j >= d) continue;
+                        const float wr = ln.r * w[i];
+                        T2[s * d + j] = ln.r * f[i] - ln.r * suG * ln.xh[i] / d;   // dP
+                        float dv;
+                        if (p.ip) {
+                            dv = -gam[j] * wr;
+                            dgam_acc[i] = fmaf(-Vt[s * d + j], wr, dgam_acc[i]);
+                            Vt[s * d + j] = 0.f;          // no dy term in dK
+                        } else {
+                            const float y = Vt[s * d + j] - Kt[s * d + j];
+                            dv = -gam[j] * wr;            // dy
+                            dgam_acc[i] = fmaf(2.f * gam[j] * ln.xh[i] + bet[j] - y, wr, dgam_acc[i]);
+                            dbet_acc[i] = fmaf(gam[j], wr, dbet_acc[i]);
+                            Vt[s * d + j] = dv;           // dy, for dK
+                        }
+                        store_io(dVg, s * d + j, dv);
+                    }
+                }
+            } else {
+                for (int i = tid; i < nt; i += kThreads) {
+                    T2[i] = kf * dG[i];
+                    store_io(dVg, i, -dG[i]);
+                }
+            }
             __syncthreads();
-            // dK = kf dG W^T - E G dW'^T - E D^T Q
+            // T3 <- G dW'^T again (the LN rows above overwrote it), T1 <- dP W^T
+            if (LN) mm_xyt(T3, G, dW, mb, d, d);
+            mm_xyt(T1, T2, W, mb, d, d);
+            __syncthreads();
+            // dK = dP W^T - E G dW'^T - E D^T Q (- dy with the residual LN)
             for (int tile = tid; tile < nt / 4; tile += kThreads) {
                 const int s = tile / (d / 4), j = (tile - s * (d / 4)) * 4;
                 const float4 t1 = f4(T1 + s * d + j), t3 = f4(T3 + s * d + j);
-                float4 a = make_float4(kf * t1.x - et[s] * t3.x, kf * t1.y - et[s] * t3.y,
-                                       kf * t1.z - et[s] * t3.z, kf * t1.w - et[s] * t3.w);
+                float4 a = make_float4(t1.x - et[s] * t3.x, t1.y - et[s] * t3.y, t1.z - et[s] * t3.z,
+                                       t1.w - et[s] * t3.w);
+                if (LN) {
+                    const float4 dy = f4(Vt + s * d + j);
+                    a.x -= dy.x; a.y -= dy.y; a.z -= dy.z; a.w -= dy.w;
+                }
                 for (int t = s; t < mb; ++t) fma4(a, -et[s] * Dm[t * mb + s], f4(Qt + t * d + j));
                 store_io(dKg, s * d + j, a.x);
                 store_io(dKg, s * d + j + 1, a.y);
                 store_io(dKg, s * d + j + 2, a.z);
                 store_io(dKg, s * d + j + 3, a.w);
             }
-            // dW += Q^T dZ + kf K^T dG;  dc += 1^T dZ + kf 1^T dG
-            mm_xty_acc(dW, Qt, dZt, nullptr, 1.f, mb, d, d);
-            if (kf != 0.f) mm_xty_acc(dW, Kt, dG, nullptr, 1.f, mb, d, d);
+            // dW += Q^T dZbar + K^T dP;  dc += 1^T dZbar + 1^T dP
+            mm_xty_acc(dW, Qt, dZb, nullptr, 1.f, mb, d, d);
+            mm_xty_acc(dW, Kt, T2, nullptr, 1.f, mb, d, d);
             for (int j = tid; j < d; j += kThreads) {
                 float a = 0.f;
-                for (int s = 0; s < mb; ++s) a += dZt[s * d + j] + kf * dG[s * d + j];
+                for (int s = 0; s < mb; ++s) a += dZb[s * d + j] + T2[s * d + j];
                 dc[j] += a;
             }
         }
@@ -317,11 +530,30 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
     __syncthreads();
     for (int i = tid; i < dd; i += kThreads) p.dW0[(size_t)bh * dd + i] = dW[i];
     for (int j = tid; j < d; j += kThreads) p.db0[(size_t)bh * d + j] = dc[j];
+    if (LN) {
+        // dgamma, dbeta of this row: the warps' accumulators summed in warp order
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) {
+            const int j = lane + 32 * i;
+            if (j < d) {
+                red[warp * 2 * d + j] = dgam_acc[i];
+                red[warp * 2 * d + d + j] = dbet_acc[i];
+            }
+        }
+        __syncthreads();
+        for (int j = tid; j < 2 * d; j += kThreads) {
+            float a = 0.f;
+            for (int w = 0; w < kWarps; ++w) a += red[w * 2 * d + j];
+            p.dgb[(size_t)bh * 2 * d + j] = a;
+        }
+    }
 }
 
-// out[h] = sum of part[i] over the call's rows i of head h = (hoff + i) mod H, in row order
-// (deterministic), for a head-shared initial state; heads without a row get 0
-__global__ void sum_over_rows_kernel(const float *part, float *out, int rows, int H, int hoff, int n)
+// out[h][e] = sum of part[i * stride + off + e] (e < n) over the call's rows i of head
+// h = (hoff + i) mod H, in row order (deterministic); heads without a row get 0
+__global__ void sum_over_rows_kernel(const float *part, float *out, int rows, int H, int hoff, int stride, int n,
+                                     int off)
 {
     const size_t total = (size_t)H * n;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
@@ -329,7 +561,7 @@ __global__ void sum_over_rows_kernel(const float *part, float *out, int rows, in
         const size_t e = i - (size_t)hh * n;
         const int first = ((hh - hoff) % H + H) % H;   // the first row of head hh
         float a = 0.f;
-        for (int r = first; r < rows; r += H) a += part[(size_t)r * n + e];
+        for (int r = first; r < rows; r += H) a += part[(size_t)r * stride + off + e];
         out[i] = a;
     }
 }
@@ -338,8 +570,10 @@ constexpr size_t kMaxSmem = 227 * 1024;
 
 size_t smem_for(const ttt_desc &s, int ck)
 {
-    const size_t d = s.d, mb = s.mini_batch;
-    const size_t n = ck * (d * d + d) + d * d + d + 10 * mb * d + 2 * mb * mb + 2 * mb;
+    const size_t d = s.d, mb = s.mini_batch, states = ck * (d * d + d);
+    const size_t red = 2 * d * (kThreads / 32);
+    size_t n = states + d * d + d + 9 * mb * d + 2 * mb * mb + mb;
+    if (s.residual_ln) n += 2 * mb * d + 2 * d + (red <= states ? 0 : red);
     return n * sizeof(float);
 }
 
@@ -347,7 +581,7 @@ size_t smem_for(const ttt_desc &s, int ck)
 
 int linear_bwd_checkpoint_every(const ttt_desc &s)
 {
-    if (s.d > 128 || s.d % 4 != 0 || s.mini_batch > 64 || s.residual_ln || s.weight_decay != 0.f) return 0;
+    if (s.d > 128 || s.d % 4 != 0 || s.mini_batch > 64 || s.weight_decay != 0.f) return 0;
     for (int ck : {4, 2, 1})
         if (smem_for(s, ck) <= kMaxSmem) return ck;
     return 0;
@@ -361,6 +595,7 @@ size_t linear_bwd_workspace_bytes(const ttt_desc &s)
     const size_t nmb = s.L / s.mini_batch, nck = (nmb + ck - 1) / ck;
     size_t bytes = rows * nck * (d * d + d) * sizeof(float);
     if (!s.init_per_batch) bytes += rows * (d * d + d) * sizeof(float);   // per-(batch, head) partials
+    if (s.residual_ln) bytes += rows * 2 * d * sizeof(float);              // dgamma, dbeta partials
     return (bytes + 255) / 256 * 256;
 }
 
@@ -372,22 +607,35 @@ cudaError_t launch_linear_bwd(const LinearBwdArgs &a)
     const size_t d = s.d, nmb = s.L / s.mini_batch, nck = (nmb + ck - 1) / ck;
     float *ckpt = static_cast<float *>(a.workspace);
     float *part = ckpt + (size_t)rows * nck * (d * d + d);
+    float *dgb = part + (s.init_per_batch ? 0 : (size_t)rows * (d * d + d));
     BwdParams p{s.H, s.L, s.d, s.mini_batch, ck, s.init_per_batch, s.loss == TTT_LOSS_INNER_PRODUCT,
-                a.Q, a.K, a.V, a.dZ, a.eta, a.W0, a.b0, a.dW_final, a.db_final, a.dQ, a.dK, a.dV,
-                a.deta, s.init_per_batch ? a.dW0 : part, s.init_per_batch ? a.db0 : part + (size_t)rows * d * d,
-                ckpt, head_offset(s)};
+                s.ln_eps, a.Q, a.K, a.V, a.dZ, a.eta, a.W0, a.b0, a.gamma, a.beta, a.dW_final, a.db_final,
+                a.dQ, a.dK, a.dV, a.deta, s.init_per_batch ? a.dW0 : part,
+                s.init_per_batch ? a.db0 : part + (size_t)rows * d * d, dgb, ckpt, head_offset(s)};
     const size_t smem = smem_for(s, ck);
-    const void *k = s.io_dtype == TTT_F32 ? (const void *)linear_bwd_kernel<float>
-                                          : (const void *)linear_bwd_kernel<__nv_bfloat16>;
+    const bool f32 = s.io_dtype == TTT_F32, ln = s.residual_ln != 0;
+    const void *k = f32 ? (ln ? (const void *)linear_bwd_kernel<float, true> : (const void *)linear_bwd_kernel<float, false>)
+                        : (ln ? (const void *)linear_bwd_kernel<__nv_bfloat16, true>
+                              : (const void *)linear_bwd_kernel<__nv_bfloat16, false>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     void *args[] = {&p};
     e = cudaLaunchKernel(k, dim3(rows), dim3(kThreads), args, smem, a.stream);
-    if (e != cudaSuccess || s.init_per_batch) return e;
+    if (e != cudaSuccess) return e;
+    if (ln) {   // dgamma, dbeta [H, d]: per-head sums of the rows' partials ([rows][dgamma | dbeta])
+        sum_over_rows_kernel<<<148, 256, 0, a.stream>>>(dgb, a.dgamma, rows, s.H, head_offset(s), (int)(2 * d),
+                                                       (int)d, 0);
+        sum_over_rows_kernel<<<148, 256, 0, a.stream>>>(dgb, a.dbeta, rows, s.H, head_offset(s), (int)(2 * d),
+                                                       (int)d, (int)d);
+        if ((e = cudaGetLastError()) != cudaSuccess || s.init_per_batch) return e;
+    } else if (s.init_per_batch) {
+        return e;
+    }
     // head-shared initial state: sum the per-(batch, head) gradients over the call's rows
-    sum_over_rows_kernel<<<148, 256, 0, a.stream>>>(part, a.dW0, rows, s.H, head_offset(s), (int)(d * d));
+    sum_over_rows_kernel<<<148, 256, 0, a.stream>>>(part, a.dW0, rows, s.H, head_offset(s), (int)(d * d),
+                                                   (int)(d * d), 0);
     sum_over_rows_kernel<<<148, 256, 0, a.stream>>>(part + (size_t)rows * d * d, a.db0, rows, s.H,
-                                                   head_offset(s), (int)d);
+                                                   head_offset(s), (int)d, (int)d, 0);
     return cudaGetLastError();
 }
 

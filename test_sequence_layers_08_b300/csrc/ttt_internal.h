@@ -47,15 +47,14 @@ struct DecodeArgs {
 struct LinearBwdArgs {
     ttt_desc desc;
     const void *Q, *K, *V, *dZ;
-    const float *eta, *W0, *b0, *dW_final, *db_final;   // dW_final, db_final may be null (0)
+    const float *eta, *W0, *b0, *gamma, *beta, *dW_final, *db_final;   // dW_final, db_final may be null (0)
     void *dQ, *dK, *dV;
-    float *deta, *dW0, *db0;
+    float *deta, *dW0, *db0, *dgamma, *dbeta;   // gamma, beta, dgamma, dbeta: residual LN only
     void *workspace;
     cudaStream_t stream;
 };
 
-// TTT-Linear backward (no residual LayerNorm, no weight decay; d <= 128, d % 4 == 0,
-// b <= 64).  *_checkpoint_every returns the mini-batches per state checkpoint (0: the
+// TTT-Linear backward (no weight decay; d <= 128, d % 4 == 0, b <= 64).  *_checkpoint_every returns the mini-batches per state checkpoint (0: the
 // shape is not supported).
 int linear_bwd_checkpoint_every(const ttt_desc &d);
 size_t linear_bwd_workspace_bytes(const ttt_desc &d);

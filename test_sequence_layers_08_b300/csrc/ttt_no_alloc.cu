@@ -52,9 +52,10 @@ extern "C" {
 size_t ttt_linear_bwd_static_scratch_bytes(void) { return kScratchBytes; }
 
 ttt_status ttt_linear_bwd_static(const ttt_desc *desc, const void *Q, const void *K, const void *V,
-                                 const float *eta, const float *W0, const float *b0, const void *dZ,
-                                 const float *dW_final, const float *db_final, void *dQ, void *dK,
-                                 void *dV, float *deta, float *dW0, float *db0, ttt_stream_t stream)
+                                 const float *eta, const float *W0, const float *b0, const float *gamma,
+                                 const float *beta, const void *dZ, const float *dW_final,
+                                 const float *db_final, void *dQ, void *dK, void *dV, float *deta,
+                                 float *dW0, float *db0, float *dgamma, float *dbeta, ttt_stream_t stream)
 {
     const size_t need = ttt_linear_bwd_workspace_size(desc);
     if (need > kScratchBytes) {
@@ -67,8 +68,8 @@ ttt_status ttt_linear_bwd_static(const ttt_desc *desc, const void *Q, const void
         if (e != cudaSuccess) return ttt::fail_cuda("static scratch address", e);
     }
     // need == 0 (invalid or unsupported descriptor): ttt_linear_bwd reports the reason
-    return ttt_linear_bwd(desc, Q, K, V, eta, W0, b0, dZ, dW_final, db_final, dQ, dK, dV, deta, dW0,
-                          db0, scratch, kScratchBytes, stream);
+    return ttt_linear_bwd(desc, Q, K, V, eta, W0, b0, gamma, beta, dZ, dW_final, db_final, dQ, dK, dV,
+                          deta, dW0, db0, dgamma, dbeta, scratch, kScratchBytes, stream);
 }
 
 }  // extern "C"

@@ -200,43 +200,62 @@ def test_variant_kernel_choice(lib):
         assert k(1, residual_ln=1, d_hidden=256, **var) == "ttt_mlp_generic"
 
 
+# ttt_linear_bwd pointer slots: Q K V eta W0 b0 gamma beta dZ dW_final db_final dQ dK dV deta
+# dW0 db0 dgamma dbeta workspace
+BWD_SLOTS = 20
+BWD_WS, BWD_DQ = 19, 11
+BWD_OPTIONAL = (9, 10)               # dW_final, db_final: NULL means zero
+BWD_LN_ONLY = (6, 7, 17, 18)         # gamma, beta, dgamma, dbeta: NULL allowed without LN
+
+
+def bwd_ptrs():
+    return [FAKE + i * (1 << 30) for i in range(BWD_SLOTS)]
+
+
 def call_bwd(lib, dsc, ptrs=None, ws_bytes=1 << 30):
-    p = [FAKE + i * (1 << 30) for i in range(17)] if ptrs is None else ptrs
-    args = [ctypes.c_void_p(x) if x else None for x in p[:16]]
+    """Every call here must fail the host checks: the pointers are fake."""
+    p = bwd_ptrs() if ptrs is None else ptrs
+    args = [ctypes.c_void_p(x) if x else None for x in p]
     return lib.ttt_linear_bwd(ctypes.byref(dsc), *args, ctypes.c_size_t(ws_bytes),
-                              ctypes.c_void_p(p[16]) if p[16] else None)
+                              ctypes.c_void_p(FAKE + 31 * (1 << 30)))
 
 
 def test_backward_declared_and_checked(lib):
-    """ttt_linear_bwd: supported shapes report a workspace size; LayerNorm and weight decay
-    are unsupported; a short or misaligned workspace, a NULL or overlapping buffer are
-    invalid arguments (all rejected before any launch)."""
+    """ttt_linear_bwd: supported shapes report a workspace size; weight decay is unsupported;
+    a short or misaligned workspace, a NULL or overlapping buffer are invalid arguments (all
+    rejected before any launch)."""
     assert "ttt_linear_bwd" in header_functions()
     assert "ttt_linear_bwd_workspace_size" in header_functions()
     ws = lib.ttt_linear_bwd_workspace_size
     assert ws(ctypes.byref(desc())) > 0 and ws(ctypes.byref(desc())) % 256 == 0
-    assert ws(ctypes.byref(desc(residual_ln=1))) == 0
+    assert ws(ctypes.byref(desc(residual_ln=1))) > ws(ctypes.byref(desc()))   # + dgamma/dbeta partials
     assert ws(ctypes.byref(desc(weight_decay=0.1))) == 0
     assert ws(ctypes.byref(desc(d=6))) == 0
     assert ws(ctypes.byref(desc(L=40))) == 0      # invalid descriptor
     # per-batch initial state needs no per-row partials: a smaller workspace
     assert ws(ctypes.byref(desc(init_per_batch=1))) < ws(ctypes.byref(desc()))
-    assert call_bwd(lib, desc(residual_ln=1)) == 2
     assert call_bwd(lib, desc(weight_decay=0.5)) == 2
     need = ws(ctypes.byref(desc()))
     assert call_bwd(lib, desc(), ws_bytes=need - 256) == 1
-    p = [FAKE + i * (1 << 30) for i in range(17)]
-    p[15] += 16                                    # workspace not 256-byte aligned
+    p = bwd_ptrs()
+    p[BWD_WS] += 16                               # workspace not 256-byte aligned
     assert call_bwd(lib, desc(), p) == 1
-    for i in range(15):                            # every pointer but dW_final/db_final
-        if i in (7, 8):
+    for i in range(BWD_SLOTS):                    # every required pointer
+        if i in BWD_OPTIONAL or i in BWD_LN_ONLY:
             continue
-        q = [FAKE + j * (1 << 30) for j in range(17)]
+        q = bwd_ptrs()
         q[i] = 0
         assert call_bwd(lib, desc(), q) == 1, i
-    q = [FAKE + j * (1 << 30) for j in range(17)]
-    q[9] = q[0]                                    # dQ on top of Q
+    for i in BWD_LN_ONLY:                         # required with the residual LayerNorm
+        q = bwd_ptrs()
+        q[i] = 0
+        assert call_bwd(lib, desc(residual_ln=1), q) == 1, i
+    q = bwd_ptrs()
+    q[BWD_DQ] = q[0]                              # dQ on top of Q
     assert call_bwd(lib, desc(), q) == 1
-    q = [FAKE + j * (1 << 30) for j in range(17)]
-    q[15] = q[9]                                   # workspace on top of dQ
+    q = bwd_ptrs()
+    q[BWD_WS] = q[BWD_DQ]                         # workspace on top of dQ
     assert call_bwd(lib, desc(), q) == 1
+    q = bwd_ptrs()
+    q[17] = q[6]                                  # dgamma on top of gamma
+    assert call_bwd(lib, desc(residual_ln=1), q) == 1

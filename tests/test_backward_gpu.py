@@ -1,7 +1,8 @@
 """GPU parity of the TTT-Linear backward pass (ttt_linear_bwd) with the backward oracle:
-every gradient of every (batch, head), for fp32 and bf16 I/O, both losses, head-shared and
-per-batch initial states, several mini-batch sizes and head dims, a (batch, head)
-partition, and repeated calls on one workspace."""
+every gradient of every (batch, head), with and without the residual LayerNorm (then also
+dgamma, dbeta), for fp32 and bf16 I/O, both losses, head-shared and per-batch initial
+states, several mini-batch sizes and head dims, a (batch, head) partition, and repeated
+calls on one workspace."""
 import numpy as np
 import pytest
 import torch
@@ -17,7 +18,7 @@ pytestmark = pytest.mark.gpu
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 
 
-def problem(B, H, L, d, io, seed, init_per_batch=False, finals=True):
+def problem(B, H, L, d, io, seed, init_per_batch=False, finals=True, ln=False):
     rng = np.random.default_rng(seed)
     f = (lambda a: round_bf16(a.astype(np.float32))) if io == "bf16" else (lambda a: a.astype(np.float32))
     x = dict(Q=f(rng.standard_normal((B, H, L, d)) / np.sqrt(d)),
@@ -30,6 +31,8 @@ def problem(B, H, L, d, io, seed, init_per_batch=False, finals=True):
     x["b0"] = (0.05 * rng.standard_normal(shape0 + (d,))).astype(np.float32)
     x["dW_final"] = rng.standard_normal((B, H, d, d)).astype(np.float32) if finals else None
     x["db_final"] = rng.standard_normal((B, H, d)).astype(np.float32) if finals else None
+    x["gamma"] = (1.0 + 0.2 * rng.standard_normal((H, d))).astype(np.float32) if ln else None
+    x["beta"] = (0.2 * rng.standard_normal((H, d))).astype(np.float32) if ln else None
     return x
 
 
@@ -48,26 +51,31 @@ def to_dev(x, io):
 
 def run(x, io, mb, loss="mse", init_per_batch=False, **kw):
     t = to_dev(x, io)
+    ln = x.get("gamma") is not None
     res = ttt.ttt_linear_bwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], t["b0"], t["dZ"],
-                             t["dW_final"], t["db_final"], mini_batch=mb, loss=loss,
-                             init_per_batch=init_per_batch, **kw)
+                             t["dW_final"], t["db_final"], t.get("gamma"), t.get("beta"),
+                             mini_batch=mb, loss=loss, residual_ln=ln, init_per_batch=init_per_batch,
+                             **kw)
     ttt.ttt_sync_status()
     return [r.float().cpu().numpy().astype(np.float64) for r in res]
 
 
 def reference(x, mb, loss="mse", init_per_batch=False):
-    g = ttt_linear_grad(x["Q"], x["K"], x["V"], x["eta"], x["W0"], x["b0"], None, None, x["dZ"],
-                        x["dW_final"], x["db_final"], mini_batch=mb, loss=loss,
-                        init_per_batch=init_per_batch)
-    return [g[k] for k in ("dQ", "dK", "dV", "deta", "dW0", "db0")]
+    ln = x.get("gamma") is not None
+    g = ttt_linear_grad(x["Q"], x["K"], x["V"], x["eta"], x["W0"], x["b0"], x.get("gamma"),
+                        x.get("beta"), x["dZ"], x["dW_final"], x["db_final"], mini_batch=mb, ln=ln,
+                        eps=1e-6, loss=loss, init_per_batch=init_per_batch)
+    names = ("dQ", "dK", "dV", "deta", "dW0", "db0") + (("dgamma", "dbeta") if ln else ())
+    return [g[k] for k in names]
 
 
 def compare(got, ref, io, init_per_batch=False, case=None):
     case = case or current_case("bwd")
     tol = TOL[io]
-    names = ("dQ", "dK", "dV", "deta", "dW0", "db0")
+    names = ("dQ", "dK", "dV", "deta", "dW0", "db0", "dgamma", "dbeta")
+    assert len(got) == len(ref)
     for name, g, r in zip(names, got, ref):
-        if name in ("dW0", "db0") and not init_per_batch:
+        if name in ("dgamma", "dbeta") or (name in ("dW0", "db0") and not init_per_batch):
             for hi in range(g.shape[0]):
                 check_scan(case, name, g[hi], r[hi], tol)
             continue
@@ -139,3 +147,22 @@ def test_backward_two_calls_on_one_workspace_agree_bit_for_bit():
         outs.append([a.clone() for a in r])
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("loss", ["mse", "ip"])
+def test_backward_residual_ln_matches_oracle(io, loss):
+    x = problem(B=2, H=3, L=96, d=64, io=io, seed=41, ln=True)
+    compare(run(x, io, 16, loss), reference(x, 16, loss), io)
+
+
+@pytest.mark.parametrize("mb,d", [(8, 32), (16, 128), (4, 64)])
+def test_backward_residual_ln_shapes(mb, d):
+    x = problem(B=1, H=2, L=4 * mb + mb * 3, d=d, io="f32", seed=43 + mb + d, ln=True)
+    compare(run(x, "f32", mb), reference(x, mb), "f32")
+
+
+def test_backward_residual_ln_per_batch_initial_state():
+    x = problem(B=2, H=2, L=64, d=64, io="f32", seed=45, init_per_batch=True, ln=True)
+    compare(run(x, "f32", 16, init_per_batch=True), reference(x, 16, init_per_batch=True), "f32",
+            init_per_batch=True)

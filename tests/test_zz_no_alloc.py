@@ -18,7 +18,7 @@ def test_static_scratch_refuses_calls_beyond_its_size():
     desc = ttt.Desc(B=8, H=12, L=16384, d=64, d_hidden=0, mini_batch=16, io_dtype=1, residual_ln=0,
                     ln_eps=1e-6, init_per_batch=0)
     assert lib.ttt_linear_bwd_workspace_size(ctypes.byref(desc)) > cap
-    fake = [ctypes.c_void_p((1 << 20) + i * (1 << 30)) for i in range(16)]
+    fake = [ctypes.c_void_p((1 << 20) + i * (1 << 30)) for i in range(20)]
     st = lib.ttt_linear_bwd_static(ctypes.byref(desc), *fake, None)
     assert st == 1
     assert "static scratch" in lib.ttt_last_error().decode()
