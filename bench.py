@@ -720,6 +720,8 @@ def run_backward(args, cfg, world, rank, local):
     alg_bytes = float(seq * (7 * d * es + 8) + 2 * H * (d * d + d) * 4 + 2 * B * H * (d * d + d) * 4)
     alg_flops = float(2 * ((12 if cfg.ln else 11) * d * d + 4 * cfg.mini_batch * d) * seq)
     n_sets = max(1, min(4, math.ceil(3 * L2_BYTES / alg_bytes)))
+    learner_tag = ("" if args.loss == "mse" else f"+loss_{args.loss}") + \
+                  ("" if args.weight_decay == 0 else f"+wd{args.weight_decay:g}")
 
     def make_set():
         t = {k: torch.from_numpy(x[k]).to(dev).to(io) for k in ("Q", "K", "V")}
@@ -730,7 +732,9 @@ def run_backward(args, cfg, world, rank, local):
         t["beta"] = None if x["beta"] is None else torch.from_numpy(x["beta"]).to(dev)
         t["dWf"], t["dbf"] = torch.from_numpy(dWf_h).to(dev), torch.from_numpy(dbf_h).to(dev)
         t["ws"] = torch.empty(ttt.ttt_linear_bwd_workspace_size(t["Q"], mini_batch=cfg.mini_batch,
-                                                               residual_ln=cfg.ln, ln_eps=cfg.eps),
+                                                               residual_ln=cfg.ln, ln_eps=cfg.eps,
+                                                               loss=args.loss,
+                                                               weight_decay=args.weight_decay),
                               dtype=torch.uint8, device=dev)
         t["out"] = (torch.empty_like(t["Q"]), torch.empty_like(t["K"]), torch.empty_like(t["V"]),
                     torch.empty_like(t["eta"]), torch.empty_like(t["W0"]), torch.empty_like(t["b0"]))
@@ -743,7 +747,8 @@ def run_backward(args, cfg, world, rank, local):
     def call(t, strm):
         ttt.ttt_linear_bwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], t["b0"], t["dZ"], t["dWf"],
                            t["dbf"], t["gamma"], t["beta"], mini_batch=cfg.mini_batch,
-                           residual_ln=cfg.ln, ln_eps=cfg.eps, out=t["out"], workspace=t["ws"],
+                           residual_ln=cfg.ln, ln_eps=cfg.eps, loss=args.loss,
+                           weight_decay=args.weight_decay, out=t["out"], workspace=t["ws"],
                            stream=strm)
 
     clocks = ClockSampler(local)
@@ -828,7 +833,8 @@ def run_backward(args, cfg, world, rank, local):
                             x["b0"][hi:hi + 1],
                             None if x["gamma"] is None else x["gamma"][hi:hi + 1],
                             None if x["beta"] is None else x["beta"][hi:hi + 1], sl(dZ_h), sl(dWf_h),
-                            sl(dbf_h), mini_batch=cfg.mini_batch, ln=cfg.ln, eps=cfg.eps)
+                            sl(dbf_h), mini_batch=cfg.mini_batch, ln=cfg.ln, eps=cfg.eps,
+                            loss=args.loss, weight_decay=args.weight_decay)
             done += 1
             dt = time.perf_counter() - t_start
             if dt >= args.cpu_seconds:
@@ -842,7 +848,8 @@ def run_backward(args, cfg, world, rank, local):
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None,
                 "dtype": "f32", "data": "synthetic",
-                "config": {"workload": cfg.name + "+backward", "kind": "linear_backward",
+                "config": {"workload": cfg.name + "+backward" + learner_tag, "kind": "linear_backward",
+                           "learner": {"loss": args.loss, "weight_decay": args.weight_decay},
                            "B": B, "H": H, "L": L, "d": d, "mini_batch": cfg.mini_batch, "io": cfg.io,
                            "l2": f"inputs rotate over {n_sets} sets "
                                  f"({n_sets * alg_bytes / 1e6:.0f} MB of I/O, plus the checkpoint "

@@ -176,9 +176,9 @@ TTT_API ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const vo
  *        256-byte aligned, owned by the caller; the call overwrites it (state checkpoints
  *        of a forward re-run and per-row partial gradients).  Calls that share a workspace
  *        must not overlap in time.
- * Supported: with or without the residual LayerNorm, either loss, no weight decay
- * (desc->weight_decay == 0), d <= 128 with d a multiple of 4, b <= 64; fp32 arithmetic.
- * Otherwise TTT_ERR_UNSUPPORTED.  Outputs may overlap neither each other, the workspace
+ * Supported: with or without the residual LayerNorm, either loss, with or without weight
+ * decay, d <= 128 with d a multiple of 4, b <= 64 (as far as the state checkpoints fit in
+ * shared memory); fp32 arithmetic.  Otherwise TTT_ERR_UNSUPPORTED.  Outputs may overlap neither each other, the workspace
  * nor an input.
  */
 TTT_API size_t ttt_linear_bwd_workspace_size(const ttt_desc *desc);   /* 0: invalid or unsupported */

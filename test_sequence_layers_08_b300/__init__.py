@@ -256,11 +256,12 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: i
 
 def ttt_linear_bwd_workspace_size(Q, *, mini_batch: int = 16, init_per_batch: bool = False,
                                   heads=None, bh_offset: int = 0, loss: str = "mse",
-                                  residual_ln: bool = False, ln_eps: float = 1e-6) -> int:
+                                  residual_ln: bool = False, ln_eps: float = 1e-6,
+                                  weight_decay: float = 0.0) -> int:
     """Bytes of device workspace ttt_linear_bwd needs for inputs shaped like Q (0 when the
     shape is not supported)."""
     desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, heads=heads,
-                     bh_offset=bh_offset, loss=loss)
+                     bh_offset=bh_offset, loss=loss, weight_decay=weight_decay)
     return int(load().ttt_linear_bwd_workspace_size(ctypes.byref(desc)))
 
 
@@ -296,9 +297,9 @@ def _bwd_check(Q, K, V, eta, W0, b0, gamma, beta, dZ, dW_final, db_final, out, r
 
 def ttt_linear_bwd(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, gamma=None, beta=None,
                    *, mini_batch: int = 16, residual_ln: bool = False, ln_eps: float = 1e-6,
-                   init_per_batch: bool = False, loss: str = "mse", out=None, workspace=None,
-                   stream=None, heads=None, bh_offset: int = 0):
-    """TTT-Linear backward on the GPU (no weight decay): the gradients of
+                   init_per_batch: bool = False, loss: str = "mse", weight_decay: float = 0.0,
+                   out=None, workspace=None, stream=None, heads=None, bh_offset: int = 0):
+    """TTT-Linear backward on the GPU: the gradients of
     F = <Z, dZ> + <W_final, dW_final> + <b_final, db_final> for the forward
     ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma, beta, ...).  Returns (dQ, dK, dV, deta, dW0,
     db0), plus (dgamma, dbeta) with the residual LayerNorm; dW0, db0 are shaped like W0, b0.
@@ -310,7 +311,7 @@ def ttt_linear_bwd(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, gamma
                      init_per_batch, heads, bh_offset)
     lib = load()
     desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, heads=heads,
-                     bh_offset=bh_offset, loss=loss)
+                     bh_offset=bh_offset, loss=loss, weight_decay=weight_decay)
     need = int(lib.ttt_linear_bwd_workspace_size(ctypes.byref(desc)))
     if need == 0:
         raise TTTError(2, "ttt_linear_bwd: shape not supported")
@@ -332,7 +333,7 @@ def ttt_linear_bwd(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, gamma
 def ttt_linear_bwd_static(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None, gamma=None,
                           beta=None, *, out, mini_batch: int = 16, residual_ln: bool = False,
                           ln_eps: float = 1e-6, init_per_batch: bool = False, loss: str = "mse",
-                          stream=None, heads=None, bh_offset: int = 0):
+                          weight_decay: float = 0.0, stream=None, heads=None, bh_offset: int = 0):
     """ttt_linear_bwd on the library's static device scratch: allocates nothing, so the
     output buffers ``out=(dQ, dK, dV, deta, dW0, db0[, dgamma, dbeta])`` are required.  Calls
     on one device share the scratch and must not overlap in time.  Returns ``out``."""
@@ -340,7 +341,7 @@ def ttt_linear_bwd_static(Q, K, V, eta, W0, b0, dZ, dW_final=None, db_final=None
                init_per_batch, heads, bh_offset)
     lib = load()
     desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, heads=heads,
-                     bh_offset=bh_offset, loss=loss)
+                     bh_offset=bh_offset, loss=loss, weight_decay=weight_decay)
     dgam, dbet = (out[6], out[7]) if residual_ln else (None, None)
     _check(lib.ttt_linear_bwd_static(ctypes.byref(desc), _ptr(Q), _ptr(K), _ptr(V), _ptr(eta),
                                      _ptr(W0), _ptr(b0), _ptr(gamma if residual_ln else None),

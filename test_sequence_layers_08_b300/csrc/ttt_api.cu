@@ -246,10 +246,10 @@ ttt_status ttt_linear_bwd(const ttt_desc *desc, const void *Q, const void *K, co
     ttt_status st = check_desc(desc, false);
     if (st != TTT_OK) return st;
     const ttt_desc &s = *desc;
-    if (s.weight_decay != 0.f || !ttt::linear_bwd_checkpoint_every(s))
+    if (!ttt::linear_bwd_checkpoint_every(s))
         return fail(TTT_ERR_UNSUPPORTED,
-                    "the backward pass takes no weight decay, d <= 128 (a multiple of 4) and "
-                    "mini_batch <= 64");
+                    "the backward pass takes d <= 128 (a multiple of 4) and mini_batch <= 64 "
+                    "(with the state checkpoints in shared memory)");
     if (s.residual_ln) {
         const void *lp[] = {gamma, beta, dgamma, dbeta};
         const char *ln_names[] = {"gamma", "beta", "dgamma", "dbeta"};

@@ -15,7 +15,13 @@
 //   dV  = -dG
 //   deta_s = -(K dW')_s . g_s - g_s . dc' - sum_t D[t, s] (q_t . k_s + 1)
 //   dW  = dW' + Q^T dZ + K^T dG,   dc = dc' + 1^T dZ + 1^T dG   (K^T dG, 1^T dG: squared error)
-// and dW, dc are the gradients of the state before the mini-batch.  The scan reads the
+// and dW, dc are the gradients of the state before the mini-batch.  With the residual
+// LayerNorm dZ above is the output LayerNorm's backward of dZ (dQ also gets dZ itself), and G's
+// dependence on P and on v (and k) is taken through the per-token Hessian-vector product of
+// the LN-L2 loss.  With weight decay lambda (W' = (1 - lambda S) W - ..., query row t reading
+// (1 - lambda cum_t) W, ai-feeds Modular TTT page): dW' is scaled by 1 - lambda S, Q^T dZ and
+// dZ W^T by 1 - lambda cum_t per token, and
+//   deta_s gains -lambda <W, dW'> - lambda sum_{t >= s} <dZ_t, q_t W>.  The scan reads the
 // states in reverse, so the kernel first re-runs the forward and checkpoints the state
 // every `ck` mini-batches in the workspace; the reverse pass restores a chunk's states
 // from its checkpoint in shared memory and walks its mini-batches backwards.
@@ -84,10 +90,10 @@ __device__ void mm_xyt(float *out, const float *X, const float *Y, int m, int k,
     }
 }
 
-// acc[u][j..j+3] += sum_s w_s X[s][u] Y[s][j..j+3]   (X^T diag(w) Y, 4 x 4 blocks; X: m x k,
-// Y: m x n; w may be null (1); sign -1 subtracts)
+// acc[u][j..j+3] = scale acc + sign sum_s w_s X[s][u] Y[s][j..j+3]   (X^T diag(w) Y, 4 x 4
+// blocks; X: m x k, Y: m x n; w may be null (1))
 __device__ void mm_xty_acc(float *acc, const float *X, const float *Y, const float *w, float sign, int m,
-                           int k, int n)
+                           int k, int n, float scale = 1.f)
 {
     const int n4 = n >> 2, k4 = k >> 2;
     for (int tile = threadIdx.x; tile < k4 * n4; tile += kThreads) {
@@ -105,19 +111,23 @@ __device__ void mm_xty_acc(float *acc, const float *X, const float *Y, const flo
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             float4 o = f4(acc + (u + r) * n + j);
-            o.x = fmaf(sign, a[r].x, o.x);
-            o.y = fmaf(sign, a[r].y, o.y);
-            o.z = fmaf(sign, a[r].z, o.z);
-            o.w = fmaf(sign, a[r].w, o.w);
+            o.x = fmaf(sign, a[r].x, scale * o.x);
+            o.y = fmaf(sign, a[r].y, scale * o.y);
+            o.z = fmaf(sign, a[r].z, scale * o.z);
+            o.w = fmaf(sign, a[r].w, scale * o.w);
             st4(acc + (u + r) * n + j, o);
         }
     }
 }
 
+// floats of the block A, D, eta, f_t, reduction (rounded up to 4: the tiles after it are read
+// as float4)
+__host__ __device__ constexpr int small_floats(int mb) { return (2 * mb * mb + 2 * mb + kThreads / 32 + 3) & ~3; }
+
 struct BwdParams {
     int H, L, d, mb, ck;      // ck: mini-batches per checkpoint
     int init_per_batch, ip;
-    float eps;
+    float eps, wd;            // wd: weight decay lambda
     const void *Q, *K, *V, *dZ;
     const float *eta, *W0, *b0, *gamma, *beta, *dWf, *dbf;
     void *dQ, *dK, *dV;
@@ -216,7 +226,7 @@ __device__ __forceinline__ void ln_grad_row(float *G, const float *z, const floa
 }
 
 template <typename IO, bool LN>
-__global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
+__global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
 {
     extern __shared__ float4 sm4[];
     float *sm = reinterpret_cast<float *>(sm4);
@@ -241,16 +251,23 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
     float *T1 = dG + nt;            // dZbar W^T, later dP W^T
     float *T2 = T1 + nt;            // K dW', later dP
     float *T3 = T2 + nt;            // G dW'^T
+    // the layout below is mirrored by smem_for(); change both together
     float *A = T3 + nt;             // mb mb: R = M . (Q K^T + 1) (A = R E)
     float *Dm = A + mb * mb;        // mb mb
     float *et = Dm + mb * mb;       // mb
-    float *Pz = et + mb;            // LN: P = K W + c
-    float *dZb = Pz + nt;           // LN: Zbar, then dZbar (without LN: dZ itself)
-    float *gam = dZb + nt;          // LN: d
-    float *bet = gam + d;           // LN: d
+    float *fq = et + mb;            // mb: 1 - lambda cum_t (1 without weight decay)
+    float *wred = fq + mb;          // kWarps: a block reduction
+    float *Pz = A + small_floats(mb);   // LN or weight decay: P = K W + c
+    float *dZb = Pz + nt;           // LN or weight decay: Zbar, then dZbar
+    float *gam = dZb + nt;          // d
+    float *bet = gam + d;           // d
+    const bool wdec = p.wd != 0.f;
+    // Q W (no bias): with weight decay its own tile (read again for deta); with LN alone it is
+    // read only before T1 is first written, so it shares T1
+    float *Yq = wdec ? bet + d : T1;
     // kWarps x 2 d for the final dgamma / dbeta reduction: the state area once the scan is
     // done, or its own area when the states are smaller (d < 16)
-    float *red = (2 * d * kWarps <= ck * sd) ? S : bet + d;
+    float *red = (2 * d * kWarps <= ck * sd) ? S : (wdec ? Yq + nt : bet + d);
     if (!LN) dZb = dZt;
 
     const IO *Qg = static_cast<const IO *>(p.Q) + (size_t)bh * L * d;
@@ -289,7 +306,10 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
         __syncthreads();
         gradient_rows(G, LN ? Pz : G);
         __syncthreads();
-        mm_xty_acc(X, Kt, G, et, -1.f, mb, d, d);
+        float esum = 0.f;
+        if (wdec)
+            for (int s2 = 0; s2 < mb; ++s2) esum += et[s2];
+        mm_xty_acc(X, Kt, G, et, -1.f, mb, d, d, 1.f - p.wd * esum);
         for (int j = tid; j < d; j += kThreads) {
             float a = 0.f;
             for (int s = 0; s < mb; ++s) a = fmaf(et[s], G[s * d + j], a);
@@ -337,10 +357,17 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
             load_tile(dZt, dZg + (size_t)n0 * d, nt);
             for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
             __syncthreads();
-            // P (LN: kept in Pz), K dW', R = M . (Q K^T + 1); LN: Q W + c into dZb
+            // P (LN: kept in Pz), K dW', R = M . (Q K^T + 1); Q W (with LN or weight decay)
             mm_xy(LN ? Pz : G, Kt, W, c, mb, d, d);
             mm_xy(T2, Kt, dW, nullptr, mb, d, d);
-            if (LN) mm_xy(dZb, Qt, W, c, mb, d, d);
+            if (LN || wdec) mm_xy(Yq, Qt, W, nullptr, mb, d, d);
+            if (tid == 0) {   // f_t = 1 - lambda sum_{s <= t} eta_s
+                float cum = 0.f;
+                for (int t = 0; t < mb; ++t) {
+                    cum += et[t];
+                    fq[t] = 1.f - p.wd * cum;
+                }
+            }
             for (int i = tid; i < mb * mb; i += kThreads) {
                 const int t = i / mb, s = i - t * mb;
                 float a = 0.f;
@@ -355,11 +382,14 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
             gradient_rows(G, LN ? Pz : G);
             __syncthreads();
             if (LN) {
-                // Zbar = Q W + c - A G, then dZbar = r Pi(gamma dZ) (output LayerNorm backward);
+                // Zbar = f_t Q W + c - A G, then dZbar = r Pi(gamma dZ) (output LayerNorm backward);
                 // dgamma += dZ . xh_o, dbeta += dZ
                 for (int tile = tid; tile < nt / 4; tile += kThreads) {
                     const int t = tile / (d / 4), j = (tile - t * (d / 4)) * 4;
-                    float4 z = f4(dZb + t * d + j);
+                    const float4 y = f4(Yq + t * d + j), cj = f4(c + j);
+                    const float f = fq[t];
+                    float4 z = make_float4(fmaf(f, y.x, cj.x), fmaf(f, y.y, cj.y), fmaf(f, y.z, cj.z),
+                                           fmaf(f, y.w, cj.w));
                     for (int s = 0; s <= t; ++s) fma4(z, -et[s] * A[t * mb + s], f4(G + s * d + j));
                     st4(dZb + t * d + j, z);
                 }
@@ -414,6 +444,8 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
             for (int tile = tid; tile < nt / 4; tile += kThreads) {
                 const int t = tile / (d / 4), j = (tile - t * (d / 4)) * 4;
                 float4 a = f4(T1 + t * d + j);
+                const float f = fq[t];
+                a.x *= f; a.y *= f; a.z *= f; a.w *= f;
                 if (LN) {
                     const float4 z = f4(dZt + t * d + j);
                     a.x += z.x; a.y += z.y; a.z += z.z; a.w += z.w;
@@ -425,6 +457,23 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
                 store_io(dQg, t * d + j + 3, a.w);
             }
             // deta_s = -(K dW')_s . g_s - g_s . dc' - sum_{t >= s} D[t, s] (q_t . k_s + 1)
+            //          [- lambda <W, dW'> - lambda sum_{t >= s} <dZbar_t, q_t W>]
+            float wdw = 0.f;
+            if (wdec) {
+                float part = 0.f;
+                for (int i = tid; i < dd; i += kThreads) part = fmaf(W[i], dW[i], part);
+                part = warp_sum(part);
+                if (lane == 0) wred[warp] = part;
+                for (int t = warp; t < mb; t += kWarps) {   // <dZbar_t, q_t W>
+                    float x = 0.f;
+                    for (int u = lane; u < d; u += 32) x = fmaf(dZb[t * d + u], Yq[t * d + u], x);
+                    x = warp_sum(x);
+                    __syncwarp();
+                    if (lane == 0) Yq[t * d] = x;   // row t of Q W is not read again: keep the dot there
+                }
+                __syncthreads();
+                for (int w2 = 0; w2 < kWarps; ++w2) wdw += wred[w2];
+            }
             for (int s = tid; s < mb; s += kThreads) {
                 float a = 0.f;
                 for (int u = 0; u < d; u += 4) {
@@ -432,6 +481,10 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
                     a -= dot4(f4(T2 + s * d + u), g) + dot4(g, f4(dc + u));
                 }
                 for (int t = s; t < mb; ++t) a -= Dm[t * mb + s] * A[t * mb + s];
+                if (wdec) {
+                    a -= p.wd * wdw;
+                    for (int t = s; t < mb; ++t) a -= p.wd * Yq[t * d];
+                }
                 p.deta[(size_t)bh * L + n0 + s] = a;
             }
             __syncthreads();
@@ -518,7 +571,13 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(BwdParams p)
                 store_io(dKg, s * d + j + 3, a.w);
             }
             // dW += Q^T dZbar + K^T dP;  dc += 1^T dZbar + 1^T dP
-            mm_xty_acc(dW, Qt, dZb, nullptr, 1.f, mb, d, d);
+            {
+                float esum = 0.f;
+                if (wdec)
+                    for (int s2 = 0; s2 < mb; ++s2) esum += et[s2];
+                mm_xty_acc(dW, Qt, dZb, fq, 1.f, mb, d, d, 1.f - p.wd * esum);
+            }
+            __syncthreads();
             mm_xty_acc(dW, Kt, T2, nullptr, 1.f, mb, d, d);
             for (int j = tid; j < d; j += kThreads) {
                 float a = 0.f;
@@ -570,10 +629,15 @@ constexpr size_t kMaxSmem = 227 * 1024;
 
 size_t smem_for(const ttt_desc &s, int ck)
 {
+    // states, dW and dc, nine mb x d tiles, the small block; with LN or weight decay P, Zbar,
+    // gamma, beta and Q W; with LN and d < 16 the dgamma/dbeta reduction's own area
     const size_t d = s.d, mb = s.mini_batch, states = ck * (d * d + d);
     const size_t red = 2 * d * (kThreads / 32);
-    size_t n = states + d * d + d + 9 * mb * d + 2 * mb * mb + mb;
-    if (s.residual_ln) n += 2 * mb * d + 2 * d + (red <= states ? 0 : red);
+    const bool wd = s.weight_decay != 0.f;
+    size_t n = states + d * d + d + 9 * mb * d + small_floats((int)mb);
+    if (s.residual_ln || wd) n += 2 * mb * d + 2 * d;   // P, Zbar / dZbar, gamma, beta
+    if (wd) n += mb * d;                                // Q W
+    if (s.residual_ln && red > states) n += red;
     return n * sizeof(float);
 }
 
@@ -581,7 +645,7 @@ size_t smem_for(const ttt_desc &s, int ck)
 
 int linear_bwd_checkpoint_every(const ttt_desc &s)
 {
-    if (s.d > 128 || s.d % 4 != 0 || s.mini_batch > 64 || s.weight_decay != 0.f) return 0;
+    if (s.d > 128 || s.d % 4 != 0 || s.mini_batch > 64) return 0;
     for (int ck : {4, 2, 1})
         if (smem_for(s, ck) <= kMaxSmem) return ck;
     return 0;
@@ -609,7 +673,7 @@ cudaError_t launch_linear_bwd(const LinearBwdArgs &a)
     float *part = ckpt + (size_t)rows * nck * (d * d + d);
     float *dgb = part + (s.init_per_batch ? 0 : (size_t)rows * (d * d + d));
     BwdParams p{s.H, s.L, s.d, s.mini_batch, ck, s.init_per_batch, s.loss == TTT_LOSS_INNER_PRODUCT,
-                s.ln_eps, a.Q, a.K, a.V, a.dZ, a.eta, a.W0, a.b0, a.gamma, a.beta, a.dW_final, a.db_final,
+                s.ln_eps, s.weight_decay, a.Q, a.K, a.V, a.dZ, a.eta, a.W0, a.b0, a.gamma, a.beta, a.dW_final, a.db_final,
                 a.dQ, a.dK, a.dV, a.deta, s.init_per_batch ? a.dW0 : part,
                 s.init_per_batch ? a.db0 : part + (size_t)rows * d * d, dgb, ckpt, head_offset(s)};
     const size_t smem = smem_for(s, ck);

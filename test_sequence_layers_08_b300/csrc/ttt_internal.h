@@ -54,7 +54,7 @@ struct LinearBwdArgs {
     cudaStream_t stream;
 };
 
-// TTT-Linear backward (no weight decay; d <= 128, d % 4 == 0, b <= 64).  *_checkpoint_every returns the mini-batches per state checkpoint (0: the
+// TTT-Linear backward (d <= 128, d % 4 == 0, b <= 64, shared memory permitting).  *_checkpoint_every returns the mini-batches per state checkpoint (0: the
 // shape is not supported).
 int linear_bwd_checkpoint_every(const ttt_desc &d);
 size_t linear_bwd_workspace_bytes(const ttt_desc &d);

@@ -221,20 +221,20 @@ def call_bwd(lib, dsc, ptrs=None, ws_bytes=1 << 30):
 
 
 def test_backward_declared_and_checked(lib):
-    """ttt_linear_bwd: supported shapes report a workspace size; weight decay is unsupported;
-    a short or misaligned workspace, a NULL or overlapping buffer are invalid arguments (all
-    rejected before any launch)."""
+    """ttt_linear_bwd: supported shapes report a workspace size; a head dim that is no multiple
+    of 4 is unsupported; a short or misaligned workspace, a NULL or overlapping buffer are
+    invalid arguments (all rejected before any launch)."""
     assert "ttt_linear_bwd" in header_functions()
     assert "ttt_linear_bwd_workspace_size" in header_functions()
     ws = lib.ttt_linear_bwd_workspace_size
     assert ws(ctypes.byref(desc())) > 0 and ws(ctypes.byref(desc())) % 256 == 0
     assert ws(ctypes.byref(desc(residual_ln=1))) > ws(ctypes.byref(desc()))   # + dgamma/dbeta partials
-    assert ws(ctypes.byref(desc(weight_decay=0.1))) == 0
+    assert ws(ctypes.byref(desc(weight_decay=0.1))) > 0
     assert ws(ctypes.byref(desc(d=6))) == 0
     assert ws(ctypes.byref(desc(L=40))) == 0      # invalid descriptor
     # per-batch initial state needs no per-row partials: a smaller workspace
     assert ws(ctypes.byref(desc(init_per_batch=1))) < ws(ctypes.byref(desc()))
-    assert call_bwd(lib, desc(weight_decay=0.5)) == 2
+    assert call_bwd(lib, desc(d=6, io_dtype=0)) == 2   # d not a multiple of 4: no kernel
     need = ws(ctypes.byref(desc()))
     assert call_bwd(lib, desc(), ws_bytes=need - 256) == 1
     p = bwd_ptrs()

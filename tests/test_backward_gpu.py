@@ -49,22 +49,22 @@ def to_dev(x, io):
     return out
 
 
-def run(x, io, mb, loss="mse", init_per_batch=False, **kw):
+def run(x, io, mb, loss="mse", init_per_batch=False, weight_decay=0.0, **kw):
     t = to_dev(x, io)
     ln = x.get("gamma") is not None
     res = ttt.ttt_linear_bwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], t["b0"], t["dZ"],
                              t["dW_final"], t["db_final"], t.get("gamma"), t.get("beta"),
                              mini_batch=mb, loss=loss, residual_ln=ln, init_per_batch=init_per_batch,
-                             **kw)
+                             weight_decay=weight_decay, **kw)
     ttt.ttt_sync_status()
     return [r.float().cpu().numpy().astype(np.float64) for r in res]
 
 
-def reference(x, mb, loss="mse", init_per_batch=False):
+def reference(x, mb, loss="mse", init_per_batch=False, weight_decay=0.0):
     ln = x.get("gamma") is not None
     g = ttt_linear_grad(x["Q"], x["K"], x["V"], x["eta"], x["W0"], x["b0"], x.get("gamma"),
                         x.get("beta"), x["dZ"], x["dW_final"], x["db_final"], mini_batch=mb, ln=ln,
-                        eps=1e-6, loss=loss, init_per_batch=init_per_batch)
+                        eps=1e-6, loss=loss, weight_decay=weight_decay, init_per_batch=init_per_batch)
     names = ("dQ", "dK", "dV", "deta", "dW0", "db0") + (("dgamma", "dbeta") if ln else ())
     return [g[k] for k in names]
 
@@ -166,3 +166,17 @@ def test_backward_residual_ln_per_batch_initial_state():
     x = problem(B=2, H=2, L=64, d=64, io="f32", seed=45, init_per_batch=True, ln=True)
     compare(run(x, "f32", 16, init_per_batch=True), reference(x, 16, init_per_batch=True), "f32",
             init_per_batch=True)
+
+
+@pytest.mark.parametrize("ln", [False, True])
+@pytest.mark.parametrize("loss", ["mse", "ip"])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_backward_weight_decay(io, loss, ln):
+    """Weight decay (ai-feeds Modular TTT page): lambda = 0.5 on eta up to ~0.13 per token."""
+    x = problem(B=2, H=2, L=80, d=64, io=io, seed=61 + ln, ln=ln)
+    compare(run(x, io, 16, loss, weight_decay=0.5), reference(x, 16, loss, weight_decay=0.5), io)
+
+
+def test_backward_weight_decay_small_shapes():
+    x = problem(B=1, H=2, L=40, d=32, io="f32", seed=63, ln=True)
+    compare(run(x, "f32", 8, weight_decay=0.3), reference(x, 8, weight_decay=0.3), "f32")
