@@ -75,18 +75,33 @@ __device__ void mm_xy(float *out, const float *X, const float *Y, const float *i
     }
 }
 
+// Dot product of two k-long shared-memory rows, starting at column `start` (a multiple of 4)
+// and wrapping: threads whose rows are k floats apart start 4 floats apart, so their 16-byte
+// loads fall in different banks.
+__device__ __forceinline__ float rot_dot(const float *x, const float *y, int k, int start)
+{
+    float a0 = 0.f, a1 = 0.f;
+    int u = start;
+    for (int c = 0; c < k; c += 8) {
+        a0 += dot4(f4(x + u), f4(y + u));
+        u += 4;
+        if (u >= k) u -= k;
+        if (c + 4 < k) {
+            a1 += dot4(f4(x + u), f4(y + u));
+            u += 4;
+            if (u >= k) u -= k;
+        }
+    }
+    return a0 + a1;
+}
+__device__ __forceinline__ int rot_start(int row, int k) { return (4 * row) % k; }
+
 // out[r][i] = sum_j X[r][j] Y[i][j]   (X Y^T; X: m x k, Y: n x k; k a multiple of 4)
 __device__ void mm_xyt(float *out, const float *X, const float *Y, int m, int k, int n)
 {
     for (int idx = threadIdx.x; idx < m * n; idx += kThreads) {
         const int r = idx / n, i = idx - r * n;
-        const float *xr = X + r * k, *yr = Y + i * k;
-        float a0 = 0.f, a1 = 0.f;
-        for (int u = 0; u < k; u += 8) {
-            a0 += dot4(f4(xr + u), f4(yr + u));
-            if (u + 4 < k) a1 += dot4(f4(xr + u + 4), f4(yr + u + 4));
-        }
-        out[idx] = a0 + a1;
+        out[idx] = rot_dot(X + r * k, Y + i * k, k, rot_start(i, k));
     }
 }
 
@@ -370,13 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
             }
             for (int i = tid; i < mb * mb; i += kThreads) {
                 const int t = i / mb, s = i - t * mb;
-                float a = 0.f;
-                if (s <= t) {
-                    float x = 0.f;
-                    for (int u = 0; u < d; u += 4) x += dot4(f4(Qt + t * d + u), f4(Kt + s * d + u));
-                    a = x + 1.f;
-                }
-                A[i] = a;
+                A[i] = s <= t ? rot_dot(Qt + t * d, Kt + s * d, d, rot_start(s, d)) + 1.f : 0.f;
             }
             __syncthreads();
             gradient_rows(G, LN ? Pz : G);
@@ -420,10 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
             mm_xyt(T3, G, dW, mb, d, d);
             for (int i = tid; i < mb * mb; i += kThreads) {
                 const int t = i / mb, s = i - t * mb;
-                float x = 0.f;
-                if (s <= t)
-                    for (int u = 0; u < d; u += 4) x += dot4(f4(dZb + t * d + u), f4(G + s * d + u));
-                Dm[i] = x;
+                Dm[i] = s <= t ? rot_dot(dZb + t * d, G + s * d, d, rot_start(s, d)) : 0.f;
             }
             for (int tile = tid; tile < nt / 4; tile += kThreads) {
                 const int s = tile / (d / 4), j = (tile - s * (d / 4)) * 4;
@@ -475,11 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
                 for (int w2 = 0; w2 < kWarps; ++w2) wdw += wred[w2];
             }
             for (int s = tid; s < mb; s += kThreads) {
-                float a = 0.f;
-                for (int u = 0; u < d; u += 4) {
-                    const float4 g = f4(G + s * d + u);
-                    a -= dot4(f4(T2 + s * d + u), g) + dot4(g, f4(dc + u));
-                }
+                float a = -rot_dot(T2 + s * d, G + s * d, d, rot_start(s, d)) -
+                          rot_dot(dc, G + s * d, d, rot_start(s, d));
                 for (int t = s; t < mb; ++t) a -= Dm[t * mb + s] * A[t * mb + s];
                 if (wdec) {
                     a -= p.wd * wdw;
