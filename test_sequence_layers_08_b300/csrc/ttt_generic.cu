@@ -320,20 +320,25 @@ __global__ void __launch_bounds__(kLinThreads) linear_generic_kernel(LinearParam
             *reinterpret_cast<float4 *>(Zb + t * d + j) =
                 make_float4(fmaf(f, aq.x, cj.x), fmaf(f, aq.y, cj.y), fmaf(f, aq.z, cj.z), fmaf(f, aq.w, cj.w));
         }
-        // A[t, s] = eta_s (q_t . k_s + 1), s <= t
+        // A[t, s] = eta_s (q_t . k_s + 1), s <= t.  Neighbouring threads take neighbouring s,
+        // whose K rows are d floats apart: each starts its dot product 4 s columns further on
+        // (wrapping), so their 16-byte loads fall in different shared-memory banks.
         for (int i = tid; i < mb * mb; i += kThreads) {
             const int t = i / mb, s = i - t * mb;
             float a = 0.f;
             if (s <= t) {
                 const float *qr = Qt + t * d, *kr = Kt + s * d;
                 float a0 = 0.f, a1 = 0.f;
+                int u = (4 * s) % d;
 #pragma unroll(DC ? DC / 4 : 1)
-                for (int u = 0; u < d; u += 4) {
+                for (int c = 0; c < d; c += 4) {
                     const float4 q4 = f4(qr + u), k4 = f4(kr + u);
                     a0 = fmaf(q4.x, k4.x, a0);
                     a1 = fmaf(q4.y, k4.y, a1);
                     a0 = fmaf(q4.z, k4.z, a0);
                     a1 = fmaf(q4.w, k4.w, a1);
+                    u += 4;
+                    if (u >= d) u -= d;
                 }
                 a = (a0 + a1 + 1.f) * et[s];
             }
