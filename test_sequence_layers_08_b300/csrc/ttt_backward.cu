@@ -1,4 +1,5 @@
-// ttt_backward.cu -- backward pass of the TTT-Linear inner loop (no residual LayerNorm).
+// ttt_backward.cu -- backward pass of the TTT-Linear inner loop (with or without the residual
+// LayerNorm, either loss, optional weight decay).
 //
 // Training through the inner loop (the meta-learning gradient of the damodev.csdn.net TTT
 // article, section 6.1) needs the vector-Jacobian product of the mini-batch scan of
