@@ -74,7 +74,8 @@ def algorithmic_bytes(cfg) -> float:
 KERNEL_SOURCES = {"ttt_linear_fused": "ttt_linear_tc.cu", "ttt_linear_chunked": "ttt_linear_chunk.cu",
                   "ttt_mlp_fused": "ttt_mlp_tc.cu", "ttt_linear_decode": "ttt_decode.cu",
                   "ttt_linear_bwd": "ttt_backward.cu",
-                  "ttt_linear_generic": "ttt_generic.cu", "ttt_mlp_generic": "ttt_generic.cu"}
+                  "ttt_linear_generic": "ttt_generic.cu", "ttt_mlp_generic": "ttt_generic.cu",
+                  "ttt_linear_cols": "ttt_linear_cols.cu"}
 
 
 def measured_traffic(kname, workload):

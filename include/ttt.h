@@ -112,10 +112,13 @@ enum { TTT_LOSS_MSE = 0, TTT_LOSS_INNER_PRODUCT = 1 };
  *   out: Z [B,H,L,d] (io_dtype): z_t = f(q_t; W_t, c_t) with the weights after
  *        token t's update; W_final [B,H,d,d], b_final [B,H,d]: state after
  *        the last mini-batch.
- * Supported: d <= 128 with d a multiple of 4, and b <= 64 (generic kernel, fp32
- * arithmetic); bf16 I/O with d = 64, b = 16 runs a tensor-core kernel: without the
- * residual LayerNorm and weight decay the chunked kernel (the state carried across
- * 64-token chunks), otherwise the fused kernel (every loss and decay).
+ * Supported: d <= 128 with d a multiple of 4, and b <= 64 (generic kernels, fp32
+ * arithmetic: without the residual LayerNorm and with at most 2 x 148 CTAs' worth of
+ * (batch, head) rows, each row split over CTAs by output column, since the columns of the
+ * state evolve independently there; otherwise one CTA per row); bf16 I/O with d = 64,
+ * b = 16 runs a tensor-core kernel: without the residual LayerNorm and weight decay the
+ * chunked kernel (the state carried across 64-token chunks), otherwise the fused kernel
+ * (every loss and decay).
  */
 TTT_API ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
                           const float *eta, const float *W0, const float *b0,

@@ -136,6 +136,7 @@ const char *linear_kernel(const ttt_desc &s)
 {
     if (ttt::linear_chunk_supported(s)) return "ttt_linear_chunked";
     if (ttt::linear_tc_supported(s)) return "ttt_linear_fused";
+    if (ttt::linear_cols_dc(s)) return "ttt_linear_cols";
     if (ttt::linear_generic_smem_bytes(s)) return "ttt_linear_generic";
     return nullptr;
 }
@@ -225,6 +226,7 @@ ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, co
     if (st != TTT_OK) return st;
     cudaError_t e = ttt::linear_chunk_supported(s) ? ttt::launch_linear_chunk(a)
                     : ttt::linear_tc_supported(s)  ? ttt::launch_linear_tc(a)
+                    : ttt::linear_cols_dc(s)       ? ttt::launch_linear_cols(a)
                                                    : ttt::launch_linear_generic(a);
     if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "%s launch: %s", kname, cudaGetErrorString(e));
     return ok();

@@ -83,6 +83,13 @@ cudaError_t launch_linear_generic(const LinearArgs &a);
 size_t mlp_generic_smem_bytes(const ttt_desc &d);
 cudaError_t launch_mlp_generic(const MlpArgs &a);
 
+// Column-split TTT-Linear kernel without the residual LayerNorm (fp32 FFMA, d <= 128,
+// d % 4 == 0, b <= 64): each (batch, head) row runs on d / dc CTAs of dc output columns.
+// linear_cols_dc returns dc, or 0 when the kernel is not used for the shape (LN, or too
+// many rows for a split to pay).
+int linear_cols_dc(const ttt_desc &d);
+cudaError_t launch_linear_cols(const LinearArgs &a);
+
 // Tensor-core TTT-Linear kernel (bf16 I/O, d = 64, b = 16).
 bool linear_tc_supported(const ttt_desc &d);
 cudaError_t launch_linear_tc(const LinearArgs &a);

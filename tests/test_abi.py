@@ -109,8 +109,13 @@ def test_kernel_choice(lib):
     k = lambda **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), 0))
     assert k() in LINEAR_TC_KERNELS
     assert k(residual_ln=1) in LINEAR_TC_KERNELS
-    assert k(io_dtype=0) == "ttt_linear_generic"
-    assert k(d=32) == "ttt_linear_generic"
+    # without LN, few (batch, head) rows: split by output column; with LN, or with more rows
+    # than two CTAs per SM hold at 16 columns each: one CTA per row
+    assert k(io_dtype=0) == "ttt_linear_cols"
+    assert k(d=32) == "ttt_linear_cols"
+    assert k(io_dtype=0, residual_ln=1) == "ttt_linear_generic"
+    assert k(io_dtype=0, B=8, H=12) == "ttt_linear_generic"
+    assert k(io_dtype=0, B=2, H=12) == "ttt_linear_cols"
     assert k(d=256) is None
     assert k(d=6, io_dtype=0) is None   # the generic kernel takes d a multiple of 4
     m = lambda **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), 1))

@@ -18,6 +18,7 @@ CASES = {
     "linear_ln_bf16": CONFIGS["linear_ln_bf16_B4_H16_L8192"].with_(B=3, H=5, L=128),
     "linear_bf16": CONFIGS["linear_bf16_B8_H12_L2048"].with_(B=3, H=5, L=96),
     "linear_f32": CONFIGS["linear_ln_bf16_B4_H16_L8192"].with_(B=3, H=5, L=64, io="f32"),
+    "linear_f32_noln": CONFIGS["linear_f32_B1_H2_L256"].with_(B=3, H=5, L=64),   # column split
     "mlp_ln_bf16": CONFIGS["mlp_ln_bf16_B4_H12_L4096"].with_(B=3, H=5, L=64),
 }
 RANGES = [(0, 4), (4, 11), (11, 15)]
