@@ -20,17 +20,23 @@
 // last), so the kernel shortens the chain per token: the d x d state update, the key
 // product of the next chunk and the query product of this one are 64-token warp-MMA
 // GEMMs, and only the intra-chunk correction (three dependent 16 x 16 x 16 products)
-// sits between them.  One CTA per (batch, head), four warps:
+// sits between them.  One CTA per (batch, head), eight warps in two roles:
 //   * 64-token stages of Q, K, V (TMA, 128-byte swizzle) and eta (bulk copy) stream into
-//     a 3-deep shared-memory ring; one thread refills a slot after the barrier that
+//     a 4-deep shared-memory ring; one thread refills a slot after the barrier that
 //     retires it;
-//   * warp w owns output features 16w..16w+15: W^T rows live in registers as fp32
-//     accumulators, and P, Zbar, G are 16 x 64 register tiles (features x tokens);
-//   * the 16 input-only 16 x 16 blocks of a chunk (6 chain blocks L_{ml}, 10 output
-//     blocks) are computed one chunk ahead, four per warp, and shared as ready-made bf16
-//     B fragments through shared memory;
-//   * one named barrier per chunk; Z tiles are transposed with stmatrix into a swizzled
-//     staging tile and written by a TMA store.
+//   * state warps 0-3: warp w owns output features 16w..16w+15, its W^T rows live in
+//     registers as fp32 accumulators; per chunk it forms G (P, Zbar, G are 16 x 64 register
+//     tiles, features x tokens), runs the intra-chunk chain and the state update, then the
+//     next chunk's key product and its six chain blocks L_{ml}; it publishes the chunk's
+//     starting W^T (bf16 fragments) and -G through shared memory;
+//   * output warps 4-7: one chunk behind, warp 4 + w forms Zbar for features 16w..16w+15:
+//     the query product with the published starting state, the output corrections with the
+//     published G, the Z tile (transposed with stmatrix into a swizzled staging tile and
+//     written by a TMA store); it also computes the next chunk's ten output blocks.
+//   So the state warps, whose chunk-to-chunk dependence is the critical path, issue only
+//   the key side (about half of the per-chunk products), and the query side overlaps it;
+//   the 16 x 16 blocks depend on the inputs alone and are shared as ready-made bf16 B
+//   fragments through shared memory; one named barrier of all eight warps per chunk.
 // Every mbarrier wait is bounded; a wait that runs out sets the library's failure flag
 // and the kernel finishes without waiting again.
 #include <cuda.h>
@@ -47,9 +53,10 @@ constexpr int D = 64;           // head dim
 constexpr int MB = 16;          // mini-batch
 constexpr int CT = 64;          // tokens per chunk (= per pipeline stage)
 constexpr int NMB = CT / MB;    // mini-batches per chunk
-constexpr int NSS = 3;          // stages in the ring
-constexpr int kThreads = 128;
-constexpr int kRefill = 96;     // thread that refills ring slots (warp 3; warp 0 stores Z)
+constexpr int NSS = 4;          // stages in the ring (chunks i - 1, i, i + 1 are read in iteration i)
+constexpr int kStateWarps = 4, kThreads = 256;
+constexpr int kRefill = 96;     // thread that refills ring slots (a state warp)
+constexpr int kStorer = 128;    // thread that stores Z tiles (an output warp)
 constexpr uint32_t kTileBytes = CT * D * 2;   // 8 KB
 constexpr int kBlocks = 16;     // 6 chain blocks + 10 output blocks
 
@@ -59,6 +66,9 @@ struct __align__(1024) Smem {
     __nv_bfloat16 v[NSS][CT * D];
     __nv_bfloat16 z[2][CT * D];
     uint2 blk[2][kBlocks][2][32];   // [chunk parity][block][source half][lane]
+    uint4 ng[2][kStateWarps][NMB][32];   // -G_m A fragments [chunk parity][feature warp][m][lane]
+    uint4 wa[2][kStateWarps][4][32];     // starting W^T A fragments [chunk parity][feature warp][k-step][lane]
+    float2 cb[2][kStateWarps][32];       // starting c of the lane's features j0, j1
     float eta[NSS][CT];
     unsigned long long full[NSS];
     int abort_flag;
@@ -129,7 +139,9 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     __syncthreads();
 
     const int g = lane >> 2, c = lane & 3, mrow = lane & 7, mat = lane >> 3;
-    const int j0 = warp * 16 + g, j1 = j0 + 8;   // this thread's two features
+    const int fw = warp & 3;                         // feature group of this warp (both roles)
+    const bool state_warp = warp < kStateWarps;
+    const int j0 = fw * 16 + g, j1 = j0 + 8;         // this thread's two features
     bool aborted = false;
 
     auto wait_stage = [&](int st) {
@@ -157,10 +169,11 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
     };
 
-    // ---- initial state: W^T rows j0/j1 as fp32 accumulators, c
+    // ---- initial state (state warps): W^T rows j0/j1 as fp32 accumulators, c
     float wt[8][4];
+    float cb0 = 0.f, cb1 = 0.f;
     const size_t init = p.init_per_batch ? (size_t)bh : (size_t)h;
-    {
+    if (state_warp) {
         const float *W0 = p.W0 + init * D * D;
 #pragma unroll
         for (int pt = 0; pt < 8; ++pt) {
@@ -170,9 +183,9 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             wt[pt][2] = W0[i * D + j1];
             wt[pt][3] = W0[(i + 1) * D + j1];
         }
+        cb0 = p.b0[init * D + j0];
+        cb1 = p.b0[init * D + j1];
     }
-    float cb0 = p.b0[init * D + j0];
-    float cb1 = p.b0[init * D + j1];
     const float kf = p.ip ? 0.f : 1.f;   // weight of P in G (0: inner-product loss, G = -V)
 
     uint32_t wa[4][4];   // bf16 A fragments of W^T, k-steps of 16 input features
@@ -187,7 +200,7 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     };
 
     // acc[nt] = W^T X^T + c over the 64 tokens of chunk cc (n-tile nt = tokens 8 nt..8 nt + 7)
-    auto product = [&](float (*acc)[4], const __nv_bfloat16 (*arr)[CT * D], int cc) {
+    auto product = [&](float (*acc)[4], const __nv_bfloat16 (*arr)[CT * D], int cc, float c0, float c1) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
 #pragma unroll
@@ -196,8 +209,8 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 uint32_t r[4];
                 ptx::ldsm_x4(tile_addr(arr, cc, (2 * tb + (mat >> 1)) * 8 + mrow, 2 * q + (mat & 1)), r);
                 if (q == 0) {
-                    ptx::mma_bf16_c(acc[2 * tb], wa[q], r[0], r[1], cb0, cb0, cb1, cb1);
-                    ptx::mma_bf16_c(acc[2 * tb + 1], wa[q], r[2], r[3], cb0, cb0, cb1, cb1);
+                    ptx::mma_bf16_c(acc[2 * tb], wa[q], r[0], r[1], c0, c0, c1, c1);
+                    ptx::mma_bf16_c(acc[2 * tb + 1], wa[q], r[2], r[3], c0, c0, c1, c1);
                 } else {
                     ptx::mma_bf16(acc[2 * tb], wa[q], r[0], r[1]);
                     ptx::mma_bf16(acc[2 * tb + 1], wa[q], r[2], r[3]);
@@ -244,13 +257,25 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             s.blk[cc & 1][b][hf][lane] = make_uint2(ptx::pack_bf16(v0, v1), ptx::pack_bf16(v2, v3));
         }
     };
-    // this warp's four blocks of chunk cc: the output blocks of target mini-batch w and the
-    // chain blocks of target mini-batch 3 - w
-    auto blocks = [&](int cc) {
+    // chain blocks L_{ml} (m > l; numbers 0..5) of chunk cc: state warp w takes those with
+    // number = w mod 4
+    auto chain_blocks = [&](int cc) {
         zero_eta_tail(cc);
-        for (int l = 0; l <= warp; ++l) block(s.q, cc, warp, l, l == warp, out_blk(warp, l));
-        const int mc = NMB - 1 - warp;
-        for (int l = 0; l < mc; ++l) block(s.k, cc, mc, l, false, chain_blk(mc, l));
+#pragma unroll
+        for (int m = 1; m < NMB; ++m)
+#pragma unroll
+            for (int l = 0; l < m; ++l)
+                if (chain_blk(m, l) % kStateWarps == fw) block(s.k, cc, m, l, false, chain_blk(m, l));
+    };
+    // output blocks (m, l), l <= m (numbers 6..15) of chunk cc: output warp 4 + w takes those
+    // with (number - 6) = w mod 4
+    auto out_blocks = [&](int cc) {
+        zero_eta_tail(cc);
+#pragma unroll
+        for (int m = 0; m < NMB; ++m)
+#pragma unroll
+            for (int l = 0; l <= m; ++l)
+                if ((out_blk(m, l) - 6) % kStateWarps == fw) block(s.q, cc, m, l, l == m, out_blk(m, l));
     };
     // both n-tiles of a block: (f0.x, f1.x) for target tokens 0-7, (f0.y, f1.y) for 8-15
     auto read_blk = [&](int cc, int b, uint2 &f0, uint2 &f1) {
@@ -258,134 +283,166 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         f1 = s.blk[cc & 1][b][1][lane];
     };
 
-    // ---- prologue: P_0 = K_0 W_0 + c_0 and the blocks of chunk 0
-    wait_stage(0);
-    pack_w();
+    // ---- prologue (state warps): P_0 = K_0 W_0 + c_0 and the chain blocks of chunk 0
     float pacc[8][4];
-    product(pacc, s.k, 0);
-    blocks(0);
-    ptx::named_bar(1, kThreads);
-
-    for (int cc = 0; cc < NC; ++cc) {
-        const bool more = cc + 1 < NC;
-        if (more) wait_stage(cc + 1);
-
-        // query-side product with the chunk's starting state
-        float yacc[8][4];
-        product(yacc, s.q, cc);
-
-        // intra-chunk chain: G_m, then its corrections to the later mini-batches' P and to Zbar,
-        // and its k-step of the state update
-        uint32_t ng[NMB][4];
-        float d0 = 0.f, d1 = 0.f;   // eta^T G for features j0, j1 (this thread's tokens)
-#pragma unroll
-        for (int m = 0; m < NMB; ++m) {
-            float vt[2][4];
-            {
-                uint32_t r[4];   // V^T of mini-batch m: matrices (t0, j0), (t0, j1), (t1, j0), (t1, j1)
-                ptx::ldsm_x4_t(tile_addr(s.v, cc, m * MB + (mat >> 1) * 8 + mrow, warp * 2 + (mat & 1)), r);
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    vt[u][0] = ptx::bf16_lo(r[2 * u]);
-                    vt[u][1] = ptx::bf16_hi(r[2 * u]);
-                    vt[u][2] = ptx::bf16_lo(r[2 * u + 1]);
-                    vt[u][3] = ptx::bf16_hi(r[2 * u + 1]);
-                }
-            }
-            float gm[2][4];
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) gm[u][i] = fmaf(pacc[2 * m + u][i], kf, -vt[u][i]);
-            ng[m][0] = ptx::pack_bf16(-gm[0][0], -gm[0][1]);
-            ng[m][1] = ptx::pack_bf16(-gm[0][2], -gm[0][3]);
-            ng[m][2] = ptx::pack_bf16(-gm[1][0], -gm[1][1]);
-            ng[m][3] = ptx::pack_bf16(-gm[1][2], -gm[1][3]);
-            // chain: P_{m'} -= G_m L_{m'm}^T for the later mini-batches
-#pragma unroll
-            for (int mp = m + 1; mp < NMB; ++mp) {
-                uint2 f0, f1;
-                read_blk(cc, chain_blk(mp, m), f0, f1);
-                ptx::mma_bf16(pacc[2 * mp], ng[m], f0.x, f1.x);
-                ptx::mma_bf16(pacc[2 * mp + 1], ng[m], f0.y, f1.y);
-            }
-            // outputs: Zbar_{m'} -= G_m B_{m'm}^T for m' >= m (independent accumulators)
-#pragma unroll
-            for (int mp = m; mp < NMB; ++mp) {
-                uint2 f0, f1;
-                read_blk(cc, out_blk(mp, m), f0, f1);
-                ptx::mma_bf16(yacc[2 * mp], ng[m], f0.x, f1.x);
-                ptx::mma_bf16(yacc[2 * mp + 1], ng[m], f0.y, f1.y);
-            }
-            // state update, k-step m: W^T += (-eta G_m)^T K_m
-            const int s0 = m * MB + 2 * c;
-            const float2 ea = eta2(cc, s0), eb = eta2(cc, s0 + 8);
-            const float e00 = ea.x, e01 = ea.y, e10 = eb.x, e11 = eb.y;
-            uint32_t nge[4];
-            nge[0] = ptx::pack_bf16(-e00 * gm[0][0], -e01 * gm[0][1]);
-            nge[1] = ptx::pack_bf16(-e00 * gm[0][2], -e01 * gm[0][3]);
-            nge[2] = ptx::pack_bf16(-e10 * gm[1][0], -e11 * gm[1][1]);
-            nge[3] = ptx::pack_bf16(-e10 * gm[1][2], -e11 * gm[1][3]);
-            d0 += e00 * gm[0][0] + e01 * gm[0][1] + e10 * gm[1][0] + e11 * gm[1][1];
-            d1 += e00 * gm[0][2] + e01 * gm[0][3] + e10 * gm[1][2] + e11 * gm[1][3];
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp) {
-                // matrices (s-block, i-chunk): (0, 2pp), (1, 2pp), (0, 2pp + 1), (1, 2pp + 1)
-                uint32_t r[4];
-                ptx::ldsm_x4_t(tile_addr(s.k, cc, m * MB + (mat & 1) * 8 + mrow, 2 * pp + (mat >> 1)), r);
-                ptx::mma_bf16(wt[2 * pp], nge, r[0], r[1]);
-                ptx::mma_bf16(wt[2 * pp + 1], nge, r[2], r[3]);
-            }
-        }
-        // c -= eta^T G over the chunk (sum over the four lanes sharing g)
-        d0 += __shfl_xor_sync(0xffffffffu, d0, 1);
-        d1 += __shfl_xor_sync(0xffffffffu, d1, 1);
-        d0 += __shfl_xor_sync(0xffffffffu, d0, 2);
-        d1 += __shfl_xor_sync(0xffffffffu, d1, 2);
-        cb0 -= d0;
-        cb1 -= d1;
+    if (state_warp) {
+        wait_stage(0);
         pack_w();
+        product(pacc, s.k, 0, cb0, cb1);
+        chain_blocks(0);
+    }
+    ptx::named_bar(1, kThreads);   // every state warp reads all six chain blocks of chunk 0
 
-        // next chunk: its key product from the new state, and its input-only blocks
-        if (more) {
-            product(pacc, s.k, cc + 1);
-            blocks(cc + 1);
-        }
+    // Iteration i: the state warps run chunk i (i < NC); the output warps compute the output
+    // blocks of chunk i (i < NC) and the outputs of chunk i - 1 (i >= 1).  The barrier at the
+    // end of the iteration publishes both; stage i - 1 is then no longer read.
+    for (int it = 0; it <= NC; ++it) {
+        if (state_warp && it < NC) {
+            const int cc = it;
+            const bool more = cc + 1 < NC;
+            if (more) wait_stage(cc + 1);
+            // the chunk's starting state for the output warps
+#pragma unroll
+            for (int q = 0; q < 4; ++q) s.wa[cc & 1][fw][q][lane] = make_uint4(wa[q][0], wa[q][1], wa[q][2], wa[q][3]);
+            s.cb[cc & 1][fw][lane] = make_float2(cb0, cb1);
 
-        // Zbar -> bf16 staging tile cc % 2 (rows = tokens), TMA-stored after the barrier
-        {
-            const uint32_t zaddr = ptx::smem_addr(s.z[cc & 1]);
+            // intra-chunk chain: G_m, then its corrections to the later mini-batches' P and its
+            // k-step of the state update
+            float d0 = 0.f, d1 = 0.f;   // eta^T G for features j0, j1 (this thread's tokens)
 #pragma unroll
             for (int m = 0; m < NMB; ++m) {
-                uint32_t r[4];
-                r[0] = ptx::pack_bf16(yacc[2 * m][0], yacc[2 * m][1]);
-                r[1] = ptx::pack_bf16(yacc[2 * m][2], yacc[2 * m][3]);
-                r[2] = ptx::pack_bf16(yacc[2 * m + 1][0], yacc[2 * m + 1][1]);
-                r[3] = ptx::pack_bf16(yacc[2 * m + 1][2], yacc[2 * m + 1][3]);
-                // matrices (j-block, t-block): (0,0), (1,0), (0,1), (1,1)
-                ptx::stsm_x4_t(zaddr + ptx::sw128(m * MB + (mat >> 1) * 8 + mrow, warp * 2 + (mat & 1)), r);
+                float vt[2][4];
+                {
+                    uint32_t r[4];   // V^T of mini-batch m: matrices (t0, j0), (t0, j1), (t1, j0), (t1, j1)
+                    ptx::ldsm_x4_t(tile_addr(s.v, cc, m * MB + (mat >> 1) * 8 + mrow, fw * 2 + (mat & 1)), r);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        vt[u][0] = ptx::bf16_lo(r[2 * u]);
+                        vt[u][1] = ptx::bf16_hi(r[2 * u]);
+                        vt[u][2] = ptx::bf16_lo(r[2 * u + 1]);
+                        vt[u][3] = ptx::bf16_hi(r[2 * u + 1]);
+                    }
+                }
+                float gm[2][4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) gm[u][i] = fmaf(pacc[2 * m + u][i], kf, -vt[u][i]);
+                uint32_t ng[4];
+                ng[0] = ptx::pack_bf16(-gm[0][0], -gm[0][1]);
+                ng[1] = ptx::pack_bf16(-gm[0][2], -gm[0][3]);
+                ng[2] = ptx::pack_bf16(-gm[1][0], -gm[1][1]);
+                ng[3] = ptx::pack_bf16(-gm[1][2], -gm[1][3]);
+                s.ng[cc & 1][fw][m][lane] = make_uint4(ng[0], ng[1], ng[2], ng[3]);
+                // chain: P_{m'} -= G_m L_{m'm}^T for the later mini-batches
+#pragma unroll
+                for (int mp = m + 1; mp < NMB; ++mp) {
+                    uint2 f0, f1;
+                    read_blk(cc, chain_blk(mp, m), f0, f1);
+                    ptx::mma_bf16(pacc[2 * mp], ng, f0.x, f1.x);
+                    ptx::mma_bf16(pacc[2 * mp + 1], ng, f0.y, f1.y);
+                }
+                // state update, k-step m: W^T += (-eta G_m)^T K_m
+                const int s0 = m * MB + 2 * c;
+                const float2 ea = eta2(cc, s0), eb = eta2(cc, s0 + 8);
+                const float e00 = ea.x, e01 = ea.y, e10 = eb.x, e11 = eb.y;
+                uint32_t nge[4];
+                nge[0] = ptx::pack_bf16(-e00 * gm[0][0], -e01 * gm[0][1]);
+                nge[1] = ptx::pack_bf16(-e00 * gm[0][2], -e01 * gm[0][3]);
+                nge[2] = ptx::pack_bf16(-e10 * gm[1][0], -e11 * gm[1][1]);
+                nge[3] = ptx::pack_bf16(-e10 * gm[1][2], -e11 * gm[1][3]);
+                d0 += e00 * gm[0][0] + e01 * gm[0][1] + e10 * gm[1][0] + e11 * gm[1][1];
+                d1 += e00 * gm[0][2] + e01 * gm[0][3] + e10 * gm[1][2] + e11 * gm[1][3];
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {
+                    // matrices (s-block, i-chunk): (0, 2pp), (1, 2pp), (0, 2pp + 1), (1, 2pp + 1)
+                    uint32_t r[4];
+                    ptx::ldsm_x4_t(tile_addr(s.k, cc, m * MB + (mat & 1) * 8 + mrow, 2 * pp + (mat >> 1)), r);
+                    ptx::mma_bf16(wt[2 * pp], nge, r[0], r[1]);
+                    ptx::mma_bf16(wt[2 * pp + 1], nge, r[2], r[3]);
+                }
             }
-            ptx::fence_proxy_async();
+            // c -= eta^T G over the chunk (sum over the four lanes sharing g)
+            d0 += __shfl_xor_sync(0xffffffffu, d0, 1);
+            d1 += __shfl_xor_sync(0xffffffffu, d1, 1);
+            d0 += __shfl_xor_sync(0xffffffffu, d0, 2);
+            d1 += __shfl_xor_sync(0xffffffffu, d1, 2);
+            cb0 -= d0;
+            cb1 -= d1;
+            pack_w();
+
+            // next chunk: its key product from the new state, and its chain blocks
+            if (more) {
+                product(pacc, s.k, cc + 1, cb0, cb1);
+                chain_blocks(cc + 1);
+            }
+        } else if (!state_warp) {
+            if (it < NC) {
+                wait_stage(it);
+                out_blocks(it);
+            }
+            if (it >= 1) {
+                const int cc = it - 1;
+                // query-side product with the chunk's starting state (published by the state warp
+                // of the same features)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w4 = s.wa[cc & 1][fw][q][lane];
+                    wa[q][0] = w4.x;
+                    wa[q][1] = w4.y;
+                    wa[q][2] = w4.z;
+                    wa[q][3] = w4.w;
+                }
+                const float2 cbs = s.cb[cc & 1][fw][lane];
+                float yacc[8][4];
+                product(yacc, s.q, cc, cbs.x, cbs.y);
+                // outputs: Zbar_{m'} -= G_m B_{m'm}^T for m' >= m
+#pragma unroll
+                for (int m = 0; m < NMB; ++m) {
+                    const uint4 n4 = s.ng[cc & 1][fw][m][lane];
+                    const uint32_t ng[4] = {n4.x, n4.y, n4.z, n4.w};
+#pragma unroll
+                    for (int mp = m; mp < NMB; ++mp) {
+                        uint2 f0, f1;
+                        read_blk(cc, out_blk(mp, m), f0, f1);
+                        ptx::mma_bf16(yacc[2 * mp], ng, f0.x, f1.x);
+                        ptx::mma_bf16(yacc[2 * mp + 1], ng, f0.y, f1.y);
+                    }
+                }
+                // Zbar -> bf16 staging tile cc % 2 (rows = tokens), TMA-stored after the barrier
+                const uint32_t zaddr = ptx::smem_addr(s.z[cc & 1]);
+#pragma unroll
+                for (int m = 0; m < NMB; ++m) {
+                    uint32_t r[4];
+                    r[0] = ptx::pack_bf16(yacc[2 * m][0], yacc[2 * m][1]);
+                    r[1] = ptx::pack_bf16(yacc[2 * m][2], yacc[2 * m][3]);
+                    r[2] = ptx::pack_bf16(yacc[2 * m + 1][0], yacc[2 * m + 1][1]);
+                    r[3] = ptx::pack_bf16(yacc[2 * m + 1][2], yacc[2 * m + 1][3]);
+                    // matrices (j-block, t-block): (0,0), (1,0), (0,1), (1,1)
+                    ptx::stsm_x4_t(zaddr + ptx::sw128(m * MB + (mat >> 1) * 8 + mrow, fw * 2 + (mat & 1)), r);
+                }
+                ptx::fence_proxy_async();
+            }
+            // the store of chunk it - 2 has read its tile (which chunk it overwrites next)
+            if (tid == kStorer) ptx::bulk_wait_read<0>();
         }
-        // the store of chunk cc - 1 has read its tile (which chunk cc + 1 overwrites)
-        if (tid == 0) ptx::bulk_wait_read<0>();
         ptx::named_bar(1, kThreads);
-        if (tid == 0) {
-            ptx::tma_store_3d(&tmZ, ptx::smem_addr(s.z[cc & 1]), 0, cc * CT, bh);
+        if (tid == kStorer && it >= 1) {
+            ptx::tma_store_3d(&tmZ, ptx::smem_addr(s.z[(it - 1) & 1]), 0, (it - 1) * CT, bh);
             ptx::bulk_commit();
         }
-        if (tid == kRefill && cc + NSS < nissue && !aborted) {
-            // stage cc is no longer read: refill its slot with stage cc + NSS
+        if (tid == kRefill && it >= 1 && it - 1 + NSS < nissue && !aborted) {
+            // stage it - 1 is no longer read: refill its slot with stage it - 1 + NSS
             ptx::fence_proxy_async();
-            issue_stage(cc + NSS);
-            issued = cc + NSS + 1;
+            issue_stage(it - 1 + NSS);
+            issued = it - 1 + NSS + 1;
         }
     }
-    if (tid == 0) ptx::bulk_wait<0>();
+    if (tid == kStorer) ptx::bulk_wait<0>();
     if (tid == kRefill)   // copies still in flight (only after a wait ran out) land before exit
         for (int st = max(0, issued - NSS); st < issued; ++st)
             ptx::mbar_wait_bounded(ptx::smem_addr(&s.full[st % NSS]), (st / NSS) & 1, kDrainNs);
-    {
+    if (state_warp) {
         float *Wf = p.Wf + (size_t)bh * D * D;
 #pragma unroll
         for (int pt = 0; pt < 8; ++pt) {
