@@ -58,13 +58,15 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) { return fmaf(a.x, b.x
 
 // out[r][j..j+3] = init[j..j+3] + sum_u X[r][u] Y[u][j..j+3]   (X: m x k, Y: k x n, row-major;
 // n, k multiples of 4; init may be null)
-__device__ void mm_xy(float *out, const float *X, const float *Y, const float *init, int m, int k, int n)
+__device__ __forceinline__ void mm_xy(float *out, const float *X, const float *Y, const float *init, int m, int k,
+                                      int n)
 {
     const int n4 = n >> 2;
     for (int tile = threadIdx.x; tile < m * n4; tile += kThreads) {
         const int r = tile / n4, j = (tile - r * n4) * 4;
         float4 a = init ? f4(init + j) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float *xr = X + r * k;
+#pragma unroll
         for (int u = 0; u < k; u += 4) {
             const float4 x = f4(xr + u);
             fma4(a, x.x, f4(Y + u * n + j));
@@ -83,6 +85,7 @@ __device__ __forceinline__ float rot_dot(const float *x, const float *y, int k, 
 {
     float a0 = 0.f, a1 = 0.f;
     int u = start;
+#pragma unroll
     for (int c = 0; c < k; c += 8) {
         a0 += dot4(f4(x + u), f4(y + u));
         u += 4;
@@ -98,7 +101,7 @@ __device__ __forceinline__ float rot_dot(const float *x, const float *y, int k, 
 __device__ __forceinline__ int rot_start(int row, int k) { return (4 * row) % k; }
 
 // out[r][i] = sum_j X[r][j] Y[i][j]   (X Y^T; X: m x k, Y: n x k; k a multiple of 4)
-__device__ void mm_xyt(float *out, const float *X, const float *Y, int m, int k, int n)
+__device__ __forceinline__ void mm_xyt(float *out, const float *X, const float *Y, int m, int k, int n)
 {
     for (int idx = threadIdx.x; idx < m * n; idx += kThreads) {
         const int r = idx / n, i = idx - r * n;
@@ -108,13 +111,14 @@ __device__ void mm_xyt(float *out, const float *X, const float *Y, int m, int k,
 
 // acc[u][j..j+3] = scale acc + sign sum_s w_s X[s][u] Y[s][j..j+3]   (X^T diag(w) Y, 4 x 4
 // blocks; X: m x k, Y: m x n; w may be null (1))
-__device__ void mm_xty_acc(float *acc, const float *X, const float *Y, const float *w, float sign, int m,
-                           int k, int n, float scale = 1.f)
+__device__ __forceinline__ void mm_xty_acc(float *acc, const float *X, const float *Y, const float *w, float sign,
+                                           int m, int k, int n, float scale = 1.f)
 {
     const int n4 = n >> 2, k4 = k >> 2;
     for (int tile = threadIdx.x; tile < k4 * n4; tile += kThreads) {
         const int u = (tile / n4) * 4, j = (tile - (tile / n4) * n4) * 4;
         float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
         for (int s = 0; s < m; ++s) {
             const float e = w ? w[s] : 1.f;
             const float4 x = f4(X + s * k + u), y = f4(Y + s * n + j);
@@ -154,7 +158,7 @@ struct BwdParams {
 };
 
 template <typename IO>
-__device__ void load_tile(float *dst, const IO *src, int n)
+__device__ __forceinline__ void load_tile(float *dst, const IO *src, int n)
 {
     for (int i = threadIdx.x; i < n; i += kThreads) dst[i] = load_io(src, i);
 }
@@ -241,12 +245,16 @@ __device__ __forceinline__ void ln_grad_row(float *G, const float *z, const floa
     (void)z;
 }
 
-template <typename IO, bool LN>
+// DT, MT: the head dim and the mini-batch size as compile-time constants (0: taken from the
+// parameters at run time).  With both fixed, tile decodes are shifts and the fixed-length
+// loops (the d-long dot products, the b-long sums, the causal b x b loops as predicated full
+// loops) unroll, so their shared-memory loads are issued back to back.
+template <typename IO, bool LN, int DT, int MT>
 __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
 {
     extern __shared__ float4 sm4[];
     float *sm = reinterpret_cast<float *>(sm4);
-    const int d = p.d, mb = p.mb, L = p.L, ck = p.ck, dd = d * d;
+    const int d = DT ? DT : p.d, mb = MT ? MT : p.mb, L = p.L, ck = p.ck, dd = d * d;
     const int sd = dd + d;                        // one state: W then c
     const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -328,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
         mm_xty_acc(X, Kt, G, et, -1.f, mb, d, d, 1.f - p.wd * esum);
         for (int j = tid; j < d; j += kThreads) {
             float a = 0.f;
+#pragma unroll
             for (int s = 0; s < mb; ++s) a = fmaf(et[s], G[s * d + j], a);
             X[dd + j] -= a;
         }
@@ -400,7 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
                     const float f = fq[t];
                     float4 z = make_float4(fmaf(f, y.x, cj.x), fmaf(f, y.y, cj.y), fmaf(f, y.z, cj.z),
                                            fmaf(f, y.w, cj.w));
-                    for (int s = 0; s <= t; ++s) fma4(z, -et[s] * A[t * mb + s], f4(G + s * d + j));
+#pragma unroll
+                    for (int s = 0; s < mb; ++s)
+                        if (s <= t) fma4(z, -et[s] * A[t * mb + s], f4(G + s * d + j));
                     st4(dZb + t * d + j, z);
                 }
                 __syncthreads();
@@ -440,7 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
                 a.y = -et[s] * (a.y + dcj.y);
                 a.z = -et[s] * (a.z + dcj.z);
                 a.w = -et[s] * (a.w + dcj.w);
-                for (int t = s; t < mb; ++t) fma4(a, -et[s] * A[t * mb + s], f4(dZb + t * d + j));
+#pragma unroll
+                for (int t = 0; t < mb; ++t)
+                    if (t >= s) fma4(a, -et[s] * A[t * mb + s], f4(dZb + t * d + j));
                 st4(dG + s * d + j, a);
             }
             __syncthreads();
@@ -457,7 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
                     const float4 z = f4(dZt + t * d + j);
                     a.x += z.x; a.y += z.y; a.z += z.z; a.w += z.w;
                 }
-                for (int s = 0; s <= t; ++s) fma4(a, -Dm[t * mb + s] * et[s], f4(Kt + s * d + j));
+#pragma unroll
+                for (int s = 0; s < mb; ++s)
+                    if (s <= t) fma4(a, -Dm[t * mb + s] * et[s], f4(Kt + s * d + j));
                 store_io(dQg, t * d + j, a.x);
                 store_io(dQg, t * d + j + 1, a.y);
                 store_io(dQg, t * d + j + 2, a.z);
@@ -484,7 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
             for (int s = tid; s < mb; s += kThreads) {
                 float a = -rot_dot(T2 + s * d, G + s * d, d, rot_start(s, d)) -
                           rot_dot(dc, G + s * d, d, rot_start(s, d));
-                for (int t = s; t < mb; ++t) a -= Dm[t * mb + s] * A[t * mb + s];
+#pragma unroll
+                for (int t = 0; t < mb; ++t)
+                    if (t >= s) a -= Dm[t * mb + s] * A[t * mb + s];
                 if (wdec) {
                     a -= p.wd * wdw;
                     for (int t = s; t < mb; ++t) a -= p.wd * Yq[t * d];
@@ -568,7 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
                     const float4 dy = f4(Vt + s * d + j);
                     a.x -= dy.x; a.y -= dy.y; a.z -= dy.z; a.w -= dy.w;
                 }
-                for (int t = s; t < mb; ++t) fma4(a, -et[s] * Dm[t * mb + s], f4(Qt + t * d + j));
+#pragma unroll
+                for (int t = 0; t < mb; ++t)
+                    if (t >= s) fma4(a, -et[s] * Dm[t * mb + s], f4(Qt + t * d + j));
                 store_io(dKg, s * d + j, a.x);
                 store_io(dKg, s * d + j + 1, a.y);
                 store_io(dKg, s * d + j + 2, a.z);
@@ -585,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
             mm_xty_acc(dW, Kt, T2, nullptr, 1.f, mb, d, d);
             for (int j = tid; j < d; j += kThreads) {
                 float a = 0.f;
+#pragma unroll
                 for (int s = 0; s < mb; ++s) a += dZb[s * d + j] + T2[s * d + j];
                 dc[j] += a;
             }
@@ -681,10 +701,16 @@ cudaError_t launch_linear_bwd(const LinearBwdArgs &a)
                 a.dQ, a.dK, a.dV, a.deta, s.init_per_batch ? a.dW0 : part,
                 s.init_per_batch ? a.db0 : part + (size_t)rows * d * d, dgb, ckpt, head_offset(s)};
     const size_t smem = smem_for(s, ck);
-    const bool f32 = s.io_dtype == TTT_F32, ln = s.residual_ln != 0;
-    const void *k = f32 ? (ln ? (const void *)linear_bwd_kernel<float, true> : (const void *)linear_bwd_kernel<float, false>)
-                        : (ln ? (const void *)linear_bwd_kernel<__nv_bfloat16, true>
-                              : (const void *)linear_bwd_kernel<__nv_bfloat16, false>);
+    const bool f32 = s.io_dtype == TTT_F32, ln = s.residual_ln != 0, fixed = s.d == 64 && s.mini_batch == 16;
+    const void *k;
+    if (fixed)
+        k = f32 ? (ln ? (const void *)linear_bwd_kernel<float, true, 64, 16> : (const void *)linear_bwd_kernel<float, false, 64, 16>)
+                : (ln ? (const void *)linear_bwd_kernel<__nv_bfloat16, true, 64, 16>
+                      : (const void *)linear_bwd_kernel<__nv_bfloat16, false, 64, 16>);
+    else
+        k = f32 ? (ln ? (const void *)linear_bwd_kernel<float, true, 0, 0> : (const void *)linear_bwd_kernel<float, false, 0, 0>)
+                : (ln ? (const void *)linear_bwd_kernel<__nv_bfloat16, true, 0, 0>
+                      : (const void *)linear_bwd_kernel<__nv_bfloat16, false, 0, 0>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     void *args[] = {&p};
