@@ -100,12 +100,40 @@ __device__ __forceinline__ float rot_dot(const float *x, const float *y, int k, 
 }
 __device__ __forceinline__ int rot_start(int row, int k) { return (4 * row) % k; }
 
-// out[r][i] = sum_j X[r][j] Y[i][j]   (X Y^T; X: m x k, Y: n x k; k a multiple of 4)
+// out[r][i] = sum_j X[r][j] Y[i][j]   (X Y^T; X: m x k, Y: n x k; k a multiple of 4).
+// With m and n even each thread takes a 2 x 2 block (rows r, r + 1 of X against rows i, i + 1
+// of Y): four independent sums and two loads per four products; neighbouring threads take
+// neighbouring row pairs of Y, each starting 4 columns further on (wrapping), so their
+// 16-byte loads fall in different banks.
 __device__ __forceinline__ void mm_xyt(float *out, const float *X, const float *Y, int m, int k, int n)
 {
-    for (int idx = threadIdx.x; idx < m * n; idx += kThreads) {
-        const int r = idx / n, i = idx - r * n;
-        out[idx] = rot_dot(X + r * k, Y + i * k, k, rot_start(i, k));
+    if ((m | n) & 1) {
+        for (int idx = threadIdx.x; idx < m * n; idx += kThreads) {
+            const int r = idx / n, i = idx - r * n;
+            out[idx] = rot_dot(X + r * k, Y + i * k, k, rot_start(i, k));
+        }
+        return;
+    }
+    const int np = n >> 1;
+    for (int idx = threadIdx.x; idx < (m >> 1) * np; idx += kThreads) {
+        const int r = (idx / np) * 2, i = (idx - (idx / np) * np) * 2;
+        const float *x0 = X + r * k, *x1 = x0 + k, *y0 = Y + i * k, *y1 = y0 + k;
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+        int u = rot_start(i >> 1, k);
+#pragma unroll
+        for (int c = 0; c < k; c += 4) {
+            const float4 xa = f4(x0 + u), xb = f4(x1 + u), ya = f4(y0 + u), yb = f4(y1 + u);
+            a00 += dot4(xa, ya);
+            a01 += dot4(xa, yb);
+            a10 += dot4(xb, ya);
+            a11 += dot4(xb, yb);
+            u += 4;
+            if (u >= k) u -= k;
+        }
+        out[r * n + i] = a00;
+        out[r * n + i + 1] = a01;
+        out[(r + 1) * n + i] = a10;
+        out[(r + 1) * n + i + 1] = a11;
     }
 }
 
