@@ -32,6 +32,13 @@
 //     reads k_i and q_i as 16-byte broadcasts;
 //   * sums over the 64 features are warp butterflies; the LayerNorm statistics take two
 //     passes (the mean, then the centred second moment).
+// Without the LayerNorm the columns of the state never mix (column j of W and c evolves from
+// column j of k W + c and of v alone), so a (batch, head) is split over four warps of 16
+// columns each: lane l owns column 16 w + (l mod 16) and rows 32 (l / 16) .. + 31 of it (32
+// registers), a token costs three 32-long sweeps and one shuffle per product, and the
+// warps of a head need no communication.  Tokens are staged eight at a time (q, k rows in
+// shared memory, v and eta in registers) while the next eight are loaded, so the short
+// per-token chain does not wait on a global load round trip per token.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -256,6 +263,129 @@ linear_decode_kernel(DecodeParams p)
     bg[j0 + 1] = c1;
 }
 
+constexpr int kColWarps = 4;                    // warps per (batch, head) without the LayerNorm
+constexpr int kColsPerWarp = D / kColWarps;     // 16: lanes l and l + 16 share a column
+constexpr int kRowPad = 4;                      // the staged rows' second half starts 16 bytes late
+
+template <bool BF16>
+__device__ __forceinline__ float load_one(const void *base, size_t idx)
+{
+    if (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[idx]);
+    return reinterpret_cast<const float *>(base)[idx];
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store_one(void *base, size_t idx, float x)
+{
+    if (BF16)
+        reinterpret_cast<__nv_bfloat16 *>(base)[idx] = __float2bfloat16_rn(x);
+    else
+        reinterpret_cast<float *>(base)[idx] = x;
+}
+
+constexpr int kTokBlock = 8;                    // tokens staged per block (the next block is loaded meanwhile)
+
+// Decode without the residual LayerNorm, a (batch, head) over kColWarps warps by column.
+template <bool BF16, bool WD>
+__global__ void __launch_bounds__(kWarps * 32)
+linear_decode_cols_kernel(DecodeParams p)
+{
+    // per warp and staged token: q and k, features 32..63 placed kRowPad floats late so that
+    // the two half-warps' 16-byte broadcasts fall in different banks
+    __shared__ __align__(16) float rows[kWarps][kTokBlock][2][D + kRowPad];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * kWarps + warp;
+    const int bh = gw / kColWarps, part = gw - bh * kColWarps;
+    if (bh >= p.BH) return;   // whole warps leave; the kernel uses no block-wide barrier
+    const int col = part * kColsPerWarp + (lane & 15), r0 = (lane >> 4) * 32;
+    const int off = (lane >> 4) * (32 + kRowPad);   // this half's rows in a staged row
+    const int j0 = 2 * lane;                        // the pair of features this lane stages
+    const int sp = j0 < 32 ? j0 : j0 + kRowPad;     // staged position of feature j0
+
+    float w[32];
+    float *Wg = p.W + (size_t)bh * D * D;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = Wg[(r0 + i) * D + col];
+    float *bg = p.b + (size_t)bh * D;
+    float c = bg[col];
+
+    // this half's partial of x W[:, col] for the staged row xs (four partial sums), completed
+    // with the other half's through one shuffle
+    auto half_dot = [&](const float *xs) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(xs + off);
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 x = x4[i4];
+            a[0] = fmaf(x.x, w[4 * i4], a[0]);
+            a[1] = fmaf(x.y, w[4 * i4 + 1], a[1]);
+            a[2] = fmaf(x.z, w[4 * i4 + 2], a[2]);
+            a[3] = fmaf(x.w, w[4 * i4 + 3], a[3]);
+        }
+        const float part_sum = (a[0] + a[1]) + (a[2] + a[3]);
+        return part_sum + __shfl_xor_sync(0xffffffffu, part_sum, 16);
+    };
+
+    // a block of tokens in registers: this lane's pairs of q and k, v of its column, eta
+    const size_t row0 = (size_t)bh * p.T;
+    float2 qn[kTokBlock], kn[kTokBlock];
+    float vn[kTokBlock], en[kTokBlock];
+    auto fetch = [&](int t0) {
+#pragma unroll
+        for (int u = 0; u < kTokBlock; ++u)
+            if (t0 + u < p.T) {
+                const size_t base = (row0 + t0 + u) * D;
+                qn[u] = load_pair<BF16>(p.Q, base + j0);
+                kn[u] = load_pair<BF16>(p.K, base + j0);
+                vn[u] = load_one<BF16>(p.V, base + col);
+                en[u] = p.eta[row0 + t0 + u];
+            }
+    };
+    fetch(0);
+    for (int t0 = 0; t0 < p.T; t0 += kTokBlock) {
+        float vb[kTokBlock], eb[kTokBlock];
+#pragma unroll
+        for (int u = 0; u < kTokBlock; ++u) {
+            if (t0 + u < p.T) {
+                *reinterpret_cast<float2 *>(&rows[warp][u][0][sp]) = qn[u];
+                *reinterpret_cast<float2 *>(&rows[warp][u][1][sp]) = kn[u];
+            }
+            vb[u] = vn[u];
+            eb[u] = en[u];
+        }
+        __syncwarp();
+        if (t0 + kTokBlock < p.T) fetch(t0 + kTokBlock);   // the next block, while this one runs
+#pragma unroll
+        for (int u = 0; u < kTokBlock; ++u) {
+            if (t0 + u >= p.T) break;
+            const float *qs = rows[warp][u][0], *ks = rows[warp][u][1];
+            const float z = half_dot(ks) + c;
+            const float g = p.ip ? -vb[u] : z - vb[u];
+            // W[:, col] <- (1 - eta lambda) W[:, col] - eta k^T g,  c -= eta g
+            const float eg = eb[u] * g;
+            const float dec = WD ? 1.f - eb[u] * p.wd : 1.f;
+            const float4 *k4 = reinterpret_cast<const float4 *>(ks + off);
+#pragma unroll
+            for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 x = k4[i4];
+                w[4 * i4] = fmaf(-eg, x.x, WD ? dec * w[4 * i4] : w[4 * i4]);
+                w[4 * i4 + 1] = fmaf(-eg, x.y, WD ? dec * w[4 * i4 + 1] : w[4 * i4 + 1]);
+                w[4 * i4 + 2] = fmaf(-eg, x.z, WD ? dec * w[4 * i4 + 2] : w[4 * i4 + 2]);
+                w[4 * i4 + 3] = fmaf(-eg, x.w, WD ? dec * w[4 * i4 + 3] : w[4 * i4 + 3]);
+            }
+            c -= eg;
+            // the output with the weights after this token's update
+            const float o = half_dot(qs) + c;
+            if (lane < 16) store_one<BF16>(p.Z, (row0 + t0 + u) * D + col, o);
+        }
+        __syncwarp();   // every lane is done with the staged rows before the next block
+    }
+
+#pragma unroll
+    for (int i = 0; i < 32; ++i) Wg[(r0 + i) * D + col] = w[i];
+    if (lane < 16) bg[col] = c;
+}
+
 }  // namespace
 
 bool linear_decode_supported(const ttt_desc &d) { return d.d == D && d.mini_batch == 1; }
@@ -269,6 +399,13 @@ cudaError_t launch_linear_decode(const DecodeArgs &a)
     const int grid = (BH + kWarps - 1) / kWarps;
     const bool bf16 = d.io_dtype == TTT_BF16, ln = d.residual_ln != 0, wd = d.weight_decay != 0.f;
     using K = void (*)(DecodeParams);
+    if (!ln) {   // split by column: kColWarps warps per (batch, head)
+        const K cols[2][2] = {{linear_decode_cols_kernel<false, false>, linear_decode_cols_kernel<false, true>},
+                              {linear_decode_cols_kernel<true, false>, linear_decode_cols_kernel<true, true>}};
+        const int cgrid = (int)(((long long)BH * kColWarps + kWarps - 1) / kWarps);
+        cols[bf16][wd]<<<cgrid, kWarps * 32, 0, a.stream>>>(p);
+        return cudaGetLastError();
+    }
     const K table[2][2][2] = {{{linear_decode_kernel<false, false, false>, linear_decode_kernel<false, false, true>},
                                {linear_decode_kernel<false, true, false>, linear_decode_kernel<false, true, true>}},
                               {{linear_decode_kernel<true, false, false>, linear_decode_kernel<true, false, true>},
