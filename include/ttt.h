@@ -101,6 +101,13 @@ typedef struct {
      * W_t = (1 - lambda sum_{s<=t} eta_s) W_start - sum_{s<=t} eta_s grad l_s. */
     int loss;
     float weight_decay;
+    /* Optional per-call failure word: a device pointer to a caller-owned, 4-byte aligned
+     * unsigned int.  When it is non-NULL, the call's kernels report a bounded wait that ran
+     * out by setting bit 0 of this word (atomic OR) instead of the device-wide flag that
+     * ttt_sync_status reads, so callers on different streams see only their own calls'
+     * failures; the caller clears it and reads it after synchronising its stream.  NULL:
+     * the device-wide flag.  (Kernels without bounded waits never write it.) */
+    unsigned int *status;
 } ttt_desc;
 
 enum { TTT_LOSS_MSE = 0, TTT_LOSS_INNER_PRODUCT = 1 };
@@ -269,7 +276,7 @@ TTT_API const char *ttt_kernel_name(const ttt_desc *desc, int is_mlp);
 
 /* Library ABI version (major * 100 + minor); 101 added bh_offset/bh_count, 102 loss and
  * weight_decay, 103 ttt_linear_bwd, 104 its residual-LayerNorm form (gamma, beta, dgamma,
- * dbeta arguments). */
+ * dbeta arguments), 105 the per-call status word (ttt_desc.status). */
 TTT_API int ttt_version(void);
 
 #ifdef __cplusplus

@@ -49,7 +49,8 @@ class Desc(ctypes.Structure):
                 ("io_dtype", ctypes.c_int), ("residual_ln", ctypes.c_int),
                 ("ln_eps", ctypes.c_float), ("init_per_batch", ctypes.c_int),
                 ("bh_offset", ctypes.c_int), ("bh_count", ctypes.c_int),
-                ("loss", ctypes.c_int), ("weight_decay", ctypes.c_float)]
+                ("loss", ctypes.c_int), ("weight_decay", ctypes.c_float),
+                ("status", ctypes.c_void_p)]   # optional per-call failure word (device pointer)
 
 LOSSES = {"mse": 0, "ip": 1}   # 1/2 ||f(k) - v||^2, or the inner product -<f(k), v>
 
@@ -124,10 +125,12 @@ def _stream_handle(stream):
 
 def make_desc(Q, mini_batch: int, residual_ln: bool, ln_eps: float = 1e-6,
               init_per_batch: bool = False, d_hidden: int = 0, heads=None, bh_offset: int = 0,
-              loss: str = "mse", weight_decay: float = 0.0) -> Desc:
+              loss: str = "mse", weight_decay: float = 0.0, status=None) -> Desc:
     """Descriptor of a call on Q [B, H, L, d], or on the row form Q [rows, L, d] covering rows
     bh_offset .. bh_offset + rows - 1 of a (batch, head) grid with `heads` heads.  loss: "mse"
-    or "ip" (inner product); weight_decay: lambda on the weight matrices."""
+    or "ip" (inner product); weight_decay: lambda on the weight matrices; status: an int32
+    CUDA tensor whose first element is the call's own failure word (None: the device-wide
+    flag that ttt_sync_status reads)."""
     import torch
     io = {torch.float32: TTT_F32, torch.bfloat16: TTT_BF16}.get(Q.dtype)
     if io is None:
@@ -135,8 +138,13 @@ def make_desc(Q, mini_batch: int, residual_ln: bool, ln_eps: float = 1e-6,
     lead, H, L, d, B, off, cnt = _geometry(Q, heads, bh_offset)
     if loss not in LOSSES:
         raise ValueError(f"loss must be one of {sorted(LOSSES)}")
+    if status is not None:
+        if not (isinstance(status, torch.Tensor) and status.dtype == torch.int32 and status.is_cuda
+                and status.numel() >= 1 and status.device == Q.device):
+            raise ValueError("status must be an int32 CUDA tensor on Q's device with >= 1 element")
     return Desc(B, H, L, d, d_hidden, mini_batch, io, int(residual_ln), float(ln_eps),
-                int(init_per_batch), off, cnt, LOSSES[loss], float(weight_decay))
+                int(init_per_batch), off, cnt, LOSSES[loss], float(weight_decay),
+                None if status is None else status.data_ptr())
 
 
 def partition_rows(total_rows: int, world: int, rank: int):
@@ -219,7 +227,7 @@ def _require_cuda(dev):
 def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: int = 16,
                    residual_ln: bool = False, ln_eps: float = 1e-6, init_per_batch: bool = False,
                    out=None, stream=None, heads=None, bh_offset: int = 0, loss: str = "mse",
-                   weight_decay: float = 0.0):
+                   weight_decay: float = 0.0, status=None):
     """TTT-Linear forward on the GPU.  Q,K,V: [B,H,L,d] (float32 or bfloat16);
     eta [B,H,L] float32; W0 [H,d,d] (or [B,H,d,d] with init_per_batch); b0 [H,d]
     (or [B,H,d]); gamma, beta [H,d] float32 (residual LayerNorm only).  Returns
@@ -228,6 +236,8 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: i
     [rows, L], the outputs [rows, ...], W0/b0 [H, ...] (or [rows, ...] with init_per_batch),
     and the rows are rows bh_offset .. bh_offset + rows - 1 of the B*H grid (row b*H + h).
     Every operand is checked (shape, dtype, device, contiguity) before the C call.
+    ``status``: an int32 CUDA tensor; its first element receives this call's timeout flag
+    instead of the device-wide one (clear it before, read it after synchronising).
     The call is asynchronous on ``stream`` (default: torch's current stream)."""
     import torch
     lead, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln, heads, bh_offset)
@@ -242,7 +252,7 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b0, gamma=None, beta=None, *, mini_batch: i
     _require_cuda(dev)
     lib = load()
     desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, heads=heads,
-                     bh_offset=bh_offset, loss=loss, weight_decay=weight_decay)
+                     bh_offset=bh_offset, loss=loss, weight_decay=weight_decay, status=status)
     if out is None:
         out = (torch.empty_like(Q), torch.empty(lead + (d, d), device=dev, dtype=torch.float32),
                torch.empty(lead + (d,), device=dev, dtype=torch.float32))
@@ -379,10 +389,10 @@ def ttt_linear_step(Q, K, V, eta, W, b, gamma=None, beta=None, *, residual_ln: b
 def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_batch: int = 16,
                 residual_ln: bool = False, ln_eps: float = 1e-6, init_per_batch: bool = False,
                 out=None, stream=None, heads=None, bh_offset: int = 0, loss: str = "mse",
-                weight_decay: float = 0.0):
+                weight_decay: float = 0.0, status=None):
     """TTT-MLP forward on the GPU.  W1 [H,d,dh], b1 [H,dh], W2 [H,dh,d], b2 [H,d]
-    (leading B when init_per_batch).  Returns (Z, W1_f, b1_f, W2_f, b2_f).  Row form as for
-    ttt_linear_fwd.  Every operand is checked before the C call."""
+    (leading B when init_per_batch).  Returns (Z, W1_f, b1_f, W2_f, b2_f).  Row form and
+    ``status`` as for ttt_linear_fwd.  Every operand is checked before the C call."""
     import torch
     lead, H, L, d, dev = _check_sequence(Q, K, V, eta, gamma, beta, residual_ln, heads, bh_offset)
     if not isinstance(b1, torch.Tensor) or b1.dim() < 1:
@@ -403,7 +413,7 @@ def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_bat
     _require_cuda(dev)
     lib = load()
     desc = make_desc(Q, mini_batch, residual_ln, ln_eps, init_per_batch, d_hidden=dh, heads=heads,
-                     bh_offset=bh_offset, loss=loss, weight_decay=weight_decay)
+                     bh_offset=bh_offset, loss=loss, weight_decay=weight_decay, status=status)
     if out is None:
         f32 = dict(device=dev, dtype=torch.float32)
         out = (torch.empty_like(Q), torch.empty(lead + (d, dh), **f32), torch.empty(lead + (dh,), **f32),

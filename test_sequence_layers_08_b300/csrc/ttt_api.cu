@@ -94,6 +94,8 @@ ttt_status check_desc(const ttt_desc *s, bool mlp)
     if ((long long)s->bh_offset + s->bh_count > (long long)s->B * s->H)
         return fail(TTT_ERR_INVALID_ARG, "rows [%d, %d) exceed B * H = %d", s->bh_offset,
                     s->bh_offset + s->bh_count, s->B * s->H);
+    if (reinterpret_cast<uintptr_t>(s->status) % alignof(unsigned int) != 0)
+        return fail(TTT_ERR_INVALID_ARG, "status must be 4-byte aligned");
     return TTT_OK;
 }
 
@@ -152,7 +154,7 @@ const char *mlp_kernel(const ttt_desc &s)
 
 extern "C" {
 
-int ttt_version(void) { return 104; }
+int ttt_version(void) { return 105; }
 
 const char *ttt_status_string(ttt_status s)
 {
@@ -222,7 +224,7 @@ ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, co
 
     ttt::LinearArgs a{s, Q, K, V, eta, W0, b0, gamma, beta, Z, W_final, b_final,
                       reinterpret_cast<cudaStream_t>(stream), nullptr};
-    a.status = failure_flag(&st);
+    a.status = s.status ? s.status : failure_flag(&st);
     if (st != TTT_OK) return st;
     cudaError_t e = ttt::linear_chunk_supported(s) ? ttt::launch_linear_chunk(a)
                     : ttt::linear_tc_supported(s)  ? ttt::launch_linear_tc(a)
@@ -335,7 +337,7 @@ ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const void *K, c
                        reinterpret_cast<cudaStream_t>(stream), nullptr};
     if (!ttt::linear_decode_supported(s) && !ttt::linear_generic_smem_bytes(s))
         return fail(TTT_ERR_UNSUPPORTED, "no decode kernel for d=%d", s.d);
-    la.status = failure_flag(&st);
+    la.status = s.status ? s.status : failure_flag(&st);
     if (st != TTT_OK) return st;
     cudaError_t e;
     if (ttt::linear_decode_supported(s)) {
@@ -396,7 +398,7 @@ ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const
                     s.d_hidden, s.mini_batch);
     ttt::MlpArgs a{s, Q, K, V, eta, W1_0, b1_0, W2_0, b2_0, gamma, beta, Z,
                    W1_f, b1_f, W2_f, b2_f, reinterpret_cast<cudaStream_t>(stream), nullptr};
-    a.status = failure_flag(&st);
+    a.status = s.status ? s.status : failure_flag(&st);
     if (st != TTT_OK) return st;
     cudaError_t e = ttt::mlp_tc_supported(s) ? ttt::launch_mlp_tc(a) : ttt::launch_mlp_generic(a);
     if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "%s launch: %s", kname, cudaGetErrorString(e));

@@ -187,6 +187,24 @@ def test_gate_null_misaligned_and_overlap(lib):
     assert "overlap" in lib.ttt_last_error().decode()
 
 
+def test_descriptor_matches_the_header_struct():
+    """The binding's Desc has the header's ttt_desc fields in order, ending with the per-call
+    status pointer (8-byte aligned after the fourteen 4-byte fields)."""
+    import re
+    text = open(os.path.join(ROOT, "include", "ttt.h")).read()
+    body = re.search(r"typedef struct \{(.*?)\} ttt_desc;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = re.findall(r"(\w+);", body)
+    assert names == [f[0] for f in ttt.Desc._fields_]
+    assert ctypes.sizeof(ttt.Desc) == 64 and ttt.Desc.status.offset == 56
+
+
+def test_status_word_must_be_aligned(lib):
+    assert call_linear(lib, desc(status=FAKE + 2)) == 1
+    assert "status" in lib.ttt_last_error().decode()
+    assert lib.ttt_kernel_name(ctypes.byref(desc(status=FAKE)), 0) is not None
+
+
 def test_partition_fields_accepted(lib):
     """A call on rows [2, 6) of a 2 x 3 grid passes the descriptor checks (the kernel choice
     does not depend on the partition)."""

@@ -72,3 +72,26 @@ def test_bounded_wait_reports_timeout_and_context_survives(ln):
     # the flag was cleared and the context still works
     ttt.ttt_sync_status()
     compare_all(cfg, run_gpu(cfg, dev), run_oracle(cfg, x))
+
+
+@pytest.mark.parametrize("ln", [False, True])   # the chunked and the fused kernel
+def test_per_call_status_word_takes_the_timeout(ln):
+    """With a per-call status word in the descriptor, a bounded wait that runs out is reported
+    in that word only: the device-wide flag (ttt_sync_status) stays clear, and a later call
+    with its own word reports nothing."""
+    import torch
+    cfg = (LIN_LN if ln else LIN).with_(name="status_word", B=1, H=2, L=256)
+    x = inputs(cfg, seed=23)
+    dev = to_device(cfg, x)
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    try:
+        ttt.set_wait_timeout_ns(5_000_000)     # 5 ms
+        ttt.debug_withhold_loads(True)
+        run_gpu(cfg, dev, status=word)         # syncs through ttt_sync_status: must not raise
+    finally:
+        ttt.debug_withhold_loads(False)
+        ttt.set_wait_timeout_ns(0)
+    assert int(word.item()) == 1
+    word.zero_()
+    compare_all(cfg, run_gpu(cfg, dev, status=word), run_oracle(cfg, x))
+    assert int(word.item()) == 0
