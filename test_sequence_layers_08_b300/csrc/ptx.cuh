@@ -101,6 +101,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
+// 16-byte asynchronous copy global -> shared without an mbarrier (both addresses 16-byte
+// aligned); completion by cp_async_wait_all in the issuing thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 template <int N>
 __device__ __forceinline__ void bulk_wait_read()
 {

@@ -28,11 +28,15 @@
 // from its checkpoint in shared memory and walks its mini-batches backwards.
 //
 // B300 design: one CTA per (batch, head), 256 threads, fp32 FFMA on shared-memory tiles
-// (register-tiled loops with 16-byte loads).  The gradients of a head-shared initial state
+// (register-tiled loops with 16-byte loads).  For d = 64, b = 16 the tiles of the next
+// forward or reverse step (its K, V or K, Q, V, dZ rows and eta) are copied global -> shared
+// with cp.async while the current step computes: the order of the steps is fixed (pass 1,
+// then per chunk the re-runs and the reverse steps), so the next one is always known.  The gradients of a head-shared initial state
 // are summed over the batch by a second kernel, in a fixed order (deterministic).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "ptx.cuh"
 #include "ttt_internal.h"
 
 namespace ttt {
@@ -183,6 +187,7 @@ struct BwdParams {
     float *dgb;               // LN: per-row partials [rows][2 d] of dgamma, dbeta
     float *ckpt;              // [rows][nck][d d + d]
     int hoff;
+    int pf_off;               // float offset of the prefetch buffer in shared memory (d = 64, b = 16)
 };
 
 template <typename IO>
@@ -321,6 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
     // done, or its own area when the states are smaller (d < 16)
     float *red = (2 * d * kWarps <= ck * sd) ? S : (wdec ? Yq + nt : bet + d);
     if (!LN) dZb = dZt;
+    // d = 64, b = 16: the next step's rows arrive by cp.async in `pf` (raw I/O elements:
+    // K, Q, V, dZ tiles, then eta), placed after the last region of the plan
+    constexpr bool kAsync = DT != 0 && MT != 0;
+    unsigned char *pf = reinterpret_cast<unsigned char *>(sm + p.pf_off);
+    constexpr int kEs = sizeof(IO);
 
     const IO *Qg = static_cast<const IO *>(p.Q) + (size_t)bh * L * d;
     const IO *Kg = static_cast<const IO *>(p.K) + (size_t)bh * L * d;
@@ -347,13 +357,64 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
         }
     };
 
+    // The steps in order, each with the rows it reads: forward step n (K, V, eta of
+    // mini-batch n) in pass 1 (n = 0 .. nmb - 2) and as a re-run in pass 2, reverse step n
+    // (K, Q, V, dZ, eta).  kind: 0 forward, 1 reverse, -1 none.
+    struct Op {
+        int kind, n;
+    };
+    auto first_of_chunk = [&](int ci) -> Op {
+        const int m0 = ci * ck, mcount = min(ck, nmb - m0);
+        return mcount > 1 ? Op{0, m0} : Op{1, m0};
+    };
+    // copy the rows of `op` into pf (each thread its 16-byte chunks; one commit group)
+    auto prefetch = [&](Op op) {
+        if (!kAsync || op.kind < 0) return;
+        const size_t off = (size_t)op.n * mb * d;
+        constexpr int tile_chunks = (MT * DT * kEs) / 16;
+        const IO *src[4] = {Kg + off, Qg + off, Vg + off, dZg + off};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            if (op.kind == 0 && (w == 1 || w == 3)) continue;   // forward: K and V only
+            for (int ch = tid; ch < tile_chunks; ch += kThreads)
+                ptx::cp_async16(ptx::smem_addr(pf + (w * tile_chunks + ch) * 16),
+                                reinterpret_cast<const unsigned char *>(src[w]) + ch * 16);
+        }
+        if (tid < MT / 4)
+            ptx::cp_async16(ptx::smem_addr(pf + 4 * tile_chunks * 16 + tid * 16), eg + (size_t)op.n * mb + tid * 4);
+        ptx::cp_async_commit();
+    };
+    // the rows of `op` into the fp32 tiles (from pf when prefetched), then prefetch `next`
+    auto stage_op = [&](Op op, Op next) {
+        const int n0 = op.n * mb;
+        if (kAsync) {
+            ptx::cp_async_wait_all();
+            __syncthreads();   // every thread's copies have landed; the last step's readers are done
+            const IO *pk = reinterpret_cast<const IO *>(pf);
+            float *dst[4] = {Kt, Qt, Vt, dZt};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                if (op.kind == 0 && (w == 1 || w == 3)) continue;
+                for (int i = tid; i < nt; i += kThreads) dst[w][i] = load_io(pk + w * nt, i);
+            }
+            for (int s = tid; s < mb; s += kThreads)
+                et[s] = reinterpret_cast<const float *>(pf + 4 * nt * kEs)[s];
+            __syncthreads();   // pf is free again
+            prefetch(next);
+        } else {
+            __syncthreads();
+            load_tile(Kt, Kg + (size_t)n0 * d, nt);
+            if (op.kind == 1) load_tile(Qt, Qg + (size_t)n0 * d, nt);
+            load_tile(Vt, Vg + (size_t)n0 * d, nt);
+            if (op.kind == 1) load_tile(dZt, dZg + (size_t)n0 * d, nt);
+            for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
+            __syncthreads();
+        }
+    };
+
     // one forward mini-batch on the state X (in place): G, W -= K^T E G, c -= G^T eta
-    auto forward_step = [&](float *X, int n0) {
-        __syncthreads();
-        load_tile(Kt, Kg + (size_t)n0 * d, nt);
-        load_tile(Vt, Vg + (size_t)n0 * d, nt);
-        for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
-        __syncthreads();
+    auto forward_step = [&](float *X, int n, Op next) {
+        stage_op(Op{0, n}, next);
         mm_xy(LN ? Pz : G, Kt, X, X + dd, mb, d, d);
         __syncthreads();
         gradient_rows(G, LN ? Pz : G);
@@ -374,13 +435,15 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
     const size_t init = p.init_per_batch ? (size_t)bh : (size_t)h;
     for (int i = tid; i < dd; i += kThreads) S[i] = p.W0[init * dd + i];
     for (int j = tid; j < d; j += kThreads) S[dd + j] = p.b0[init * d + j];
+    prefetch(nmb >= 2 ? Op{0, 0} : first_of_chunk(nck - 1));
     for (int n = 0; n < nmb; ++n) {
         if (n % ck == 0) {
             __syncthreads();
             float *dst = ck_base + (size_t)(n / ck) * sd;
             for (int i = tid; i < sd; i += kThreads) dst[i] = S[i];
         }
-        if (n + 1 < nmb) forward_step(S, n * mb);   // the last state is never needed
+        if (n + 1 < nmb)   // the last state is never needed
+            forward_step(S, n, n + 2 < nmb ? Op{0, n + 1} : first_of_chunk(nck - 1));
     }
 
     // ---- pass 2: reverse
@@ -398,18 +461,12 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
         for (int m = 1; m < mcount; ++m) {
             __syncthreads();
             for (int i = tid; i < sd; i += kThreads) S[m * sd + i] = S[(m - 1) * sd + i];
-            forward_step(S + m * sd, (m0 + m - 1) * mb);
+            forward_step(S + m * sd, m0 + m - 1, m + 1 < mcount ? Op{0, m0 + m} : Op{1, m0 + mcount - 1});
         }
         for (int m = mcount - 1; m >= 0; --m) {
             const int n0 = (m0 + m) * mb;
             const float *W = S + m * sd, *c = W + dd;
-            __syncthreads();
-            load_tile(Kt, Kg + (size_t)n0 * d, nt);
-            load_tile(Qt, Qg + (size_t)n0 * d, nt);
-            load_tile(Vt, Vg + (size_t)n0 * d, nt);
-            load_tile(dZt, dZg + (size_t)n0 * d, nt);
-            for (int s = tid; s < mb; s += kThreads) et[s] = eg[n0 + s];
-            __syncthreads();
+            stage_op(Op{1, m0 + m}, m > 0 ? Op{1, m0 + m - 1} : (ci > 0 ? first_of_chunk(ci - 1) : Op{-1, 0}));
             // P (LN: kept in Pz), K dW', R = M . (Q K^T + 1); Q W (with LN or weight decay)
             mm_xy(LN ? Pz : G, Kt, W, c, mb, d, d);
             mm_xy(T2, Kt, dW, nullptr, mb, d, d);
@@ -679,6 +736,15 @@ __global__ void sum_over_rows_kernel(const float *part, float *out, int rows, in
 
 constexpr size_t kMaxSmem = 227 * 1024;
 
+// bytes of the prefetch buffer (four mb x d tiles of I/O elements and mb floats of eta), used
+// by the kernel specialised for d = 64, b = 16
+size_t prefetch_bytes(const ttt_desc &s)
+{
+    if (!(s.d == 64 && s.mini_batch == 16)) return 0;
+    const size_t es = s.io_dtype == TTT_BF16 ? 2 : 4;
+    return 4 * (size_t)s.mini_batch * s.d * es + (size_t)s.mini_batch * 4;
+}
+
 size_t smem_for(const ttt_desc &s, int ck)
 {
     // states, dW and dc, nine mb x d tiles, the small block; with LN or weight decay P, Zbar,
@@ -690,7 +756,8 @@ size_t smem_for(const ttt_desc &s, int ck)
     if (s.residual_ln || wd) n += 2 * mb * d + 2 * d;   // P, Zbar / dZbar, gamma, beta
     if (wd) n += mb * d;                                // Q W
     if (s.residual_ln && red > states) n += red;
-    return n * sizeof(float);
+    n = (n + 3) & ~(size_t)3;   // the prefetch buffer starts 16-byte aligned
+    return n * sizeof(float) + prefetch_bytes(s);
 }
 
 }  // namespace
@@ -729,6 +796,7 @@ cudaError_t launch_linear_bwd(const LinearBwdArgs &a)
                 a.dQ, a.dK, a.dV, a.deta, s.init_per_batch ? a.dW0 : part,
                 s.init_per_batch ? a.db0 : part + (size_t)rows * d * d, dgb, ckpt, head_offset(s)};
     const size_t smem = smem_for(s, ck);
+    p.pf_off = (int)((smem - prefetch_bytes(s)) / sizeof(float));
     const bool f32 = s.io_dtype == TTT_F32, ln = s.residual_ln != 0, fixed = s.d == 64 && s.mini_batch == 16;
     const void *k;
     if (fixed)
