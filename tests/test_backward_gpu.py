@@ -180,3 +180,37 @@ def test_backward_weight_decay(io, loss, ln):
 def test_backward_weight_decay_small_shapes():
     x = problem(B=1, H=2, L=40, d=32, io="f32", seed=63, ln=True)
     compare(run(x, "f32", 8, weight_decay=0.3), reference(x, 8, weight_decay=0.3), "f32")
+
+
+@pytest.mark.parametrize("B,H,L,ln", [(8, 12, 2048, False), (4, 16, 8192, True)],
+                         ids=["B8_H12_L2048", "B4_H16_L8192_ln"])
+def test_backward_full_size_sampled_rows(B, H, L, ln):
+    """The backward at the full sizes the bench times (the 8 x 12 x 2048 workload without LN,
+    the 4 x 16 x 8192 one with LN), one call over every row with a distinct initial state per
+    (batch, head); three sampled rows' gradients against the oracle run on those rows alone,
+    and with LN the dgamma, dbeta of one head against the oracle's sum over that head's rows."""
+    from gpu_util import sample_pairs
+    from test_sequence_layers_08_b300.inputs import CONFIGS
+    x = problem(B, H, L, 64, "bf16", seed=47, init_per_batch=True, ln=ln)
+    got = run(x, "bf16", 16, init_per_batch=True)
+    cfg = CONFIGS["linear_bf16_B8_H12_L2048"].with_(B=B, H=H, L=L)
+    names = ("dQ", "dK", "dV", "deta", "dW0", "db0")
+    row = lambda a, b, h: None if a is None else a[b:b + 1, h:h + 1]
+
+    def oracle_row(b, h):
+        return ttt_linear_grad(row(x["Q"], b, h), row(x["K"], b, h), row(x["V"], b, h), row(x["eta"], b, h),
+                               row(x["W0"], b, h), row(x["b0"], b, h),
+                               None if not ln else x["gamma"][h:h + 1], None if not ln else x["beta"][h:h + 1],
+                               row(x["dZ"], b, h), row(x["dW_final"], b, h), row(x["db_final"], b, h),
+                               mini_batch=16, ln=ln, eps=1e-6, init_per_batch=True)
+    case = current_case("bwd_full")
+    for b, h in sample_pairs(cfg, 3, seed=9):
+        ref = oracle_row(b, h)
+        for name, g in zip(names, got[:6]):
+            check_scan(case, name, g[b, h], ref[name][0, 0], TOL["bf16"],
+                       seq_axis=0 if name not in ("dW0", "db0") else None)
+    if ln:
+        h = 5
+        refs = [oracle_row(b, h) for b in range(B)]
+        check_scan(case, "dgamma", got[6][h], sum(r["dgamma"][0] for r in refs), TOL["bf16"])
+        check_scan(case, "dbeta", got[7][h], sum(r["dbeta"][0] for r in refs), TOL["bf16"])
