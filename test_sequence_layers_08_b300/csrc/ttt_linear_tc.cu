@@ -54,6 +54,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -742,8 +743,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode()
     return fn;
 }
 
-long long g_wait_ns = kDefaultWaitNs;
-int g_withhold_loads = 0;
+// test hooks: process-wide, set by any host thread and read when a call launches
+std::atomic<long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_withhold_loads{0};
 
 }  // namespace
 
@@ -778,10 +780,10 @@ bool make_bf16_tile_map(CUtensorMap *m, const void *base, int L, int BH, int row
     return r == CUDA_SUCCESS;
 }
 
-void set_wait_timeout_ns(long long ns) { g_wait_ns = ns > 0 ? ns : kDefaultWaitNs; }
-void set_withhold_loads(int on) { g_withhold_loads = on != 0; }
-long long wait_timeout_ns() { return g_wait_ns; }
-int withhold_loads() { return g_withhold_loads; }
+void set_wait_timeout_ns(long long ns) { g_wait_ns.store(ns > 0 ? ns : kDefaultWaitNs, std::memory_order_relaxed); }
+void set_withhold_loads(int on) { g_withhold_loads.store(on != 0, std::memory_order_relaxed); }
+long long wait_timeout_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int withhold_loads() { return g_withhold_loads.load(std::memory_order_relaxed); }
 
 bool linear_tc_supported(const ttt_desc &d)
 {
@@ -796,7 +798,7 @@ cudaError_t launch_linear_tc(const LinearArgs &a)
     if (!make_bf16_tile_map(&mq, a.Q, d.L, BH, ST) || !make_bf16_tile_map(&mk, a.K, d.L, BH, ST) ||
         !make_bf16_tile_map(&mv, a.V, d.L, BH, ST) || !make_bf16_tile_map(&mz, a.Z, d.L, BH, MB))
         return cudaErrorInvalidValue;
-    Params p{d.H, d.L, d.residual_ln, d.ln_eps, g_wait_ns, g_withhold_loads, a.eta, a.W0, a.b0, a.gamma, a.beta,
+    Params p{d.H, d.L, d.residual_ln, d.ln_eps, wait_timeout_ns(), withhold_loads(), a.eta, a.W0, a.b0, a.gamma, a.beta,
              a.W_final, a.b_final, a.status, d.init_per_batch};
     p.hoff = head_offset(d);
     p.ip = d.loss == TTT_LOSS_INNER_PRODUCT;
