@@ -15,7 +15,7 @@ from gpu_util import compare_all, inputs, run_gpu, run_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
-C1 = CONFIGS["linear_f32_B1_H2_L256"]          # fp32, const eta 0.1, no LN
+F32_WL = CONFIGS["linear_f32_B1_H2_L256"]          # fp32, const eta 0.1, no LN
 LIN = CONFIGS["linear_bf16_B8_H12_L2048"]      # gated eta, b0 != 0, no LN
 
 VARIANTS = [("mse", 0.0), ("ip", 0.0), ("mse", 0.5), ("ip", 0.5)]
@@ -35,7 +35,7 @@ def check(cfg, seed, **variant):
 
 def test_cols_full_fp32_workload():
     """The 1 x 2 x 256 fp32 workload itself (16 CTAs of 4 columns per head)."""
-    check(C1, seed=0)
+    check(F32_WL, seed=0)
 
 
 @pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: f"{v[0]}-wd{v[1]}")
@@ -49,7 +49,7 @@ def test_cols_variants(io, variant):
 
 @pytest.mark.parametrize("d,mb", [(8, 1), (16, 4), (32, 8), (128, 16), (64, 64), (128, 64), (64, 2)])
 def test_cols_shapes(d, mb):
-    cfg = C1.with_(name=f"cols_d{d}_b{mb}", B=1, H=2, L=5 * mb if mb > 2 else 40, d=d, mini_batch=mb)
+    cfg = F32_WL.with_(name=f"cols_d{d}_b{mb}", B=1, H=2, L=5 * mb if mb > 2 else 40, d=d, mini_batch=mb)
     check(cfg, seed=83 + d + mb)
 
 
@@ -61,7 +61,7 @@ def test_cols_widths(B, H):
 
 
 def test_cols_single_mini_batch():
-    cfg = C1.with_(name="cols_one_step", L=16)
+    cfg = F32_WL.with_(name="cols_one_step", L=16)
     check(cfg, seed=89)
 
 
