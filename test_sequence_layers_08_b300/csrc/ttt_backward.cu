@@ -581,17 +581,21 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
                 __syncthreads();
                 for (int w2 = 0; w2 < kWarps; ++w2) wdw += wred[w2];
             }
-            for (int s = tid; s < mb; s += kThreads) {
-                float a = -rot_dot(T2 + s * d, G + s * d, d, rot_start(s, d)) -
-                          rot_dot(dc, G + s * d, d, rot_start(s, d));
-#pragma unroll
-                for (int t = 0; t < mb; ++t)
-                    if (t >= s) a -= Dm[t * mb + s] * A[t * mb + s];
-                if (wdec) {
-                    a -= p.wd * wdw;
-                    for (int t = s; t < mb; ++t) a -= p.wd * Yq[t * d];
+            // sixteen lanes per token s: lane i takes features i, i + 16, ... and targets
+            // t = i, i + 16, ... (t >= s), then the sixteen partials are summed by shuffles
+            for (int s0 = 0; s0 < mb; s0 += kThreads / 16) {
+                const int s = s0 + tid / 16, i16 = tid & 15;
+                float a = 0.f;
+                if (s < mb) {
+                    for (int u = i16; u < d; u += 16) a -= (T2[s * d + u] + dc[u]) * G[s * d + u];
+                    for (int t = s + i16; t < mb; t += 16) {
+                        a -= Dm[t * mb + s] * A[t * mb + s];
+                        if (wdec) a -= p.wd * Yq[t * d];
+                    }
                 }
-                p.deta[(size_t)bh * L + n0 + s] = a;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+                if (s < mb && i16 == 0) p.deta[(size_t)bh * L + n0 + s] = wdec ? a - p.wd * wdw : a;
             }
             __syncthreads();
             // dP (into T2) and dV: through G's dependence on P and on v (and k)
