@@ -160,8 +160,10 @@ TTT_API ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *
  * Calling it T times with one token each gives the same result as one call
  * with the T tokens.  desc->init_per_batch is ignored (the state is always
  * [B, H, ...]).  Supported: d <= 128 with d a multiple of 4; d = 64 runs the decode
- * kernel (one warp per (batch, head), FP32), other d the generic kernel.  Z must not alias
- * an input, and W, b must not alias any other buffer.
+ * kernel (FP32: one warp per (batch, head) with the residual LayerNorm, four warps of 16
+ * output columns each without it, since the columns of the state then evolve
+ * independently), other d the generic kernel.  Z must not alias an input, and W, b must
+ * not alias any other buffer.
  */
 TTT_API ttt_status ttt_linear_step(const ttt_desc *desc, const void *Q, const void *K, const void *V,
                                    const float *eta, float *W, float *b, const float *gamma,
