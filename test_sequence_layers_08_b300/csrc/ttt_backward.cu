@@ -82,6 +82,30 @@ __device__ __forceinline__ void mm_xy(float *out, const float *X, const float *Y
     }
 }
 
+// The same with two left factors sharing Y: outA = XA Y + initA, outB = XB Y (one read of
+// each Y row serves both products)
+__device__ __forceinline__ void mm_xy2(float *outA, float *outB, const float *XA, const float *XB, const float *Y,
+                                      const float *initA, int m, int k, int n)
+{
+    const int n4 = n >> 2;
+    for (int tile = threadIdx.x; tile < m * n4; tile += kThreads) {
+        const int r = tile / n4, j = (tile - r * n4) * 4;
+        float4 a = initA ? f4(initA + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float *xa = XA + r * k, *xb = XB + r * k;
+#pragma unroll
+        for (int u = 0; u < k; u += 4) {
+            const float4 x = f4(xa + u), y = f4(xb + u);
+            const float4 w0 = f4(Y + u * n + j), w1 = f4(Y + (u + 1) * n + j);
+            const float4 w2 = f4(Y + (u + 2) * n + j), w3 = f4(Y + (u + 3) * n + j);
+            fma4(a, x.x, w0); fma4(a, x.y, w1); fma4(a, x.z, w2); fma4(a, x.w, w3);
+            fma4(b, y.x, w0); fma4(b, y.y, w1); fma4(b, y.z, w2); fma4(b, y.w, w3);
+        }
+        st4(outA + r * n + j, a);
+        st4(outB + r * n + j, b);
+    }
+}
+
 // Dot product of two k-long shared-memory rows, starting at column `start` (a multiple of 4)
 // and wrapping: threads whose rows are k floats apart start 4 floats apart, so their 16-byte
 // loads fall in different banks.
@@ -292,6 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
     const int bh = blockIdx.x, h = (p.hoff + bh) % p.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int kWarps = kThreads / 32;
+    // rows per warp in the warp-per-row loops (a compile-time count for b = 16, so they unroll
+    // and the rows' shuffle reductions interleave)
+    const int kRowIters = MT ? (MT + kWarps - 1) / kWarps : (mb + kWarps - 1) / kWarps;
     const int nmb = L / mb, nck = (nmb + ck - 1) / ck;
     const int nt = mb * d;
     const float kf = p.ip ? 0.f : 1.f;
@@ -347,7 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
     // G = dl/dz of the tile's rows, from P (in G on entry for the plain loss; in src for LN)
     auto gradient_rows = [&](float *Gout, const float *src) {
         if (LN) {
-            for (int s = warp; s < mb; s += kWarps) {
+            #pragma unroll
+            for (int s = warp, it_ = 0; it_ < kRowIters; s += kWarps, ++it_) {
+                if (s >= mb) break;
                 const LnRow ln = ln_row(src + s * d, d, p.eps);
                 ln_grad_row(Gout + s * d, src + s * d, Kt + s * d, Vt + s * d, gam, bet, d, p.eps, p.ip != 0, ln,
                             nullptr);
@@ -423,11 +452,14 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
         if (wdec)
             for (int s2 = 0; s2 < mb; ++s2) esum += et[s2];
         mm_xty_acc(X, Kt, G, et, -1.f, mb, d, d, 1.f - p.wd * esum);
-        for (int j = tid; j < d; j += kThreads) {
+        for (int j0 = 0; j0 < d; j0 += kThreads / 4) {   // four lanes per feature
+            const int j = j0 + (tid >> 2), q4 = tid & 3;
             float a = 0.f;
-#pragma unroll
-            for (int s = 0; s < mb; ++s) a = fmaf(et[s], G[s * d + j], a);
-            X[dd + j] -= a;
+            if (j < d)
+                for (int s = q4; s < mb; s += 4) a = fmaf(et[s], G[s * d + j], a);
+            a += __shfl_xor_sync(0xffffffffu, a, 1);
+            a += __shfl_xor_sync(0xffffffffu, a, 2);
+            if (j < d && q4 == 0) X[dd + j] -= a;
         }
     };
 
@@ -468,9 +500,11 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
             const float *W = S + m * sd, *c = W + dd;
             stage_op(Op{1, m0 + m}, m > 0 ? Op{1, m0 + m - 1} : (ci > 0 ? first_of_chunk(ci - 1) : Op{-1, 0}));
             // P (LN: kept in Pz), K dW', R = M . (Q K^T + 1); Q W (with LN or weight decay)
-            mm_xy(LN ? Pz : G, Kt, W, c, mb, d, d);
+            if (LN || wdec)
+                mm_xy2(LN ? Pz : G, Yq, Kt, Qt, W, c, mb, d, d);
+            else
+                mm_xy(G, Kt, W, c, mb, d, d);
             mm_xy(T2, Kt, dW, nullptr, mb, d, d);
-            if (LN || wdec) mm_xy(Yq, Qt, W, nullptr, mb, d, d);
             if (tid == 0) {   // f_t = 1 - lambda sum_{s <= t} eta_s
                 float cum = 0.f;
                 for (int t = 0; t < mb; ++t) {
@@ -500,7 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
                     st4(dZb + t * d + j, z);
                 }
                 __syncthreads();
-                for (int t = warp; t < mb; t += kWarps) {
+                #pragma unroll
+                for (int t = warp, it_ = 0; it_ < kRowIters; t += kWarps, ++it_) {
+                    if (t >= mb) break;
                     const LnRow lo = ln_row(dZb + t * d, d, p.eps);
                     float w[kMaxPerLane];
 #pragma unroll
@@ -571,7 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
                 for (int i = tid; i < dd; i += kThreads) part = fmaf(W[i], dW[i], part);
                 part = warp_sum(part);
                 if (lane == 0) wred[warp] = part;
-                for (int t = warp; t < mb; t += kWarps) {   // <dZbar_t, q_t W>
+                #pragma unroll
+                for (int t = warp, it_ = 0; it_ < kRowIters; t += kWarps, ++it_) {
+                    if (t >= mb) break;   // <dZbar_t, q_t W>
                     float x = 0.f;
                     for (int u = lane; u < d; u += 32) x = fmaf(dZb[t * d + u], Yq[t * d + u], x);
                     x = warp_sum(x);
@@ -600,7 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
             __syncthreads();
             // dP (into T2) and dV: through G's dependence on P and on v (and k)
             if (LN) {
-                for (int s = warp; s < mb; s += kWarps) {
+                #pragma unroll
+                for (int s = warp, it_ = 0; it_ < kRowIters; s += kWarps, ++it_) {
+                    if (s >= mb) break;
                     const float *z = Pz + s * d;
                     const LnRow ln = ln_row(z, d, p.eps);
                     float gx[kMaxPerLane], Gv[kMaxPerLane], u[kMaxPerLane];
@@ -691,11 +731,15 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
             }
             __syncthreads();
             mm_xty_acc(dW, Kt, T2, nullptr, 1.f, mb, d, d);
-            for (int j = tid; j < d; j += kThreads) {
+            // four lanes per feature, each a quarter of the tokens, then two shuffles
+            for (int j0 = 0; j0 < d; j0 += kThreads / 4) {
+                const int j = j0 + (tid >> 2), q4 = tid & 3;
                 float a = 0.f;
-#pragma unroll
-                for (int s = 0; s < mb; ++s) a += dZb[s * d + j] + T2[s * d + j];
-                dc[j] += a;
+                if (j < d)
+                    for (int s = q4; s < mb; s += 4) a += dZb[s * d + j] + T2[s * d + j];
+                a += __shfl_xor_sync(0xffffffffu, a, 1);
+                a += __shfl_xor_sync(0xffffffffu, a, 2);
+                if (j < d && q4 == 0) dc[j] += a;
             }
         }
     }
