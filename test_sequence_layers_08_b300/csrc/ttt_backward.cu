@@ -452,14 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
         if (wdec)
             for (int s2 = 0; s2 < mb; ++s2) esum += et[s2];
         mm_xty_acc(X, Kt, G, et, -1.f, mb, d, d, 1.f - p.wd * esum);
-        for (int j0 = 0; j0 < d; j0 += kThreads / 4) {   // four lanes per feature
-            const int j = j0 + (tid >> 2), q4 = tid & 3;
+        for (int j = tid; j < d; j += kThreads) {
             float a = 0.f;
-            if (j < d)
-                for (int s = q4; s < mb; s += 4) a = fmaf(et[s], G[s * d + j], a);
-            a += __shfl_xor_sync(0xffffffffu, a, 1);
-            a += __shfl_xor_sync(0xffffffffu, a, 2);
-            if (j < d && q4 == 0) X[dd + j] -= a;
+#pragma unroll
+            for (int s = 0; s < mb; ++s) a = fmaf(et[s], G[s * d + j], a);
+            X[dd + j] -= a;
         }
     };
 
@@ -731,15 +728,11 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_kernel(BwdParams p)
             }
             __syncthreads();
             mm_xty_acc(dW, Kt, T2, nullptr, 1.f, mb, d, d);
-            // four lanes per feature, each a quarter of the tokens, then two shuffles
-            for (int j0 = 0; j0 < d; j0 += kThreads / 4) {
-                const int j = j0 + (tid >> 2), q4 = tid & 3;
+            for (int j = tid; j < d; j += kThreads) {
                 float a = 0.f;
-                if (j < d)
-                    for (int s = q4; s < mb; s += 4) a += dZb[s * d + j] + T2[s * d + j];
-                a += __shfl_xor_sync(0xffffffffu, a, 1);
-                a += __shfl_xor_sync(0xffffffffu, a, 2);
-                if (j < d && q4 == 0) dc[j] += a;
+#pragma unroll
+                for (int s = 0; s < mb; ++s) a += dZb[s * d + j] + T2[s * d + j];
+                dc[j] += a;
             }
         }
     }
