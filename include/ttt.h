@@ -123,8 +123,8 @@ enum { TTT_LOSS_MSE = 0, TTT_LOSS_INNER_PRODUCT = 1 };
  * arithmetic: without the residual LayerNorm and with at most 2 x 148 CTAs' worth of
  * (batch, head) rows, each row split over CTAs by output column, since the columns of the
  * state evolve independently there; otherwise one CTA per row); bf16 I/O with d = 64,
- * b = 16 runs a tensor-core kernel: without the residual LayerNorm and weight decay the
- * chunked kernel (the state carried across 64-token chunks), otherwise the fused kernel
+ * b = 16 runs a tensor-core kernel: without the residual LayerNorm the chunked kernel (the
+ * state carried across 64-token chunks; every loss and decay), with it the fused kernel
  * (every loss and decay).
  */
 TTT_API ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,

@@ -15,6 +15,15 @@
 // i.e. the dual form of section 4.2 applied to a chunk of mini-batches, with the
 // block-triangular correction L that keeps every gradient at its own mini-batch's state.
 // With the inner-product loss -<f(k), v> of the ai-feeds Modular TTT page, G_m = -V_m.
+// With its weight decay lambda (W only, the gradient at the mini-batch's start: inside
+// mini-batch l, W_t = (1 - lambda cum_t) W_l - sum_{s<=t} eta_s k_s^T g_s, and
+// W_{l+1} = d_l W_l - K_l^T E_l G_l with d_l = 1 - lambda sum_{s in l} eta_s), the unrolling stays
+// exact with D_m = prod_{j<m} d_j and rho_{ml} = prod_{l<j<m} d_j:
+//   G_m  = (D_m K_m W + 1 c - V_m) - sum_{l<m} [eta_s (rho_{ml} k_{m,t} . k_{l,s} + 1)] G_l
+//   Z_t  = f_t D_m q_t W + c - sum_{l<m} [eta_s (f_t rho_{ml} q_t . k_{l,s} + 1)] G_l
+//          - sum_{s in m, s<=t} eta_s (q_t . k_s + 1) g_s,          f_t = 1 - lambda cum_t
+//   W'   = D_4 W - sum_l rho_{4l} K_l^T E_l G_l,  c' = c - sum_l G_l^T eta_l  (bias not decayed)
+// (a template switch: the default learner pays none of it).
 //
 // B300 design.  The scan is latency-bound (one chunk of one (batch, head) waits on the
 // last), so the kernel shortens the chain per token: the d x d state update, the key
@@ -89,6 +98,7 @@ struct Params {
     int init_per_batch;
     int hoff;                // head index of row 0 of this call
     int ip;                  // inner-product loss
+    float wd;                // weight decay lambda (the WD instantiation)
 };
 
 constexpr long long kDrainNs = 1000000000ll;
@@ -103,6 +113,7 @@ __device__ __noinline__ bool chunk_wait_slow(uint32_t bar, uint32_t parity, long
     return false;
 }
 
+template <bool WD>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmZ,
@@ -222,7 +233,9 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // Input-only block: rows t = target tokens of mini-batch mt of X (Q or K), columns s =
     // source tokens of mini-batch l of K; value eta_s (x_t . k_s + 1), masked to s <= t on a
     // diagonal output block.  Stored as the lane's own B fragments (k = s, n = t).
-    auto block = [&](const __nv_bfloat16 (*X)[CT * D], int cc, int mt, int l, bool causal, int b) {
+    // With weight decay the Gram part of rows t = g (t = g + 8) is scaled by sc0 (sc1).
+    auto block = [&](const __nv_bfloat16 (*X)[CT * D], int cc, int mt, int l, bool causal, int b, float sc0,
+                     float sc1) {
         uint32_t a[4][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)   // A: matrices (t0, ch 2q), (t1, 2q), (t0, 2q + 1), (t1, 2q + 1)
@@ -248,8 +261,14 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const int s0 = hf * 8 + 2 * c;
             const float2 e = eta2(cc, l * MB + s0);
             const float e0 = e.x, e1 = e.y;
-            const float x0 = acc[hf][0] + ac2[hf][0], x1 = acc[hf][1] + ac2[hf][1];
-            const float x2 = acc[hf][2] + ac2[hf][2], x3 = acc[hf][3] + ac2[hf][3];
+            float x0 = acc[hf][0] + ac2[hf][0], x1 = acc[hf][1] + ac2[hf][1];
+            float x2 = acc[hf][2] + ac2[hf][2], x3 = acc[hf][3] + ac2[hf][3];
+            if (WD) {
+                x0 *= sc0;
+                x1 *= sc0;
+                x2 *= sc1;
+                x3 *= sc1;
+            }
             const float v0 = (causal && s0 > g) ? 0.f : e0 * (x0 + 1.f);
             const float v1 = (causal && s0 + 1 > g) ? 0.f : e1 * (x1 + 1.f);
             const float v2 = (causal && s0 > g + 8) ? 0.f : e0 * (x2 + 1.f);
@@ -257,25 +276,95 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             s.blk[cc & 1][b][hf][lane] = make_uint2(ptx::pack_bf16(v0, v1), ptx::pack_bf16(v2, v3));
         }
     };
+    // Weight decay.  An inclusive scan of eta within each mini-batch of chunk cc: lane l holds the
+    // prefix sums at tokens l and l + 32 (mini-batches l / 16 and 2 + l / 16).  The mini-batch
+    // factors d_l = 1 - lambda sum eta are the segment ends; rho_{ml} = prod_{l<j<m} d_j; the
+    // query factor of token t of mini-batch m is one shuffle away.
+    struct EtaScan {
+        float ca, cb;
+    };
+    auto eta_scan = [&](int cc, float *dl) -> EtaScan {
+        zero_eta_tail(cc);
+        float a = s.eta[cc % NSS][lane], b2 = s.eta[cc % NSS][lane + 32];
+#pragma unroll
+        for (int o = 1; o < MB; o <<= 1) {
+            const float ta = __shfl_up_sync(0xffffffffu, a, o, MB), tb = __shfl_up_sync(0xffffffffu, b2, o, MB);
+            if ((lane & (MB - 1)) >= o) {
+                a += ta;
+                b2 += tb;
+            }
+        }
+        dl[0] = 1.f - p.wd * __shfl_sync(0xffffffffu, a, MB - 1);
+        dl[1] = 1.f - p.wd * __shfl_sync(0xffffffffu, a, 2 * MB - 1);
+        dl[2] = 1.f - p.wd * __shfl_sync(0xffffffffu, b2, MB - 1);
+        dl[3] = 1.f - p.wd * __shfl_sync(0xffffffffu, b2, 2 * MB - 1);
+        return EtaScan{a, b2};
+    };
+    auto rho = [&](const float *dl, int m, int l) {
+        float r = 1.f;
+#pragma unroll
+        for (int j = 0; j < NMB; ++j)
+            if (j > l && j < m) r *= dl[j];
+        return r;
+    };
+    // 1 - lambda cum_t for token t of mini-batch m (m uniform across the warp; every lane shuffles)
+    auto fq_tok = [&](const EtaScan &es, int m, int t) {
+        const int idx = (m * MB + t) & 31;
+        const float va = __shfl_sync(0xffffffffu, es.ca, idx), vb = __shfl_sync(0xffffffffu, es.cb, idx);
+        return 1.f - p.wd * (m < 2 ? va : vb);
+    };
+    // P (or the query product) of mini-batch m from the product without bias: f D_m x + c
+    auto scale_rows = [&](float (*acc)[4], const float *dl, const EtaScan &es, bool per_token, float c0, float c1) {
+        float Dm = 1.f;
+#pragma unroll
+        for (int m = 0; m < NMB; ++m) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float f = (per_token ? fq_tok(es, m, 8 * u + 2 * c + e) : 1.f) * Dm;
+                    acc[2 * m + u][e] = fmaf(f, acc[2 * m + u][e], c0);
+                    acc[2 * m + u][2 + e] = fmaf(f, acc[2 * m + u][2 + e], c1);
+                }
+            Dm *= dl[m];
+        }
+    };
     // chain blocks L_{ml} (m > l; numbers 0..5) of chunk cc: state warp w takes those with
     // number = w mod 4
     auto chain_blocks = [&](int cc) {
         zero_eta_tail(cc);
+        float dl[NMB] = {1.f, 1.f, 1.f, 1.f};
+        if (WD) eta_scan(cc, dl);
 #pragma unroll
         for (int m = 1; m < NMB; ++m)
 #pragma unroll
             for (int l = 0; l < m; ++l)
-                if (chain_blk(m, l) % kStateWarps == fw) block(s.k, cc, m, l, false, chain_blk(m, l));
+                if (chain_blk(m, l) % kStateWarps == fw) {
+                    const float r = WD ? rho(dl, m, l) : 1.f;
+                    block(s.k, cc, m, l, false, chain_blk(m, l), r, r);
+                }
     };
     // output blocks (m, l), l <= m (numbers 6..15) of chunk cc: output warp 4 + w takes those
     // with (number - 6) = w mod 4
     auto out_blocks = [&](int cc) {
         zero_eta_tail(cc);
+        float dl[NMB] = {1.f, 1.f, 1.f, 1.f};
+        EtaScan es{0.f, 0.f};
+        if (WD) es = eta_scan(cc, dl);
 #pragma unroll
         for (int m = 0; m < NMB; ++m)
 #pragma unroll
             for (int l = 0; l <= m; ++l)
-                if ((out_blk(m, l) - 6) % kStateWarps == fw) block(s.q, cc, m, l, l == m, out_blk(m, l));
+                if ((out_blk(m, l) - 6) % kStateWarps == fw) {
+                    // earlier mini-batches: f_t rho_{ml} on the Gram part; the diagonal block: none
+                    float s0 = 1.f, s1 = 1.f;
+                    if (WD && l < m) {
+                        const float r = rho(dl, m, l);
+                        s0 = r * fq_tok(es, m, g);
+                        s1 = r * fq_tok(es, m, g + 8);
+                    }
+                    block(s.q, cc, m, l, l == m, out_blk(m, l), s0, s1);
+                }
     };
     // both n-tiles of a block: (f0.x, f1.x) for target tokens 0-7, (f0.y, f1.y) for 8-15
     auto read_blk = [&](int cc, int b, uint2 &f0, uint2 &f1) {
@@ -288,7 +377,14 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     if (state_warp) {
         wait_stage(0);
         pack_w();
-        product(pacc, s.k, 0, cb0, cb1);
+        if (WD) {
+            float dl[NMB];
+            const EtaScan es = eta_scan(0, dl);
+            product(pacc, s.k, 0, 0.f, 0.f);
+            scale_rows(pacc, dl, es, false, cb0, cb1);
+        } else {
+            product(pacc, s.k, 0, cb0, cb1);
+        }
         chain_blocks(0);
     }
     ptx::named_bar(1, kThreads);   // every state warp reads all six chain blocks of chunk 0
@@ -305,6 +401,17 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 #pragma unroll
             for (int q = 0; q < 4; ++q) s.wa[cc & 1][fw][q][lane] = make_uint4(wa[q][0], wa[q][1], wa[q][2], wa[q][3]);
             s.cb[cc & 1][fw][lane] = make_float2(cb0, cb1);
+
+            // weight decay: W' = D_4 W - sum_m rho_{4m} K_m^T E_m G_m (the carried W^T scaled first)
+            float dl[NMB] = {1.f, 1.f, 1.f, 1.f};
+            if (WD) {
+                eta_scan(cc, dl);
+                const float D4 = dl[0] * dl[1] * dl[2] * dl[3];
+#pragma unroll
+                for (int pt = 0; pt < 8; ++pt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) wt[pt][i] *= D4;
+            }
 
             // intra-chunk chain: G_m, then its corrections to the later mini-batches' P and its
             // k-step of the state update
@@ -347,10 +454,11 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const float2 ea = eta2(cc, s0), eb = eta2(cc, s0 + 8);
                 const float e00 = ea.x, e01 = ea.y, e10 = eb.x, e11 = eb.y;
                 uint32_t nge[4];
-                nge[0] = ptx::pack_bf16(-e00 * gm[0][0], -e01 * gm[0][1]);
-                nge[1] = ptx::pack_bf16(-e00 * gm[0][2], -e01 * gm[0][3]);
-                nge[2] = ptx::pack_bf16(-e10 * gm[1][0], -e11 * gm[1][1]);
-                nge[3] = ptx::pack_bf16(-e10 * gm[1][2], -e11 * gm[1][3]);
+                const float r4 = WD ? rho(dl, NMB, m) : 1.f;   // rho_{4m}
+                nge[0] = ptx::pack_bf16(-r4 * e00 * gm[0][0], -r4 * e01 * gm[0][1]);
+                nge[1] = ptx::pack_bf16(-r4 * e00 * gm[0][2], -r4 * e01 * gm[0][3]);
+                nge[2] = ptx::pack_bf16(-r4 * e10 * gm[1][0], -r4 * e11 * gm[1][1]);
+                nge[3] = ptx::pack_bf16(-r4 * e10 * gm[1][2], -r4 * e11 * gm[1][3]);
                 d0 += e00 * gm[0][0] + e01 * gm[0][1] + e10 * gm[1][0] + e11 * gm[1][1];
                 d1 += e00 * gm[0][2] + e01 * gm[0][3] + e10 * gm[1][2] + e11 * gm[1][3];
 #pragma unroll
@@ -373,7 +481,14 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
             // next chunk: its key product from the new state, and its chain blocks
             if (more) {
-                product(pacc, s.k, cc + 1, cb0, cb1);
+                if (WD) {
+                    float dn[NMB];
+                    const EtaScan es = eta_scan(cc + 1, dn);
+                    product(pacc, s.k, cc + 1, 0.f, 0.f);
+                    scale_rows(pacc, dn, es, false, cb0, cb1);
+                } else {
+                    product(pacc, s.k, cc + 1, cb0, cb1);
+                }
                 chain_blocks(cc + 1);
             }
         } else if (!state_warp) {
@@ -395,7 +510,14 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 const float2 cbs = s.cb[cc & 1][fw][lane];
                 float yacc[8][4];
-                product(yacc, s.q, cc, cbs.x, cbs.y);
+                if (WD) {   // token t of mini-batch m reads f_t D_m W (and c, not decayed)
+                    float dl[NMB];
+                    const EtaScan es = eta_scan(cc, dl);
+                    product(yacc, s.q, cc, 0.f, 0.f);
+                    scale_rows(yacc, dl, es, true, cbs.x, cbs.y);
+                } else {
+                    product(yacc, s.q, cc, cbs.x, cbs.y);
+                }
                 // outputs: Zbar_{m'} -= G_m B_{m'm}^T for m' >= m
 #pragma unroll
                 for (int m = 0; m < NMB; ++m) {
@@ -463,8 +585,7 @@ linear_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
 bool linear_chunk_supported(const ttt_desc &d)
 {
-    return d.io_dtype == TTT_BF16 && d.d == D && d.mini_batch == MB && !d.residual_ln &&
-           d.weight_decay == 0.f;
+    return d.io_dtype == TTT_BF16 && d.d == D && d.mini_batch == MB && !d.residual_ln;
 }
 
 cudaError_t launch_linear_chunk(const LinearArgs &a)
@@ -476,12 +597,12 @@ cudaError_t launch_linear_chunk(const LinearArgs &a)
         !make_bf16_tile_map(&mv, a.V, d.L, BH, CT) || !make_bf16_tile_map(&mz, a.Z, d.L, BH, CT))
         return cudaErrorInvalidValue;
     Params p{d.H, d.L, wait_timeout_ns(), withhold_loads(), a.eta, a.W0, a.b0, a.W_final, a.b_final,
-             a.status, d.init_per_batch, head_offset(d), d.loss == TTT_LOSS_INNER_PRODUCT};
+             a.status, d.init_per_batch, head_offset(d), d.loss == TTT_LOSS_INNER_PRODUCT, d.weight_decay};
     const size_t smem = sizeof(Smem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(linear_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    const auto kern = d.weight_decay != 0.f ? linear_chunk_kernel<true> : linear_chunk_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    linear_chunk_kernel<<<BH, kThreads, smem, a.stream>>>(mq, mk, mv, mz, p);
+    kern<<<BH, kThreads, smem, a.stream>>>(mq, mk, mv, mz, p);
     return cudaGetLastError();
 }
 
