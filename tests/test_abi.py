@@ -213,12 +213,13 @@ def test_partition_fields_accepted(lib):
 
 
 def test_variant_kernel_choice(lib):
-    """The fused TTT-Linear kernel runs both inner-learner variants; the fused TTT-MLP kernel
-    runs the default learner only, so MLP variants go to the generic kernel."""
+    """The tensor-core TTT-Linear kernels run both inner-learner variants (the chunked kernel
+    without the residual LayerNorm, the fused one with it); the fused TTT-MLP kernel runs the
+    default learner only, so MLP variants go to the generic kernel."""
     k = lambda mlp, **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), mlp))
     for var in (dict(loss=1), dict(weight_decay=0.1), dict(loss=1, weight_decay=0.1)):
-        assert k(0, **var) in LINEAR_TC_KERNELS
-        assert k(0, residual_ln=1, **var) in LINEAR_TC_KERNELS
+        assert k(0, **var) == "ttt_linear_chunked"
+        assert k(0, residual_ln=1, **var) == "ttt_linear_fused"
         assert k(1, **var) == "ttt_mlp_generic"
         assert k(1, residual_ln=1, d_hidden=256, **var) == "ttt_mlp_generic"
 
