@@ -2,8 +2,9 @@
 "loss" and "weight decay"): the inner-product loss -<f(k), v> and weight decay lambda on the
 fast weights, alone and together, for every kernel family, against the oracle.
 
-The fused bf16 TTT-Linear kernel runs them in place of the default learner; the TTT-MLP
-variants and every fp32 case run on the generic kernels; the decode step has its own."""
+The tensor-core bf16 TTT-Linear kernels run them in place of the default learner (the
+chunked kernel without the residual LayerNorm, the fused one with it); the TTT-MLP variants
+and every fp32 case run on the generic kernels; the decode step has its own."""
 import numpy as np
 import pytest
 import torch
@@ -37,7 +38,8 @@ def kernel(cfg, mlp=False):
 @pytest.mark.parametrize("io", ["bf16", "f32"])
 def test_linear_variants(io, ln, variant):
     loss, wd = variant
-    # bf16: the fused kernel, 65 mini-batches (a ragged last 64-token stage); f32: generic
+    # bf16: chunked (no LN) or fused (LN), 65 mini-batches (a ragged last 64-token stage);
+    # f32: the column-split (no LN) or generic (LN) kernel
     L = 1040 if io == "bf16" else 272
     cfg = (LIN_LN if ln else LIN).with_(name=f"lin_var_{io}", B=2, H=3, L=L, io=io)
     if io == "bf16":
