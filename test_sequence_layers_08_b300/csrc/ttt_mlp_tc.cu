@@ -88,6 +88,7 @@ struct Params {
     float *W1f, *b1f, *W2f, *b2f;
     unsigned int *status;
     int hoff;                // head index of row 0 of this call
+    int ip;                  // inner-product loss
 };
 
 constexpr long long kDrainNs = 1000000000ll;
@@ -256,7 +257,11 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             ptx::named_bar(kBarLn, 128);
         }
     }
-    const float g20 = ga0 * ga0, g21 = ga1 * ga1;
+    // inner-product loss -<f(k), v> (ai-feeds Modular TTT page): G2 = -V, or the LayerNorm
+    // backward of the upstream -v; the same code path with the gamma^2, beta and k terms zeroed
+    const float kf = p.ip ? 0.f : 1.f;
+    C1 *= kf;
+    const float g20 = kf * ga0 * ga0, g21 = kf * ga1 * ga1;
     const int tk = g >> 1, qh = g & 1;
     const int t_own = 8 * (tk >> 1) + 2 * c + (tk & 1);
 
@@ -454,10 +459,10 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 load_T(kt, s.k, n);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    gb[u][0] = ga0 * (be0 - vt[u][0] + kt[u][0]);
-                    gb[u][1] = ga0 * (be0 - vt[u][1] + kt[u][1]);
-                    gb[u][2] = ga1 * (be1 - vt[u][2] + kt[u][2]);
-                    gb[u][3] = ga1 * (be1 - vt[u][3] + kt[u][3]);
+                    gb[u][0] = ga0 * fmaf(kf, be0 + kt[u][0], -vt[u][0]);
+                    gb[u][1] = ga0 * fmaf(kf, be0 + kt[u][1], -vt[u][1]);
+                    gb[u][2] = ga1 * fmaf(kf, be1 + kt[u][2], -vt[u][2]);
+                    gb[u][3] = ga1 * fmaf(kf, be1 + kt[u][3], -vt[u][3]);
                 }
                 float vs[24];
 #pragma unroll
@@ -542,7 +547,7 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
                 for (int u = 0; u < 2; ++u)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) gm[u][i] = z2[u][i] - vt[u][i];
+                    for (int i = 0; i < 4; ++i) gm[u][i] = fmaf(z2[u][i], kf, -vt[u][i]);
             }
             // publish G2 and -eta G2 as [t][o] tiles; b2 -= eta^T G2
             const int s0 = 2 * c;
@@ -841,7 +846,7 @@ bool make_map_mlp(CUtensorMap *m, const void *base, int L, int BH)
 
 bool mlp_tc_supported(const ttt_desc &d)
 {
-    if (d.loss != TTT_LOSS_MSE || d.weight_decay != 0.f) return false;   // default learner only
+    if (d.weight_decay != 0.f) return false;   // either loss, no weight decay
     return d.io_dtype == TTT_BF16 && d.d == D && d.d_hidden == DH && d.mini_batch == MB;
 }
 
@@ -874,6 +879,7 @@ cudaError_t launch_mlp_tc(const MlpArgs &a)
     p.b2f = a.b2_f;
     p.status = a.status;
     p.hoff = head_offset(d);
+    p.ip = d.loss == TTT_LOSS_INNER_PRODUCT;
     const size_t smem = sizeof(Smem) + 1024;
     auto kern = d.residual_ln ? mlp_fused_kernel<true> : mlp_fused_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -103,3 +103,14 @@ def test_decode_variants(io, ln, variant):
                             mini_batch=1, ln=ln, eps=cfg.eps, init_per_batch=True, loss=loss,
                             weight_decay=wd)
     compare_all(cfg, [Z.float().cpu().numpy(), Wd.cpu().numpy(), bd.cpu().numpy()], ref)
+
+
+def test_full_size_mlp_inner_product():
+    """The 4 x 12 x 4096 TTT-MLP workload with the inner-product loss (the fused MLP kernel),
+    sampled (batch, head)."""
+    cfg = MLP
+    assert kernel(cfg, mlp=True) == "ttt_mlp_fused"
+    x = inputs(cfg, seed=0)
+    got = run_gpu(cfg, to_device(cfg, x), loss="ip")
+    pairs = sample_pairs(cfg, 2, seed=11)
+    compare_pairs(cfg, got, run_oracle(cfg, x, pairs, loss="ip"))
