@@ -138,8 +138,8 @@ TTT_API ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const voi
  *        W2_0 [H or B,H, dh, d]; b2_0 [H or B,H, d]; gamma, beta [H, d].
  *   out: Z [B,H,L,d]; W1_f [B,H,d,dh]; b1_f [B,H,dh]; W2_f [B,H,dh,d]; b2_f [B,H,d].
  * Supported: d <= 128, dh <= 512, b <= 64 while the state fits on chip; the
- * tensor-core kernel (bf16, d = 64, dh = 256, b = 16) runs either loss without weight
- * decay, the generic kernel every variant.
+ * tensor-core kernel (bf16, d = 64, dh = 256, b = 16) and the generic kernel run every
+ * loss and decay.
  */
 TTT_API ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
                        const float *eta, const float *W1_0, const float *b1_0,

@@ -89,6 +89,7 @@ struct Params {
     unsigned int *status;
     int hoff;                // head index of row 0 of this call
     int ip;                  // inner-product loss
+    float wd;                // weight decay lambda (the WD instantiation)
 };
 
 constexpr long long kDrainNs = 1000000000ll;
@@ -146,7 +147,7 @@ __device__ __forceinline__ void gelu_and_prime(float x, float &y, float &dy)
     dy = fmaf(x * du2, pr - pr * pr, pr);
 }
 
-template <bool LN>
+template <bool LN, bool WD>
 __global__ void __maxnreg__(255)
 mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, Params p, __nv_bfloat16 *Zg)
@@ -374,12 +375,48 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
         // ======== phase 1: first layer (key and query side), W2 copy, the Q K^T block
         float y1[2][2][4];
+        float fq[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, dn = 1.f;   // weight decay factors (below)
         uint32_t dz[2][2][2];   // GELU'(Z1) as bf16 pairs (it only scales G1, a bf16 operand)
         uint32_t xa[2][4];      // X2 = GELU(Z1) as bf16 A fragments (rows = hidden, k = tokens)
         {
         float z1[2][2][4];
         first_layer(z1, s.k, n);
         first_layer(y1, s.q, n);
+        // weight decay (ai-feeds Modular TTT page; W1, W2 only, gradient at the mini-batch's
+        // start): query token t reads f_t = 1 - lambda cum_t times W1, W2 (a prefix sum of eta
+        // by a scan over the four lanes sharing g), and the carried weights are scaled by
+        // dn = 1 - lambda sum eta before their updates
+        if (WD) {
+            const float a0 = eta_at(n, 2 * c), a1 = eta_at(n, 2 * c + 1);
+            const float bb0 = eta_at(n, 2 * c + 8), bb1 = eta_at(n, 2 * c + 9);
+            float ia = a0 + a1, ib = bb0 + bb1;
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                const float ta = __shfl_up_sync(0xffffffffu, ia, o, 4);
+                const float tb = __shfl_up_sync(0xffffffffu, ib, o, 4);
+                if (c >= o) {
+                    ia += ta;
+                    ib += tb;
+                }
+            }
+            const float ta = __shfl_sync(0xffffffffu, ia, 3, 4);   // tokens 0..7
+            const float tb = __shfl_sync(0xffffffffu, ib, 3, 4);   // tokens 8..15
+            fq[0][0] = 1.f - p.wd * (ia - a1);
+            fq[0][1] = 1.f - p.wd * ia;
+            fq[1][0] = 1.f - p.wd * (ta + ib - bb1);
+            fq[1][1] = 1.f - p.wd * (ta + ib);
+            dn = 1.f - p.wd * (ta + tb);
+            // Y1 = f (Q W1) + b1 from Y1 = Q W1 + b1
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float f = fq[u][i & 1];
+                        y1[m][u][i] = fmaf(f, y1[m][u][i], (1.f - f) * b1r[m][i >> 1]);
+                    }
+        }
         // X2 also goes to the shared [t][h] tile
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
@@ -626,8 +663,15 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                     for (int i = 0; i < 4; ++i) y1[m][u][i] = gelu(y1[m][u][i]);
             store_th(xb2t, y1);
         }
-        // W1^T += (-eta G1)^T K,  b1 -= eta^T G1
+        // W1^T += (-eta G1)^T K,  b1 -= eta^T G1   (W1 scaled by dn first with weight decay)
         {
+            if (WD)
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) w1[m][q][i] *= dn;
             const int s0 = 2 * c;
             const float e00 = eta_at(n, s0), e01 = eta_at(n, s0 + 1);
             const float e10 = eta_at(n, s0 + 8), e11 = eta_at(n, s0 + 9);
@@ -654,8 +698,16 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 b1r[m][1] -= d1;
             }
         }
-        // W2 += X2^T (-eta G2)   (A = X2^T rows = hidden, k = tokens; B = -eta G2 [t][o])
+        // W2 += X2^T (-eta G2)   (A = X2^T rows = hidden, k = tokens; B = -eta G2 [t][o]); W2 is
+        // no longer read as the step's starting weights (G1 above used it): scale by dn first
         {
+            if (WD)
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) w2[m][q][i] *= dn;
             const uint32_t eg = ptx::smem_addr(s.eg2);
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp) {
@@ -700,6 +752,14 @@ mlp_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                 zb[0][0] += p0.x; zb[0][1] += p0.y; zb[0][2] += p0.z; zb[0][3] += p0.w;
                 zb[1][0] += p1.x; zb[1][1] += p1.y; zb[1][2] += p1.z; zb[1][3] += p1.w;
             }
+            if (WD)   // Zb2 = f (Xb2 W2) + b2 from Xb2 W2 + b2 (the starting b2)
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float f = fq[u][i & 1];
+                        zb[u][i] = fmaf(f, zb[u][i], (1.f - f) * (i < 2 ? b2_start0 : b2_start1));
+                    }
             // B fragments (k = source s, n = target t) of the block, per source half
             uint32_t f[2][2];
 #pragma unroll
@@ -846,7 +906,6 @@ bool make_map_mlp(CUtensorMap *m, const void *base, int L, int BH)
 
 bool mlp_tc_supported(const ttt_desc &d)
 {
-    if (d.weight_decay != 0.f) return false;   // either loss, no weight decay
     return d.io_dtype == TTT_BF16 && d.d == D && d.d_hidden == DH && d.mini_batch == MB;
 }
 
@@ -880,8 +939,11 @@ cudaError_t launch_mlp_tc(const MlpArgs &a)
     p.status = a.status;
     p.hoff = head_offset(d);
     p.ip = d.loss == TTT_LOSS_INNER_PRODUCT;
+    p.wd = d.weight_decay;
     const size_t smem = sizeof(Smem) + 1024;
-    auto kern = d.residual_ln ? mlp_fused_kernel<true> : mlp_fused_kernel<false>;
+    const bool wd = d.weight_decay != 0.f;
+    auto kern = d.residual_ln ? (wd ? mlp_fused_kernel<true, true> : mlp_fused_kernel<true, false>)
+                              : (wd ? mlp_fused_kernel<false, true> : mlp_fused_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<BH, kThreads, smem, a.stream>>>(mq, mk, mv, p, static_cast<__nv_bfloat16 *>(a.Z));

@@ -213,16 +213,15 @@ def test_partition_fields_accepted(lib):
 
 
 def test_variant_kernel_choice(lib):
-    """The tensor-core TTT-Linear kernels run both inner-learner variants (the chunked kernel
-    without the residual LayerNorm, the fused one with it); the fused TTT-MLP kernel runs
-    either loss without weight decay, so MLP weight decay goes to the generic kernel."""
+    """The tensor-core kernels run both inner-learner variants: for TTT-Linear the chunked
+    kernel without the residual LayerNorm and the fused one with it, for TTT-MLP the fused
+    kernel."""
     k = lambda mlp, **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), mlp))
     for var in (dict(loss=1), dict(weight_decay=0.1), dict(loss=1, weight_decay=0.1)):
         assert k(0, **var) == "ttt_linear_chunked"
         assert k(0, residual_ln=1, **var) == "ttt_linear_fused"
-        mlp = "ttt_mlp_generic" if "weight_decay" in var else "ttt_mlp_fused"
-        assert k(1, **var) == mlp
-        assert k(1, residual_ln=1, d_hidden=256, **var) == mlp
+        assert k(1, **var) == "ttt_mlp_fused"
+        assert k(1, residual_ln=1, d_hidden=256, **var) == "ttt_mlp_fused"
 
 
 # ttt_linear_bwd pointer slots: Q K V eta W0 b0 gamma beta dZ dW_final db_final dQ dK dV deta

@@ -2,9 +2,9 @@
 "loss" and "weight decay"): the inner-product loss -<f(k), v> and weight decay lambda on the
 fast weights, alone and together, for every kernel family, against the oracle.
 
-The tensor-core bf16 TTT-Linear kernels run them in place of the default learner (the
-chunked kernel without the residual LayerNorm, the fused one with it); the TTT-MLP variants
-and every fp32 case run on the generic kernels; the decode step has its own."""
+The tensor-core bf16 kernels run them in place of the default learner (for TTT-Linear the
+chunked kernel without the residual LayerNorm and the fused one with it, for TTT-MLP the fused
+kernel); every fp32 case runs on the FFMA kernels; the decode step has its own."""
 import numpy as np
 import pytest
 import torch
@@ -105,12 +105,14 @@ def test_decode_variants(io, ln, variant):
     compare_all(cfg, [Z.float().cpu().numpy(), Wd.cpu().numpy(), bd.cpu().numpy()], ref)
 
 
-def test_full_size_mlp_inner_product():
-    """The 4 x 12 x 4096 TTT-MLP workload with the inner-product loss (the fused MLP kernel),
+@pytest.mark.parametrize("variant", VARIANTS, ids=VID)
+def test_full_size_mlp_variants(variant):
+    """The 4 x 12 x 4096 TTT-MLP workload with a variant learner (the fused MLP kernel),
     sampled (batch, head)."""
+    loss, wd = variant
     cfg = MLP
     assert kernel(cfg, mlp=True) == "ttt_mlp_fused"
     x = inputs(cfg, seed=0)
-    got = run_gpu(cfg, to_device(cfg, x), loss="ip")
+    got = run_gpu(cfg, to_device(cfg, x), loss=loss, weight_decay=wd)
     pairs = sample_pairs(cfg, 2, seed=11)
-    compare_pairs(cfg, got, run_oracle(cfg, x, pairs, loss="ip"))
+    compare_pairs(cfg, got, run_oracle(cfg, x, pairs, loss=loss, weight_decay=wd))
