@@ -2,9 +2,11 @@
 //
 // One CTA per (batch, head) scans the L / b mini-batches in order.  The fast
 // weights live in shared memory in fp32 for the whole scan; every contraction
-// is plain fp32 FFMA.  These kernels serve the fp32-I/O workload (where a
-// relative error of 1e-5 rules out tf32/bf16 tensor-core operands) and every
-// shape the tensor-core kernels do not take.
+// is plain fp32 FFMA.  These kernels serve fp32 I/O (where a relative error of
+// 1e-5 rules out tf32/bf16 tensor-core operands) with the residual LayerNorm or
+// with many (batch, head) rows (without LayerNorm and with few rows the
+// column-split kernel takes it), the TTT-MLP in fp32, and every shape the
+// tensor-core kernels do not take.
 //
 // Per mini-batch (damodev.csdn.net TTT article, sections 4.1-4.2; lryc.cn TTT
 // article, section 2.1 for the MLP and the residual LayerNorm):

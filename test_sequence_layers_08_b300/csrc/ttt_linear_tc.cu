@@ -23,9 +23,10 @@
 //   * warps 0-3 each own 16 output features.  W^T lives in registers as fp32
 //     warp-MMA accumulators for the whole scan; every contraction is a
 //     bf16 m16n8k16 MMA on register fragments, so the recurrence never leaves
-//     the register file.  (A tcgen05 MMA pays ~80 issue cycles and a ~250-cycle
-//     round trip through TMEM and an mbarrier; a dependent warp MMA takes ~21
-//     cycles.  On a chain of 16-token steps the warp MMA wins.)
+//     the register file.  (Measured on B300: a tcgen05 MMA's round trip through
+//     tensor memory and an mbarrier takes ~290 cycles and each further MMA ~46
+//     cycles of issue; a dependent warp MMA takes ~19 cycles.  On a chain of
+//     16-token steps the warp MMA wins.)
 //   * each step is one straight-line block on either side of a single named
 //     barrier, so the compiler can fill the latency of the LayerNorm chain
 //     (shuffle rounds, the barrier, rsqrt) with the off-chain work: the

@@ -32,6 +32,10 @@
 //     the same way over warps 4-7.
 // Per mini-batch all eight warps meet at five named barriers (warps 4-7 run into the next
 // mini-batch's first layer while warps 0-3 finish the output); every mbarrier wait is bounded.
+// Inner-learner variants (ai-feeds Modular TTT page): the inner-product loss -<f(k), v> zeroes
+// the gamma^2, beta and k coefficients of the LayerNorm backward (G2 = -V without it); weight
+// decay (a template switch) scales W1, W2 by 1 - lambda S before their updates and the
+// query-side products of both layers by 1 - lambda cum_t around the bias.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
