@@ -75,7 +75,7 @@ KERNEL_SOURCES = {"ttt_linear_fused": "ttt_linear_tc.cu", "ttt_linear_chunked": 
                   "ttt_mlp_fused": "ttt_mlp_tc.cu", "ttt_linear_decode": "ttt_decode.cu",
                   "ttt_linear_bwd": "ttt_backward.cu",
                   "ttt_linear_generic": "ttt_generic.cu", "ttt_mlp_generic": "ttt_generic.cu",
-                  "ttt_linear_cols": "ttt_linear_cols.cu"}
+                  "ttt_linear_cols": "ttt_linear_cols.cu", "ttt_qkv_proj": "ttt_proj.cu"}
 
 
 def measured_traffic(kname, workload):
@@ -873,6 +873,129 @@ def run_backward(args, cfg, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_project(args, cfg, world, rank, local):
+    """The whole layer from its input tokens: each step is the input projections
+    (ttt_qkv_proj: Q, K, V = views of x through the stacked projection matrices, tcgen05),
+    the learning-rate gate (ttt_eta_gate) and the scan, on a gated workload (x [B, L, 768],
+    seeded random projection matrices [3 H d, 768] ~ N(0, 1/768)).  Consecutive steps rotate
+    over two input/output sets (each step writes 3 B H L d bf16 of Q, K, V: more than L2).
+    The projection call is also timed alone: its roofline is the bf16 tensor peak."""
+    import torch
+    import test_sequence_layers_08_b300 as ttt
+    if cfg.eta != "gate" or cfg.io != "bf16":
+        raise SystemExit("--project needs a bf16 workload with the per-token gate")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    x = make_inputs(cfg, 0)
+    B, H, L, d = cfg.B, cfg.H, cfg.L, cfg.d
+    Dx = x["x"].shape[-1]
+    rng = np.random.default_rng(2)
+    W_h = (rng.standard_normal((3 * H * d, Dx)) / np.sqrt(Dx)).astype(np.float32)
+    theta = torch.from_numpy(x["theta"]).to(dev)
+    W = torch.from_numpy(W_h).to(dev).to(torch.bfloat16)
+    state = {k: (None if x.get(k) is None else torch.from_numpy(x[k]).to(dev))
+             for k in ("W0", "b0", "W1", "b1", "W2", "b2", "gamma", "beta")}
+    proj_flops = 2.0 * B * L * Dx * 3 * H * d
+    learner_tag = ("" if args.loss == "mse" else f"+loss_{args.loss}") + \
+                  ("" if args.weight_decay == 0 else f"+wd{args.weight_decay:g}")
+    variant = dict(loss=args.loss, weight_decay=args.weight_decay)
+
+    def make_set():
+        t = {"x": torch.from_numpy(x["x"]).to(dev).to(torch.bfloat16)}
+        t["qkv"] = tuple(torch.empty((B, H, L, d), device=dev, dtype=torch.bfloat16) for _ in range(3))
+        t["eta"] = torch.empty((B, H, L), device=dev, dtype=torch.float32)
+        return t
+    sets = [make_set() for _ in range(2)]
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps, stream=stream, **variant)
+
+    def layer(t, out=None):
+        Q, K, V = ttt.ttt_qkv_proj(t["x"], W, H, d, out=t["qkv"], stream=stream)
+        ttt.ttt_eta_gate(t["x"], theta, x["eta_base"], out=t["eta"], stream=stream)
+        if cfg.kind == "linear":
+            return ttt.ttt_linear_fwd(Q, K, V, t["eta"], state["W0"], state["b0"], state["gamma"],
+                                      state["beta"], out=out, **kw)
+        return ttt.ttt_mlp_fwd(Q, K, V, t["eta"], state["W1"], state["b1"], state["W2"], state["b2"],
+                               state["gamma"], state["beta"], out=out, **kw)
+
+    outs = [layer(t) for t in sets]
+    ttt.ttt_sync_status(stream)
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(args.warmup):
+        layer(sets[i % 2], outs[i % 2])
+    ttt.ttt_sync_status(stream)
+    t_soak = time.time()
+    soak_end = time.time() + args.soak_ms / 1e3
+    i = 0
+    while time.time() < soak_end:
+        layer(sets[i % 2], outs[i % 2])
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        layer(sets[i % 2], outs[i % 2])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ttt.ttt_sync_status(stream)
+    ms_step = max_over_ranks(world, start.elapsed_time(end)) / args.steps
+    # the projection call alone (same rotation)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for i in range(args.steps):
+        ttt.ttt_qkv_proj(sets[i % 2]["x"], W, H, d, out=sets[i % 2]["qkv"], stream=stream)
+    p1.record(stream)
+    torch.cuda.synchronize(dev)
+    ttt.ttt_sync_status(stream)
+    ms_proj = max_over_ranks(world, p0.elapsed_time(p1)) / args.steps
+    value = world * cfg.tokens / (ms_step * 1e-3)
+    time.sleep(0.4)
+    clk = clocks.summary(t_soak, time.time())
+
+    # end to end: every step copies x in from pinned host memory and Z out
+    hx = torch.from_numpy(x["x"]).to(torch.bfloat16).pin_memory()
+    hz = torch.empty(tuple(outs[0][0].shape), dtype=outs[0][0].dtype).pin_memory()
+    n_e2e = max(3, min(args.steps, 20))
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    s0.record(stream)
+    for i in range(n_e2e):
+        sets[0]["x"].copy_(hx, non_blocking=True)
+        layer(sets[0], outs[0])
+        hz.copy_(outs[0][0], non_blocking=True)
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(world, s0.elapsed_time(s1)) / n_e2e
+    clocks.stop()
+
+    peaks = load_peaks()
+    achieved = proj_flops / (ms_proj * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"], "traffic": measured_traffic("ttt_qkv_proj", cfg.name + "_proj"),
+            "peak_source": peaks["source"], "kernel": "ttt_qkv_proj", "algorithmic_flops": proj_flops,
+            "ms_per_call": ms_proj, "roofline_ms": proj_flops / (peaks["bf16_tflops"] * 1e12) * 1e3}
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": cfg.name + "+proj+gate" + learner_tag, "kind": cfg.kind, "B": B, "H": H,
+                           "L": L, "d": d, "d_model": Dx, "mini_batch": cfg.mini_batch, "io": "bf16",
+                           "step": "ttt_qkv_proj + ttt_eta_gate + scan from the layer input x",
+                           "l2": "two input/output sets; each step writes 3 B H L d bf16 (> L2)",
+                           "parallelism": f"replica x{world}"},
+                "roofline": roof, "cpu_baseline": None,
+                "e2e": {"value": world * cfg.tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                        "h2d_bytes_per_step": int(hx.numel() * hx.element_size()),
+                        "d2h_bytes_per_step": int(hz.numel() * hz.element_size())},
+                "gpu_launches": args.steps * 3, "clocks": clk}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -900,6 +1023,9 @@ def main():
     ap.add_argument("--gated", action="store_true",
                     help="each step also computes eta from the layer input with the learning-rate "
                          "gate (ttt_eta_gate) before the scan")
+    ap.add_argument("--project", action="store_true",
+                    help="time the whole layer from its input tokens: the input projections "
+                         "(ttt_qkv_proj), the gate and the scan per step (a gated bf16 workload)")
     ap.add_argument("--soak-ms", type=float, default=1500.0,
                     help="untimed load before the timed region, so the clock samples describe "
                          "this workload (0 under a profiler)")
@@ -919,6 +1045,8 @@ def main():
             run_decode(args, cfg, world, rank, local)
         elif args.backward:
             run_backward(args, cfg, world, rank, local)
+        elif args.project:
+            run_project(args, cfg, world, rank, local)
         else:
             run_ours(args, cfg, world, rank, local)
     finally:

@@ -239,6 +239,23 @@ TTT_API ttt_status ttt_eta_gate(int B, int H, int L, int d_model, ttt_dtype x_dt
                                 ttt_stream_t stream);
 
 /*
+ * The TTT layer's input projections (the views theta_Q x, theta_K x, theta_V x of the
+ * layer's input tokens, lryc.cn TTT article, section 2.2), written in the layout the scan
+ * reads:
+ *   Q[b, h, t, j] = sum_i x[b, t, i] W[h d + j, i],  K from rows H d + h d + j,
+ *   V from rows 2 H d + h d + j.
+ *   in : x [B, L, d_model] bf16; W [3 H d, d_model] bf16 (the three projection matrices
+ *        stacked, one row per output unit, as a linear layer stores its weight);
+ *   out: Q, K, V [B, H, L, d] bf16 (fp32 accumulation, rounded once).
+ * Supported: d = 64, d_model a multiple of 64, 3 H d a multiple of 256 (tcgen05 kernel);
+ * otherwise TTT_ERR_UNSUPPORTED.  x, W, Q, K, V 16-byte aligned; the outputs may overlap
+ * neither each other nor an input.  A bounded wait that runs out is reported by
+ * ttt_sync_status.
+ */
+TTT_API ttt_status ttt_qkv_proj(int B, int H, int L, int d_model, int d, const void *x, const void *W,
+                                void *Q, void *K, void *V, ttt_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports TTT_ERR_CUDA if a CUDA error is pending
  * and TTT_ERR_TIMEOUT if any kernel launched by this library on the stream's
  * device (the current device for the legacy default stream) since the previous
@@ -278,7 +295,7 @@ TTT_API const char *ttt_kernel_name(const ttt_desc *desc, int is_mlp);
 
 /* Library ABI version (major * 100 + minor); 101 added bh_offset/bh_count, 102 loss and
  * weight_decay, 103 ttt_linear_bwd, 104 its residual-LayerNorm form (gamma, beta, dgamma,
- * dbeta arguments), 105 the per-call status word (ttt_desc.status). */
+ * dbeta arguments), 105 the per-call status word (ttt_desc.status), 106 ttt_qkv_proj. */
 TTT_API int ttt_version(void);
 
 #ifdef __cplusplus

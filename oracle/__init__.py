@@ -108,6 +108,21 @@ def eta_gate(x, theta, eta_base: float):
     return eta
 
 
+def qkv_proj(x, W, H: int, d: int):
+    """The layer's input projections (the views theta_Q x, theta_K x, theta_V x of the lryc.cn
+    TTT article, section 2.2): for tokens x [B, L, Dx] and the stacked projection matrices
+    W [3 H d, Dx] (row n = one output unit), Q[b, h, t, j] = sum_i x[b, t, i] W[h d + j, i],
+    K from rows H d + h d + j, V from rows 2 H d + h d + j; each [B, H, L, d], float64.
+    (A library matrix product; pinned against a plain triple loop.)"""
+    x, W = _f64(x), _f64(W)
+    B, L, Dx = x.shape
+    if W.shape != (3 * H * d, Dx):
+        raise ValueError("W must be [3 H d, Dx]")
+    Y = np.matmul(x, W.T)                                   # [B, L, 3 H d]
+    return tuple(Y[..., k * H * d:(k + 1) * H * d].reshape(B, L, H, d).transpose(0, 2, 1, 3).copy()
+                 for k in range(3))
+
+
 # --------------------------------------------------------------------------
 # elementwise pieces and per-token losses/gradients (for the FD pins)
 # --------------------------------------------------------------------------

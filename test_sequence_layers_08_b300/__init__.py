@@ -24,7 +24,7 @@ import threading
 
 __all__ = ["TTTError", "Desc", "load", "library_path", "partition_rows", "ttt_eta_gate", "ttt_linear_fwd", "ttt_mlp_fwd", "ttt_linear_step",
            "ttt_linear_bwd", "ttt_linear_bwd_workspace_size", "ttt_linear_bwd_static",
-           "ttt_sync_status", "kernel_name", "version", "STATUS", "set_wait_timeout_ns",
+           "ttt_qkv_proj", "ttt_sync_status", "kernel_name", "version", "STATUS", "set_wait_timeout_ns",
            "debug_withhold_loads"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -85,6 +85,8 @@ def load():
             lib.ttt_linear_bwd_workspace_size.argtypes = [dp]
             lib.ttt_eta_gate.restype = ctypes.c_int
             lib.ttt_eta_gate.argtypes = [ctypes.c_int] * 5 + [ctypes.c_float] + [vp] * 4
+            lib.ttt_qkv_proj.restype = ctypes.c_int
+            lib.ttt_qkv_proj.argtypes = [ctypes.c_int] * 5 + [vp] * 6
             lib.ttt_sync_status.restype = ctypes.c_int
             lib.ttt_sync_status.argtypes = [vp]
             lib.ttt_status_string.restype = ctypes.c_char_p
@@ -451,6 +453,34 @@ def ttt_eta_gate(x, theta, eta_base: float, *, out=None, stream=None):
     _check(lib.ttt_eta_gate(B, H, L, Dx, io, float(eta_base), _ptr(x), _ptr(theta), _ptr(eta),
                             _stream_handle(stream)))
     return eta
+
+
+def ttt_qkv_proj(x, W, heads: int, d: int = 64, *, out=None, stream=None):
+    """The layer's input projections on the GPU (tcgen05): x [B, L, d_model] bfloat16 and the
+    stacked projection matrices W [3 heads d, d_model] bfloat16 (one row per output unit, as
+    a linear layer stores its weight) give (Q, K, V), each [B, heads, L, d] bfloat16, the
+    layout the scan reads.  Pass ``out=(Q, K, V)`` to reuse buffers.  Asynchronous on
+    ``stream``."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.dim() != 3:
+        raise ValueError("x must be a [B, L, d_model] tensor")
+    B, L, Dx = x.shape
+    dev = x.device
+    _expect("x", x, (B, L, Dx), torch.bfloat16, dev)
+    _expect("W", W, (3 * heads * d, Dx), torch.bfloat16, dev)
+    shape = (B, heads, L, d)
+    if out is not None:
+        if len(out) != 3:
+            raise ValueError("out must hold (Q, K, V)")
+        for name, t in zip("QKV", out):
+            _expect("out " + name, t, shape, torch.bfloat16, dev)
+    _require_cuda(dev)
+    lib = load()
+    Q, K, V = out if out is not None else tuple(torch.empty(shape, device=dev, dtype=torch.bfloat16)
+                                                for _ in range(3))
+    _check(lib.ttt_qkv_proj(B, heads, L, Dx, d, _ptr(x), _ptr(W), _ptr(Q), _ptr(K), _ptr(V),
+                            _stream_handle(stream)))
+    return Q, K, V
 
 
 def set_wait_timeout_ns(ns: int):

@@ -154,7 +154,7 @@ const char *mlp_kernel(const ttt_desc &s)
 
 extern "C" {
 
-int ttt_version(void) { return 105; }
+int ttt_version(void) { return 106; }
 
 const char *ttt_status_string(ttt_status s)
 {
@@ -432,6 +432,39 @@ ttt_status ttt_eta_gate(int B, int H, int L, int d_model, ttt_dtype x_dtype, flo
     if (st != TTT_OK) return st;
     cudaError_t e = ttt::launch_eta_gate(a);
     if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "eta gate launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+ttt_status ttt_qkv_proj(int B, int H, int L, int d_model, int d, const void *x, const void *W, void *Q,
+                        void *K, void *V, ttt_stream_t stream)
+{
+    if (B <= 0 || H <= 0 || L <= 0 || d_model <= 0 || d <= 0)
+        return fail(TTT_ERR_INVALID_ARG, "B, H, L, d_model and d must be positive");
+    if ((long long)B * L > 0x7fffffffLL || 3LL * H * d > 0x7fffffffLL || (long long)B * H * L * d > (1LL << 40))
+        return fail(TTT_ERR_INVALID_ARG, "the sizes exceed the supported range");
+    ttt_status st;
+    const void *ptrs[] = {x, W, Q, K, V};
+    const char *names[] = {"x", "W", "Q", "K", "V"};
+    for (int i = 0; i < 5; ++i)
+        if ((st = check_ptr(ptrs[i], names[i])) != TTT_OK) return st;
+    if (!ttt::qkv_proj_supported(B, H, L, d_model, d))
+        return fail(TTT_ERR_UNSUPPORTED, "the projection kernel takes d = 64, d_model a multiple of 64 and "
+                                         "3 H d a multiple of 256 (B=%d H=%d d_model=%d d=%d)", B, H, d_model, d);
+    const size_t nx = (size_t)B * L * d_model * 2, nw = (size_t)3 * H * d * d_model * 2, no = (size_t)B * H * L * d * 2;
+    const Range outs[] = {range_of(Q, no), range_of(K, no), range_of(V, no)};
+    const Range ins[] = {range_of(x, nx), range_of(W, nw)};
+    for (int o = 0; o < 3; ++o) {
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlap(outs[o], outs[o2])) return fail(TTT_ERR_INVALID_ARG, "Q, K, V overlap");
+        for (const Range &r : ins)
+            if (overlap(outs[o], r)) return fail(TTT_ERR_INVALID_ARG, "an output overlaps an input");
+    }
+    ttt::ProjArgs a{B, H, L, d_model, d, x, W, static_cast<__nv_bfloat16 *>(Q), static_cast<__nv_bfloat16 *>(K),
+                    static_cast<__nv_bfloat16 *>(V), reinterpret_cast<cudaStream_t>(stream), nullptr};
+    a.status = failure_flag(&st);
+    if (st != TTT_OK) return st;
+    cudaError_t e = ttt::launch_qkv_proj(a);
+    if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "projection launch: %s", cudaGetErrorString(e));
     return ok();
 }
 

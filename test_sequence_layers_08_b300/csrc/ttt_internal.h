@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 
@@ -71,6 +72,18 @@ struct GateArgs {
     cudaStream_t stream;
     unsigned int *status;
 };
+
+// One input-projection call: Q, K, V [B, H, L, d] (bf16) from x [B, L, Dx] and the stacked
+// projection matrices W [3 H d, Dx] (bf16).
+struct ProjArgs {
+    int B, H, L, Dx, d;
+    const void *x, *W;
+    __nv_bfloat16 *Q, *K, *V;
+    cudaStream_t stream;
+    unsigned int *status;
+};
+bool qkv_proj_supported(int B, int H, int L, int Dx, int d);
+cudaError_t launch_qkv_proj(const ProjArgs &a);
 
 // Gate kernels: warp-MMA kernel for bf16 tokens (H <= 32, Dx % 16 == 0), FP32 otherwise.
 bool gate_mma_supported(int H, int Dx, ttt_dtype x_dtype);

@@ -283,3 +283,29 @@ def test_backward_declared_and_checked(lib):
     q = bwd_ptrs()
     q[17] = q[6]                                  # dgamma on top of gamma
     assert call_bwd(lib, desc(residual_ln=1), q) == 1
+
+
+def test_projection_declared_and_checked(lib):
+    """ttt_qkv_proj: unsupported shapes, NULL, misaligned or overlapping buffers are rejected
+    before any launch."""
+    assert "ttt_qkv_proj" in header_functions()
+    p = [FAKE + i * (1 << 30) for i in range(5)]   # x W Q K V
+    call = lambda B=2, H=4, L=256, Dx=128, d=64, q=None: lib.ttt_qkv_proj(
+        B, H, L, Dx, d, *[ctypes.c_void_p(v) if v else None for v in (q or p)], None)
+    assert call(d=32) == 2                          # d = 64 only
+    assert call(Dx=96) == 2                         # d_model a multiple of 64
+    assert call(H=3) == 2                           # 3 H d = 576: no multiple of 256
+    assert call(B=0) == 1
+    for i in range(5):
+        q = list(p)
+        q[i] = 0
+        assert call(q=q) == 1, i
+    q = list(p)
+    q[2] += 8                                       # Q misaligned
+    assert call(q=q) == 1
+    q = list(p)
+    q[3] = q[2]                                     # K on top of Q
+    assert call(q=q) == 1
+    q = list(p)
+    q[4] = q[0]                                     # V on top of x
+    assert call(q=q) == 1

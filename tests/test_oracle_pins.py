@@ -555,3 +555,36 @@ def test_inner_product_gradients_by_finite_differences(ln):
         args_m = (W1 if M is not W1 else Mm, b1, W2 if M is not W2 else Mm, b2)
         fd = (oracle.mlp_token_loss(k, v, *args_p, **kw) - oracle.mlp_token_loss(k, v, *args_m, **kw)) / (2 * h)
         assert abs(fd - G[ij]) <= 1e-6 * max(1.0, abs(fd))
+
+
+def test_qkv_projection_against_a_triple_loop():
+    """The input projections (lryc.cn TTT article, section 2.2: Q, K, V as views of the
+    layer's input tokens) against a plain triple loop on a tiny case with every dimension
+    distinct (a transposed weight or a swapped Q/K/V slice fails it)."""
+    rng = np.random.default_rng(3)
+    B, L, Dx, H, d = 2, 3, 5, 2, 3
+    x = rng.standard_normal((B, L, Dx))
+    W = rng.standard_normal((3 * H * d, Dx))
+    got = oracle.qkv_proj(x, W, H, d)
+    for k in range(3):
+        want = np.zeros((B, H, L, d))
+        for b in range(B):
+            for h in range(H):
+                for t in range(L):
+                    for j in range(d):
+                        n = k * H * d + h * d + j
+                        want[b, h, t, j] = sum(x[b, t, i] * W[n, i] for i in range(Dx))
+        np.testing.assert_allclose(got[k], want, rtol=1e-12, atol=1e-12)
+
+
+def test_qkv_projection_selection_matrix_copies_features():
+    """W selecting input features (row n picks feature n mod Dx) makes Q, K, V copies of x."""
+    rng = np.random.default_rng(4)
+    B, L, H, d = 1, 4, 2, 4
+    Dx = 3 * H * d
+    x = rng.standard_normal((B, L, Dx))
+    W = np.eye(3 * H * d, Dx)
+    Q, K, V = oracle.qkv_proj(x, W, H, d)
+    for k, out in enumerate((Q, K, V)):
+        for h in range(H):
+            np.testing.assert_array_equal(out[0, h], x[0, :, k * H * d + h * d:k * H * d + (h + 1) * d])
