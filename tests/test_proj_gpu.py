@@ -32,8 +32,10 @@ def run(x, W, H, d):
     return [o.float().cpu().numpy().astype(np.float64) for o in out]
 
 
-@pytest.mark.parametrize("B,L,Dx,H", [(2, 256, 128, 4), (1, 200, 64, 4), (3, 128, 768, 8), (2, 384, 256, 12)],
-                         ids=["small", "ragged_tokens", "d_model768", "twelve_heads"])
+@pytest.mark.parametrize("B,L,Dx,H", [(2, 256, 128, 4), (1, 200, 64, 4), (3, 128, 768, 8), (2, 384, 256, 12),
+                                      (1, 96, 192, 4), (3, 20, 64, 4), (2, 1000, 128, 4)],
+                         ids=["small", "ragged_tokens", "d_model768", "twelve_heads", "one_tile_short_k",
+                              "short_sequences", "sequences_cross_groups"])
 def test_projection_matches_oracle(B, L, Dx, H):
     d = 64
     x, W = problem(B, L, Dx, H, d, seed=B * L + Dx + H)
