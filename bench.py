@@ -72,7 +72,8 @@ def algorithmic_bytes(cfg) -> float:
 
 
 KERNEL_SOURCES = {"ttt_linear_fused": "ttt_linear_tc.cu", "ttt_linear_chunked": "ttt_linear_chunk.cu",
-                  "ttt_mlp_fused": "ttt_mlp_tc.cu", "ttt_linear_decode": "ttt_decode.cu",
+                  "ttt_mlp_fused": "ttt_mlp_tc.cu", "ttt_mlp_tmem": "ttt_mlp_tmem.cu",
+                  "ttt_linear_decode": "ttt_decode.cu",
                   "ttt_linear_bwd": "ttt_backward.cu",
                   "ttt_linear_generic": "ttt_generic.cu", "ttt_mlp_generic": "ttt_generic.cu",
                   "ttt_linear_cols": "ttt_linear_cols.cu", "ttt_qkv_proj": "ttt_proj.cu"}
@@ -1026,10 +1027,15 @@ def main():
     ap.add_argument("--project", action="store_true",
                     help="time the whole layer from its input tokens: the input projections "
                          "(ttt_qkv_proj), the gate and the scan per step (a gated bf16 workload)")
+    ap.add_argument("--mlp-kernel", choices=["fused", "tmem"], default=None,
+                    help="TTT-MLP kernel: the warp-MMA one (default) or the tcgen05 one with the "
+                         "fast weights in tensor memory (sets TTT_MLP_KERNEL)")
     ap.add_argument("--soak-ms", type=float, default=1500.0,
                     help="untimed load before the timed region, so the clock samples describe "
                          "this workload (0 under a profiler)")
     args = ap.parse_args()
+    if args.mlp_kernel:
+        os.environ["TTT_MLP_KERNEL"] = args.mlp_kernel
     if args.warmup < 3:
         args.warmup = 3
     cfg = CONFIGS[args.workload]

@@ -139,7 +139,10 @@ TTT_API ttt_status ttt_linear_fwd(const ttt_desc *desc, const void *Q, const voi
  *   out: Z [B,H,L,d]; W1_f [B,H,d,dh]; b1_f [B,H,dh]; W2_f [B,H,dh,d]; b2_f [B,H,d].
  * Supported: d <= 128, dh <= 512, b <= 64 while the state fits on chip; the
  * tensor-core kernel (bf16, d = 64, dh = 256, b = 16) and the generic kernel run every
- * loss and decay.
+ * loss and decay.  With TTT_MLP_KERNEL=tmem in the environment (read at each call), bf16
+ * calls with d = 64, dh = 256, b = 16 and no weight decay run the tcgen05 kernel instead:
+ * W1^T and W2 resident in tensor memory as fp32, the hidden-width products on tcgen05 (same
+ * results within bf16 rounding; slower at b = 16, hence not the default).
  */
 TTT_API ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const void *V,
                        const float *eta, const float *W1_0, const float *b1_0,

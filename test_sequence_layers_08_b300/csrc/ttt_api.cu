@@ -9,6 +9,8 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 
 #include "ttt_internal.h"
 
@@ -143,9 +145,20 @@ const char *linear_kernel(const ttt_desc &s)
     return nullptr;
 }
 
+constexpr const char *kMlpTmem = "ttt_mlp_tmem", *kMlpFused = "ttt_mlp_fused";
+
+// TTT_MLP_KERNEL=tmem in the environment selects the tcgen05 kernel (fast weights in tensor
+// memory) where it applies; by default the warp-MMA kernel runs, which is faster at b = 16.
+bool mlp_tmem_requested()
+{
+    const char *v = std::getenv("TTT_MLP_KERNEL");
+    return v && std::strcmp(v, "tmem") == 0;
+}
+
 const char *mlp_kernel(const ttt_desc &s)
 {
-    if (ttt::mlp_tc_supported(s)) return "ttt_mlp_fused";
+    if (ttt::mlp_tmem_supported(s) && mlp_tmem_requested()) return kMlpTmem;
+    if (ttt::mlp_tc_supported(s)) return kMlpFused;
     if (ttt::mlp_generic_smem_bytes(s)) return "ttt_mlp_generic";
     return nullptr;
 }
@@ -400,7 +413,9 @@ ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const
                    W1_f, b1_f, W2_f, b2_f, reinterpret_cast<cudaStream_t>(stream), nullptr};
     a.status = s.status ? s.status : failure_flag(&st);
     if (st != TTT_OK) return st;
-    cudaError_t e = ttt::mlp_tc_supported(s) ? ttt::launch_mlp_tc(a) : ttt::launch_mlp_generic(a);
+    cudaError_t e = kname == kMlpTmem    ? ttt::launch_mlp_tmem(a)
+                    : kname == kMlpFused ? ttt::launch_mlp_tc(a)
+                                         : ttt::launch_mlp_generic(a);
     if (e != cudaSuccess) return fail(TTT_ERR_CUDA, "%s launch: %s", kname, cudaGetErrorString(e));
     return ok();
 }

@@ -121,6 +121,10 @@ cudaError_t launch_linear_decode(const DecodeArgs &a);
 // Tensor-core TTT-MLP kernel (bf16 I/O, d = 64, d_hidden = 256, b = 16).
 bool mlp_tc_supported(const ttt_desc &d);
 cudaError_t launch_mlp_tc(const MlpArgs &a);
+// TTT-MLP with the hidden-width products on tcgen05 and W1^T, W2 resident in tensor memory
+// (bf16 I/O, d = 64, d_hidden = 256, b = 16, no weight decay).
+bool mlp_tmem_supported(const ttt_desc &d);
+cudaError_t launch_mlp_tmem(const MlpArgs &a);
 // Test hooks of the bounded waits (process-wide; see ttt.h), read by both fused kernels.
 void set_wait_timeout_ns(long long ns);
 void set_withhold_loads(int on);

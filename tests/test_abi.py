@@ -214,8 +214,8 @@ def test_partition_fields_accepted(lib):
 
 def test_variant_kernel_choice(lib):
     """The tensor-core kernels run both inner-learner variants: for TTT-Linear the chunked
-    kernel without the residual LayerNorm and the fused one with it, for TTT-MLP the fused
-    kernel."""
+    kernel without the residual LayerNorm and the fused one with it; for TTT-MLP the tcgen05
+    kernel (on request) the inner-product loss, the warp-MMA kernel both."""
     k = lambda mlp, **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), mlp))
     for var in (dict(loss=1), dict(weight_decay=0.1), dict(loss=1, weight_decay=0.1)):
         assert k(0, **var) == "ttt_linear_chunked"
@@ -309,3 +309,17 @@ def test_projection_declared_and_checked(lib):
     q = list(p)
     q[4] = q[0]                                     # V on top of x
     assert call(q=q) == 1
+
+
+def test_mlp_tmem_kernel_on_request(lib, monkeypatch):
+    """TTT_MLP_KERNEL=tmem selects the tcgen05 TTT-MLP kernel where it applies (bf16, d = 64,
+    d_hidden = 256, b = 16, no weight decay); anything else keeps the default choice."""
+    m = lambda **kw: (lambda n: n and n.decode())(lib.ttt_kernel_name(ctypes.byref(desc(**kw)), 1))
+    monkeypatch.setenv("TTT_MLP_KERNEL", "tmem")
+    assert m() == "ttt_mlp_tmem"
+    assert m(residual_ln=1, d_hidden=256) == "ttt_mlp_tmem"
+    assert m(loss=1) == "ttt_mlp_tmem"
+    assert m(weight_decay=0.1) == "ttt_mlp_fused"
+    assert m(io_dtype=0) == "ttt_mlp_generic"
+    monkeypatch.setenv("TTT_MLP_KERNEL", "fused")
+    assert m() == "ttt_mlp_fused"

@@ -26,10 +26,11 @@ VARIANTS = [("ip", 0.0), ("mse", 0.5), ("ip", 0.5)]
 VID = lambda v: f"{v[0]}-wd{v[1]}"
 
 
-def kernel(cfg, mlp=False):
+def kernel(cfg, mlp=False, loss="mse", weight_decay=0.0):
     dev = torch.empty((cfg.B, cfg.H, cfg.L, cfg.d),
                       dtype=torch.bfloat16 if cfg.io == "bf16" else torch.float32)
-    desc = ttt.make_desc(dev, cfg.mini_batch, cfg.ln, cfg.eps, d_hidden=cfg.dh if mlp else 0)
+    desc = ttt.make_desc(dev, cfg.mini_batch, cfg.ln, cfg.eps, d_hidden=cfg.dh if mlp else 0,
+                         loss=loss, weight_decay=weight_decay)
     return ttt.kernel_name(desc, mlp)
 
 
@@ -111,7 +112,7 @@ def test_full_size_mlp_variants(variant):
     sampled (batch, head)."""
     loss, wd = variant
     cfg = MLP
-    assert kernel(cfg, mlp=True) == "ttt_mlp_fused"
+    assert kernel(cfg, mlp=True, loss=loss, weight_decay=wd) == "ttt_mlp_fused"
     x = inputs(cfg, seed=0)
     got = run_gpu(cfg, to_device(cfg, x), loss=loss, weight_decay=wd)
     pairs = sample_pairs(cfg, 2, seed=11)
