@@ -880,7 +880,11 @@ def run_project(args, cfg, world, rank, local):
     the learning-rate gate (ttt_eta_gate) and the scan, on a gated workload (x [B, L, 768],
     seeded random projection matrices [3 H d, 768] ~ N(0, 1/768)).  Consecutive steps rotate
     over two input/output sets (each step writes 3 B H L d bf16 of Q, K, V: more than L2).
-    The projection call is also timed alone: its roofline is the bf16 tensor peak."""
+    Steps are pipelined: the scan of step i runs on a high-priority stream and holds one SM
+    per (batch, head); the projections and gate of step i + 1 run beside it on a low-priority
+    stream, their grids capped at the SMs the scan leaves idle (every step's work is in the
+    timed region, the first step's projections included).  The projection call is also timed
+    alone: its roofline is the bf16 tensor peak."""
     import torch
     import test_sequence_layers_08_b300 as ttt
     if cfg.eta != "gate" or cfg.io != "bf16":
@@ -908,43 +912,94 @@ def run_project(args, cfg, world, rank, local):
         return t
     sets = [make_set() for _ in range(2)]
     stream = torch.cuda.current_stream(dev)
-    kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps, stream=stream, **variant)
+    # the scan on a high-priority stream, the next step's projections and gate beside it
+    s_scan = torch.cuda.Stream(dev, priority=-1)
+    s_side = torch.cuda.Stream(dev, priority=0)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    scan_ctas = B * H   # one CTA per (batch, head)
+    side_sms = n_sm - scan_ctas if scan_ctas <= n_sm - 16 else 0   # 0: no cap (all SMs)
 
-    def layer(t, out=None):
-        Q, K, V = ttt.ttt_qkv_proj(t["x"], W, H, d, out=t["qkv"], stream=stream)
-        ttt.ttt_eta_gate(t["x"], theta, x["eta_base"], out=t["eta"], stream=stream)
+    def prep(t, st, cap=0):
+        ttt.ttt_qkv_proj(t["x"], W, H, d, out=t["qkv"], stream=st, max_sms=cap)
+        ttt.ttt_eta_gate(t["x"], theta, x["eta_base"], out=t["eta"], stream=st, max_sms=cap)
+
+    def scan(t, st, out=None):
+        kw = dict(mini_batch=cfg.mini_batch, residual_ln=cfg.ln, ln_eps=cfg.eps, stream=st, **variant)
+        Q, K, V = t["qkv"]
         if cfg.kind == "linear":
             return ttt.ttt_linear_fwd(Q, K, V, t["eta"], state["W0"], state["b0"], state["gamma"],
                                       state["beta"], out=out, **kw)
         return ttt.ttt_mlp_fwd(Q, K, V, t["eta"], state["W1"], state["b1"], state["W2"], state["b2"],
                                state["gamma"], state["beta"], out=out, **kw)
 
+    def layer(t, out=None):   # one step, serial on the current stream
+        prep(t, stream)
+        return scan(t, stream, out)
+
+    ev_prep = [torch.cuda.Event() for _ in range(2)]
+    ev_scan = [torch.cuda.Event() for _ in range(2)]
+
+    def pipeline(nsteps, first=None):
+        """nsteps layer steps: scan i on s_scan, projections and gate of step i + 1 on s_side
+        once scan i - 1 no longer reads their set.  Starts after `first` (an event on the
+        current stream) and everything queued before; ends with the current stream waiting
+        for both."""
+        s_scan.wait_stream(stream)
+        s_side.wait_stream(stream)
+        if first is not None:
+            s_scan.wait_event(first)
+            s_side.wait_event(first)
+        prep(sets[0], s_side, side_sms)
+        ev_prep[0].record(s_side)
+        for i in range(nsteps):
+            b = i % 2
+            s_scan.wait_event(ev_prep[b])
+            scan(sets[b], s_scan, outs[b])
+            ev_scan[b].record(s_scan)
+            if i + 1 < nsteps:
+                nb = (i + 1) % 2
+                if i >= 1:
+                    s_side.wait_event(ev_scan[nb])
+                prep(sets[nb], s_side, side_sms)
+                ev_prep[nb].record(s_side)
+        stream.wait_stream(s_scan)
+        stream.wait_stream(s_side)
+
     outs = [layer(t) for t in sets]
     ttt.ttt_sync_status(stream)
     clocks = ClockSampler(local)
     clocks.start()
-    for i in range(args.warmup):
-        layer(sets[i % 2], outs[i % 2])
+    pipeline(max(2, args.warmup))
     ttt.ttt_sync_status(stream)
     t_soak = time.time()
     soak_end = time.time() + args.soak_ms / 1e3
-    i = 0
     while time.time() < soak_end:
-        layer(sets[i % 2], outs[i % 2])
-        i += 1
-        if i % 16 == 0:
-            torch.cuda.synchronize(dev)
+        pipeline(16)
+        torch.cuda.synchronize(dev)
     barrier(world)
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for i in range(args.steps):
-        layer(sets[i % 2], outs[i % 2])
+    pipeline(args.steps, first=start)
     end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     ttt.ttt_sync_status(stream)
     ms_step = max_over_ranks(world, start.elapsed_time(end)) / args.steps
+    # the same steps one after another on one stream (no overlap), for comparison
+    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    q0.record(stream)
+    for i in range(args.steps):
+        layer(sets[i % 2], outs[i % 2])
+    q1.record(stream)
+    torch.cuda.synchronize(dev)
+    ttt.ttt_sync_status(stream)
+    ms_serial = max_over_ranks(world, q0.elapsed_time(q1)) / args.steps
+    # the faster of the two schedules is the step (both run every step's whole work); the
+    # overlap pays when the capped projections and gate take less than the scan
+    ms_pipe = ms_step
+    pipelined = ms_pipe <= ms_serial
+    ms_step = min(ms_pipe, ms_serial)
     # the projection call alone (same rotation)
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     p0.record(stream)
@@ -987,6 +1042,11 @@ def run_project(args, cfg, world, rank, local):
                 "config": {"workload": cfg.name + "+proj+gate" + learner_tag, "kind": cfg.kind, "B": B, "H": H,
                            "L": L, "d": d, "d_model": Dx, "mini_batch": cfg.mini_batch, "io": "bf16",
                            "step": "ttt_qkv_proj + ttt_eta_gate + scan from the layer input x",
+                           "schedule": ((f"pipelined: step i + 1's projections and gate beside the scan of step i, "
+                                         f"capped at {side_sms or n_sm} SMs (serial: {ms_serial * 1e3:.1f} us per step)")
+                                        if pipelined else
+                                        (f"serial on one stream (pipelined with the projections and gate capped at "
+                                         f"{side_sms or n_sm} SMs: {ms_pipe * 1e3:.1f} us per step)")),
                            "l2": "two input/output sets; each step writes 3 B H L d bf16 (> L2)",
                            "parallelism": f"replica x{world}"},
                 "roofline": roof, "cpu_baseline": None,

@@ -234,12 +234,14 @@ TTT_API ttt_status ttt_linear_bwd_static(const ttt_desc *desc, const void *Q, co
  *   out: eta [B, H, L] float -- the eta the scan entry points take.
  * The contraction is carried in fp32 (bf16 tokens meet theta split into two bf16
  * parts, so theta keeps ~16 mantissa bits).  bf16 tokens need d_model % 8 == 0.
- * eta must not overlap x or theta.  Errors as for the other entry points; a
- * bounded wait that runs out is reported by ttt_sync_status.
+ * eta must not overlap x or theta.  max_sms > 0 caps the grid at that many SMs' worth of
+ * CTAs (0: every SM), so that the call can run beside a scan that holds the other SMs;
+ * max_sms < 0 is TTT_ERR_INVALID_ARG.  Errors as for the other entry points; a bounded wait
+ * that runs out is reported by ttt_sync_status.
  */
 TTT_API ttt_status ttt_eta_gate(int B, int H, int L, int d_model, ttt_dtype x_dtype,
                                 float eta_base, const void *x, const float *theta, float *eta,
-                                ttt_stream_t stream);
+                                int max_sms, ttt_stream_t stream);
 
 /*
  * The TTT layer's input projections (the views theta_Q x, theta_K x, theta_V x of the
@@ -252,11 +254,12 @@ TTT_API ttt_status ttt_eta_gate(int B, int H, int L, int d_model, ttt_dtype x_dt
  *   out: Q, K, V [B, H, L, d] bf16 (fp32 accumulation, rounded once).
  * Supported: d = 64, d_model a multiple of 64, 3 H d a multiple of 256 (tcgen05 kernel);
  * otherwise TTT_ERR_UNSUPPORTED.  x, W, Q, K, V 16-byte aligned; the outputs may overlap
- * neither each other nor an input.  A bounded wait that runs out is reported by
- * ttt_sync_status.
+ * neither each other nor an input.  max_sms > 0 caps the persistent grid at that many SMs
+ * (0: every SM), for a call that runs beside a scan holding the other SMs; max_sms < 0 is
+ * TTT_ERR_INVALID_ARG.  A bounded wait that runs out is reported by ttt_sync_status.
  */
 TTT_API ttt_status ttt_qkv_proj(int B, int H, int L, int d_model, int d, const void *x, const void *W,
-                                void *Q, void *K, void *V, ttt_stream_t stream);
+                                void *Q, void *K, void *V, int max_sms, ttt_stream_t stream);
 
 /*
  * Synchronises `stream`, then reports TTT_ERR_CUDA if a CUDA error is pending
@@ -298,7 +301,8 @@ TTT_API const char *ttt_kernel_name(const ttt_desc *desc, int is_mlp);
 
 /* Library ABI version (major * 100 + minor); 101 added bh_offset/bh_count, 102 loss and
  * weight_decay, 103 ttt_linear_bwd, 104 its residual-LayerNorm form (gamma, beta, dgamma,
- * dbeta arguments), 105 the per-call status word (ttt_desc.status), 106 ttt_qkv_proj. */
+ * dbeta arguments), 105 the per-call status word (ttt_desc.status), 106 ttt_qkv_proj, 107 the
+ * max_sms argument of ttt_eta_gate and ttt_qkv_proj. */
 TTT_API int ttt_version(void);
 
 #ifdef __cplusplus

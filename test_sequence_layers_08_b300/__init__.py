@@ -84,9 +84,9 @@ def load():
             lib.ttt_linear_bwd_workspace_size.restype = ctypes.c_size_t
             lib.ttt_linear_bwd_workspace_size.argtypes = [dp]
             lib.ttt_eta_gate.restype = ctypes.c_int
-            lib.ttt_eta_gate.argtypes = [ctypes.c_int] * 5 + [ctypes.c_float] + [vp] * 4
+            lib.ttt_eta_gate.argtypes = [ctypes.c_int] * 5 + [ctypes.c_float] + [vp] * 3 + [ctypes.c_int, vp]
             lib.ttt_qkv_proj.restype = ctypes.c_int
-            lib.ttt_qkv_proj.argtypes = [ctypes.c_int] * 5 + [vp] * 6
+            lib.ttt_qkv_proj.argtypes = [ctypes.c_int] * 5 + [vp] * 5 + [ctypes.c_int, vp]
             lib.ttt_sync_status.restype = ctypes.c_int
             lib.ttt_sync_status.argtypes = [vp]
             lib.ttt_status_string.restype = ctypes.c_char_p
@@ -428,10 +428,11 @@ def ttt_mlp_fwd(Q, K, V, eta, W1, b1, W2, b2, gamma=None, beta=None, *, mini_bat
     return Z, W1f, b1f, W2f, b2f
 
 
-def ttt_eta_gate(x, theta, eta_base: float, *, out=None, stream=None):
+def ttt_eta_gate(x, theta, eta_base: float, *, out=None, stream=None, max_sms: int = 0):
     """Per-token learning rate on the GPU: eta [B,H,L] = eta_base * sigmoid(theta[h] . x[b,t])
     for the layer input x [B,L,d_model] (float32 or bfloat16) and theta [H,d_model] float32.
-    Pass ``out=eta`` to reuse a buffer.  Asynchronous on ``stream``."""
+    Pass ``out=eta`` to reuse a buffer.  Asynchronous on ``stream``; ``max_sms`` > 0 caps the
+    grid at that many SMs (for a call beside a scan that holds the others)."""
     import torch
     if not isinstance(x, torch.Tensor) or x.dim() != 3:
         raise ValueError("x must be a [B, L, d_model] tensor")
@@ -451,16 +452,16 @@ def ttt_eta_gate(x, theta, eta_base: float, *, out=None, stream=None):
     eta = torch.empty((B, H, L), device=dev, dtype=torch.float32) if out is None else out
     io = TTT_BF16 if x.dtype == torch.bfloat16 else TTT_F32
     _check(lib.ttt_eta_gate(B, H, L, Dx, io, float(eta_base), _ptr(x), _ptr(theta), _ptr(eta),
-                            _stream_handle(stream)))
+                            int(max_sms), _stream_handle(stream)))
     return eta
 
 
-def ttt_qkv_proj(x, W, heads: int, d: int = 64, *, out=None, stream=None):
+def ttt_qkv_proj(x, W, heads: int, d: int = 64, *, out=None, stream=None, max_sms: int = 0):
     """The layer's input projections on the GPU (tcgen05): x [B, L, d_model] bfloat16 and the
     stacked projection matrices W [3 heads d, d_model] bfloat16 (one row per output unit, as
     a linear layer stores its weight) give (Q, K, V), each [B, heads, L, d] bfloat16, the
     layout the scan reads.  Pass ``out=(Q, K, V)`` to reuse buffers.  Asynchronous on
-    ``stream``."""
+    ``stream``; ``max_sms`` > 0 caps the persistent grid at that many SMs."""
     import torch
     if not isinstance(x, torch.Tensor) or x.dim() != 3:
         raise ValueError("x must be a [B, L, d_model] tensor")
@@ -479,7 +480,7 @@ def ttt_qkv_proj(x, W, heads: int, d: int = 64, *, out=None, stream=None):
     Q, K, V = out if out is not None else tuple(torch.empty(shape, device=dev, dtype=torch.bfloat16)
                                                 for _ in range(3))
     _check(lib.ttt_qkv_proj(B, heads, L, Dx, d, _ptr(x), _ptr(W), _ptr(Q), _ptr(K), _ptr(V),
-                            _stream_handle(stream)))
+                            int(max_sms), _stream_handle(stream)))
     return Q, K, V
 
 

@@ -167,7 +167,7 @@ const char *mlp_kernel(const ttt_desc &s)
 
 extern "C" {
 
-int ttt_version(void) { return 106; }
+int ttt_version(void) { return 107; }
 
 const char *ttt_status_string(ttt_status s)
 {
@@ -421,10 +421,11 @@ ttt_status ttt_mlp_fwd(const ttt_desc *desc, const void *Q, const void *K, const
 }
 
 ttt_status ttt_eta_gate(int B, int H, int L, int d_model, ttt_dtype x_dtype, float eta_base,
-                        const void *x, const float *theta, float *eta, ttt_stream_t stream)
+                        const void *x, const float *theta, float *eta, int max_sms, ttt_stream_t stream)
 {
     if (B <= 0 || H <= 0 || L <= 0 || d_model <= 0)
         return fail(TTT_ERR_INVALID_ARG, "B, H, L and d_model must be positive");
+    if (max_sms < 0) return fail(TTT_ERR_INVALID_ARG, "max_sms must be >= 0");
     if (x_dtype != TTT_F32 && x_dtype != TTT_BF16)
         return fail(TTT_ERR_INVALID_ARG, "x_dtype must be TTT_F32 or TTT_BF16");
     if (!std::isfinite(eta_base)) return fail(TTT_ERR_INVALID_ARG, "eta_base must be finite");
@@ -442,7 +443,7 @@ ttt_status ttt_eta_gate(int B, int H, int L, int d_model, ttt_dtype x_dtype, flo
         overlap(re, range_of(theta, (size_t)H * d_model * 4)))
         return fail(TTT_ERR_INVALID_ARG, "eta overlaps an input");
     ttt::GateArgs a{B, H, L, d_model, x_dtype, eta_base, x, theta, eta,
-                    reinterpret_cast<cudaStream_t>(stream), nullptr};
+                    reinterpret_cast<cudaStream_t>(stream), nullptr, max_sms};
     a.status = failure_flag(&st);
     if (st != TTT_OK) return st;
     cudaError_t e = ttt::launch_eta_gate(a);
@@ -451,10 +452,11 @@ ttt_status ttt_eta_gate(int B, int H, int L, int d_model, ttt_dtype x_dtype, flo
 }
 
 ttt_status ttt_qkv_proj(int B, int H, int L, int d_model, int d, const void *x, const void *W, void *Q,
-                        void *K, void *V, ttt_stream_t stream)
+                        void *K, void *V, int max_sms, ttt_stream_t stream)
 {
     if (B <= 0 || H <= 0 || L <= 0 || d_model <= 0 || d <= 0)
         return fail(TTT_ERR_INVALID_ARG, "B, H, L, d_model and d must be positive");
+    if (max_sms < 0) return fail(TTT_ERR_INVALID_ARG, "max_sms must be >= 0");
     if ((long long)B * L > 0x7fffffffLL || 3LL * H * d > 0x7fffffffLL || (long long)B * H * L * d > (1LL << 40))
         return fail(TTT_ERR_INVALID_ARG, "the sizes exceed the supported range");
     ttt_status st;
@@ -475,7 +477,7 @@ ttt_status ttt_qkv_proj(int B, int H, int L, int d_model, int d, const void *x, 
             if (overlap(outs[o], r)) return fail(TTT_ERR_INVALID_ARG, "an output overlaps an input");
     }
     ttt::ProjArgs a{B, H, L, d_model, d, x, W, static_cast<__nv_bfloat16 *>(Q), static_cast<__nv_bfloat16 *>(K),
-                    static_cast<__nv_bfloat16 *>(V), reinterpret_cast<cudaStream_t>(stream), nullptr};
+                    static_cast<__nv_bfloat16 *>(V), reinterpret_cast<cudaStream_t>(stream), nullptr, max_sms};
     a.status = failure_flag(&st);
     if (st != TTT_OK) return st;
     cudaError_t e = ttt::launch_qkv_proj(a);

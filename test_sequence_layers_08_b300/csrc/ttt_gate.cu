@@ -464,6 +464,7 @@ cudaError_t launch_eta_gate(const GateArgs &a)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (a.max_sms > 0) sms = min(sms, a.max_sms);   // the caller leaves the other SMs to a scan
     GateParams p{};
     p.rows = a.B * a.L;
     p.L = a.L;

@@ -71,6 +71,7 @@ struct GateArgs {
     float *eta;
     cudaStream_t stream;
     unsigned int *status;
+    int max_sms;   // > 0: at most this many SMs' worth of CTAs
 };
 
 // One input-projection call: Q, K, V [B, H, L, d] (bf16) from x [B, L, Dx] and the stacked
@@ -81,6 +82,7 @@ struct ProjArgs {
     __nv_bfloat16 *Q, *K, *V;
     cudaStream_t stream;
     unsigned int *status;
+    int max_sms;   // > 0: at most this many SMs
 };
 bool qkv_proj_supported(int B, int H, int L, int Dx, int d);
 cudaError_t launch_qkv_proj(const ProjArgs &a);

@@ -305,6 +305,7 @@ cudaError_t launch_qkv_proj(const ProjArgs &a)
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int cap = a.max_sms > 0 ? max(1, min(a.max_sms, sms) / kCluster) : sms;   // clusters
     const size_t smem = proj_smem_bytes();
     cudaError_t e = cudaFuncSetAttribute(qkv_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -331,7 +332,7 @@ cudaError_t launch_qkv_proj(const ProjArgs &a)
         }
         if (dev >= 0 && dev < 64) resident[dev].store(active, std::memory_order_relaxed);
     }
-    cfg.gridDim = dim3(kCluster * min(p.npair, active));
+    cfg.gridDim = dim3(kCluster * min(min(p.npair, active), cap));
     return cudaLaunchKernelEx(&cfg, qkv_proj_kernel, mx, mw, mq, mk, mv, p);
 }
 

@@ -160,14 +160,14 @@ def test_step_aliasing_rules(lib):
 
 
 
-def call_gate(lib, B=2, H=3, L=64, Dx=768, io=1, eta_base=0.5, ptrs=None):
+def call_gate(lib, B=2, H=3, L=64, Dx=768, io=1, eta_base=0.5, ptrs=None, max_sms=0):
     p = [FAKE + i * (1 << 30) for i in range(3)] if ptrs is None else ptrs
     return lib.ttt_eta_gate(B, H, L, Dx, io, eta_base,
-                            *[ctypes.c_void_p(x) if x else None for x in p], None)
+                            *[ctypes.c_void_p(x) if x else None for x in p], max_sms, None)
 
 
 @pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(L=-1), dict(Dx=0), dict(io=5),
-                                dict(Dx=20), dict(eta_base=float("inf"))])
+                                dict(Dx=20), dict(eta_base=float("inf")), dict(max_sms=-1)])
 def test_gate_bad_arguments(lib, kw):
     assert call_gate(lib, **kw) == 1
     assert lib.ttt_last_error().decode() != ""
@@ -290,8 +290,9 @@ def test_projection_declared_and_checked(lib):
     before any launch."""
     assert "ttt_qkv_proj" in header_functions()
     p = [FAKE + i * (1 << 30) for i in range(5)]   # x W Q K V
-    call = lambda B=2, H=4, L=256, Dx=128, d=64, q=None: lib.ttt_qkv_proj(
-        B, H, L, Dx, d, *[ctypes.c_void_p(v) if v else None for v in (q or p)], None)
+    call = lambda B=2, H=4, L=256, Dx=128, d=64, q=None, max_sms=0: lib.ttt_qkv_proj(
+        B, H, L, Dx, d, *[ctypes.c_void_p(v) if v else None for v in (q or p)], max_sms, None)
+    assert call(max_sms=-1) == 1                    # a negative SM cap
     assert call(d=32) == 2                          # d = 64 only
     assert call(Dx=96) == 2                         # d_model a multiple of 64
     assert call(H=3) == 2                           # 3 H d = 576: no multiple of 256

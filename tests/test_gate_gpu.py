@@ -25,10 +25,10 @@ def problem(B, L, H, Dx, io, seed, scale=0.02):
     return x, theta
 
 
-def run(x, theta, eta_base, io):
+def run(x, theta, eta_base, io, max_sms=0):
     dt = torch.bfloat16 if io == "bf16" else torch.float32
     eta = ttt.ttt_eta_gate(torch.from_numpy(x).cuda().to(dt), torch.from_numpy(theta).cuda(),
-                           eta_base)
+                           eta_base, max_sms=max_sms)
     ttt.ttt_sync_status()
     return eta.cpu().numpy()
 
@@ -79,3 +79,11 @@ def test_gate_reuses_output_and_stream():
         ttt.ttt_eta_gate(xd, td, 0.5, out=out, stream=s)
     ttt.ttt_sync_status(s)
     compare(out.cpu().numpy(), oracle.eta_gate(x, theta, 0.5))
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+@pytest.mark.parametrize("max_sms", [1, 7])
+def test_gate_sm_cap(io, max_sms):
+    """A grid capped at a few SMs still covers every tile of tokens."""
+    x, theta = problem(2, 700, 16, 768, io, seed=50 + max_sms)
+    compare(run(x, theta, 0.3, io, max_sms=max_sms), oracle.eta_gate(x, theta, 0.3))

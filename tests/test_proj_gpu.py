@@ -24,10 +24,10 @@ def problem(B, L, Dx, H, d, seed):
     return x, W
 
 
-def run(x, W, H, d):
+def run(x, W, H, d, max_sms=0):
     xt = torch.from_numpy(x).cuda().to(torch.bfloat16)
     Wt = torch.from_numpy(W).cuda().to(torch.bfloat16)
-    out = ttt.ttt_qkv_proj(xt, Wt, H, d)
+    out = ttt.ttt_qkv_proj(xt, Wt, H, d, max_sms=max_sms)
     ttt.ttt_sync_status()
     return [o.float().cpu().numpy().astype(np.float64) for o in out]
 
@@ -42,6 +42,21 @@ def test_projection_matches_oracle(B, L, Dx, H):
     got = run(x, W, H, d)
     ref = oracle.qkv_proj(x, W, H, d)
     case = current_case("proj")
+    for name, g, r in zip("QKV", got, ref):
+        for b in range(B):
+            for h in range(H):
+                check_scan(case, name, g[b, h], r[b, h], TOL, seq_axis=0)
+
+
+@pytest.mark.parametrize("max_sms", [1, 3, 20])
+def test_projection_sm_cap(max_sms):
+    """A capped grid (one cluster of two for max_sms 1 and 3, ten for 20) covers every tile:
+    same parity."""
+    B, L, Dx, H, d = 2, 640, 192, 4, 64
+    x, W = problem(B, L, Dx, H, d, seed=30 + max_sms)
+    got = run(x, W, H, d, max_sms=max_sms)
+    ref = oracle.qkv_proj(x, W, H, d)
+    case = current_case("proj_cap")
     for name, g, r in zip("QKV", got, ref):
         for b in range(B):
             for h in range(H):
