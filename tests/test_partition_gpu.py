@@ -20,6 +20,8 @@ CASES = {
     "linear_f32": CONFIGS["linear_ln_bf16_B4_H16_L8192"].with_(B=3, H=5, L=64, io="f32"),
     "linear_f32_noln": CONFIGS["linear_f32_B1_H2_L256"].with_(B=3, H=5, L=64),   # column split
     "mlp_ln_bf16": CONFIGS["mlp_ln_bf16_B4_H12_L4096"].with_(B=3, H=5, L=64),
+    # the tcgen05 TTT-MLP kernel (TTT_MLP_KERNEL=tmem)
+    "mlp_ln_bf16_tmem": CONFIGS["mlp_ln_bf16_B4_H12_L4096"].with_(B=3, H=5, L=64),
 }
 RANGES = [(0, 4), (4, 11), (11, 15)]
 
@@ -49,8 +51,10 @@ def call(cfg, dev, r=None, init_per_batch=False):
 
 @pytest.mark.parametrize("name", list(CASES))
 @pytest.mark.parametrize("init_per_batch", [False, True])
-def test_row_ranges_reproduce_one_call(name, init_per_batch):
+def test_row_ranges_reproduce_one_call(name, init_per_batch, monkeypatch):
     cfg = CASES[name]
+    if name.endswith("_tmem"):
+        monkeypatch.setenv("TTT_MLP_KERNEL", "tmem")
     x = inputs(cfg, seed=61)
     dev = to_device(cfg, x)
     if init_per_batch:   # a distinct initial state per (batch, head)
