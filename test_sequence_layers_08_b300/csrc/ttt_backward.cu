@@ -66,6 +66,40 @@ __device__ __forceinline__ void mm_xy(float *out, const float *X, const float *Y
                                       int n)
 {
     const int n4 = n >> 2;
+    if ((m & 1) == 0 && (k & 7) == 0 && n4 == 16 && (m >> 1) * n4 * 2 == kThreads) {
+        // A 2 x 4 block (rows r, r + 1; columns j..j+3) per pair of lanes l, l + 16, each lane
+        // summing one half of k: 6 shared loads per 32 FMAs instead of 5 per 16.  The 16 lanes
+        // of a half read one 256-byte row of Y, so no two lanes of a quarter-warp share a bank;
+        // one shuffle adds the halves, and each lane of the pair stores one row.
+        const int lane = threadIdx.x & 31, half = lane >> 4;
+        const int r = (threadIdx.x >> 5) * 2, j = (lane & 15) * 4;
+        const int kh = k >> 1, u0 = half * kh;
+        const float *x0 = X + r * k, *x1 = x0 + k;
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll
+        for (int u = u0; u < u0 + kh; u += 4) {
+            const float4 xa = f4(x0 + u), xb = f4(x1 + u);
+            const float4 w0 = f4(Y + u * n + j), w1 = f4(Y + (u + 1) * n + j);
+            const float4 w2 = f4(Y + (u + 2) * n + j), w3 = f4(Y + (u + 3) * n + j);
+            fma4(a0, xa.x, w0); fma4(a0, xa.y, w1); fma4(a0, xa.z, w2); fma4(a0, xa.w, w3);
+            fma4(a1, xb.x, w0); fma4(a1, xb.y, w1); fma4(a1, xb.z, w2); fma4(a1, xb.w, w3);
+        }
+        a0.x += __shfl_xor_sync(0xffffffffu, a0.x, 16);
+        a0.y += __shfl_xor_sync(0xffffffffu, a0.y, 16);
+        a0.z += __shfl_xor_sync(0xffffffffu, a0.z, 16);
+        a0.w += __shfl_xor_sync(0xffffffffu, a0.w, 16);
+        a1.x += __shfl_xor_sync(0xffffffffu, a1.x, 16);
+        a1.y += __shfl_xor_sync(0xffffffffu, a1.y, 16);
+        a1.z += __shfl_xor_sync(0xffffffffu, a1.z, 16);
+        a1.w += __shfl_xor_sync(0xffffffffu, a1.w, 16);
+        float4 a = half ? a1 : a0;
+        if (init) {
+            const float4 b = f4(init + j);
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+        }
+        st4(out + (r + half) * n + j, a);
+        return;
+    }
     for (int tile = threadIdx.x; tile < m * n4; tile += kThreads) {
         const int r = tile / n4, j = (tile - r * n4) * 4;
         float4 a = init ? f4(init + j) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -88,6 +122,43 @@ __device__ __forceinline__ void mm_xy2(float *outA, float *outB, const float *XA
                                       const float *initA, int m, int k, int n)
 {
     const int n4 = n >> 2;
+    if ((m & 1) == 0 && (k & 7) == 0 && n4 == 16 && (m >> 1) * n4 * 2 == kThreads) {
+        // rows r, r + 1 of both products per pair of lanes l, l + 16 splitting k (as in mm_xy):
+        // 8 shared loads per 64 FMAs
+        const int lane = threadIdx.x & 31, half = lane >> 4;
+        const int r = (threadIdx.x >> 5) * 2, j = (lane & 15) * 4;
+        const int kh = k >> 1, u0 = half * kh;
+        const float *xa = XA + r * k, *xb = XB + r * k;
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
+#pragma unroll
+        for (int u = u0; u < u0 + kh; u += 4) {
+            const float4 p0 = f4(xa + u), p1 = f4(xa + k + u), q0 = f4(xb + u), q1 = f4(xb + k + u);
+            const float4 w0 = f4(Y + u * n + j), w1 = f4(Y + (u + 1) * n + j);
+            const float4 w2 = f4(Y + (u + 2) * n + j), w3 = f4(Y + (u + 3) * n + j);
+            fma4(a0, p0.x, w0); fma4(a0, p0.y, w1); fma4(a0, p0.z, w2); fma4(a0, p0.w, w3);
+            fma4(a1, p1.x, w0); fma4(a1, p1.y, w1); fma4(a1, p1.z, w2); fma4(a1, p1.w, w3);
+            fma4(b0, q0.x, w0); fma4(b0, q0.y, w1); fma4(b0, q0.z, w2); fma4(b0, q0.w, w3);
+            fma4(b1, q1.x, w0); fma4(b1, q1.y, w1); fma4(b1, q1.z, w2); fma4(b1, q1.w, w3);
+        }
+        // each lane keeps (and stores) its own row: row r on the low half, r + 1 on the high one
+        float4 a = half ? a1 : a0, b = half ? b1 : b0;
+        const float4 ao = half ? a0 : a1, bo = half ? b0 : b1;   // the partner's row, sent over
+        a.x += __shfl_xor_sync(0xffffffffu, ao.x, 16);
+        a.y += __shfl_xor_sync(0xffffffffu, ao.y, 16);
+        a.z += __shfl_xor_sync(0xffffffffu, ao.z, 16);
+        a.w += __shfl_xor_sync(0xffffffffu, ao.w, 16);
+        b.x += __shfl_xor_sync(0xffffffffu, bo.x, 16);
+        b.y += __shfl_xor_sync(0xffffffffu, bo.y, 16);
+        b.z += __shfl_xor_sync(0xffffffffu, bo.z, 16);
+        b.w += __shfl_xor_sync(0xffffffffu, bo.w, 16);
+        if (initA) {
+            const float4 c = f4(initA + j);
+            a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+        }
+        st4(outA + (r + half) * n + j, a);
+        st4(outB + (r + half) * n + j, b);
+        return;
+    }
     for (int tile = threadIdx.x; tile < m * n4; tile += kThreads) {
         const int r = tile / n4, j = (tile - r * n4) * 4;
         float4 a = initA ? f4(initA + j) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -135,6 +206,37 @@ __device__ __forceinline__ int rot_start(int row, int k) { return (4 * row) % k;
 // 16-byte loads fall in different banks.
 __device__ __forceinline__ void mm_xyt(float *out, const float *X, const float *Y, int m, int k, int n)
 {
+    if ((m & 1) == 0 && (k & 7) == 0 && n == 64 && (m >> 1) * (n >> 2) * 2 == kThreads) {
+        // A 2 x 4 block (rows r, r + 1 of X against rows i..i+3 of Y) per pair of lanes l, l + 16,
+        // each lane summing one half of k: 6 loads per 32 FMAs instead of 4 per 16.  Each lane
+        // starts its half at column 4 (l mod 8), wrapping, so the eight lanes of a quarter-warp
+        // read eight different banks; one shuffle adds the halves, each lane stores one row.
+        const int lane = threadIdx.x & 31, half = lane >> 4, q = lane & 15;
+        const int r = (threadIdx.x >> 5) * 2, i = q * 4;
+        const int kh = k >> 1;
+        const float *x0 = X + r * k + half * kh, *x1 = x0 + k, *y0 = Y + i * k + half * kh;
+        float a[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        int u = (4 * (q & 7)) % kh;
+#pragma unroll
+        for (int c = 0; c < kh; c += 4) {
+            const float4 xa = f4(x0 + u), xb = f4(x1 + u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 y = f4(y0 + e * k + u);
+                a[0][e] += dot4(xa, y);
+                a[1][e] += dot4(xb, y);
+            }
+            u += 4;
+            if (u >= kh) u -= kh;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[h][e] += __shfl_xor_sync(0xffffffffu, a[h][e], 16);
+        st4(out + (r + half) * n + i, half ? make_float4(a[1][0], a[1][1], a[1][2], a[1][3])
+                                           : make_float4(a[0][0], a[0][1], a[0][2], a[0][3]));
+        return;
+    }
     if ((m | n) & 1) {
         for (int idx = threadIdx.x; idx < m * n; idx += kThreads) {
             const int r = idx / n, i = idx - r * n;
