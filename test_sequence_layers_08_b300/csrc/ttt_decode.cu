@@ -99,6 +99,17 @@ __device__ __forceinline__ float2 warp_sum2(float a, float b)
     return make_float2(a, b);
 }
 
+__device__ __forceinline__ float3 warp_sum3(float a, float b, float c)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+        c += __shfl_xor_sync(0xffffffffu, c, o);
+    }
+    return make_float3(a, b, c);
+}
+
 template <bool BF16, bool LN, bool WD>
 __global__ void __launch_bounds__(kWarps * 32)
 linear_decode_kernel(DecodeParams p)
@@ -191,21 +202,24 @@ linear_decode_kernel(DecodeParams p)
         // key-side product with the state before this token's update (with the LayerNorm also
         // the query-side product and q . k)
         float z0, z1, y0 = 0.f, y1 = 0.f, qk = 0.f;
-        if (LN) {
+        if (LN)
             rows_times_w(rows[warp][1], rows[warp][0], z0, z1, y0, y1);
-            qk = warp_sum(fmaf(q.x, k.x, q.y * k.y));
-        } else {
+        else
             row_times_w(rows[warp][1], z0, z1);
-        }
         z0 += c0;
         z1 += c1;
         float g0, g1;
         if (LN) {
-            // two passes (mean, then the centred second moment): no cancellation when z has a
-            // common offset much larger than its spread
-            const float mu = warp_sum(z0 + z1) * (1.f / D);
+            // one reduction round for q . k and the sums of z - z_0 and (z - z_0)^2, z_0 this
+            // token's first feature: shifted one-pass sums, free of cancellation when z has a
+            // common offset much larger than its spread, and depending on this token alone
+            const float sh = __shfl_sync(0xffffffffu, z0, 0);
+            const float d0 = z0 - sh, d1 = z1 - sh;
+            const float3 s3 = warp_sum3(fmaf(q.x, k.x, q.y * k.y), d0 + d1, fmaf(d0, d0, d1 * d1));
+            qk = s3.x;
+            const float md = s3.y * (1.f / D), mu = sh + md;
             const float zc0 = z0 - mu, zc1 = z1 - mu;
-            const float r = rsqrtf(warp_sum(fmaf(zc0, zc0, zc1 * zc1)) * (1.f / D) + p.eps);
+            const float r = rsqrtf(fmaxf(s3.z * (1.f / D) - md * md, 0.f) + p.eps);
             const float xh0 = zc0 * r, xh1 = zc1 * r;
             const float gx0 = p.ip ? -ga0 * v.x : ga0 * (fmaf(ga0, xh0, be0) - (v.x - k.x));
             const float gx1 = p.ip ? -ga1 * v.y : ga1 * (fmaf(ga1, xh1, be1) - (v.y - k.y));
@@ -246,10 +260,13 @@ linear_decode_kernel(DecodeParams p)
             o0 += c0;
             o1 += c1;
         }
-        if (LN) {
-            const float mu = warp_sum(o0 + o1) * (1.f / D);
+        if (LN) {   // shifted one-pass sums of o, as for z
+            const float sh = __shfl_sync(0xffffffffu, o0, 0);
+            const float d0 = o0 - sh, d1 = o1 - sh;
+            const float2 s2 = warp_sum2(d0 + d1, fmaf(d0, d0, d1 * d1));
+            const float md = s2.x * (1.f / D), mu = sh + md;
             const float oc0 = o0 - mu, oc1 = o1 - mu;
-            const float r = rsqrtf(warp_sum(fmaf(oc0, oc0, oc1 * oc1)) * (1.f / D) + p.eps);
+            const float r = rsqrtf(fmaxf(s2.y * (1.f / D) - md * md, 0.f) + p.eps);
             o0 = q.x + fmaf(ga0 * oc0, r, be0);
             o1 = q.y + fmaf(ga1 * oc1, r, be1);
         }

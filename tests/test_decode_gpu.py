@@ -91,12 +91,15 @@ def test_decode_many_heads_full_width():
                 oracle_ref(cfg, x, W, b))
 
 
+@pytest.mark.parametrize("spread", [0.0, 0.5])
 @pytest.mark.parametrize("ln", [False, True])
-def test_decode_large_bias_offset(ln):
-    """A state whose bias carries a large common offset (about 4 on every feature): the
-    LayerNorm statistics of k W + c must not lose the token's spread to cancellation."""
+def test_decode_large_bias_offset(ln, spread):
+    """A state whose bias carries a large common offset (about 4 on every feature, exactly or
+    with a per-feature spread): the LayerNorm statistics of k W + c must not lose the token's
+    spread to cancellation."""
     cfg, x, W, b = problem("bf16", ln, B=2, H=3, L=24, seed=41)
-    b = (b + 4.0).astype(np.float32)
+    rng = np.random.default_rng(42)
+    b = (b + 4.0 + spread * rng.standard_normal(b.shape)).astype(np.float32)
     d = to_dev(cfg, x, W, b)
     Z = step(cfg, d)
     compare_all(cfg, [Z.float().cpu().numpy(), d["W"].cpu().numpy(), d["b"].cpu().numpy()],
