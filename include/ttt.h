@@ -255,8 +255,10 @@ TTT_API ttt_status ttt_eta_gate(int B, int H, int L, int d_model, ttt_dtype x_dt
  * Supported: d = 64, d_model a multiple of 64, 3 H d a multiple of 256 (tcgen05 kernel);
  * otherwise TTT_ERR_UNSUPPORTED.  x, W, Q, K, V 16-byte aligned; the outputs may overlap
  * neither each other nor an input.  max_sms > 0 caps the persistent grid at that many SMs
- * (0: every SM), for a call that runs beside a scan holding the other SMs; max_sms < 0 is
- * TTT_ERR_INVALID_ARG.  A bounded wait that runs out is reported by ttt_sync_status.
+ * (0: every SM; the kernel runs in pairs of CTAs, so an odd cap is rounded down to an even
+ * one, and a cap of 1 to one pair), for a call that runs beside a scan holding the other
+ * SMs; max_sms < 0 is TTT_ERR_INVALID_ARG.  A bounded wait that runs out is reported by
+ * ttt_sync_status.
  */
 TTT_API ttt_status ttt_qkv_proj(int B, int H, int L, int d_model, int d, const void *x, const void *W,
                                 void *Q, void *K, void *V, int max_sms, ttt_stream_t stream);
